@@ -1,0 +1,426 @@
+"""Plain float64 CPU oracle for the batched speculative-decoding verify-and-sample step.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` are the only callers.  The CUDA
+library never calls this module and shares no code, table or constant with it.
+
+What it computes, in the pages' order (sources are listed at the end of this
+docstring and cited as ``[tag §section]``):
+
+1. The production transforms that turn logits into the distribution actually
+   sampled from: temperature, then top-k, then top-p.  p (target) and q (draft)
+   each use their own parameters.  [wrblog §2.3, §7.2, §7.3; magicnet §2]
+2. Left-to-right verification: draft token d_i is accepted with probability
+   a_i = min(1, p_i(d_i) / q_i(d_i)); the scan stops at the first rejection and
+   every later draft is discarded.  [wrblog §4.1, §6; rainlin §1-§2; baisen §4]
+3. At the first rejection j the replacement token is drawn from the residual
+   (p_j - q_j)+ / Z with Z = sum (p_j - q_j)+.  If all drafts are accepted a
+   bonus token is drawn from p_{gamma+1}.  [wrblog §5, §6; rainlin §2; baisen §4]
+4. Greedy mode: accept while d_i equals argmax p_i; at the first mismatch emit
+   argmax p_i; if every draft matches emit argmax p_{gamma+1}.
+   [wrblog §7.1; baisen §2, §6; rainlin §2]
+
+All arithmetic is float64 NumPy.  bf16 logits are widened exactly (bit shift).
+Sorting, cumulative sums and ``searchsorted`` are library primitives; nothing
+is blocked, fused or reordered beyond the definitions below.
+
+Readings where the pages are silent (each is named where it is used):
+
+* R1  transform order: temperature, top-k on the tempered logits, renormalise,
+      top-p on the renormalised probabilities, renormalise.
+* R2  ties: every ordering is (value descending, token index ascending).
+* R3  top-p keeps the shortest prefix of that order whose cumulative
+      probability is >= top_p; top_p == 1 keeps everything; top_k == 0 or
+      top_k >= V keeps everything.
+* R4  accept iff u < a (strict), u in [0, 1)  -- as in the demo of [wrblog §8].
+* R5  a uniform u picks the smallest token x (vocabulary order) whose
+      cumulative weight C(x) = sum_{y<=x} w(y) exceeds u * C(V-1).
+* R6  q(d) == 0: a = 1 if p(d) > 0 else 0, and the sequence is flagged.
+* R7  Z == 0 after a rejection (only reachable through rounding): draw from
+      p_j instead and flag the sequence.
+* R8  one uniform per draft position plus one uniform u_sample that the
+      residual draw or the bonus draw consumes.
+* R9  the bonus token is part of the output ([wrblog §6], [rainlin §1]).
+* R10 a NaN or +inf logit in any row the sequence uses, or a row whose logits
+      are all -inf, fails the whole sequence: nothing is committed
+      ([wrblog §15]).  -inf marks a banned token ([wrblog §2.3]).
+
+Pins (tests/test_oracle_*.py): the worked examples of [wrblog §4.3, §5, §7.1]
+and [baisen §2, §4, §6]; the identities Z = sum (p-q)+ = sum (q-p)+ =
+1 - sum min(p,q) [rainlin §2; baisen §5; magicnet §3]; the exact single- and
+multi-token output law by exhaustive enumeration; the truncated-geometric law
+of tokens per round and its mean (1 - a^{g+1}) / (1 - a) [magicnet §4;
+rainlin §3; wrblog §10]; the textbook softmax; brute-force top-k / top-p sets.
+Parity unpinned: the tie rule R2 and the transform order R1 are readings, not
+statements of the pages; only self-consistency and the brute-force set
+definitions check them.
+
+Sources:
+  [wrblog]   "推测解码：草稿模型、接受率、正确性与加速边界" (wrblog.cn)
+  [aiqz]     "投机解码：草稿小模型 + 大模型并行验证的无损加速" (aiqz.cc)
+  [rainlin]  "投机解码" (rainlin-net.pages.dev, llm-inference/speculative-decoding)
+  [baisen]   "投机采样 / 投机解码（Speculative Decoding）" (baisen.site)
+  [magicnet] "投机解码到底能加速多少：把接受率、草稿成本与墙钟收益算清楚"
+             (magicnetworld.com)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# Per-sequence status codes.  The numeric values are an interface convention
+# that the C header states independently.
+SEQ_OK = 0
+SEQ_BAD_LENGTH = 1      # gamma_b outside [0, gamma_max]
+SEQ_BAD_TOKEN = 2       # a draft token outside [0, V)
+SEQ_BAD_UNIFORM = 3     # a uniform outside [0, 1) or NaN
+SEQ_NONFINITE = 4       # NaN or +inf logit in a row the sequence uses
+SEQ_EMPTY_SUPPORT = 5   # a row whose logits are all -inf
+SEQ_ERROR_MASK = 0xFF
+SEQ_FLAG_ZERO_Q = 0x100  # an evaluated draft token had q(d) == 0 (R6)
+SEQ_FLAG_Z_ZERO = 0x200  # residual mass was 0 after a rejection (R7)
+
+
+# --------------------------------------------------------------------------
+# Input widening
+# --------------------------------------------------------------------------
+def bf16_bits_to_float64(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to float64 exactly.
+
+    A bf16 value is the upper half of an IEEE float32, so shifting the 16 bits
+    into the high half of a 32-bit word reproduces the value bit for bit.
+    """
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def float32_to_float64(x: np.ndarray) -> np.ndarray:
+    """Widen float32 logits to float64 exactly."""
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Step 1: logits -> sampling distribution   [wrblog §2.3, §7.2, §7.3]
+# --------------------------------------------------------------------------
+def order_desc(z: np.ndarray) -> np.ndarray:
+    """Token indices sorted by (logit descending, index ascending)  (R2).
+
+    ``np.lexsort`` sorts by its last key first: -z ascending is z descending,
+    ties fall back to the index key, ascending.  -0.0 and +0.0 compare equal,
+    so they tie and the lower index wins.
+    """
+    idx = np.arange(z.size)
+    return np.lexsort((idx, -z))
+
+
+@dataclass
+class RowDist:
+    """One transformed row: the distribution p (or q) over the vocabulary."""
+    status: int
+    probs: np.ndarray                  # (V,) float64; zeros unless status == SEQ_OK
+    kept: np.ndarray                   # kept token ids in (value desc, index asc) order
+    top_p_margin: float = np.inf       # distance of the top-p decision from top_p (R3)
+
+
+def row_status(z: np.ndarray) -> int:
+    """R10: NaN / +inf logits are invalid; a row of only -inf has no support."""
+    if np.isnan(z).any() or np.isposinf(z).any():
+        return SEQ_NONFINITE
+    if np.all(np.isneginf(z)):
+        return SEQ_EMPTY_SUPPORT
+    return SEQ_OK
+
+
+def transform_row(z: np.ndarray, temperature: float, top_k: int, top_p: float) -> RowDist:
+    """p_T = softmax(z / T) restricted by top-k then top-p  [wrblog §7.2, §7.3] (R1-R3).
+
+    Temperature is order preserving for T > 0, so the top-k set is taken on the
+    raw logits.  The softmax over the kept set subtracts the largest kept logit
+    (a constant shift that leaves softmax unchanged).
+    """
+    z = np.asarray(z, dtype=np.float64)
+    V = z.size
+    status = row_status(z)
+    if status != SEQ_OK:
+        return RowDist(status, np.zeros(V), np.zeros(0, dtype=np.int64))
+    if not temperature > 0:
+        raise ValueError("temperature must be > 0; use greedy verification for T -> 0")
+    order = order_desc(z)
+    kept = order if (top_k <= 0 or top_k >= V) else order[:top_k]
+    zk = z[kept]
+    m = zk[0]
+    w = np.exp((zk - m) / temperature)          # -inf logits give weight 0
+    p_tilde = w / w.sum()
+    margin = np.inf
+    if top_p < 1.0:
+        cum = np.cumsum(p_tilde)
+        reached = np.flatnonzero(cum >= top_p)
+        n = int(reached[0]) + 1 if reached.size else kept.size
+        above = cum[n - 1] - top_p
+        below = top_p - cum[n - 2] if n >= 2 else np.inf
+        margin = float(min(abs(above), abs(below)))
+        kept = kept[:n]
+        w = w[:n]
+    probs = np.zeros(V)
+    probs[kept] = w / w.sum()
+    return RowDist(SEQ_OK, probs, kept, margin)
+
+
+def one_hot_row(V: int, token: int) -> RowDist:
+    """A draft that proposes one token with certainty (n-gram style, q = delta)."""
+    probs = np.zeros(V)
+    if 0 <= token < V:
+        probs[token] = 1.0
+    return RowDist(SEQ_OK, probs, np.array([token], dtype=np.int64))
+
+
+# --------------------------------------------------------------------------
+# Step 2: acceptance   [wrblog §4.1, §4.2, §6]
+# --------------------------------------------------------------------------
+def acceptance_probability(p_x: float, q_x: float) -> tuple[float, bool]:
+    """a(x) = min(1, p(x)/q(x)) [wrblog §4.1]; returns (a, q_was_zero) (R6)."""
+    if q_x > 0.0:
+        return min(1.0, p_x / q_x), False
+    return (1.0 if p_x > 0.0 else 0.0), True
+
+
+def acceptance_rate(p: np.ndarray, q: np.ndarray) -> float:
+    """Expected acceptance at one position: sum_x min(p(x), q(x))  [wrblog §4.2]."""
+    return float(np.minimum(p, q).sum())
+
+
+def residual_weights(p: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """Unnormalised residual (p - q)+  [wrblog §5]."""
+    return np.maximum(p - q, 0.0)
+
+
+# --------------------------------------------------------------------------
+# Step 3: draw one token from a weight vector (R5)
+# --------------------------------------------------------------------------
+def inverse_cdf(w: np.ndarray, u: float) -> tuple[int, float, float]:
+    """Smallest x with C(x) > u * C(V-1), C the running sum in vocabulary order.
+
+    Returns (token, lo, hi): the token's normalised CDF interval [lo, hi).
+    """
+    C = np.cumsum(np.asarray(w, dtype=np.float64))
+    Z = C[-1]
+    if not Z > 0:
+        raise ValueError("cannot sample from an all-zero weight vector")
+    x = int(np.searchsorted(C, u * Z, side="right"))
+    x = min(x, C.size - 1)
+    lo = C[x - 1] / Z if x > 0 else 0.0
+    return x, float(lo), float(C[x] / Z)
+
+
+# --------------------------------------------------------------------------
+# One sequence
+# --------------------------------------------------------------------------
+@dataclass
+class SeqResult:
+    tokens: np.ndarray          # (gamma_max + 1,) int64; -1 after the last emitted token
+    num_accepted: int           # -1 on error (commit nothing)
+    status: int
+    accept_prob: np.ndarray     # (gamma_max,) a_i for i < gamma_b, -1 elsewhere
+    residual_Z: float           # Z at the rejected position, -1 when nothing was rejected
+    accept_margin: float = np.inf   # min |u_i - a_i| over evaluated positions
+    top_p_margin: float = np.inf    # min top-p margin over the rows used
+    sample_u: float = np.nan
+    sample_lo: float = np.nan
+    sample_hi: float = np.nan
+    sample_cdf: np.ndarray | None = field(default=None, repr=False)  # normalised CDF drawn from
+
+
+def _error_result(status: int, gamma_max: int) -> SeqResult:
+    return SeqResult(np.full(gamma_max + 1, -1, dtype=np.int64), -1, status,
+                     np.full(gamma_max, -1.0), -1.0)
+
+
+def _valid_uniform(u: float) -> bool:
+    return bool(0.0 <= u < 1.0)
+
+
+def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarray,
+                           u_accept: np.ndarray, u_sample: float,
+                           target_params: tuple[float, int, float],
+                           draft_params: tuple[float, int, float],
+                           gamma_b: int, gamma_max: int, one_hot: bool,
+                           keep_cdf: bool = False) -> SeqResult:
+    """Verify one sequence in sampling mode  [wrblog §6; rainlin §1].
+
+    target: (gamma_max+1, V) float64 logits; rows 0..gamma_b are used.
+    draft:  (gamma_max, V) float64 logits, rows 0..gamma_b-1 used; ignored when one_hot.
+    tokens: (gamma_max,) draft tokens d_1..d_gamma (0-based positions).
+    """
+    V = target.shape[1]
+    if not 0 <= gamma_b <= gamma_max:
+        return _error_result(SEQ_BAD_LENGTH, gamma_max)
+    d = [int(t) for t in tokens[:gamma_b]]
+    if any(not 0 <= t < V for t in d):
+        return _error_result(SEQ_BAD_TOKEN, gamma_max)
+    if not all(_valid_uniform(float(u)) for u in u_accept[:gamma_b]) or not _valid_uniform(float(u_sample)):
+        return _error_result(SEQ_BAD_UNIFORM, gamma_max)
+
+    # Step 1: p_1..p_{gamma+1} and q_1..q_gamma, each with its own transform [wrblog §7.2].
+    p_rows, q_rows = [], []
+    for i in range(gamma_b + 1):
+        p_i = transform_row(target[i], *target_params)
+        if p_i.status != SEQ_OK:
+            return _error_result(p_i.status, gamma_max)
+        p_rows.append(p_i)
+        if i < gamma_b:
+            q_i = one_hot_row(V, d[i]) if one_hot else transform_row(draft[i], *draft_params)
+            if q_i.status != SEQ_OK:
+                return _error_result(q_i.status, gamma_max)
+            q_rows.append(q_i)
+
+    # Step 2: a_i for every draft position; the scan stops at the first rejection [wrblog §6].
+    a = np.full(gamma_max, -1.0)
+    zero_q = np.zeros(gamma_max, dtype=bool)
+    for i in range(gamma_b):
+        a[i], zero_q[i] = acceptance_probability(p_rows[i].probs[d[i]], q_rows[i].probs[d[i]])
+    status = SEQ_OK
+    rejected_at = None
+    accept_margin = np.inf
+    for i in range(gamma_b):
+        if zero_q[i]:
+            status |= SEQ_FLAG_ZERO_Q
+        accept_margin = min(accept_margin, abs(float(u_accept[i]) - a[i]))
+        if not float(u_accept[i]) < a[i]:          # R4: strict comparison
+            rejected_at = i
+            break
+
+    # Step 3: residual at the rejected position, else the bonus from p_{gamma+1}.
+    residual_Z = -1.0
+    if rejected_at is not None:
+        j = rejected_at
+        w = residual_weights(p_rows[j].probs, q_rows[j].probs)     # [wrblog §5]
+        residual_Z = float(w.sum())
+        if not residual_Z > 0:                                      # R7
+            w = p_rows[j].probs
+            status |= SEQ_FLAG_Z_ZERO
+        n_acc = j
+    else:
+        w = p_rows[gamma_b].probs                                   # bonus [wrblog §6]
+        n_acc = gamma_b
+    tok, lo, hi = inverse_cdf(w, float(u_sample))
+
+    out = np.full(gamma_max + 1, -1, dtype=np.int64)
+    out[:n_acc] = d[:n_acc]
+    out[n_acc] = tok
+    used = p_rows[: n_acc + 1] + ([] if one_hot else q_rows[: min(n_acc + 1, gamma_b)])
+    top_p_margin = min([r.top_p_margin for r in used] + [np.inf])
+    res = SeqResult(out, n_acc, status, a, residual_Z, accept_margin, top_p_margin,
+                    float(u_sample), lo, hi)
+    if keep_cdf:
+        C = np.cumsum(w)
+        res.sample_cdf = C / C[-1]
+    return res
+
+
+def greedy_row(z: np.ndarray) -> tuple[int, int]:
+    """argmax with the lowest index on ties (R2), and the row status (R10)."""
+    status = row_status(z)
+    if status != SEQ_OK:
+        return -1, status
+    return int(order_desc(z)[0]), SEQ_OK
+
+
+def verify_greedy_sequence(target: np.ndarray, tokens: np.ndarray, gamma_b: int,
+                           gamma_max: int) -> SeqResult:
+    """Greedy verification: longest argmax-matching prefix plus one target token.
+
+    [wrblog §7.1; baisen §2 (the "mat and the cat" walk-through), §6; rainlin §2]
+    """
+    V = target.shape[1]
+    if not 0 <= gamma_b <= gamma_max:
+        return _error_result(SEQ_BAD_LENGTH, gamma_max)
+    d = [int(t) for t in tokens[:gamma_b]]
+    if any(not 0 <= t < V for t in d):
+        return _error_result(SEQ_BAD_TOKEN, gamma_max)
+    g = []
+    for i in range(gamma_b + 1):
+        gi, st = greedy_row(target[i])
+        if st != SEQ_OK:
+            return _error_result(st, gamma_max)
+        g.append(gi)
+    n_acc = gamma_b
+    for i in range(gamma_b):
+        if d[i] != g[i]:
+            n_acc = i
+            break
+    out = np.full(gamma_max + 1, -1, dtype=np.int64)
+    out[:n_acc] = d[:n_acc]
+    out[n_acc] = g[n_acc]
+    return SeqResult(out, n_acc, SEQ_OK, np.full(gamma_max, -1.0), -1.0)
+
+
+# --------------------------------------------------------------------------
+# Batches  [aiqz "加速收益与工程" -- requests verified together as one batch]
+# --------------------------------------------------------------------------
+@dataclass
+class BatchResult:
+    tokens: np.ndarray
+    num_accepted: np.ndarray
+    status: np.ndarray
+    accept_prob: np.ndarray
+    residual_Z: np.ndarray
+    seqs: list
+
+
+def _collect(results: list[SeqResult]) -> BatchResult:
+    return BatchResult(np.stack([r.tokens for r in results]),
+                       np.array([r.num_accepted for r in results], dtype=np.int64),
+                       np.array([r.status for r in results], dtype=np.int64),
+                       np.stack([r.accept_prob for r in results]) if results else np.zeros((0, 0)),
+                       np.array([r.residual_Z for r in results]),
+                       results)
+
+
+def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarray,
+                  u_accept: np.ndarray, u_sample: np.ndarray,
+                  target_params: tuple[float, int, float], draft_params: tuple[float, int, float],
+                  gamma_per_seq: np.ndarray | None = None, one_hot: np.ndarray | None = None,
+                  seqs: list[int] | None = None, keep_cdf: bool = False) -> BatchResult:
+    """Batched sampling verification, one sequence at a time.
+
+    target (B, gamma_max+1, V), draft (B, gamma_max, V) or None (all one-hot),
+    tokens / u_accept (B, gamma_max), u_sample (B,), all float64 / int.
+    ``seqs`` restricts the work to a subset of sequence indices.
+    """
+    B, G1, _ = target.shape
+    gamma_max = G1 - 1
+    seqs = range(B) if seqs is None else seqs
+    out = []
+    for b in seqs:
+        g = gamma_max if gamma_per_seq is None else int(gamma_per_seq[b])
+        oh = draft is None or (one_hot is not None and bool(one_hot[b]))
+        out.append(verify_sample_sequence(target[b], None if oh else draft[b], tokens[b],
+                                          u_accept[b], float(u_sample[b]), target_params,
+                                          draft_params, g, gamma_max, oh, keep_cdf))
+    return _collect(out)
+
+
+def verify_greedy(target: np.ndarray, tokens: np.ndarray,
+                  gamma_per_seq: np.ndarray | None = None,
+                  seqs: list[int] | None = None) -> BatchResult:
+    """Batched greedy verification, one sequence at a time."""
+    B, G1, _ = target.shape
+    gamma_max = G1 - 1
+    seqs = range(B) if seqs is None else seqs
+    out = []
+    for b in seqs:
+        g = gamma_max if gamma_per_seq is None else int(gamma_per_seq[b])
+        out.append(verify_greedy_sequence(target[b], tokens[b], g, gamma_max))
+    return _collect(out)
+
+
+def transform_rows(z: np.ndarray, temperature: float, top_k: int, top_p: float) -> tuple[np.ndarray, np.ndarray]:
+    """Row-wise transform of a (rows, V) logits array: returns (probs, top_p_margin)."""
+    probs = np.zeros(z.shape)
+    margins = np.full(z.shape[0], np.inf)
+    for r in range(z.shape[0]):
+        rd = transform_row(z[r], temperature, top_k, top_p)
+        probs[r] = rd.probs
+        margins[r] = rd.top_p_margin
+    return probs, margins
