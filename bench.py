@@ -1,0 +1,371 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched speculative-decoding verify-and-sample step.
+
+One step = one spec_verify_sample call over the whole serving-shaped batch
+(B=64 sequences, gamma=5 drafts, V=128256 bf16 logits, temperature 0.7,
+top-k 50, top-p 0.9 for target and draft), inputs resident in HBM.  The step
+rotates over 4 independent input sets (4 x 180.6 MB, larger than the 126 MB
+L2), so every call streams its logits from HBM.
+
+Prints ONE JSON line (rank 0).  Metric: verified positions/s (target
+positions consumed, sum of gamma_b + 1), next to the logits HBM GB/s of the
+verify kernel as a fraction of the measured copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  torchrun --nproc-per-node N bench.py --gpus N ...   (weak scaling: one batch per GPU,
+                                                       no data-path collective)
+
+--impl reference times the float64 CPU oracle (the only reference that exists
+for this method) on the same workload, one sequence per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified positions/s and logits HBM GB/s (% of peak), B=64 g=5 V=128256 bf16"
+WID = 3
+L2_BYTES = 126 * 2 ** 20
+ROTATE = 4
+KERNEL_SOURCES = ["speculative_decoding_verification_44_gb300/csrc/spec_verify.cu",
+                  "speculative_decoding_verification_44_gb300/csrc/sv_row.cuh",
+                  "speculative_decoding_verification_44_gb300/csrc/sv_common.cuh"]
+PROFILE = os.path.join(ROOT, "profiles", "sample_kernel_serving_B64_g5_V128256.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic():
+    """dram bytes per launch from the committed ncu summary, if it matches the current kernel."""
+    try:
+        fields = {}
+        with open(PROFILE) as f:
+            for ln in f:
+                if ":" in ln:
+                    k, v = ln.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha") != kernel_source_sha():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_draft_probs(rows, params):
+    """Draft distribution q for drawing the benchmark's draft tokens (the library's transform)."""
+    import speculative_decoding_verification_44_gb300 as sv
+    probs, _ = sv.transform_probs(rows.contiguous(), params)
+    return probs
+
+
+def cpu_oracle_probs(rows, params):
+    import numpy as np
+    import oracle
+    import torch
+    p, _ = oracle.transform_rows(rows.float().double().numpy(), float(np.float32(params.temperature)),
+                                 int(params.top_k), float(np.float32(params.top_p)))
+    return torch.from_numpy(p)
+
+
+def oracle_sample_time(w, seqs, budget_s=None):
+    """Time the float64 oracle on the given sequences; returns (positions, seconds, n_seq)."""
+    import numpy as np
+    import oracle
+
+    def f64(t):
+        return t.detach().to("cpu").float().double().numpy()
+
+    tp = (float(np.float32(w.target_params.temperature)), int(w.target_params.top_k),
+          float(np.float32(w.target_params.top_p)))
+    dp = (float(np.float32(w.draft_params.temperature)), int(w.draft_params.top_k),
+          float(np.float32(w.draft_params.top_p)))
+    positions, elapsed, n = 0, 0.0, 0
+    for b in seqs:
+        tl = f64(w.target_logits[b:b + 1])
+        dl = f64(w.draft_logits[b:b + 1])
+        toks = w.draft_tokens[b:b + 1].cpu().numpy()
+        ua = w.u_accept[b:b + 1].cpu().double().numpy()
+        us = w.u_sample[b:b + 1].cpu().double().numpy()
+        t0 = time.perf_counter()
+        oracle.verify_sample(tl, dl, toks, ua, us, tp, dp)
+        elapsed += time.perf_counter() - t0
+        positions += w.G + 1
+        n += 1
+        if budget_s is not None and elapsed >= budget_s:
+            break
+    return positions, elapsed, n
+
+
+def run_reference(args, rank):
+    """Reference arm: the float64 oracle on the host cores, one sequence per step."""
+    if rank != 0:
+        return
+    from speculative_decoding_verification_44_gb300 import workloads
+    w = workloads.make(WID, "cpu", draft_probs=cpu_oracle_probs)
+    order = [s % w.B for s in range(args.warmup + args.steps)]
+    oracle_sample_time(w, order[: args.warmup])
+    pos, secs, n = oracle_sample_time(w, order[args.warmup:])
+    value = pos / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, n), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workloads.NAMES[WID], "B": w.B, "gamma": w.G, "V": w.V, "dtype": "bf16",
+                   "temperature": 0.7, "top_k": 50, "top_p": 0.9,
+                   "step": "one sequence (gamma+1 = 6 verified positions) per step"},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} sequences of the serving workload, one per step"},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from speculative_decoding_verification_44_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    import speculative_decoding_verification_44_gb300 as sv
+    from speculative_decoding_verification_44_gb300 import workloads
+
+    # independent batches: replica = rank * ROTATE + r
+    sets = [workloads.make(WID, dev, draft_probs=gpu_draft_probs, replica=rank * ROTATE + r)
+            for r in range(ROTATE)]
+    w0 = sets[0]
+    B, G, V = w0.B, w0.G, w0.V
+    rt, rd = w0.rows_used()
+    logits_bytes = (rt + rd) * V * 2
+    io_bytes = B * G * 4 * 2 + B * 4 + B * (G + 1) * 4 + B * 4 * 3 + B * G * 4
+    alg_bytes = logits_bytes + io_bytes
+    ws = sv.new_workspace(sv.workspace_size(B, G, V, w0.target_params, w0.draft_params), dev)
+    outs = [sv.alloc_outputs(B, G, dev) for _ in range(ROTATE)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        w = sets[i % ROTATE]
+        sv.verify_sample(w.target_logits, w.draft_logits, w.draft_tokens, w.u_accept, w.u_sample,
+                         w.target_params, w.draft_params, workspace=ws, out=outs[i % ROTATE])
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(local_rank) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    total_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    positions_per_step = rt * world
+    value = positions_per_step / (ms_per_step / 1e3)
+
+    # outcome statistics of the last step (emitted tokens / s etc.)
+    last = outs[(K - 1) % ROTATE]
+    emitted = int((last.num_accepted.clamp(min=-1) + 1).sum().item())
+
+    peak, peak_kind = measured_peaks()
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = alg_bytes / avg_launch_s / 1e9
+    traffic = profile_traffic()
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_kind": f"of {peak_kind}",
+                "kernel": "sv::sample_kernel<bf16>", "algorithmic_bytes_per_launch": alg_bytes,
+                "launch_ms_median": statistics.median(launch_ms),
+                "frac_of_nominal_8TBps": achieved / 8000.0}
+
+    # end to end through the public API with host buffers (pinned), rank-local
+    e2e = None
+    if not args.no_e2e:
+        w = sets[0]
+        host = {k: getattr(w, k).cpu().pin_memory() for k in
+                ("target_logits", "draft_logits", "draft_tokens", "u_accept", "u_sample")}
+        dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        hout = {"tokens": torch.empty(B, G + 1, dtype=torch.int32).pin_memory(),
+                "num_accepted": torch.empty(B, dtype=torch.int32).pin_memory(),
+                "status": torch.empty(B, dtype=torch.int32).pin_memory()}
+        dout = sv.alloc_outputs(B, G, dev, accept_prob=False, residual_z=False)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+        def e2e_step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            sv.verify_sample(dbuf["target_logits"], dbuf["draft_logits"], dbuf["draft_tokens"],
+                             dbuf["u_accept"], dbuf["u_sample"], w.target_params, w.draft_params,
+                             workspace=ws, out=dout)
+            hout["tokens"].copy_(dout.tokens, non_blocking=True)
+            hout["num_accepted"].copy_(dout.num_accepted, non_blocking=True)
+            hout["status"].copy_(dout.status, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        Ke = max(5, min(K, 30))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / Ke
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": rt * world / (e_ms / 1e3), "unit": "positions/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pos, secs, n = oracle_sample_time(w0, list(range(B)), budget_s=12.0)
+        cpu_baseline = {"value": pos / secs, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                        "sample": f"first {n} of {B} sequences of the same workload (rotation set 0), "
+                                  f"{pos} verified positions in {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workloads.NAMES[WID], "B": B, "gamma": G, "V": V,
+                       "temperature": 0.7, "top_k": 50, "top_p": 0.9, "batches_per_gpu": 1,
+                       "l2": f"inputs rotate over {ROTATE} independent sets of {logits_bytes / 1e6:.1f} MB "
+                             f"(each larger than the {L2_BYTES / 2**20:.0f} MiB L2)",
+                       "parallelism": f"replicas x{world} (one batch per GPU, no data-path collective)"},
+            "sequences_per_s": B * world / (ms_per_step / 1e3),
+            "drafts_judged_per_s": B * G * world / (ms_per_step / 1e3),
+            "emitted_tokens_per_s_last_step": emitted * world / (ms_per_step / 1e3),
+            "logits_bytes_per_verified_position": logits_bytes / rt,
+            "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
+            "gpu_launches": K,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verify-and-sample library (libspecverify.so).
+ *
+ * One call verifies a batch of B sequences after the target model's single
+ * parallel forward over gamma+1 positions.  For every sequence b it
+ *
+ *   1. turns the target logits rows 1..gamma_b+1 and the draft logits rows
+ *      1..gamma_b into the distributions actually sampled from, p and q, by
+ *      temperature, then top-k, then top-p (each side with its own
+ *      parameters)                               [wrblog §2.3, §7.2, §7.3];
+ *   2. accepts draft token d_i with probability a_i = min(1, p_i(d_i)/q_i(d_i)),
+ *      left to right, stopping at the first rejection  [wrblog §4.1, §6];
+ *   3. draws the replacement from the residual (p_j - q_j)+ / Z at the
+ *      rejected position j, or a bonus token from p_{gamma_b+1} when every
+ *      draft was accepted                   [wrblog §5, §6; rainlin §1-§2];
+ *
+ * and, in greedy mode, emits the longest argmax-matching prefix plus the
+ * target's argmax at the first mismatch (or the bonus position)
+ *                                           [wrblog §7.1; baisen §2, §6].
+ *
+ * Readings of points the sources leave open (the library and its tests use
+ * exactly these):
+ *   - transform order: temperature; top-k on the logits; renormalise; top-p
+ *     on the renormalised probabilities; renormalise.
+ *   - every ordering is (value descending, token index ascending): argmax and
+ *     top-k ties go to the lower token index.  -0.0 equals +0.0.
+ *   - top-p keeps the shortest prefix of that order whose cumulative
+ *     probability reaches top_p (the crossing token is kept).
+ *   - accept iff u < a (strict); uniforms lie in [0, 1).
+ *   - a uniform u selects the smallest token x, in vocabulary order, whose
+ *     cumulative weight C(x) exceeds u * Z.
+ *   - q(d) == 0 gives a = 1 if p(d) > 0 else 0 and sets SPEC_SEQ_FLAG_ZERO_Q.
+ *   - Z == 0 after a rejection (rounding only) draws from p_j instead and
+ *     sets SPEC_SEQ_FLAG_Z_ZERO.
+ *   - a NaN or +inf logit, or a row of only -inf, in any row a sequence uses
+ *     fails that sequence: nothing is committed [wrblog §15].  -inf marks a
+ *     banned token [wrblog §2.3].
+ *
+ * Sources cited above:
+ *   [wrblog]  "推测解码：草稿模型、接受率、正确性与加速边界" (wrblog.cn)
+ *   [rainlin] "投机解码" (rainlin-net.pages.dev, llm-inference/speculative-decoding)
+ *   [baisen]  "投机采样 / 投机解码（Speculative Decoding）" (baisen.site)
+ *
+ * Conventions common to every entry point
+ * ----------------------------------------
+ * - Pointers named *_logits, draft_tokens, gamma_per_seq, draft_is_onehot,
+ *   u_*, workspace and out_* are DEVICE pointers (cudaMalloc / torch CUDA
+ *   tensors on the current device).  Sizes are host integers.
+ * - The caller allocates and owns every buffer, including the workspace.  The
+ *   library allocates nothing, keeps no state between calls and never
+ *   synchronises: all work is enqueued on `stream` (a cudaStream_t; NULL is
+ *   the legacy default stream) and the call returns immediately.
+ * - Logits are row-major.  Element (b, i, x) of target_logits is at
+ *   ((b * (gamma_max + 1) + i) * vocab + x); of draft_logits at
+ *   ((b * gamma_max + i) * vocab + x).  Rows with i > gamma_b (target) or
+ *   i >= gamma_b (draft) are never read.
+ * - Full bandwidth needs vocab * sizeof(element) to be a multiple of 16 and
+ *   16-byte aligned logits pointers; other layouts are accepted and run a
+ *   slower element-wise load path.
+ * - Host-checkable errors (NULL where a buffer is required, sizes out of
+ *   range, temperature <= 0 or non-finite, top_p outside (0, 1], top_k < 0,
+ *   element-misaligned pointers, a workspace that is too small or not
+ *   256-byte aligned) return a non-zero spec_status_t and launch nothing.
+ *   A failed launch returns SPEC_ERR_CUDA.  Data errors are reported per
+ *   sequence through out_status / out_num_accepted (see SPEC_SEQ_*).  The
+ *   library never traps the GPU.
+ * - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,   /* a NULL, size or parameter the contract excludes  */
+    SPEC_ERR_UNSUPPORTED = 2,   /* a valid request this build does not handle       */
+    SPEC_ERR_MISALIGNED = 3,    /* a pointer not aligned to its element / 256 bytes  */
+    SPEC_ERR_WORKSPACE = 4,     /* workspace smaller than the *_workspace_size query */
+    SPEC_ERR_CUDA = 5           /* the CUDA runtime reported an error at launch      */
+} spec_status_t;
+
+/* Per-sequence status written to out_status[b] (low byte: error code; high
+ * bits: informational flags).  Any non-zero error code sets
+ * out_num_accepted[b] = -1 and out_tokens[b][*] = -1: commit nothing. */
+enum {
+    SPEC_SEQ_OK = 0,
+    SPEC_SEQ_BAD_LENGTH = 1,      /* gamma_per_seq[b] outside [0, gamma_max]          */
+    SPEC_SEQ_BAD_TOKEN = 2,       /* a draft token d_i (i < gamma_b) outside [0, V)   */
+    SPEC_SEQ_BAD_UNIFORM = 3,     /* a used uniform outside [0, 1) or NaN             */
+    SPEC_SEQ_NONFINITE = 4,       /* NaN or +inf logit in a row the sequence uses     */
+    SPEC_SEQ_EMPTY_SUPPORT = 5,   /* a used row whose logits are all -inf             */
+    SPEC_SEQ_ERROR_MASK = 0xFF,
+    SPEC_SEQ_FLAG_ZERO_Q = 0x100, /* an evaluated draft token had q(d) == 0           */
+    SPEC_SEQ_FLAG_Z_ZERO = 0x200  /* residual mass was 0 after a rejection            */
+};
+/* Checks run in this order and the first failure is reported: length, draft
+ * tokens, uniforms, then rows i = 0..gamma_b (target row i, then draft row i). */
+
+typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
+
+/* One side's production sampling rule [wrblog §2.3, §7.2-§7.3]:
+ * temperature > 0 (finite); top_k == 0 or top_k >= vocab disables top-k;
+ * top_p in (0, 1], 1 disables top-p. */
+typedef struct {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+} spec_sampling_params_t;
+
+/* Bytes of workspace spec_verify_sample needs for this shape and these
+ * parameters.  Returns SPEC_ERR_INVALID_ARG for sizes or parameters that
+ * spec_verify_sample would reject.  The workspace must be zero-filled before
+ * its first use; every call that returns SPEC_OK leaves its counter region
+ * zero again, so a workspace is reusable without clearing. */
+SPEC_API spec_status_t spec_verify_workspace_size(int32_t batch, int32_t gamma_max, int32_t vocab,
+                                         spec_sampling_params_t target_params,
+                                         spec_sampling_params_t draft_params,
+                                         size_t* bytes);
+
+/* Sampling-mode verification of `batch` sequences in one launch.
+ *
+ * target_logits   [batch][gamma_max+1][vocab] of dtype.
+ * draft_logits    [batch][gamma_max][vocab] of dtype, or NULL when every
+ *                 sequence's draft is one-hot.
+ * draft_tokens    [batch][gamma_max] int32, d_1..d_gamma_b per sequence
+ *                 (may be NULL only when gamma_max == 0).
+ * gamma_per_seq   [batch] int32 draft count per sequence, or NULL for
+ *                 gamma_max everywhere (ragged batches pad to gamma_max).
+ * draft_is_onehot [batch] uint8, non-zero = the draft proposed its tokens
+ *                 with certainty (q is a delta at d_i, so a_i = p_i(d_i));
+ *                 NULL = no one-hot sequence (ignored when draft_logits is
+ *                 NULL).  One-hot sequences never read draft_logits.
+ * u_accept        [batch][gamma_max] float, the uniform compared with a_i
+ *                 (may be NULL only when gamma_max == 0).
+ * u_sample        [batch] float, the uniform the residual or bonus draw uses.
+ * out_tokens      [batch][gamma_max+1] int32: the accepted drafts, then the
+ *                 replacement or bonus token, then -1.
+ * out_num_accepted[batch] int32: accepted draft count A (0..gamma_b); the
+ *                 sequence emits A+1 tokens; -1 = error, commit nothing.
+ * out_accept_prob [batch][gamma_max] float a_i for i < gamma_b, -1 beyond;
+ *                 or NULL.
+ * out_residual_z  [batch] float, Z = sum (p_j - q_j)+ at the rejected
+ *                 position, -1 when nothing was rejected; or NULL.
+ * out_status      [batch] int32 SPEC_SEQ_* code, or NULL.
+ * workspace       device buffer of at least spec_verify_workspace_size()
+ *                 bytes, 256-byte aligned, zero-filled before first use. */
+SPEC_API spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
+                                 spec_dtype_t dtype, const int32_t* draft_tokens,
+                                 const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                 const float* u_accept, const float* u_sample,
+                                 spec_sampling_params_t target_params,
+                                 spec_sampling_params_t draft_params,
+                                 int32_t batch, int32_t gamma_max, int32_t vocab,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* out_tokens, int32_t* out_num_accepted,
+                                 float* out_accept_prob, float* out_residual_z,
+                                 int32_t* out_status, void* stream);
+
+/* Bytes of workspace spec_verify_greedy needs (same zero-fill rule). */
+SPEC_API spec_status_t spec_greedy_workspace_size(int32_t batch, int32_t gamma_max, size_t* bytes);
+
+/* Greedy verification [wrblog §7.1; baisen §6]: g_i = argmax_x z_i(x)
+ * (lowest index on ties) for i = 1..gamma_b+1; the sequence accepts
+ * d_1..d_{j-1} where j is the first i with d_i != g_i and emits g_j, or
+ * accepts every draft and emits g_{gamma_b+1}.  No sampling parameters and
+ * no uniforms: argmax is unchanged by temperature, top-k and top-p.
+ * Arguments as for spec_verify_sample. */
+SPEC_API spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
+                                 const int32_t* draft_tokens, const int32_t* gamma_per_seq,
+                                 int32_t batch, int32_t gamma_max, int32_t vocab,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* out_tokens, int32_t* out_num_accepted,
+                                 int32_t* out_status, void* stream);
+
+/* The transform step alone [wrblog §7.2, §7.3]: writes the full probability
+ * rows p = top_p(top_k(softmax(z / T))) the verifier samples from.
+ * logits [rows][vocab] of dtype; out_probs [rows][vocab] float;
+ * out_row_status [rows] int32 (SPEC_SEQ_OK, SPEC_SEQ_NONFINITE or
+ * SPEC_SEQ_EMPTY_SUPPORT; a failed row is written as zeros), or NULL.
+ * Needs no workspace. */
+SPEC_API spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32_t rows,
+                                   int32_t vocab, spec_sampling_params_t params,
+                                   float* out_probs, int32_t* out_row_status, void* stream);
+
+/* Static, NUL-terminated description of a spec_status_t. */
+SPEC_API const char* spec_status_string(spec_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

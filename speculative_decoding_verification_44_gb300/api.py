@@ -1,0 +1,145 @@
+"""Torch-tensor front end of the C ABI (argument marshalling only).
+
+PyTorch here owns device memory and streams; every step of the verify path
+runs in libspecverify.so.  Tensors must be CUDA tensors on the current
+device, contiguous, with the layouts include/spec_verify.h documents.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+
+@dataclass(frozen=True)
+class SamplingParams:
+    """One side's sampling rule: temperature > 0, top_k (0 = off), top_p in (0, 1] (1 = off)."""
+    temperature: float = 1.0
+    top_k: int = 0
+    top_p: float = 1.0
+
+    def c(self) -> _lib.spec_sampling_params_t:
+        return _lib.spec_sampling_params_t(float(self.temperature), int(self.top_k), float(self.top_p))
+
+
+@dataclass
+class VerifyOutput:
+    tokens: torch.Tensor          # [B, gamma_max+1] int32; accepted drafts, new token, then -1
+    num_accepted: torch.Tensor    # [B] int32; -1 = error, commit nothing
+    status: torch.Tensor          # [B] int32 SPEC_SEQ_* codes
+    accept_prob: torch.Tensor | None = None   # [B, gamma_max] float32
+    residual_z: torch.Tensor | None = None    # [B] float32
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.SPEC_BF16
+    if t.dtype == torch.float32:
+        return _lib.SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("all tensors passed to the verifier must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the verifier must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream: torch.cuda.Stream | None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def workspace_size(batch: int, gamma_max: int, vocab: int, target: SamplingParams,
+                   draft: SamplingParams) -> int:
+    return _lib.spec_verify_workspace_size(batch, gamma_max, vocab, target.c(), draft.c())
+
+
+def greedy_workspace_size(batch: int, gamma_max: int) -> int:
+    return _lib.spec_greedy_workspace_size(batch, gamma_max)
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (the library needs zeros before first use and restores them)."""
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def alloc_outputs(batch: int, gamma_max: int, device, accept_prob: bool = True,
+                  residual_z: bool = True) -> VerifyOutput:
+    return VerifyOutput(
+        tokens=torch.empty(batch, gamma_max + 1, dtype=torch.int32, device=device),
+        num_accepted=torch.empty(batch, dtype=torch.int32, device=device),
+        status=torch.empty(batch, dtype=torch.int32, device=device),
+        accept_prob=torch.empty(batch, gamma_max, dtype=torch.float32, device=device) if accept_prob else None,
+        residual_z=torch.empty(batch, dtype=torch.float32, device=device) if residual_z else None)
+
+
+def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None,
+                  draft_tokens: torch.Tensor, u_accept: torch.Tensor, u_sample: torch.Tensor,
+                  target: SamplingParams, draft: SamplingParams,
+                  gamma_per_seq: torch.Tensor | None = None,
+                  draft_is_onehot: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, out: VerifyOutput | None = None,
+                  stream: torch.cuda.Stream | None = None) -> VerifyOutput:
+    """spec_verify_sample on torch tensors.
+
+    target_logits [B, G+1, V] and draft_logits [B, G, V] (or None: all one-hot) of
+    bfloat16 / float32; draft_tokens [B, G] int32; u_accept [B, G] and u_sample [B]
+    float32; gamma_per_seq [B] int32; draft_is_onehot [B] uint8.
+    """
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    dev = target_logits.device
+    if workspace is None:
+        workspace = new_workspace(workspace_size(B, G, V, target, draft), dev)
+    if out is None:
+        out = alloc_outputs(B, G, dev)
+    st = _lib.spec_verify_sample(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
+        _ptr(gamma_per_seq), _ptr(draft_is_onehot), _ptr(u_accept), _ptr(u_sample),
+        target.c(), draft.c(), B, G, V, _ptr(workspace), workspace.numel(),
+        _ptr(out.tokens), _ptr(out.num_accepted), _ptr(out.accept_prob), _ptr(out.residual_z),
+        _ptr(out.status), _stream(stream))
+    _lib.check("spec_verify_sample", st)
+    return out
+
+
+def verify_greedy(target_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                  gamma_per_seq: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, out: VerifyOutput | None = None,
+                  stream: torch.cuda.Stream | None = None) -> VerifyOutput:
+    """spec_verify_greedy on torch tensors (target_logits [B, G+1, V])."""
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    if workspace is None:
+        workspace = new_workspace(greedy_workspace_size(B, G), dev)
+    if out is None:
+        out = alloc_outputs(B, G, dev, accept_prob=False, residual_z=False)
+    st = _lib.spec_verify_greedy(
+        _ptr(target_logits), _dtype_code(target_logits), _ptr(draft_tokens), _ptr(gamma_per_seq),
+        B, G, V, _ptr(workspace), workspace.numel(), _ptr(out.tokens), _ptr(out.num_accepted),
+        _ptr(out.status), _stream(stream))
+    _lib.check("spec_verify_greedy", st)
+    return out
+
+
+def transform_probs(logits: torch.Tensor, params: SamplingParams,
+                    stream: torch.cuda.Stream | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """spec_transform_probs: full probability rows of a [rows, V] logits tensor."""
+    rows, V = logits.reshape(-1, logits.shape[-1]).shape
+    flat = logits.reshape(rows, V)
+    probs = torch.empty(rows, V, dtype=torch.float32, device=logits.device)
+    status = torch.empty(rows, dtype=torch.int32, device=logits.device)
+    st = _lib.spec_transform_probs(_ptr(flat), _dtype_code(flat), rows, V, params.c(), _ptr(probs),
+                                   _ptr(status), _stream(stream))
+    _lib.check("spec_transform_probs", st)
+    return probs.reshape(*logits.shape[:-1], V), status.reshape(logits.shape[:-1])

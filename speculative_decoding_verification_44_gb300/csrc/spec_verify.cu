@@ -1,0 +1,877 @@
+// spec_verify.cu -- kernels and C ABI of the speculative-decoding verifier
+// for GB300 (sm_103a).  Declarations and the contract: include/spec_verify.h.
+//
+// Launch structure (one launch per call, no host synchronisation):
+//   grid = one CTA per (sequence, row slot); slot 0..gamma_max are the target
+//   rows, gamma_max+1..2*gamma_max the draft rows.  A CTA whose row the
+//   sequence does not use exits at once.  Each used row is analysed by its
+//   CTA (sv_row.cuh) and its summary published to the workspace; the CTA that
+//   finishes last for a sequence (atomic counter, no waiting) runs the
+//   sequence epilogue: the left-to-right acceptance scan, the residual or
+//   bonus draw, and the output writes [wrblog §6; rainlin §1].
+//
+// Sources: [wrblog] "推测解码：草稿模型、接受率、正确性与加速边界" (wrblog.cn);
+//          [rainlin] "投机解码" (rainlin-net.pages.dev).
+#include "sv_row.cuh"
+#include "spec_verify.h"
+
+#include <cmath>
+#include <cstdint>
+
+namespace sv {
+
+struct SampleArgs {
+  const char* tgt;
+  const char* dft;
+  const int32_t* tokens;
+  const int32_t* gammas;
+  const uint8_t* onehot;
+  const float* u_acc;
+  const float* u_samp;
+  RowParams tp, dp;
+  int B, G, V;
+  int aligned;
+  size_t row_bytes;
+  uint32_t* counters;
+  RowStat* stats;
+  ListEntry* lists;
+  int32_t* out_tokens;
+  int32_t* out_nacc;
+  float* out_aprob;
+  float* out_Z;
+  int32_t* out_status;
+};
+
+__device__ __forceinline__ RowStat load_stat(const RowStat* p) {
+  RowStat s;
+  const uint4* src = reinterpret_cast<const uint4*>(p);
+  uint4* d = reinterpret_cast<uint4*>(&s);
+  d[0] = __ldcg(src);
+  d[1] = __ldcg(src + 1);
+  d[2] = __ldcg(src + 2);
+  return s;
+}
+__device__ __forceinline__ ListEntry load_entry(const ListEntry* p) {
+  ListEntry e;
+  *reinterpret_cast<uint4*>(&e) = __ldcg(reinterpret_cast<const uint4*>(p));
+  return e;
+}
+
+// Commit nothing [wrblog §15]: all threads of the CTA take part.
+__device__ void write_error(const SampleArgs& a, int b, int status) {
+  for (int t = threadIdx.x; t <= a.G; t += blockDim.x) a.out_tokens[static_cast<size_t>(b) * (a.G + 1) + t] = -1;
+  if (a.out_aprob)
+    for (int t = threadIdx.x; t < a.G; t += blockDim.x) a.out_aprob[static_cast<size_t>(b) * a.G + t] = -1.0f;
+  if (threadIdx.x == 0) {
+    a.out_nacc[b] = -1;
+    if (a.out_Z) a.out_Z[b] = -1.0f;
+    if (a.out_status) a.out_status[b] = status;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ Row seq_row(const SampleArgs& a, int b, int i, bool draft) {
+  const char* base = draft ? a.dft + (static_cast<size_t>(b) * a.G + i) * a.row_bytes
+                           : a.tgt + (static_cast<size_t>(b) * (a.G + 1) + i) * a.row_bytes;
+  return make_row<DT>(base, a.V, a.aligned != 0);
+}
+
+// Probability q(x) of a PATH_STREAM draft row: lookup in its token-sorted list.
+__device__ __forceinline__ float list_lookup(const int32_t* tok, const double* p, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    const int t = tok[mid];
+    if (t == x) return static_cast<float>(p[mid]);
+    if (t < x) lo = mid + 1; else hi = mid - 1;
+  }
+  return 0.0f;
+}
+
+// Inverse-CDF draw over a PATH_STREAM target row's kept list (warp 0 only).
+// Residual weights max(0, p - q) [wrblog §5], or p itself for the bonus draw;
+// the token is the smallest x (vocabulary order) with C(x) > u Z.
+template <int DT>
+__device__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
+                         const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
+  const int lane = threadIdx.x & 31;
+  const int slots = 2 * a.G + 1;
+  const RowStat ts = load_stat(a.stats + static_cast<size_t>(b) * slots + r);
+  const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
+  const int nt = ts.n_list;
+  SmemEpi& E = sm.u.e;
+  // draft list (PATH_STREAM draft), token-sorted for lookups
+  int nq = 0;
+  const bool draft_list = residual && !onehot && ds.path == PATH_STREAM;
+  if (draft_list) {
+    const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
+    nq = ds.n_list;
+    for (int e = lane; e < nq; e += 32) {
+      const ListEntry q = load_entry(ql + e);
+      E.tok[e] = q.token;
+      E.w[e] = q.p;
+    }
+    __syncwarp();
+    for (int e = lane; e < nq; e += 32) {
+      int rank = 0;
+      for (int j = 0; j < nq; ++j) rank += E.tok[j] < E.tok[e] ? 1 : 0;
+      E.qtok[rank] = E.tok[e];
+      E.qp[rank] = E.w[e];
+    }
+    __syncwarp();
+  }
+  const Row drow = seq_row<DT>(a, b, r, true);
+  const float invWd = (residual && !onehot && ds.path == PATH_FULL) ? static_cast<float>(1.0 / ds.W) : 0.0f;
+  // target entries with their residual / bonus weights
+  for (int e = lane; e < nt; e += 32) {
+    const ListEntry t = load_entry(tl + e);
+    double w = t.p;
+    if (residual) {
+      double q;
+      if (onehot) q = (t.token == dj) ? 1.0 : 0.0;
+      else if (ds.path == PATH_STREAM) q = list_lookup(E.qtok, E.qp, nq, t.token);
+      else q = full_prob(load_elem<DT>(drow.base, t.token), static_cast<uint32_t>(t.token), ds, a.dp.cT, invWd);
+      w = fmax(t.p - q, 0.0);
+    }
+    E.tok[kListCap + e] = t.token;
+    E.w[kListCap + e] = w;
+    E.sw[e] = t.p;   // keep p for a Z == 0 fallback
+  }
+  __syncwarp();
+  // sort by token (tokens of one list are distinct)
+  for (int e = lane; e < nt; e += 32) {
+    int rank = 0;
+    const int te = E.tok[kListCap + e];
+    for (int j = 0; j < nt; ++j) rank += E.tok[kListCap + j] < te ? 1 : 0;
+    E.stok[rank] = te;
+    E.tok[rank] = e;   // original position, to fetch p for the fallback
+  }
+  __syncwarp();
+  for (int pass = 0; pass < 2; ++pass) {
+    double w[4];
+    double s = 0.0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int pos = 4 * lane + j;
+      w[j] = 0.0;
+      if (pos < nt) {
+        const int orig = E.tok[pos];
+        w[j] = pass == 0 ? E.w[kListCap + orig] : E.sw[orig];
+      }
+      s += w[j];
+    }
+    const double incl = warp_incl_scan_f64(s, lane);
+    const double Z = __shfl_sync(kFull, incl, 31);
+    if (pass == 0 && residual) Z_resid = Z;
+    if (!(Z > 0.0)) {
+      if (pass == 0 && residual) { flags |= SEQ_FLAG_Z_ZERO; continue; }
+    }
+    const double t = u * Z;
+    double acc = incl - s;
+    int found = 0x7fffffff, last = -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int pos = 4 * lane + j;
+      if (pos < nt && w[j] > 0.0) {
+        acc += w[j];
+        last = pos;
+        if (found == 0x7fffffff && acc > t) found = pos;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      found = min(found, __shfl_xor_sync(kFull, found, o));
+      last = max(last, __shfl_xor_sync(kFull, last, o));
+    }
+    const int pos = found != 0x7fffffff ? found : last;
+    return pos >= 0 ? E.stok[pos] : -1;
+  }
+  return -1;
+}
+
+// Per-element weight for the block scan over a PATH_FULL target row.
+// mode 0: p; 1: (p - q)+ with q a PATH_FULL draft row; 2: (p - q)+ with q a
+// token-sorted list; 3: (p - delta_dj)+.
+struct ScanCtx {
+  Row trow, drow;
+  RowStat ts, ds;
+  float cTt, cTd, invWt, invWd;
+  int mode;
+  int dj;
+  int nq;
+};
+
+template <int DT>
+__device__ __forceinline__ float scan_vec(const ScanCtx& c, int v, const Smem& sm, float (&w)[Elem<DT>::kPer]) {
+  constexpr int P = Elem<DT>::kPer;
+  uint4 rt, rd;
+  const int n = load_vec<DT, false>(c.trow, v, rt);
+  float zt[P], zd[P];
+  unpack<DT>(rt, zt);
+  if (c.mode == 1) {
+    load_vec<DT, false>(c.drow, v, rd);
+    unpack<DT>(rd, zd);
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int e = 0; e < P; ++e) {
+    float we = 0.0f;
+    if (e < n) {
+      const uint32_t x = static_cast<uint32_t>(v * P + e);
+      const float p = full_prob(zt[e], x, c.ts, c.cTt, c.invWt);
+      float q = 0.0f;
+      if (c.mode == 1) q = full_prob(zd[e], x, c.ds, c.cTd, c.invWd);
+      else if (c.mode == 2) q = list_lookup(sm.u.e.qtok, sm.u.e.qp, c.nq, static_cast<int>(x));
+      else if (c.mode == 3) q = (static_cast<int>(x) == c.dj) ? 1.0f : 0.0f;
+      we = c.mode == 0 ? p : fmaxf(p - q, 0.0f);
+    }
+    w[e] = we;
+    s += we;
+  }
+  return s;
+}
+
+// Block-wide inverse-CDF draw over a full row in vocabulary order.  Each warp
+// owns a contiguous range of vectors; pass A sums the weights per warp, the
+// owning warp then re-scans its range with identical arithmetic to locate the
+// first x with C(x) > u Z.
+template <int DT>
+__device__ int block_scan_draw(ScanCtx& c, double u, bool residual, double& Z_resid, int& flags, Smem& sm) {
+  constexpr int P = Elem<DT>::kPer;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nv = c.trow.nvec;
+  const int L = (nv + kWarps - 1) / kWarps;
+  const int v0 = warp * L, v1 = min(nv, v0 + L);
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    double acc = 0.0;
+    for (int s = v0; s < v1; s += 32) {
+      const int v = s + lane;
+      float w[P];
+      const float ls = v < v1 ? scan_vec<DT>(c, v, sm, w) : 0.0f;
+      const double incl = warp_incl_scan_f64(static_cast<double>(ls), lane);
+      acc += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) sm.u.e.wtot[warp] = acc;
+    __syncthreads();
+    if (tid == 0) {
+      double Z = 0.0;
+      for (int w = 0; w < kWarps; ++w) Z += sm.u.e.wtot[w];
+      sm.b_f64[0] = Z;
+      const double t = u * Z;
+      double start = 0.0;
+      int W = -1;
+      double tl = 0.0;
+      int lastW = -1;
+      double last_start = 0.0;
+      for (int w = 0; w < kWarps; ++w) {
+        if (sm.u.e.wtot[w] > 0.0) { lastW = w; last_start = start; }
+        if (W < 0 && sm.u.e.wtot[w] > 0.0 && start + sm.u.e.wtot[w] > t) { W = w; tl = t - start; }
+        start += sm.u.e.wtot[w];
+      }
+      if (W < 0) { W = lastW; tl = t - last_start; }
+      sm.b_i32[4] = W;
+      sm.b_f64[1] = tl;
+      sm.b_i32[6] = -1;
+    }
+    __syncthreads();
+    const double Z = sm.b_f64[0];
+    if (attempt == 0 && residual) Z_resid = Z;
+    if (!(Z > 0.0)) {
+      __syncthreads();
+      if (attempt == 0 && residual) {     // Z == 0 after a rejection: draw from p instead
+        flags |= SEQ_FLAG_Z_ZERO;
+        c.mode = 0;
+        continue;
+      }
+      return -1;
+    }
+    if (warp == sm.b_i32[4]) {
+      const double tl = sm.b_f64[1];
+      double running = 0.0;
+      int last_tok = -1;
+      for (int s = v0; s < v1; s += 32) {
+        const int v = s + lane;
+        float w[P];
+        const float ls = v < v1 ? scan_vec<DT>(c, v, sm, w) : 0.0f;
+        const double incl = warp_incl_scan_f64(static_cast<double>(ls), lane);
+        const double excl_prev = __shfl_up_sync(kFull, incl, 1);
+        const unsigned bal = __ballot_sync(kFull, ls > 0.0f && running + incl > tl);
+        // remember the last positive element seen so far (fallback)
+        int lp = -1;
+#pragma unroll
+        for (int e = 0; e < P; ++e) if (w[e] > 0.0f) lp = v * P + e;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(kFull, lp, o));
+        if (bal) {
+          const int Lw = __ffs(bal) - 1;
+          if (lane == Lw) {
+            const double base = running + (lane > 0 ? excl_prev : 0.0);
+            float c32 = 0.0f;
+            int tok = -1, lastpos = -1;
+#pragma unroll
+            for (int e = 0; e < P; ++e) {
+              if (w[e] > 0.0f) {
+                c32 += w[e];
+                lastpos = v * P + e;
+                if (tok < 0 && base + static_cast<double>(c32) > tl) tok = v * P + e;
+              }
+            }
+            sm.b_i32[6] = tok >= 0 ? tok : lastpos;
+          }
+          break;
+        }
+        if (lp >= 0) last_tok = lp;
+        running += __shfl_sync(kFull, incl, 31);
+      }
+      __syncwarp();
+      if (lane == 0 && sm.b_i32[6] < 0) sm.b_i32[6] = last_tok;
+    }
+    __syncthreads();
+    return sm.b_i32[6];
+  }
+  return -1;
+}
+
+// Sequence epilogue, run by the CTA that analysed the sequence's last row.
+template <int DT>
+__device__ void sample_epilogue(const SampleArgs& a, int b, int gb, bool onehot, Smem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slots = 2 * a.G + 1;
+  const RowStat* S = a.stats + static_cast<size_t>(b) * slots;
+  const size_t tokb = static_cast<size_t>(b) * a.G;
+
+  // 1. status, in the documented order: tokens, uniforms, rows
+  if (tid == 0) {
+    int status = SEQ_OK;
+    for (int i = 0; i < gb && status == SEQ_OK; ++i) {
+      const int t = a.tokens[tokb + i];
+      if (t < 0 || t >= a.V) status = SEQ_BAD_TOKEN;
+    }
+    if (status == SEQ_OK) {
+      for (int i = 0; i < gb; ++i) {
+        const float u = a.u_acc[tokb + i];
+        if (!(u >= 0.0f && u < 1.0f)) status = SEQ_BAD_UNIFORM;
+      }
+      const float us = a.u_samp[b];
+      if (!(us >= 0.0f && us < 1.0f)) status = SEQ_BAD_UNIFORM;
+    }
+    for (int i = 0; i <= gb && status == SEQ_OK; ++i) {
+      status = load_stat(S + i).status;
+      if (status == SEQ_OK && i < gb && !onehot) status = load_stat(S + a.G + 1 + i).status;
+    }
+    sm.b_i32[0] = status;
+  }
+  __syncthreads();
+  if (sm.b_i32[0] != SEQ_OK) {
+    write_error(a, b, sm.b_i32[0]);
+    return;
+  }
+
+  // 2. a_i = min(1, p_i(d_i) / q_i(d_i)); accept iff u_i < a_i; stop at the first rejection
+  if (warp == 0) {
+    int j = gb, flags = 0;
+    for (int base = 0; base < a.G; base += 32) {
+      const int i = base + lane;
+      bool rej = false, zq = false;
+      if (i < gb) {
+        const double p = load_stat(S + i).p_tok;
+        const double q = onehot ? 1.0 : load_stat(S + a.G + 1 + i).p_tok;
+        double ai;
+        if (q > 0.0) ai = fmin(1.0, p / q);
+        else { ai = p > 0.0 ? 1.0 : 0.0; zq = true; }
+        rej = !(static_cast<double>(a.u_acc[tokb + i]) < ai);
+        if (a.out_aprob) a.out_aprob[tokb + i] = static_cast<float>(ai);
+      } else if (i < a.G && a.out_aprob) {
+        a.out_aprob[tokb + i] = -1.0f;
+      }
+      if (j == gb) {
+        const unsigned rm = __ballot_sync(kFull, rej);
+        const unsigned zm = __ballot_sync(kFull, zq);
+        if (rm) {
+          const int f = __ffs(rm) - 1;
+          j = base + f;
+          const unsigned upto = (f == 31) ? kFull : ((2u << f) - 1u);
+          if (zm & upto) flags |= SEQ_FLAG_ZERO_Q;
+        } else if (zm) {
+          flags |= SEQ_FLAG_ZERO_Q;
+        }
+      }
+    }
+    if (lane == 0) {
+      sm.b_i32[1] = j;
+      sm.b_i32[2] = flags;
+    }
+  }
+  __syncthreads();
+  const int j = sm.b_i32[1];
+  int flags = sm.b_i32[2];
+  __syncthreads();
+
+  // 3. residual draw at the rejected position, or the bonus draw [wrblog §5, §6]
+  const bool residual = j < gb;
+  const int r = j;   // == gb when every draft was accepted
+  const RowStat ts = load_stat(S + r);
+  RowStat ds;
+  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0;
+  if (residual && !onehot) ds = load_stat(S + a.G + 1 + r);
+  const int dj = residual ? a.tokens[tokb + j] : -1;
+  const double u = static_cast<double>(a.u_samp[b]);
+  double Z_resid = -1.0;
+  int tok = -1;
+  if (ts.path == PATH_STREAM) {
+    if (warp == 0) {
+      tok = list_draw<DT>(a, b, r, residual, onehot, dj, ds, u, Z_resid, flags, sm);
+      if (lane == 0) {
+        sm.b_i32[3] = tok;
+        sm.b_i32[5] = flags;
+        sm.b_f64[2] = Z_resid;
+      }
+    }
+    __syncthreads();
+    tok = sm.b_i32[3];
+    flags = sm.b_i32[5];
+    Z_resid = sm.b_f64[2];
+  } else {
+    ScanCtx c;
+    c.trow = seq_row<DT>(a, b, r, false);
+    c.drow = (residual && !onehot) ? seq_row<DT>(a, b, r, true) : c.trow;
+    c.ts = ts;
+    c.ds = ds;
+    c.cTt = a.tp.cT;
+    c.cTd = a.dp.cT;
+    c.invWt = static_cast<float>(1.0 / ts.W);
+    c.invWd = static_cast<float>(1.0 / ds.W);
+    c.dj = dj;
+    c.nq = 0;
+    c.mode = !residual ? 0 : (onehot ? 3 : (ds.path == PATH_FULL ? 1 : 2));
+    if (c.mode == 2) {   // token-sorted draft list in shared memory
+      const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
+      c.nq = ds.n_list;
+      if (tid < c.nq) {
+        const ListEntry q = load_entry(ql + tid);
+        sm.u.e.tok[tid] = q.token;
+        sm.u.e.w[tid] = q.p;
+      }
+      __syncthreads();
+      if (tid < c.nq) {
+        int rank = 0;
+        for (int jj = 0; jj < c.nq; ++jj) rank += sm.u.e.tok[jj] < sm.u.e.tok[tid] ? 1 : 0;
+        sm.u.e.qtok[rank] = sm.u.e.tok[tid];
+        sm.u.e.qp[rank] = sm.u.e.w[tid];
+      }
+      __syncthreads();
+    }
+    tok = block_scan_draw<DT>(c, u, residual, Z_resid, flags, sm);
+  }
+
+  // 4. outputs: accepted drafts, the drawn token, then -1
+  const size_t ob = static_cast<size_t>(b) * (a.G + 1);
+  for (int t = tid; t <= a.G; t += kThreads) {
+    int v = -1;
+    if (t < j) v = a.tokens[tokb + t];
+    else if (t == j) v = tok;
+    a.out_tokens[ob + t] = v;
+  }
+  if (tid == 0) {
+    a.out_nacc[b] = j;
+    if (a.out_Z) a.out_Z[b] = residual ? static_cast<float>(Z_resid) : -1.0f;
+    if (a.out_status) a.out_status[b] = flags;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int slots = 2 * a.G + 1;
+  const int b = blockIdx.x / slots;
+  const int slot = blockIdx.x - b * slots;
+  const int gb = a.gammas ? a.gammas[b] : a.G;
+  const bool onehot = a.dft == nullptr || (a.onehot != nullptr && a.onehot[b] != 0);
+  if (gb < 0 || gb > a.G) {
+    if (slot == 0) write_error(a, b, SEQ_BAD_LENGTH);
+    return;
+  }
+  const bool is_draft = slot > a.G;
+  const int i = is_draft ? slot - a.G - 1 : slot;
+  if (!is_draft && i > gb) return;
+  if (is_draft && (onehot || i >= gb)) return;
+
+  const RowParams& P = is_draft ? a.dp : a.tp;
+  const Row row = seq_row<DT>(a, b, i, is_draft);
+  int dtok = -1;
+  if (i < gb) {
+    const int t = a.tokens[static_cast<size_t>(b) * a.G + i];
+    dtok = (t >= 0 && t < a.V) ? t : -1;
+  }
+  if (P.path == PATH_STREAM) stream_row<DT>(row, P, dtok, sm);
+  else full_row<DT>(row, P, dtok, sm);
+
+  // publish the row summary, then count this row in
+  if (threadIdx.x == 0) a.stats[static_cast<size_t>(b) * slots + slot] = sm.st;
+  if (P.path == PATH_STREAM) {
+    ListEntry* dst = a.lists + (static_cast<size_t>(b) * slots + slot) * kListCap;
+    for (int e = threadIdx.x; e < sm.st.n_list; e += kThreads) {
+      ListEntry le;
+      le.p = sm.list_p[e];
+      le.token = sm.list_tok[e];
+      le.pad = 0;
+      dst[e] = le;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned rows_b = static_cast<unsigned>((gb + 1) + (onehot ? 0 : gb));
+    const unsigned prev = atomicAdd(&a.counters[b], 1u);
+    sm.b_i32[7] = (prev + 1u == rows_b) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sm.b_i32[7]) return;
+  __threadfence();
+  sample_epilogue<DT>(a, b, gb, onehot, sm);
+  __syncthreads();
+  if (threadIdx.x == 0) a.counters[b] = 0u;   // leave the workspace reusable
+}
+
+// ------------------------------------------------------------------ greedy
+struct GreedyArgs {
+  const char* tgt;
+  const int32_t* tokens;
+  const int32_t* gammas;
+  int B, G, V;
+  int aligned;
+  size_t row_bytes;
+  uint32_t* counters;
+  int2* rows;   // [B][G+1] (argmax, status)
+  int32_t* out_tokens;
+  int32_t* out_nacc;
+  int32_t* out_status;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int slots = a.G + 1;
+  const int b = blockIdx.x / slots;
+  const int i = blockIdx.x - b * slots;
+  const int gb = a.gammas ? a.gammas[b] : a.G;
+  const size_t ob = static_cast<size_t>(b) * (a.G + 1);
+  if (gb < 0 || gb > a.G) {
+    if (i == 0) {
+      for (int t = threadIdx.x; t <= a.G; t += kThreads) a.out_tokens[ob + t] = -1;
+      if (threadIdx.x == 0) {
+        a.out_nacc[b] = -1;
+        if (a.out_status) a.out_status[b] = SEQ_BAD_LENGTH;
+      }
+    }
+    return;
+  }
+  if (i > gb) return;
+  const Row row = make_row<DT>(a.tgt + (static_cast<size_t>(b) * slots + i) * a.row_bytes, a.V, a.aligned != 0);
+  int g, st;
+  greedy_row<DT>(row, sm, g, st);
+  if (threadIdx.x == 0) a.rows[static_cast<size_t>(b) * slots + i] = make_int2(g, st);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&a.counters[b], 1u);
+    sm.b_i32[7] = (prev + 1u == static_cast<unsigned>(gb + 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sm.b_i32[7]) return;
+  __threadfence();
+  if (threadIdx.x == 0) {
+    // [wrblog §7.1]: accept while d_i == argmax p_i; emit argmax at the first mismatch
+    int status = SEQ_OK;
+    for (int k = 0; k < gb && status == SEQ_OK; ++k) {
+      const int t = a.tokens[static_cast<size_t>(b) * a.G + k];
+      if (t < 0 || t >= a.V) status = SEQ_BAD_TOKEN;
+    }
+    const int2* R = a.rows + static_cast<size_t>(b) * slots;
+    for (int k = 0; k <= gb && status == SEQ_OK; ++k) status = __ldcg(&R[k].y);
+    if (status != SEQ_OK) {
+      for (int t = 0; t <= a.G; ++t) a.out_tokens[ob + t] = -1;
+      a.out_nacc[b] = -1;
+    } else {
+      int j = gb;
+      for (int k = 0; k < gb; ++k) {
+        if (a.tokens[static_cast<size_t>(b) * a.G + k] != __ldcg(&R[k].x)) { j = k; break; }
+      }
+      for (int t = 0; t <= a.G; ++t) {
+        int v = -1;
+        if (t < j) v = a.tokens[static_cast<size_t>(b) * a.G + t];
+        else if (t == j) v = __ldcg(&R[j].x);
+        a.out_tokens[ob + t] = v;
+      }
+      a.out_nacc[b] = j;
+    }
+    if (a.out_status) a.out_status[b] = status;
+    a.counters[b] = 0u;
+  }
+}
+
+// ------------------------------------------------------------------ transform (test hook)
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) transform_kernel(const char* logits, int V, RowParams P,
+                                                                 int aligned, size_t row_bytes,
+                                                                 float* out, int32_t* out_status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int r = blockIdx.x;
+  const Row row = make_row<DT>(logits + static_cast<size_t>(r) * row_bytes, V, aligned != 0);
+  if (P.path == PATH_STREAM) stream_row<DT>(row, P, -1, sm);
+  else full_row<DT>(row, P, -1, sm);
+  const RowStat st = sm.st;
+  float* o = out + static_cast<size_t>(r) * V;
+  if (st.status != SEQ_OK || st.path == PATH_STREAM) {
+    for (int x = threadIdx.x; x < V; x += kThreads) o[x] = 0.0f;
+    __syncthreads();
+    if (st.status == SEQ_OK)
+      for (int e = threadIdx.x; e < st.n_list; e += kThreads) o[sm.list_tok[e]] = static_cast<float>(sm.list_p[e]);
+  } else {
+    const float invW = static_cast<float>(1.0 / st.W);
+    for (int x = threadIdx.x; x < V; x += kThreads)
+      o[x] = full_prob(load_elem<DT>(row.base, x), static_cast<uint32_t>(x), st, P.cT, invW);
+  }
+  if (out_status && threadIdx.x == 0) out_status[r] = st.status;
+}
+
+}  // namespace sv
+
+// ====================================================================== host
+namespace {
+
+using namespace sv;
+
+constexpr size_t kAlign = 256;
+inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool params_ok(const spec_sampling_params_t& p) {
+  return std::isfinite(p.temperature) && p.temperature > 0.0f && p.top_k >= 0 &&
+         p.top_p > 0.0f && p.top_p <= 1.0f;
+}
+
+int bit_length(uint32_t v) {
+  int n = 0;
+  while (v) { ++n; v >>= 1; }
+  return n;
+}
+
+RowParams make_row_params(const spec_sampling_params_t& p, int V) {
+  RowParams r;
+  r.T = p.temperature;
+  r.cT = static_cast<float>(1.4426950408889634 / static_cast<double>(p.temperature));  // log2(e) / T
+  r.invT = 1.0 / static_cast<double>(p.temperature);
+  r.k = (p.top_k >= V) ? 0 : p.top_k;
+  r.top_p = p.top_p;
+  r.path = (r.k >= 1 && r.k <= kSmallK) ? PATH_STREAM : PATH_FULL;
+  int sh = 62 - bit_length(static_cast<uint32_t>(V));
+  r.fixed_shift = sh < 24 ? 24 : (sh > 40 ? 40 : sh);
+  return r;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elem_bytes(spec_dtype_t dt) { return dt == SPEC_BF16 ? 2 : 4; }
+int elems_per_vec(spec_dtype_t dt) { return dt == SPEC_BF16 ? 8 : 4; }
+
+struct SampleLayout {
+  size_t counters, stats, lists, total;
+};
+SampleLayout sample_layout(int B, int G, const RowParams& tp, const RowParams& dp) {
+  SampleLayout L;
+  const size_t slots = static_cast<size_t>(2 * G + 1);
+  L.counters = 0;
+  L.stats = round_up(static_cast<size_t>(B) * sizeof(uint32_t));
+  L.lists = L.stats + round_up(static_cast<size_t>(B) * slots * sizeof(RowStat));
+  const bool need_lists = tp.path == PATH_STREAM || dp.path == PATH_STREAM;
+  L.total = L.lists + (need_lists ? round_up(static_cast<size_t>(B) * slots * kListCap * sizeof(ListEntry)) : 0);
+  return L;
+}
+
+bool shape_ok(int B, int G, int V) {
+  if (B < 1 || G < 0 || V < 1) return false;
+  const long long slots = 2LL * G + 1;
+  return static_cast<long long>(B) * slots <= 0x7fffffffLL && G < (1 << 20);
+}
+
+template <typename K>
+cudaError_t prepare(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sizeof(Smem)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_status_string(spec_status_t s) {
+  switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported request";
+    case SPEC_ERR_MISALIGNED: return "misaligned pointer";
+    case SPEC_ERR_WORKSPACE: return "workspace too small";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+spec_status_t spec_verify_workspace_size(int32_t batch, int32_t gamma_max, int32_t vocab,
+                                         spec_sampling_params_t target_params,
+                                         spec_sampling_params_t draft_params, size_t* bytes) {
+  if (!bytes || !shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
+    return SPEC_ERR_INVALID_ARG;
+  *bytes = sample_layout(batch, gamma_max, make_row_params(target_params, vocab),
+                         make_row_params(draft_params, vocab)).total;
+  return SPEC_OK;
+}
+
+spec_status_t spec_greedy_workspace_size(int32_t batch, int32_t gamma_max, size_t* bytes) {
+  if (!bytes || !shape_ok(batch, gamma_max, 1)) return SPEC_ERR_INVALID_ARG;
+  *bytes = round_up(static_cast<size_t>(batch) * sizeof(uint32_t)) +
+           round_up(static_cast<size_t>(batch) * (gamma_max + 1) * sizeof(int2));
+  return SPEC_OK;
+}
+
+spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
+                                 spec_dtype_t dtype, const int32_t* draft_tokens,
+                                 const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                 const float* u_accept, const float* u_sample,
+                                 spec_sampling_params_t target_params,
+                                 spec_sampling_params_t draft_params,
+                                 int32_t batch, int32_t gamma_max, int32_t vocab,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* out_tokens, int32_t* out_num_accepted,
+                                 float* out_accept_prob, float* out_residual_z,
+                                 int32_t* out_status, void* stream) {
+  if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  if (!shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
+    return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !u_sample || !out_tokens || !out_num_accepted || !workspace) return SPEC_ERR_INVALID_ARG;
+  if (gamma_max > 0 && (!draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype);
+  if (!aligned_to(target_logits, es) || (draft_logits && !aligned_to(draft_logits, es)) ||
+      !aligned_to(draft_tokens, 4) || !aligned_to(gamma_per_seq, 4) || !aligned_to(u_accept, 4) ||
+      !aligned_to(u_sample, 4) || !aligned_to(out_tokens, 4) || !aligned_to(out_num_accepted, 4) ||
+      !aligned_to(out_accept_prob, 4) || !aligned_to(out_residual_z, 4) || !aligned_to(out_status, 4) ||
+      !aligned_to(workspace, kAlign))
+    return SPEC_ERR_MISALIGNED;
+  SampleArgs a;
+  a.tp = make_row_params(target_params, vocab);
+  a.dp = make_row_params(draft_params, vocab);
+  const SampleLayout L = sample_layout(batch, gamma_max, a.tp, a.dp);
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  a.tgt = static_cast<const char*>(target_logits);
+  a.dft = static_cast<const char*>(draft_logits);
+  a.tokens = draft_tokens;
+  a.gammas = gamma_per_seq;
+  a.onehot = draft_is_onehot;
+  a.u_acc = u_accept;
+  a.u_samp = u_sample;
+  a.B = batch;
+  a.G = gamma_max;
+  a.V = vocab;
+  a.aligned = (vocab % elems_per_vec(dtype) == 0) && aligned_to(target_logits, 16) &&
+              (!draft_logits || aligned_to(draft_logits, 16));
+  a.row_bytes = static_cast<size_t>(vocab) * es;
+  a.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  a.stats = reinterpret_cast<RowStat*>(ws + L.stats);
+  a.lists = reinterpret_cast<ListEntry*>(ws + L.lists);
+  a.out_tokens = out_tokens;
+  a.out_nacc = out_num_accepted;
+  a.out_aprob = out_accept_prob;
+  a.out_Z = out_residual_z;
+  a.out_status = out_status;
+  const unsigned grid = static_cast<unsigned>(batch) * static_cast<unsigned>(2 * gamma_max + 1);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (dtype == SPEC_BF16) {
+    err = prepare(sample_kernel<DT_BF16>);
+    if (err == cudaSuccess) sample_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
+  } else {
+    err = prepare(sample_kernel<DT_F32>);
+    if (err == cudaSuccess) sample_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
+  }
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
+                                 const int32_t* draft_tokens, const int32_t* gamma_per_seq,
+                                 int32_t batch, int32_t gamma_max, int32_t vocab,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* out_tokens, int32_t* out_num_accepted,
+                                 int32_t* out_status, void* stream) {
+  if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  if (!shape_ok(batch, gamma_max, vocab)) return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !out_tokens || !out_num_accepted || !workspace) return SPEC_ERR_INVALID_ARG;
+  if (gamma_max > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype);
+  if (!aligned_to(target_logits, es) || !aligned_to(draft_tokens, 4) || !aligned_to(gamma_per_seq, 4) ||
+      !aligned_to(out_tokens, 4) || !aligned_to(out_num_accepted, 4) || !aligned_to(out_status, 4) ||
+      !aligned_to(workspace, kAlign))
+    return SPEC_ERR_MISALIGNED;
+  size_t need = 0;
+  spec_greedy_workspace_size(batch, gamma_max, &need);
+  if (workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  GreedyArgs a;
+  a.tgt = static_cast<const char*>(target_logits);
+  a.tokens = draft_tokens;
+  a.gammas = gamma_per_seq;
+  a.B = batch;
+  a.G = gamma_max;
+  a.V = vocab;
+  a.aligned = (vocab % elems_per_vec(dtype) == 0) && aligned_to(target_logits, 16);
+  a.row_bytes = static_cast<size_t>(vocab) * es;
+  a.counters = reinterpret_cast<uint32_t*>(ws);
+  a.rows = reinterpret_cast<int2*>(ws + round_up(static_cast<size_t>(batch) * sizeof(uint32_t)));
+  a.out_tokens = out_tokens;
+  a.out_nacc = out_num_accepted;
+  a.out_status = out_status;
+  const unsigned grid = static_cast<unsigned>(batch) * static_cast<unsigned>(gamma_max + 1);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (dtype == SPEC_BF16) {
+    err = prepare(greedy_kernel<DT_BF16>);
+    if (err == cudaSuccess) greedy_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
+  } else {
+    err = prepare(greedy_kernel<DT_F32>);
+    if (err == cudaSuccess) greedy_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
+  }
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32_t rows, int32_t vocab,
+                                   spec_sampling_params_t params, float* out_probs,
+                                   int32_t* out_row_status, void* stream) {
+  if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  if (rows < 1 || vocab < 1 || !params_ok(params) || !logits || !out_probs) return SPEC_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype);
+  if (!aligned_to(logits, es) || !aligned_to(out_probs, 4) || !aligned_to(out_row_status, 4))
+    return SPEC_ERR_MISALIGNED;
+  const RowParams P = make_row_params(params, vocab);
+  const int aligned = (vocab % elems_per_vec(dtype) == 0) && aligned_to(logits, 16);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const char* lg = static_cast<const char*>(logits);
+  const size_t rb = static_cast<size_t>(vocab) * es;
+  cudaError_t err;
+  if (dtype == SPEC_BF16) {
+    err = prepare(transform_kernel<DT_BF16>);
+    if (err == cudaSuccess)
+      transform_kernel<DT_BF16><<<rows, kThreads, sizeof(Smem), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
+  } else {
+    err = prepare(transform_kernel<DT_F32>);
+    if (err == cudaSuccess)
+      transform_kernel<DT_F32><<<rows, kThreads, sizeof(Smem), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
+  }
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // extern "C"

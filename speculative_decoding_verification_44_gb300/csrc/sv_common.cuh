@@ -1,0 +1,230 @@
+// sv_common.cuh -- device helpers shared by the verify kernels (sm_103a).
+//
+// Ordering convention used everywhere (argmax, top-k, top-p): value
+// descending, token index ascending.  It is realised by the 64-bit
+// "composite" (monotone float key << 32) | ~index, so that a larger composite
+// always means "earlier in that order" and every composite of a row is unique.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int kThreads = 512;               // threads per row CTA
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kSmallK = 128;                // streaming top-k path handles 1 <= k <= kSmallK
+constexpr int kWarpCap = 256;               // per-warp candidate buffer (entries)
+constexpr int kListCap = kSmallK;           // kept-list entries stored per row
+constexpr int kUnroll = 4;                  // 16-byte loads in flight per thread
+
+enum { DT_BF16 = 0, DT_F32 = 1 };
+enum { PATH_STREAM = 0, PATH_FULL = 1 };
+
+enum {
+  SEQ_OK = 0, SEQ_BAD_LENGTH = 1, SEQ_BAD_TOKEN = 2, SEQ_BAD_UNIFORM = 3,
+  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5,
+  SEQ_FLAG_ZERO_Q = 0x100, SEQ_FLAG_Z_ZERO = 0x200
+};
+
+template <int DT> struct Elem;
+template <> struct Elem<DT_BF16> { static constexpr int kBytes = 2; static constexpr int kPer = 8; };
+template <> struct Elem<DT_F32>  { static constexpr int kBytes = 4; static constexpr int kPer = 4; };
+
+// ---------------------------------------------------------------- keys
+// Monotone unsigned key of a float: x < y  <=>  key(x) < key(y) for non-NaN
+// x, y; -0.0 is folded onto +0.0 first so the two compare equal.
+__device__ __forceinline__ uint32_t fkey(float x) {
+  uint32_t b = __float_as_uint(x);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  const uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(b);
+}
+__device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t idx) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~idx);
+}
+__device__ __forceinline__ uint32_t comp_index(uint64_t c) { return ~static_cast<uint32_t>(c); }
+__device__ __forceinline__ float comp_value(uint64_t c) { return key_value(static_cast<uint32_t>(c >> 32)); }
+
+__device__ __forceinline__ bool finite_ok(float x) { return x < __int_as_float(0x7f800000); }  // false for NaN, +inf
+
+// 2^t with the SFU (relative error about 2^-22); 0 for t = -inf.
+__device__ __forceinline__ float fast_exp2(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+
+// ---------------------------------------------------------------- loads
+// Streaming 16-byte load: read once, do not keep in L1, ask L2 to fetch 256 B.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+// Re-read load (second pass over a row that should still sit in L2).
+__device__ __forceinline__ uint4 ld_reread(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// A row is processed as "virtual vectors" of Elem<DT>::kPer consecutive
+// elements.  In aligned mode (row start 16-byte aligned and vocab a multiple
+// of kPer) every vector is one 16-byte load; otherwise the elements are
+// fetched one by one and the last vector may be partial.
+struct Row {
+  const char* base;
+  int V;
+  int nvec;
+  bool aligned;
+};
+
+template <int DT>
+__device__ __forceinline__ Row make_row(const void* base, int V, bool aligned) {
+  Row r;
+  r.base = static_cast<const char*>(base);
+  r.V = V;
+  r.nvec = (V + Elem<DT>::kPer - 1) / Elem<DT>::kPer;
+  r.aligned = aligned;
+  return r;
+}
+
+// Loads virtual vector v; returns the number of valid elements (0 if v is past the end).
+template <int DT, bool kStream>
+__device__ __forceinline__ int load_vec(const Row& row, int v, uint4& out) {
+  constexpr int P = Elem<DT>::kPer;
+  out = make_uint4(0u, 0u, 0u, 0u);
+  if (v >= row.nvec) return 0;
+  const int i0 = v * P;
+  if (row.aligned) {
+    const void* p = row.base + static_cast<size_t>(i0) * Elem<DT>::kBytes;
+    out = kStream ? ld_stream(p) : ld_reread(p);
+    return P;
+  }
+  const int n = min(P, row.V - i0);
+  if (DT == DT_BF16) {
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(row.base) + i0;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (int j = 0; j < n; ++j) w[j >> 1] |= static_cast<uint32_t>(__ldg(e + j)) << ((j & 1) * 16);
+    out = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    const uint32_t* e = reinterpret_cast<const uint32_t*>(row.base) + i0;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (int j = 0; j < n; ++j) w[j] = __ldg(e + j);
+    out = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return n;
+}
+
+// One element by index (scalar load).
+template <int DT>
+__device__ __forceinline__ float load_elem(const void* base, int x) {
+  if (DT == DT_BF16) {
+    const uint16_t b = __ldg(static_cast<const uint16_t*>(base) + x);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  return __ldg(static_cast<const float*>(base) + x);
+}
+
+template <int DT>
+__device__ __forceinline__ void unpack(const uint4& r, float (&x)[Elem<DT>::kPer]) {
+  if (DT == DT_BF16) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  } else {
+    x[0] = __uint_as_float(r.x);
+    x[1] = __uint_as_float(r.y);
+    x[2] = __uint_as_float(r.z);
+    x[3] = __uint_as_float(r.w);
+  }
+}
+
+// Largest value of a full vector and whether it holds a NaN or +inf.  bf16
+// uses packed NaN-propagating max (three HMNMX2 for eight elements).
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& r, int n, bool& bad) {
+  constexpr int P = Elem<DT>::kPer;
+  if (DT == DT_BF16 && n == P) {
+    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+    __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
+    __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
+    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    const float lo = __low2float(m), hi = __high2float(m);
+    bad = !finite_ok(lo) || !finite_ok(hi);
+    return fmaxf(lo, hi);
+  }
+  float x[P];
+  unpack<DT>(r, x);
+  float m = -__int_as_float(0x7f800000);
+  bool b = false;
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    if (j < n) {
+      b |= !finite_ok(x[j]);
+      m = fmaxf(m, x[j]);
+    }
+  }
+  bad = b;
+  return m;
+}
+
+// ---------------------------------------------------------------- warp helpers
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(kFull, static_cast<uint32_t>(v), src);
+  const uint32_t hi = __shfl_sync(kFull, static_cast<uint32_t>(v >> 32), src);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t t = shfl_xor_u64(v, o);
+    v = t > v ? t : v;
+  }
+  return v;
+}
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_incl_scan_f64(double v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+}  // namespace sv

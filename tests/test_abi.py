@@ -1,0 +1,117 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every declared
+symbol, and its host-side functions (sizes, validation, status strings) behave
+as the header states.  No call here reaches the GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_44_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert {"spec_verify_sample", "spec_verify_greedy", "spec_verify_workspace_size",
+            "spec_greedy_workspace_size", "spec_transform_probs", "spec_status_string"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from speculative_decoding_verification_44_gb300 import _lib
+    so = _lib.LIB_PATH
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", so], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(declared_functions()) <= exported
+    assert set(_lib.EXPORTED) == set(declared_functions())
+    # nothing else leaks out of the library's namespace
+    assert all(s.startswith("spec_") or s.startswith("_") for s in exported), sorted(exported)
+
+
+def test_library_is_for_sm_103a(lib):
+    from speculative_decoding_verification_44_gb300 import build
+    cmd = build.nvcc_command()
+    assert "arch=compute_103a,code=sm_103a" in " ".join(cmd)
+
+
+def test_status_strings(lib):
+    from speculative_decoding_verification_44_gb300 import _lib
+    assert _lib.spec_status_string(0) == "ok"
+    assert "workspace" in _lib.spec_status_string(4)
+    assert _lib.spec_status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    from speculative_decoding_verification_44_gb300 import SamplingParams, workspace_size, greedy_workspace_size
+    stream = SamplingParams(0.7, 50, 0.9)
+    full = SamplingParams(1.0, 0, 0.95)
+    a = workspace_size(64, 5, 128256, stream, stream)
+    b = workspace_size(64, 5, 128256, full, full)
+    assert a > b > 0            # the kept lists only exist for the streaming top-k path
+    assert a % 256 == 0 and b % 256 == 0
+    assert greedy_workspace_size(256, 8) >= 256 * 4 + 256 * 9 * 8
+
+
+@pytest.mark.parametrize("bad", [dict(temperature=0.0), dict(temperature=float("nan")),
+                                 dict(top_p=0.0), dict(top_p=1.5), dict(top_k=-1)])
+def test_invalid_params_rejected(lib, bad):
+    from speculative_decoding_verification_44_gb300 import SamplingParams, _lib
+    kw = dict(temperature=1.0, top_k=0, top_p=1.0)
+    kw.update(bad)
+    with pytest.raises(_lib.SpecError) as e:
+        _lib.spec_verify_workspace_size(4, 2, 100, SamplingParams(**kw).c(), SamplingParams().c())
+    assert e.value.status == _lib.SPEC_ERR_INVALID_ARG
+
+
+def test_host_validation_before_any_launch(lib):
+    """Arguments the contract excludes return an error and never reach the GPU."""
+    from speculative_decoding_verification_44_gb300 import SamplingParams, _lib
+    P = SamplingParams().c()
+    fake = 1 << 20                   # 1 MiB-aligned fake device address, never dereferenced
+    common = dict(d=fake, tok=fake, g=None, oh=None, ua=fake, us=fake)
+
+    def call(tgt=fake, dtype=_lib.SPEC_BF16, B=2, G=3, V=64, ws=fake, wsb=1 << 30, out=fake):
+        return _lib.spec_verify_sample(tgt, common["d"], dtype, common["tok"], None, None, common["ua"],
+                                       common["us"], P, P, B, G, V, ws, wsb, out, out, None, None, None, None)
+
+    assert call(tgt=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert call(dtype=7) == _lib.SPEC_ERR_INVALID_ARG
+    assert call(B=0) == _lib.SPEC_ERR_INVALID_ARG
+    assert call(V=0) == _lib.SPEC_ERR_INVALID_ARG
+    assert call(G=-1) == _lib.SPEC_ERR_INVALID_ARG
+    assert call(tgt=fake + 1) == _lib.SPEC_ERR_MISALIGNED
+    assert call(ws=fake + 16) == _lib.SPEC_ERR_MISALIGNED
+    assert call(wsb=16) == _lib.SPEC_ERR_WORKSPACE
+    assert _lib.spec_verify_greedy(None, 0, fake, None, 2, 3, 64, fake, 1 << 30, fake, fake, None, None) \
+        == _lib.SPEC_ERR_INVALID_ARG
+    assert _lib.spec_verify_greedy(fake, 0, fake, None, 2, 3, 64, fake, 8, fake, fake, None, None) \
+        == _lib.SPEC_ERR_WORKSPACE
+    assert _lib.spec_transform_probs(fake, 0, 0, 64, P, fake, None, None) == _lib.SPEC_ERR_INVALID_ARG
+    assert _lib.spec_transform_probs(fake + 2, 1, 1, 64, P, fake, None, None) == _lib.SPEC_ERR_MISALIGNED
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The package never imports the oracle (test infrastructure only)."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_44_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f

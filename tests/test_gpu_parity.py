@@ -1,0 +1,179 @@
+"""GPU parity: the CUDA path against the float64 oracle on the same seeded inputs.
+
+Sizes here let the oracle finish in seconds while spanning many 16-byte load
+tiles per row, several CTAs' worth of rows, ragged tails and every row path
+(streaming top-k, full-row with and without top-p, one-hot drafts).  Full
+sizes live in test_gpu_fullsize.py.  Tolerances: see tests/helpers.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import (compare_greedy, compare_sample, gpu_greedy, gpu_sample, oracle_probs,
+                     params_tuple, run_oracle_greedy, run_oracle_sample, to_f64, TOL_PROB)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from speculative_decoding_verification_44_gb300 import build
+    build.build()
+
+
+def workload(wid, **kw):
+    from speculative_decoding_verification_44_gb300 import workloads
+    return workloads.make(wid, "cpu", draft_probs=oracle_probs, **kw).to("cuda")
+
+
+# ---------------------------------------------------------------- transform
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("params", [(1.0, 0, 1.0), (0.7, 50, 0.9), (0.8, 0, 1.0), (1.0, 0, 0.95),
+                                    (1.3, 1, 1.0), (0.5, 128, 0.5), (0.9, 300, 0.8), (1.0, 2000, 1.0),
+                                    (2.0, 7, 0.3)])
+@pytest.mark.parametrize("V", [4096, 5003])
+def test_transform_probs_match_oracle(dtype, params, V):
+    import speculative_decoding_verification_44_gb300 as sv
+    from speculative_decoding_verification_44_gb300.workloads import _zipf_rows
+    g = torch.Generator().manual_seed(V + int(params[1]))
+    rows = 12
+    z = _zipf_rows(rows // 2, V, g, 0.5, "cpu")
+    z = torch.cat([z, 2.0 * torch.randn(rows // 2, V, generator=g)]).to(dtype)
+    z[3, ::7] = -float("inf")            # banned tokens
+    p = sv.SamplingParams(*params)
+    probs, status = sv.transform_probs(z.cuda(), p)
+    ref, margins = oracle.transform_rows(to_f64(z), *params_tuple(p))
+    assert (status.cpu() == 0).all()
+    got = probs.cpu().double().numpy()
+    ok = margins >= 1e-6
+    assert ok.sum() >= rows - 2
+    np.testing.assert_allclose(got[ok], ref[ok], atol=TOL_PROB, rtol=0)
+    # kept sets identical where the top-p decision is clear
+    assert ((got[ok] > 0) == (ref[ok] > 0)).all()
+
+
+def test_transform_textbook_softmax_third_opinion():
+    import speculative_decoding_verification_44_gb300 as sv
+    z = torch.randn(8, 32000, generator=torch.Generator().manual_seed(5)) * 3
+    probs, _ = sv.transform_probs(z.cuda(), sv.SamplingParams(0.8, 0, 1.0))
+    ref = torch.softmax(z.double() / float(np.float32(0.8)), dim=-1)
+    assert (probs.cpu().double() - ref).abs().max() < 1e-6
+
+
+def test_transform_ties_and_row_status():
+    import speculative_decoding_verification_44_gb300 as sv
+    z = torch.zeros(4, 1000)
+    z[0, 10] = z[0, 20] = 5.0                      # tie at the top
+    z[1] = -float("inf")                            # empty support
+    z[2, 3] = float("nan")
+    z[3, :] = 1.0                                   # all equal: top-k keeps the lowest indices
+    probs, status = sv.transform_probs(z.cuda(), sv.SamplingParams(1.0, 3, 1.0))
+    assert status.tolist() == [0, 5, 4, 0]
+    p = probs.cpu()
+    assert set(torch.nonzero(p[0]).flatten().tolist()) == {10, 20, 0}
+    assert set(torch.nonzero(p[3]).flatten().tolist()) == {0, 1, 2}
+    assert (p[1] == 0).all() and (p[2] == 0).all()
+    probs, status = sv.transform_probs(z[3:].cuda(), sv.SamplingParams(1.0, 0, 0.5))
+    assert set(torch.nonzero(probs.cpu()[0]).flatten().tolist()) == set(range(500))
+
+
+# ---------------------------------------------------------------- sampling
+def check_sample(w, seqs=None, min_exact=0.9):
+    out = gpu_sample(w)
+    torch.cuda.synchronize()
+    ref = run_oracle_sample(w, seqs)
+    c = compare_sample(out, ref, w, seqs)
+    assert c["flagged"] + c["boundary"] <= max(2, 0.02 * c["n"]), c
+    assert c["exact"] >= min_exact * (c["n"] - c["flagged"] - c["errors"]), c
+    return c
+
+
+def test_tiny_sampling_many_rounds():
+    c = check_sample(workload(1, B=2000))
+    assert c["rejected"] > 100 and c["bonus"] > 100
+
+
+def test_small_vocab_batch():
+    check_sample(workload(2))
+
+
+@pytest.mark.parametrize("V", [128256, 20000, 20001])
+def test_serving_shape_streaming_topk(V):
+    c = check_sample(workload(3, B=12, V=V))
+    assert c["n"] == 12
+
+
+def test_ragged_mixed_full_row_top_p():
+    w = workload(5, B=24, V=30000)
+    c = check_sample(w)
+    assert c["n"] == 24
+
+
+@pytest.mark.parametrize("tp,dp", [((0.7, 50, 0.9), (1.0, 0, 1.0)), ((1.0, 0, 1.0), (0.7, 20, 0.8)),
+                                   ((0.9, 0, 0.9), (0.9, 64, 1.0)), ((1.0, 200, 0.85), (1.1, 0, 0.9)),
+                                   ((0.8, 1, 1.0), (0.8, 128, 0.95))])
+def test_mixed_target_draft_paths(tp, dp):
+    """Target and draft on different row paths (streaming top-k vs full row)."""
+    import speculative_decoding_verification_44_gb300 as sv
+    w = workload(3, B=10, V=9000)
+    w.target_params, w.draft_params = sv.SamplingParams(*tp), sv.SamplingParams(*dp)
+    # redraw drafts from this q
+    from speculative_decoding_verification_44_gb300.workloads import sample_from_probs
+    q = oracle_probs(w.draft_logits.reshape(-1, w.V).cpu(), w.draft_params)
+    toks = sample_from_probs(q, torch.Generator().manual_seed(9)).reshape(w.B, w.G)
+    w.draft_tokens = toks.to(torch.int32).cuda()
+    check_sample(w)
+
+
+def test_one_hot_drafts_all_sequences():
+    w = workload(5, B=16, V=12000)
+    w.draft_is_onehot = torch.ones(w.B, dtype=torch.uint8, device="cuda")
+    check_sample(w)
+    w.draft_logits = None           # NULL draft logits: every sequence one-hot
+    check_sample(w)
+
+
+def test_zero_and_full_gamma():
+    w = workload(3, B=8, V=4096)
+    w.gamma_per_seq = torch.tensor([0, 5, 0, 1, 5, 2, 0, 3], dtype=torch.int32, device="cuda")
+    check_sample(w)
+
+
+# ---------------------------------------------------------------- greedy
+@pytest.mark.parametrize("V", [152064, 4099])
+def test_greedy_matches_oracle(V):
+    w = workload(4, B=32, V=V)
+    out = gpu_greedy(w)
+    torch.cuda.synchronize()
+    assert compare_greedy(out, run_oracle_greedy(w), w) == 32
+
+
+def test_greedy_ties_pick_lowest_index():
+    import speculative_decoding_verification_44_gb300 as sv
+    V = 3000
+    z = torch.zeros(1, 3, V, dtype=torch.bfloat16)
+    z[0, 0, [50, 7, 2999]] = 4.0        # argmax 7
+    z[0, 1, [1, 0]] = 3.0               # argmax 0
+    z[0, 2, [100, 200]] = -0.0          # all zero: argmax 0 (and -0 == +0)
+    toks = torch.tensor([[7, 1]], dtype=torch.int32)
+    out = sv.verify_greedy(z.cuda(), toks.cuda())
+    assert out.num_accepted.item() == 1
+    assert out.tokens.cpu().tolist() == [[7, 0, -1]]
+
+
+def test_top1_sampling_with_one_hot_drafts_equals_greedy():
+    """T -> 0 special case [baisen §6]: top_k = 1 sampling with one-hot drafts is greedy."""
+    import speculative_decoding_verification_44_gb300 as sv
+    w = workload(4, B=64, V=8192)
+    g = gpu_greedy(w)
+    w1 = workload(4, B=64, V=8192)
+    B, G = w1.B, w1.G
+    u = torch.rand(B, G, generator=torch.Generator().manual_seed(3)).cuda()
+    us = torch.rand(B, generator=torch.Generator().manual_seed(4)).cuda()
+    s = sv.verify_sample(w1.target_logits, None, w1.draft_tokens, u, us, sv.SamplingParams(1.0, 1, 1.0),
+                         sv.SamplingParams(), None, None)
+    torch.cuda.synchronize()
+    assert torch.equal(g.tokens, s.tokens) and torch.equal(g.num_accepted, s.num_accepted)
