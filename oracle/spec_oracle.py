@@ -114,6 +114,9 @@ def order_desc(z: np.ndarray) -> np.ndarray:
     return np.lexsort((idx, -z))
 
 
+TOP_P_AMBIGUITY = 1e-6
+
+
 @dataclass
 class RowDist:
     """One transformed row: the distribution p (or q) over the vocabulary."""
@@ -121,6 +124,11 @@ class RowDist:
     probs: np.ndarray                  # (V,) float64; zeros unless status == SEQ_OK
     kept: np.ndarray                   # kept token ids in (value desc, index asc) order
     top_p_margin: float = np.inf       # distance of the top-p decision from top_p (R3)
+    # Tokens whose membership in the top-p set turns on a cumulative probability
+    # within TOP_P_AMBIGUITY of top_p (a token is kept iff the cumulative of the
+    # tokens before it is < top_p), and their total probability before the cut.
+    ambiguous: np.ndarray = field(default_factory=lambda: np.zeros(0, dtype=np.int64))
+    ambiguous_mass: float = 0.0
 
 
 def row_status(z: np.ndarray) -> int:
@@ -153,6 +161,8 @@ def transform_row(z: np.ndarray, temperature: float, top_k: int, top_p: float) -
     w = np.exp((zk - m) / temperature)          # -inf logits give weight 0
     p_tilde = w / w.sum()
     margin = np.inf
+    ambiguous = np.zeros(0, dtype=np.int64)
+    ambiguous_mass = 0.0
     if top_p < 1.0:
         cum = np.cumsum(p_tilde)
         reached = np.flatnonzero(cum >= top_p)
@@ -160,11 +170,15 @@ def transform_row(z: np.ndarray, temperature: float, top_k: int, top_p: float) -
         above = cum[n - 1] - top_p
         below = top_p - cum[n - 2] if n >= 2 else np.inf
         margin = float(min(abs(above), abs(below)))
+        before = np.concatenate([[0.0], cum[:-1]])        # cumulative of the tokens before each
+        amb = np.abs(before - top_p) < TOP_P_AMBIGUITY
+        ambiguous = kept[amb]
+        ambiguous_mass = float(p_tilde[amb].sum())
         kept = kept[:n]
         w = w[:n]
     probs = np.zeros(V)
     probs[kept] = w / w.sum()
-    return RowDist(SEQ_OK, probs, kept, margin)
+    return RowDist(SEQ_OK, probs, kept, margin, ambiguous, ambiguous_mass)
 
 
 def one_hot_row(V: int, token: int) -> RowDist:
@@ -225,6 +239,10 @@ class SeqResult:
     residual_Z: float           # Z at the rejected position, -1 when nothing was rejected
     accept_margin: float = np.inf   # min |u_i - a_i| over evaluated positions
     top_p_margin: float = np.inf    # min top-p margin over the rows used
+    # evaluated draft tokens whose top-p membership (in p_i or q_i) is ambiguous
+    draft_ambiguous: bool = False
+    # tokens of the row(s) the final draw used whose top-p membership is ambiguous
+    sample_ambiguous: np.ndarray = field(default_factory=lambda: np.zeros(0, dtype=np.int64))
     sample_u: float = np.nan
     sample_lo: float = np.nan
     sample_hi: float = np.nan
@@ -310,8 +328,14 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
     out[n_acc] = tok
     used = p_rows[: n_acc + 1] + ([] if one_hot else q_rows[: min(n_acc + 1, gamma_b)])
     top_p_margin = min([r.top_p_margin for r in used] + [np.inf])
+    evaluated = range(min(n_acc + 1, gamma_b))
+    draft_amb = any(d[i] in p_rows[i].ambiguous or (not one_hot and d[i] in q_rows[i].ambiguous)
+                    for i in evaluated)
+    sample_rows = [p_rows[n_acc]] + ([q_rows[n_acc]] if (rejected_at is not None and not one_hot) else [])
+    sample_amb = np.unique(np.concatenate([r.ambiguous for r in sample_rows]))
     res = SeqResult(out, n_acc, status, a, residual_Z, accept_margin, top_p_margin,
-                    float(u_sample), lo, hi)
+                    draft_ambiguous=draft_amb, sample_ambiguous=sample_amb,
+                    sample_u=float(u_sample), sample_lo=lo, sample_hi=hi)
     if keep_cdf:
         C = np.cumsum(w)
         res.sample_cdf = C / C[-1]
@@ -424,3 +448,8 @@ def transform_rows(z: np.ndarray, temperature: float, top_k: int, top_p: float) 
         probs[r] = rd.probs
         margins[r] = rd.top_p_margin
     return probs, margins
+
+
+def transform_rows_detail(z: np.ndarray, temperature: float, top_k: int, top_p: float) -> list[RowDist]:
+    """Row-wise transform keeping every row's full RowDist (ambiguity diagnostics included)."""
+    return [transform_row(z[r], temperature, top_k, top_p) for r in range(z.shape[0])]

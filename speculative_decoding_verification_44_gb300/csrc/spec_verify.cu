@@ -92,7 +92,7 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const double* p
 // Residual weights max(0, p - q) [wrblog §5], or p itself for the bonus draw;
 // the token is the smallest x (vocabulary order) with C(x) > u Z.
 template <int DT>
-__device__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
+__device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
                          const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
   const int lane = threadIdx.x & 31;
   const int slots = 2 * a.G + 1;
@@ -236,7 +236,7 @@ __device__ __forceinline__ float scan_vec(const ScanCtx& c, int v, const Smem& s
 // owning warp then re-scans its range with identical arithmetic to locate the
 // first x with C(x) > u Z.
 template <int DT>
-__device__ int block_scan_draw(ScanCtx& c, double u, bool residual, double& Z_resid, int& flags, Smem& sm) {
+__device__ __noinline__ int block_scan_draw(ScanCtx& c, double u, bool residual, double& Z_resid, int& flags, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nv = c.trow.nvec;
@@ -334,7 +334,7 @@ __device__ int block_scan_draw(ScanCtx& c, double u, bool residual, double& Z_re
 
 // Sequence epilogue, run by the CTA that analysed the sequence's last row.
 template <int DT>
-__device__ void sample_epilogue(const SampleArgs& a, int b, int gb, bool onehot, Smem& sm) {
+__device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb, bool onehot, Smem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slots = 2 * a.G + 1;
   const RowStat* S = a.stats + static_cast<size_t>(b) * slots;

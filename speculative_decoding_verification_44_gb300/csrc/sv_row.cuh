@@ -92,6 +92,7 @@ struct __align__(16) Smem {
   int32_t list_tok[kListCap];
   double list_p[kListCap];
   int nw[kWarps];
+  unsigned long long shared_thr;      // PATH_STREAM: CTA-wide admission threshold
   float red_f[kWarps];
   double red_d[kWarps];
   uint64_t red_u[kWarps];
@@ -185,7 +186,7 @@ __device__ __forceinline__ void pick_digit_mass(const unsigned long long* mass, 
 
 // ------------------------------------------------------------------ warp radix select
 // k-th largest (1-based) of buf[0..n), n >= k, composites unique.
-__device__ uint64_t warp_select_kth(const uint64_t* buf, int n, int k, uint32_t* hist, int lane) {
+__device__ __noinline__ uint64_t warp_select_kth(const uint64_t* buf, int n, int k, uint32_t* hist, int lane) {
   uint64_t prefix = 0, mask = 0;
   uint32_t need = static_cast<uint32_t>(k);
   for (int shift = 56; shift >= 0; shift -= 8) {
@@ -221,7 +222,7 @@ __device__ uint64_t warp_select_kth(const uint64_t* buf, int n, int k, uint32_t*
 }
 
 // Keeps the k largest entries of buf[0..n) (n > k) and raises the threshold.
-__device__ void warp_refresh(uint64_t* buf, int& n, int k, uint32_t* hist, int lane,
+__device__ __noinline__ void warp_refresh(uint64_t* buf, int& n, int k, uint32_t* hist, int lane,
                              uint64_t& thr, float& thr_val) {
   __syncwarp();
   const uint64_t kth = warp_select_kth(buf, n, k, hist, lane);
@@ -237,8 +238,10 @@ __device__ void warp_refresh(uint64_t* buf, int& n, int k, uint32_t* hist, int l
     __syncwarp();
   }
   n = m;
-  thr = kth;
-  thr_val = comp_value(kth);
+  if (kth > thr) {
+    thr = kth;
+    thr_val = comp_value(kth);
+  }
 }
 
 // ------------------------------------------------------------------ block reductions
@@ -324,57 +327,78 @@ __device__ void greedy_row(const Row& row, Smem& sm, int& argmax, int& status) {
 }
 
 // ------------------------------------------------------------------ PATH_STREAM
-// One HBM pass; leaves the kept list (descending order) in sm.list_tok/list_p.
-template <int DT>
-__device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& sm) {
-  constexpr int PER = Elem<DT>::kPer;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = P.k;
-  uint64_t* buf = sm.u.s.wbuf[warp];
-  uint32_t* hist = sm.u.s.whist[warp];
-  uint64_t thr = 0;
-  float thr_val = -__int_as_float(0x7f800000);
-  int n = 0;
-  bool bad = false;
+// Per-warp filter state: an element is a candidate iff its composite beats thr.
+struct WarpFilter {
+  uint64_t thr;
+  float thr_val;   // value of thr's key: a candidate has x >= thr_val (cheap pre-test)
+  int n;           // entries in the warp's candidate buffer
+};
 
-  for (int base = 0; base < row.nvec; base += kThreads * kUnroll) {
-    uint4 r[kUnroll];
-    int cnt[kUnroll];
+// Overflow path of the streaming filter: admits one element slot at a time and
+// cuts the buffer back to the warp's k best (warp radix select) whenever it
+// would overflow, raising the threshold; the new threshold is also offered to
+// the whole CTA (the largest of the warps' k-th values is a lower bound for the
+// row's k-th largest).
+template <int DT>
+__device__ __noinline__ void admit_slots(const uint4 r, const int cnt, const int v, const bool maybe,
+                                         uint64_t* buf, uint32_t* hist, const int k, WarpFilter& f,
+                                         unsigned long long* shared_thr, const int lane) {
+  constexpr int PER = Elem<DT>::kPer;
+  float x[PER];
+  unpack<DT>(r, x);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) cnt[u] = load_vec<DT, true>(row, base + u * kThreads + tid, r[u]);
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int v = base + u * kThreads + tid;
-      bool vb = false;
-      const float vm = cnt[u] ? vec_max<DT>(r[u], cnt[u], vb) : -__int_as_float(0x7f800000);
-      bad |= vb;
-      const bool maybe = cnt[u] > 0 && vm >= thr_val;
-      if (__any_sync(kFull, maybe)) {
-        float x[PER];
-        unpack<DT>(r[u], x);
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-          const uint64_t c = composite(fkey(x[e]), static_cast<uint32_t>(v * PER + e));
-          bool cand = maybe && e < cnt[u] && !(x[e] != x[e]) && c > thr;
-          unsigned bal = __ballot_sync(kFull, cand);
-          if (bal) {
-            if (n + __popc(bal) > kWarpCap) {
-              warp_refresh(buf, n, k, hist, lane, thr, thr_val);
-              cand = cand && c > thr;
-              bal = __ballot_sync(kFull, cand);
-            }
-            if (cand) buf[n + __popc(bal & lanemask_lt())] = c;
-            n += __popc(bal);
-          }
-        }
+  for (int e = 0; e < PER; ++e) {
+    const uint64_t c = composite(fkey(x[e]), static_cast<uint32_t>(v * PER + e));
+    bool cand = maybe && e < cnt && !(x[e] != x[e]) && c > f.thr;
+    unsigned bal = __ballot_sync(kFull, cand);
+    if (bal) {
+      if (f.n + __popc(bal) > kWarpCap) {
+        warp_refresh(buf, f.n, k, hist, lane, f.thr, f.thr_val);
+        if (lane == 0) atomicMax(shared_thr, static_cast<unsigned long long>(f.thr));
+        cand = cand && c > f.thr;
+        bal = __ballot_sync(kFull, cand);
       }
+      if (cand) buf[f.n + __popc(bal & lanemask_lt())] = c;
+      f.n += __popc(bal);
     }
   }
-  __syncwarp();
-  if (n > k) warp_refresh(buf, n, k, hist, lane, thr, thr_val);
-  if (lane == 0) sm.nw[warp] = n;
-  const int any_bad = block_or(bad ? 1 : 0, sm);   // also orders the nw writes
+}
 
+// Slow path of the streaming filter, taken when some lane's vector may hold a
+// candidate: each lane marks its candidates, one warp scan places them all.
+template <int DT>
+__device__ __noinline__ void admit_vector(const uint4 r, const int cnt, const int v, const bool maybe,
+                                          uint64_t* buf, uint32_t* hist, const int k, WarpFilter& f,
+                                          unsigned long long* shared_thr, const int lane) {
+  constexpr int PER = Elem<DT>::kPer;
+  float x[PER];
+  unpack<DT>(r, x);
+  uint32_t m = 0;
+  uint64_t c[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    c[e] = composite(fkey(x[e]), static_cast<uint32_t>(v * PER + e));
+    if (maybe && e < cnt && x[e] >= f.thr_val && c[e] > f.thr) m |= 1u << e;   // NaN fails x >= thr_val
+  }
+  const uint32_t mine = __popc(m);
+  const uint32_t incl = warp_incl_scan_u32(mine, lane);
+  const int total = static_cast<int>(__shfl_sync(kFull, incl, 31));
+  if (f.n + total > kWarpCap) {
+    admit_slots<DT>(r, cnt, v, maybe, buf, hist, k, f, shared_thr, lane);
+    return;
+  }
+  int pos = f.n + static_cast<int>(incl - mine);
+#pragma unroll
+  for (int e = 0; e < PER; ++e)
+    if (m & (1u << e)) buf[pos++] = c[e];
+  f.n += total;
+}
+
+// Block merge of the warps' survivors, sort, float64 softmax and top-p cut.
+template <int DT>
+__device__ __noinline__ void stream_finish(const RowParams& P, const int dtok, const int any_bad, Smem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = P.k;
   // ---- block merge: the k largest of the warps' survivors
   int total = 0;
   for (int w = 0; w < kWarps; ++w) total += sm.nw[w];
@@ -516,6 +540,49 @@ __device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& s
   __syncthreads();
 }
 
+// One HBM pass; leaves the kept list (descending order) in sm.list_tok/list_p.
+template <int DT>
+__device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = P.k;
+  uint64_t* buf = sm.u.s.wbuf[warp];
+  uint32_t* hist = sm.u.s.whist[warp];
+  WarpFilter f;
+  f.thr = 0;
+  f.thr_val = -__int_as_float(0x7f800000);
+  f.n = 0;
+  bool bad = false;
+  if (tid == 0) sm.shared_thr = 0ull;
+  __syncthreads();
+
+  for (int base = 0; base < row.nvec; base += kThreads * kUnroll) {
+    uint4 r[kUnroll];
+    int cnt[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) cnt[u] = load_vec<DT, true>(row, base + u * kThreads + tid, r[u]);
+    // adopt the CTA-wide threshold (warp-uniform: lane 0's read is broadcast)
+    const uint64_t s = shfl_u64(lane == 0 ? *reinterpret_cast<volatile unsigned long long*>(&sm.shared_thr) : 0ull, 0);
+    if (s > f.thr) {
+      f.thr = s;
+      f.thr_val = comp_value(s);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      bool vb = false;
+      const float vm = cnt[u] ? vec_max<DT>(r[u], cnt[u], vb) : -__int_as_float(0x7f800000);
+      bad |= vb;
+      const bool maybe = cnt[u] > 0 && vm >= f.thr_val;
+      if (__any_sync(kFull, maybe))
+        admit_vector<DT>(r[u], cnt[u], base + u * kThreads + tid, maybe, buf, hist, k, f, &sm.shared_thr, lane);
+    }
+  }
+  __syncwarp();
+  if (f.n > k) warp_refresh(buf, f.n, k, hist, lane, f.thr, f.thr_val);
+  if (lane == 0) sm.nw[warp] = f.n;
+  const int any_bad = block_or(bad ? 1 : 0, sm);   // also orders the nw writes
+  stream_finish<DT>(P, dtok, any_bad, sm);
+}
+
 // ------------------------------------------------------------------ PATH_FULL
 // Fixed-point mass of a weight w in [0, 1].
 __device__ __forceinline__ unsigned long long fixed_mass(float w, float scale) {
@@ -579,7 +646,7 @@ __device__ void full_pass1(const Row& row, float cT, Smem& sm, float& m_out, dou
 
 // Sum over the kept set {composite >= cut} of 2^((z - m) cT), float64 across threads.
 template <int DT>
-__device__ double full_sum_kept(const Row& row, float m, float cT, uint64_t cut, Smem& sm) {
+__device__ __noinline__ double full_sum_kept(const Row& row, float m, float cT, uint64_t cut, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x;
   float s = 0.0f, comp = 0.0f;
@@ -611,7 +678,7 @@ __device__ double full_sum_kept(const Row& row, float m, float cT, uint64_t cut,
 
 // Index of the n-th (1-based) element, in index order, whose key equals K.
 template <int DT>
-__device__ int find_nth_with_key(const Row& row, uint32_t K, uint32_t n, Smem& sm) {
+__device__ __noinline__ int find_nth_with_key(const Row& row, uint32_t K, uint32_t n, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L = (row.nvec + kWarps - 1) / kWarps;
@@ -686,7 +753,7 @@ __device__ int find_nth_with_key(const Row& row, uint32_t K, uint32_t n, Smem& s
 // composite byte at `shift`.  Accumulates counts, fixed-point masses (when
 // with_mass) and the largest composite per digit.
 template <int DT>
-__device__ void full_round(const Row& row, float m, float cT, float scale, uint64_t ck, int tb,
+__device__ __noinline__ void full_round(const Row& row, float m, float cT, float scale, uint64_t ck, int tb,
                            uint64_t prefix, uint64_t mask, int kind, int shift, bool with_mass,
                            Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
@@ -728,7 +795,7 @@ __device__ void full_round(const Row& row, float m, float cT, float scale, uint6
 
 // k-th largest composite of the row (count-based radix select).
 template <int DT>
-__device__ uint64_t full_select_topk(const Row& row, float m, float cT, int k, Smem& sm) {
+__device__ __noinline__ uint64_t full_select_topk(const Row& row, float m, float cT, int k, Smem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint64_t prefix = 0, mask = 0;
   uint32_t need = static_cast<uint32_t>(k);
@@ -768,7 +835,7 @@ __device__ uint64_t full_select_topk(const Row& row, float m, float cT, int k, S
 // cumulative mass (descending order) reaches top_p of the kept mass.  Returns
 // c* and the fixed-point kept mass through c*.
 template <int DT>
-__device__ uint64_t full_select_topp(const Row& row, float m, float cT, float scale, uint64_t ck,
+__device__ __noinline__ uint64_t full_select_topp(const Row& row, float m, float cT, float scale, uint64_t ck,
                                      float top_p, Smem& sm, unsigned long long& Wfixed) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // round 0: log-probability buckets, ascending = descending probability

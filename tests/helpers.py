@@ -2,8 +2,9 @@
 
 Boundary rules (the tolerance the parity tests state):
 * accept counts and greedy tokens are bit-exact, except sequences where some
-  evaluated |u_i - a_i| < 1e-6 or a used row's top-p decision lies within
-  1e-6 of top_p ("flagged": counted, outputs checked for validity only);
+  evaluated |u_i - a_i| < 1e-6, or an evaluated draft token or the drawn token
+  is one whose top-p membership turns on a cumulative probability within 1e-6
+  of top_p ("flagged": counted, outputs checked for validity only);
 * a sampled token may differ from the oracle's only when u lies within 1e-6
   of every normalised CDF boundary between the two tokens ("boundary");
 * probabilities (a_i, Z, transformed rows) agree within 1e-5 absolute.
@@ -99,7 +100,8 @@ def compare_sample(out, ref, w, seqs=None):
             np.testing.assert_allclose(aprob[b, :gb], r.accept_prob[:gb], atol=TOL_PROB, rtol=0,
                                        err_msg=f"accept_prob seq {b}")
             assert (aprob[b, gb:] == -1).all()
-        if r.accept_margin < TOL_BOUNDARY or r.top_p_margin < TOL_BOUNDARY:
+        if (r.accept_margin < TOL_BOUNDARY or r.draft_ambiguous
+                or toks[b, n] in r.sample_ambiguous or r.tokens[r.num_accepted] in r.sample_ambiguous):
             c["flagged"] += 1
             continue
         assert n == r.num_accepted, (b, n, r.num_accepted, r.accept_margin)

@@ -45,14 +45,19 @@ def test_transform_probs_match_oracle(dtype, params, V):
     z[3, ::7] = -float("inf")            # banned tokens
     p = sv.SamplingParams(*params)
     probs, status = sv.transform_probs(z.cuda(), p)
-    ref, margins = oracle.transform_rows(to_f64(z), *params_tuple(p))
+    detail = oracle.transform_rows_detail(to_f64(z), *params_tuple(p))
     assert (status.cpu() == 0).all()
     got = probs.cpu().double().numpy()
-    ok = margins >= 1e-6
-    assert ok.sum() >= rows - 2
-    np.testing.assert_allclose(got[ok], ref[ok], atol=TOL_PROB, rtol=0)
-    # kept sets identical where the top-p decision is clear
-    assert ((got[ok] > 0) == (ref[ok] > 0)).all()
+    checked = 0
+    for r, rd in enumerate(detail):
+        if rd.ambiguous_mass > TOL_PROB:       # a near-tie at the cut moves real mass: skip the row
+            continue
+        np.testing.assert_allclose(got[r], rd.probs, atol=TOL_PROB, rtol=0, err_msg=f"row {r}")
+        clear = np.ones(V, dtype=bool)
+        clear[rd.ambiguous] = False
+        assert ((got[r] > 0) == (rd.probs > 0))[clear].all(), r   # kept sets agree off the cut
+        checked += 1
+    assert checked >= rows - 2
 
 
 def test_transform_textbook_softmax_third_opinion():

@@ -120,3 +120,16 @@ def test_temperature_scales_logits(T):
     z = np.array([2.0, 1.0, 0.0, -3.0])
     np.testing.assert_allclose(oracle.transform_row(z, T, 0, 1.0).probs,
                                scipy.special.softmax(z / T), rtol=1e-13)
+
+
+def test_top_p_ambiguity_diagnostics():
+    """Tokens whose top-p membership turns on a cumulative within 1e-6 of top_p."""
+    z = np.log(np.array([0.5, 0.25, 0.25]))
+    rd = oracle.transform_row(z, 1.0, 0, 0.75)           # cumulative before token 2 is exactly 0.75
+    assert list(rd.ambiguous) == [2] and abs(rd.ambiguous_mass - 0.25) < 1e-12
+    rd = oracle.transform_row(z, 1.0, 0, 0.6)
+    assert rd.ambiguous.size == 0 and rd.ambiguous_mass == 0.0
+    # a dense tail: many tiny tokens around the cut are ambiguous, their mass is tiny
+    p = np.concatenate([[0.5], np.full(100000, 0.5 / 100000)])
+    rd = oracle.transform_row(np.log(p), 1.0, 0, 0.9)
+    assert 0 < rd.ambiguous.size < 1000 and rd.ambiguous_mass < 1e-5
