@@ -122,7 +122,8 @@ typedef struct {
 
 /* Bytes of workspace spec_verify_sample needs for this shape and these
  * parameters.  Returns SPEC_ERR_INVALID_ARG for sizes or parameters that
- * spec_verify_sample would reject.  The workspace must be zero-filled before
+ * spec_verify_sample would reject, SPEC_ERR_UNSUPPORTED for gamma_max > 63
+ * (the sampling verifier's limit).  The workspace must be zero-filled before
  * its first use; every call that returns SPEC_OK leaves its counter region
  * zero again, so a workspace is reusable without clearing. */
 SPEC_API spec_status_t spec_verify_workspace_size(int32_t batch, int32_t gamma_max, int32_t vocab,

@@ -96,20 +96,29 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
                          const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
   const int lane = threadIdx.x & 31;
   const int slots = 2 * a.G + 1;
-  const RowStat ts = load_stat(a.stats + static_cast<size_t>(b) * slots + r);
+  SmemEpi& E = sm.u.e;
+  const RowStat ts = E.rs[r];
   const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
   const int nt = ts.n_list;
-  SmemEpi& E = sm.u.e;
-  // draft list (PATH_STREAM draft), token-sorted for lookups
-  int nq = 0;
+  // both kept lists are fetched in one round trip
   const bool draft_list = residual && !onehot && ds.path == PATH_STREAM;
+  const int nq = draft_list ? ds.n_list : 0;
+  const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
+  ListEntry te[kListCap / 32], qe[kListCap / 32];
+#pragma unroll
+  for (int j = 0; j < kListCap / 32; ++j) {
+    const int e = lane + 32 * j;
+    if (e < nt) te[j] = load_entry(tl + e);
+    if (e < nq) qe[j] = load_entry(ql + e);
+  }
   if (draft_list) {
-    const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
-    nq = ds.n_list;
-    for (int e = lane; e < nq; e += 32) {
-      const ListEntry q = load_entry(ql + e);
-      E.tok[e] = q.token;
-      E.w[e] = q.p;
+#pragma unroll
+    for (int j = 0; j < kListCap / 32; ++j) {
+      const int e = lane + 32 * j;
+      if (e < nq) {
+        E.tok[e] = qe[j].token;
+        E.w[e] = qe[j].p;
+      }
     }
     __syncwarp();
     for (int e = lane; e < nq; e += 32) {
@@ -123,8 +132,11 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
   const Row drow = seq_row<DT>(a, b, r, true);
   const float invWd = (residual && !onehot && ds.path == PATH_FULL) ? static_cast<float>(1.0 / ds.W) : 0.0f;
   // target entries with their residual / bonus weights
-  for (int e = lane; e < nt; e += 32) {
-    const ListEntry t = load_entry(tl + e);
+#pragma unroll
+  for (int j = 0; j < kListCap / 32; ++j) {
+    const int e = lane + 32 * j;
+    if (e >= nt) continue;
+    const ListEntry t = te[j];
     double w = t.p;
     if (residual) {
       double q;
@@ -340,24 +352,38 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   const RowStat* S = a.stats + static_cast<size_t>(b) * slots;
   const size_t tokb = static_cast<size_t>(b) * a.G;
 
-  // 1. status, in the documented order: tokens, uniforms, rows
+  // 1. gather, in parallel, every row's status and draft-token probability,
+  //    the draft tokens and the uniforms (one round trip for the whole CTA)
+  SmemEpi& E = sm.u.e;
+  for (int t = tid; t < slots; t += kThreads) {
+    const bool used = t <= gb || (t > a.G && !onehot && t - a.G - 1 < gb);
+    RowStat rs;
+    rs.status = SEQ_OK;
+    rs.p_tok = 0.0;
+    rs.path = PATH_FULL;
+    rs.n_list = 0;
+    if (used) rs = load_stat(S + t);
+    E.rs[t] = rs;
+  }
+  for (int t = tid; t < gb; t += kThreads) {
+    E.dtok[t] = a.tokens[tokb + t];
+    E.uacc[t] = a.u_acc[tokb + t];
+  }
+  __syncthreads();
+  // status, in the documented order: tokens, uniforms, rows
   if (tid == 0) {
     int status = SEQ_OK;
-    for (int i = 0; i < gb && status == SEQ_OK; ++i) {
-      const int t = a.tokens[tokb + i];
-      if (t < 0 || t >= a.V) status = SEQ_BAD_TOKEN;
-    }
+    for (int i = 0; i < gb && status == SEQ_OK; ++i)
+      if (E.dtok[i] < 0 || E.dtok[i] >= a.V) status = SEQ_BAD_TOKEN;
     if (status == SEQ_OK) {
-      for (int i = 0; i < gb; ++i) {
-        const float u = a.u_acc[tokb + i];
-        if (!(u >= 0.0f && u < 1.0f)) status = SEQ_BAD_UNIFORM;
-      }
+      for (int i = 0; i < gb; ++i)
+        if (!(E.uacc[i] >= 0.0f && E.uacc[i] < 1.0f)) status = SEQ_BAD_UNIFORM;
       const float us = a.u_samp[b];
       if (!(us >= 0.0f && us < 1.0f)) status = SEQ_BAD_UNIFORM;
     }
     for (int i = 0; i <= gb && status == SEQ_OK; ++i) {
-      status = load_stat(S + i).status;
-      if (status == SEQ_OK && i < gb && !onehot) status = load_stat(S + a.G + 1 + i).status;
+      status = E.rs[i].status;
+      if (status == SEQ_OK && i < gb && !onehot) status = E.rs[a.G + 1 + i].status;
     }
     sm.b_i32[0] = status;
   }
@@ -374,13 +400,13 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
       const int i = base + lane;
       bool rej = false, zq = false;
       if (i < gb) {
-        const double p = load_stat(S + i).p_tok;
-        const double q = onehot ? 1.0 : load_stat(S + a.G + 1 + i).p_tok;
-        double ai;
-        if (q > 0.0) ai = fmin(1.0, p / q);
-        else { ai = p > 0.0 ? 1.0 : 0.0; zq = true; }
-        rej = !(static_cast<double>(a.u_acc[tokb + i]) < ai);
-        if (a.out_aprob) a.out_aprob[tokb + i] = static_cast<float>(ai);
+        const float p = static_cast<float>(E.rs[i].p_tok);
+        const float q = onehot ? 1.0f : static_cast<float>(E.rs[a.G + 1 + i].p_tok);
+        float ai;
+        if (q > 0.0f) ai = fminf(1.0f, p / q);
+        else { ai = p > 0.0f ? 1.0f : 0.0f; zq = true; }
+        rej = !(E.uacc[i] < ai);
+        if (a.out_aprob) a.out_aprob[tokb + i] = ai;
       } else if (i < a.G && a.out_aprob) {
         a.out_aprob[tokb + i] = -1.0f;
       }
@@ -410,11 +436,11 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   // 3. residual draw at the rejected position, or the bonus draw [wrblog §5, §6]
   const bool residual = j < gb;
   const int r = j;   // == gb when every draft was accepted
-  const RowStat ts = load_stat(S + r);
+  const RowStat ts = E.rs[r];
   RowStat ds;
   ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0;
-  if (residual && !onehot) ds = load_stat(S + a.G + 1 + r);
-  const int dj = residual ? a.tokens[tokb + j] : -1;
+  if (residual && !onehot) ds = E.rs[a.G + 1 + r];
+  const int dj = residual ? E.dtok[j] : -1;
   const double u = static_cast<double>(a.u_samp[b]);
   double Z_resid = -1.0;
   int tok = -1;
@@ -480,7 +506,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int slots = 2 * a.G + 1;
@@ -550,7 +576,7 @@ struct GreedyArgs {
 };
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) greedy_kernel(const GreedyArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int slots = a.G + 1;
@@ -614,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs a)
 
 // ------------------------------------------------------------------ transform (test hook)
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) transform_kernel(const char* logits, int V, RowParams P,
+__global__ void __launch_bounds__(kThreads, 5) transform_kernel(const char* logits, int V, RowParams P,
                                                                  int aligned, size_t row_bytes,
                                                                  float* out, int32_t* out_status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -659,13 +685,16 @@ int bit_length(uint32_t v) {
   return n;
 }
 
-RowParams make_row_params(const spec_sampling_params_t& p, int V) {
+RowParams make_row_params(const spec_sampling_params_t& p, int V, spec_dtype_t dt) {
   RowParams r;
   r.T = p.temperature;
-  r.cT = static_cast<float>(1.4426950408889634 / static_cast<double>(p.temperature));  // log2(e) / T
+  const double cT = 1.4426950408889634 / static_cast<double>(p.temperature);  // log2(e) / T
+  r.cT = static_cast<float>(cT);
+  r.cT_lo = static_cast<float>(cT - static_cast<double>(r.cT));
   r.invT = 1.0 / static_cast<double>(p.temperature);
   r.k = (p.top_k >= V) ? 0 : p.top_k;
   r.top_p = p.top_p;
+  (void)dt;
   r.path = (r.k >= 1 && r.k <= kSmallK) ? PATH_STREAM : PATH_FULL;
   int sh = 62 - bit_length(static_cast<uint32_t>(V));
   r.fixed_shift = sh < 24 ? 24 : (sh > 40 ? 40 : sh);
@@ -694,7 +723,7 @@ SampleLayout sample_layout(int B, int G, const RowParams& tp, const RowParams& d
 bool shape_ok(int B, int G, int V) {
   if (B < 1 || G < 0 || V < 1) return false;
   const long long slots = 2LL * G + 1;
-  return static_cast<long long>(B) * slots <= 0x7fffffffLL && G < (1 << 20);
+  return static_cast<long long>(B) * slots <= 0x7fffffffLL;
 }
 
 template <typename K>
@@ -724,8 +753,9 @@ spec_status_t spec_verify_workspace_size(int32_t batch, int32_t gamma_max, int32
                                          spec_sampling_params_t draft_params, size_t* bytes) {
   if (!bytes || !shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
     return SPEC_ERR_INVALID_ARG;
-  *bytes = sample_layout(batch, gamma_max, make_row_params(target_params, vocab),
-                         make_row_params(draft_params, vocab)).total;
+  if (gamma_max > kMaxGamma) return SPEC_ERR_UNSUPPORTED;
+  *bytes = sample_layout(batch, gamma_max, make_row_params(target_params, vocab, SPEC_BF16),
+                         make_row_params(draft_params, vocab, SPEC_BF16)).total;
   return SPEC_OK;
 }
 
@@ -750,6 +780,7 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
   if (!shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
     return SPEC_ERR_INVALID_ARG;
+  if (gamma_max > kMaxGamma) return SPEC_ERR_UNSUPPORTED;
   if (!target_logits || !u_sample || !out_tokens || !out_num_accepted || !workspace) return SPEC_ERR_INVALID_ARG;
   if (gamma_max > 0 && (!draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
   const size_t es = elem_bytes(dtype);
@@ -760,8 +791,8 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
       !aligned_to(workspace, kAlign))
     return SPEC_ERR_MISALIGNED;
   SampleArgs a;
-  a.tp = make_row_params(target_params, vocab);
-  a.dp = make_row_params(draft_params, vocab);
+  a.tp = make_row_params(target_params, vocab, dtype);
+  a.dp = make_row_params(draft_params, vocab, dtype);
   const SampleLayout L = sample_layout(batch, gamma_max, a.tp, a.dp);
   if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -855,7 +886,7 @@ spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32
   const size_t es = elem_bytes(dtype);
   if (!aligned_to(logits, es) || !aligned_to(out_probs, 4) || !aligned_to(out_row_status, 4))
     return SPEC_ERR_MISALIGNED;
-  const RowParams P = make_row_params(params, vocab);
+  const RowParams P = make_row_params(params, vocab, dtype);
   const int aligned = (vocab % elems_per_vec(dtype) == 0) && aligned_to(logits, 16);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const char* lg = static_cast<const char*>(logits);
@@ -875,3 +906,6 @@ spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32
 }
 
 }  // extern "C"
+
+// Five row CTAs must fit on one SM (228 KB of shared memory, 1 KB reserved per CTA).
+static_assert(5 * (sizeof(sv::Smem) + 1024) <= 228 * 1024, "row CTA shared memory too large for 5 CTAs per SM");

@@ -12,12 +12,15 @@
 
 namespace sv {
 
-constexpr int kThreads = 512;               // threads per row CTA
+constexpr int kThreads = 256;               // threads per row CTA
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSmallK = 128;                // streaming top-k path handles 1 <= k <= kSmallK
-constexpr int kWarpCap = 256;               // per-warp candidate buffer (entries)
+constexpr int kCandCap = 1024;              // streaming top-k path: candidate buffer (entries)
+constexpr int kMaxFull = 32;                // streaming top-k path: threads re-read cooperatively
+constexpr int kStreamUnroll = 4;            // streaming top-k path: 16-byte loads in flight per thread
 constexpr int kListCap = kSmallK;           // kept-list entries stored per row
+constexpr int kMaxGamma = 63;               // largest gamma_max the sampling verifier accepts
 constexpr int kUnroll = 4;                  // 16-byte loads in flight per thread
 
 enum { DT_BF16 = 0, DT_F32 = 1 };
@@ -58,6 +61,20 @@ __device__ __forceinline__ float fast_exp2(float t) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
   return r;
+}
+
+// exp((z - m) / T) written as 2^((z - m) cT) with cT = cT_hi + cT_lo.  The
+// difference d = z - m is carried exactly as d_hi + d_lo (two-sum) and the
+// exponent as t_hi + t_lo, so the only significant error left is exp2f's own
+// (2 ulp): 2^(t_hi + t_lo) = 2^t_hi (1 + t_lo ln 2) to first order in t_lo.
+__device__ __forceinline__ float exp2_diff(float z, float m, float cT_hi, float cT_lo) {
+  const float d = z - m;                      // two-sum of z + (-m): d + d_lo == z - m exactly
+  const float bb = d - z;
+  const float d_lo = (z - (d - bb)) + (-m - bb);
+  const float t = d * cT_hi;
+  const float t_lo = fmaf(d, cT_hi, -t) + fmaf(d, cT_lo, d_lo * cT_hi);
+  const float e = exp2f(t);
+  return fmaf(e, t_lo * 0.6931471805599453f, e);
 }
 
 // ---------------------------------------------------------------- loads

@@ -31,9 +31,12 @@
 
 namespace sv {
 
+static_assert(kThreads >= 256 && kThreads % 32 == 0, "block-wide 256-bin histograms assume at least 256 threads");
+
 struct RowParams {
   float T;          // temperature (> 0)
   float cT;         // log2(e) / T as float: 2^((z - m) * cT) = exp((z - m) / T)
+  float cT_lo;      // log2(e) / T - cT (the float rounding error of cT)
   double invT;      // 1 / T in float64
   int k;            // top-k, 0 = off (the host maps k >= V to 0)
   float top_p;      // 1 = off
@@ -62,10 +65,6 @@ struct __align__(16) ListEntry {  // one kept token of a PATH_STREAM row
 };
 
 // ------------------------------------------------------------------ shared memory
-struct __align__(16) SmemStream {
-  uint64_t wbuf[kWarps][kWarpCap];   // per-warp candidate buffers
-  uint32_t whist[kWarps][256];       // per-warp radix histograms
-};
 struct __align__(16) SmemFull {
   unsigned long long mass[256];
   unsigned long long mx[256];
@@ -80,19 +79,25 @@ struct __align__(16) SmemEpi {
   int32_t qtok[kListCap];            // draft kept list sorted by token (binary search)
   double qp[kListCap];
   double wtot[kWarps];               // per-warp segment totals of the block scan
+  RowStat rs[2 * kMaxGamma + 1];     // the sequence's row summaries
+  int32_t dtok[kMaxGamma];
+  float uacc[kMaxGamma];
 };
 struct __align__(16) Smem {
   union {
-    SmemStream s;
     SmemFull f;
     SmemEpi e;
   } u;
+  uint64_t cand[kCandCap];           // PATH_STREAM: candidates (composites >= the lower bound)
   uint64_t sorted[kSmallK];          // PATH_STREAM: top-k in descending order
   uint64_t topk[kSmallK];
   int32_t list_tok[kListCap];
   double list_p[kListCap];
   int nw[kWarps];
-  unsigned long long shared_thr;      // PATH_STREAM: CTA-wide admission threshold
+  int ncand;
+  int nfull;                         // PATH_STREAM: threads whose vectors need a full re-read
+  int16_t full[kMaxFull];
+  uint32_t tmax[kThreads];           // PATH_STREAM: per-thread maxima (keys)
   float red_f[kWarps];
   double red_d[kWarps];
   uint64_t red_u[kWarps];
@@ -184,66 +189,6 @@ __device__ __forceinline__ void pick_digit_mass(const unsigned long long* mass, 
   before = shfl_u64(bf, L);
 }
 
-// ------------------------------------------------------------------ warp radix select
-// k-th largest (1-based) of buf[0..n), n >= k, composites unique.
-__device__ __noinline__ uint64_t warp_select_kth(const uint64_t* buf, int n, int k, uint32_t* hist, int lane) {
-  uint64_t prefix = 0, mask = 0;
-  uint32_t need = static_cast<uint32_t>(k);
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int d = lane; d < 256; d += 32) hist[d] = 0u;
-    __syncwarp();
-    for (int e = lane; e < n; e += 32) {
-      const uint64_t c = buf[e];
-      if ((c & mask) == prefix) atomicAdd(&hist[(c >> shift) & 255u], 1u);
-    }
-    __syncwarp();
-    int digit;
-    uint32_t before;
-    pick_digit_count(hist, need, true, lane, digit, before);
-    const uint32_t cd = hist[digit];
-    need -= before;
-    prefix |= static_cast<uint64_t>(digit) << shift;
-    mask |= 0xffull << shift;
-    __syncwarp();
-    if (cd == 1u) {
-      for (int s = 0; s < n; s += 32) {
-        const int e = s + lane;
-        const bool hit = e < n && (buf[e] & mask) == prefix;
-        const unsigned bal = __ballot_sync(kFull, hit);
-        if (bal) {
-          const int L = __ffs(bal) - 1;
-          return shfl_u64(hit ? buf[e] : 0ull, L);
-        }
-      }
-      return prefix;
-    }
-  }
-  return prefix;
-}
-
-// Keeps the k largest entries of buf[0..n) (n > k) and raises the threshold.
-__device__ __noinline__ void warp_refresh(uint64_t* buf, int& n, int k, uint32_t* hist, int lane,
-                             uint64_t& thr, float& thr_val) {
-  __syncwarp();
-  const uint64_t kth = warp_select_kth(buf, n, k, hist, lane);
-  int m = 0;
-  for (int s = 0; s < n; s += 32) {
-    const int e = s + lane;
-    const uint64_t c = e < n ? buf[e] : 0ull;
-    const bool keep = e < n && c >= kth;
-    const unsigned bal = __ballot_sync(kFull, keep);
-    __syncwarp();
-    if (keep) buf[m + __popc(bal & lanemask_lt())] = c;
-    m += __popc(bal);
-    __syncwarp();
-  }
-  n = m;
-  if (kth > thr) {
-    thr = kth;
-    thr_val = comp_value(kth);
-  }
-}
-
 // ------------------------------------------------------------------ block reductions
 __device__ __forceinline__ float block_max_f(float v, Smem& sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -324,263 +269,6 @@ __device__ void greedy_row(const Row& row, Smem& sm, int& argmax, int& status) {
   const int any_bad = block_or(bad ? 1 : 0, sm);
   status = any_bad ? SEQ_NONFINITE : (top == 0ull ? SEQ_EMPTY_SUPPORT : SEQ_OK);
   argmax = top == 0ull ? -1 : static_cast<int>(comp_index(top));
-}
-
-// ------------------------------------------------------------------ PATH_STREAM
-// Per-warp filter state: an element is a candidate iff its composite beats thr.
-struct WarpFilter {
-  uint64_t thr;
-  float thr_val;   // value of thr's key: a candidate has x >= thr_val (cheap pre-test)
-  int n;           // entries in the warp's candidate buffer
-};
-
-// Overflow path of the streaming filter: admits one element slot at a time and
-// cuts the buffer back to the warp's k best (warp radix select) whenever it
-// would overflow, raising the threshold; the new threshold is also offered to
-// the whole CTA (the largest of the warps' k-th values is a lower bound for the
-// row's k-th largest).
-template <int DT>
-__device__ __noinline__ void admit_slots(const uint4 r, const int cnt, const int v, const bool maybe,
-                                         uint64_t* buf, uint32_t* hist, const int k, WarpFilter& f,
-                                         unsigned long long* shared_thr, const int lane) {
-  constexpr int PER = Elem<DT>::kPer;
-  float x[PER];
-  unpack<DT>(r, x);
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const uint64_t c = composite(fkey(x[e]), static_cast<uint32_t>(v * PER + e));
-    bool cand = maybe && e < cnt && !(x[e] != x[e]) && c > f.thr;
-    unsigned bal = __ballot_sync(kFull, cand);
-    if (bal) {
-      if (f.n + __popc(bal) > kWarpCap) {
-        warp_refresh(buf, f.n, k, hist, lane, f.thr, f.thr_val);
-        if (lane == 0) atomicMax(shared_thr, static_cast<unsigned long long>(f.thr));
-        cand = cand && c > f.thr;
-        bal = __ballot_sync(kFull, cand);
-      }
-      if (cand) buf[f.n + __popc(bal & lanemask_lt())] = c;
-      f.n += __popc(bal);
-    }
-  }
-}
-
-// Slow path of the streaming filter, taken when some lane's vector may hold a
-// candidate: each lane marks its candidates, one warp scan places them all.
-template <int DT>
-__device__ __noinline__ void admit_vector(const uint4 r, const int cnt, const int v, const bool maybe,
-                                          uint64_t* buf, uint32_t* hist, const int k, WarpFilter& f,
-                                          unsigned long long* shared_thr, const int lane) {
-  constexpr int PER = Elem<DT>::kPer;
-  float x[PER];
-  unpack<DT>(r, x);
-  uint32_t m = 0;
-  uint64_t c[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    c[e] = composite(fkey(x[e]), static_cast<uint32_t>(v * PER + e));
-    if (maybe && e < cnt && x[e] >= f.thr_val && c[e] > f.thr) m |= 1u << e;   // NaN fails x >= thr_val
-  }
-  const uint32_t mine = __popc(m);
-  const uint32_t incl = warp_incl_scan_u32(mine, lane);
-  const int total = static_cast<int>(__shfl_sync(kFull, incl, 31));
-  if (f.n + total > kWarpCap) {
-    admit_slots<DT>(r, cnt, v, maybe, buf, hist, k, f, shared_thr, lane);
-    return;
-  }
-  int pos = f.n + static_cast<int>(incl - mine);
-#pragma unroll
-  for (int e = 0; e < PER; ++e)
-    if (m & (1u << e)) buf[pos++] = c[e];
-  f.n += total;
-}
-
-// Block merge of the warps' survivors, sort, float64 softmax and top-p cut.
-template <int DT>
-__device__ __noinline__ void stream_finish(const RowParams& P, const int dtok, const int any_bad, Smem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = P.k;
-  // ---- block merge: the k largest of the warps' survivors
-  int total = 0;
-  for (int w = 0; w < kWarps; ++w) total += sm.nw[w];
-  uint64_t kth = 0;
-  if (total > k) {
-    uint32_t* bh = sm.u.s.whist[0];
-    uint64_t prefix = 0, mask = 0;
-    uint32_t need = static_cast<uint32_t>(k);
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      if (tid < 256) bh[tid] = 0u;
-      __syncthreads();
-      for (int e = tid; e < kWarps * kSmallK; e += kThreads) {
-        const int w = e / kSmallK, j = e % kSmallK;
-        if (j < sm.nw[w]) {
-          const uint64_t c = sm.u.s.wbuf[w][j];
-          if ((c & mask) == prefix) atomicAdd(&bh[(c >> shift) & 255u], 1u);
-        }
-      }
-      __syncthreads();
-      if (warp == 0) {
-        int digit;
-        uint32_t before;
-        pick_digit_count(bh, need, true, lane, digit, before);
-        if (lane == 0) {
-          sm.b_i32[0] = digit;
-          sm.b_i32[1] = static_cast<int>(before);
-          sm.b_i32[2] = static_cast<int>(bh[digit]);
-        }
-      }
-      __syncthreads();
-      const int digit = sm.b_i32[0];
-      need -= static_cast<uint32_t>(sm.b_i32[1]);
-      const int cd = sm.b_i32[2];
-      prefix |= static_cast<uint64_t>(digit) << shift;
-      mask |= 0xffull << shift;
-      __syncthreads();
-      if (cd == 1) break;
-    }
-    // the k-th is the smallest survivor matching the final prefix (unique when cd == 1)
-    if (tid == 0) sm.b_u64[0] = ~0ull;
-    __syncthreads();
-    for (int e = tid; e < kWarps * kSmallK; e += kThreads) {
-      const int w = e / kSmallK, j = e % kSmallK;
-      if (j < sm.nw[w]) {
-        const uint64_t c = sm.u.s.wbuf[w][j];
-        if ((c & mask) == prefix) atomicMin(reinterpret_cast<unsigned long long*>(&sm.b_u64[0]),
-                                            static_cast<unsigned long long>(c));
-      }
-    }
-    __syncthreads();
-    kth = sm.b_u64[0];
-  }
-  if (tid == 0) sm.b_i32[3] = 0;
-  __syncthreads();
-  for (int e = tid; e < kWarps * kSmallK; e += kThreads) {
-    const int w = e / kSmallK, j = e % kSmallK;
-    if (j < sm.nw[w]) {
-      const uint64_t c = sm.u.s.wbuf[w][j];
-      if (c >= kth) sm.topk[atomicAdd(&sm.b_i32[3], 1)] = c;
-    }
-  }
-  __syncthreads();
-  const int ntop = sm.b_i32[3];
-  // rank sort, descending
-  if (tid < ntop) {
-    const uint64_t c = sm.topk[tid];
-    int rank = 0;
-    for (int j = 0; j < ntop; ++j) rank += sm.topk[j] > c ? 1 : 0;
-    sm.sorted[rank] = c;
-  }
-  __syncthreads();
-
-  // ---- float64 softmax over the survivors, top-p cut, kept list (warp 0)
-  if (warp == 0) {
-    RowStat st;
-    st.path = PATH_STREAM;
-    st.cut = 0;
-    st.argmax = ntop ? static_cast<int>(comp_index(sm.sorted[0])) : -1;
-    const float m = ntop ? comp_value(sm.sorted[0]) : -__int_as_float(0x7f800000);
-    st.m = m;
-    st.status = any_bad ? SEQ_NONFINITE : ((ntop == 0 || !(m > -__int_as_float(0x7f800000))) ? SEQ_EMPTY_SUPPORT : SEQ_OK);
-    st.W = 0.0;
-    st.p_tok = 0.0;
-    st.n_list = 0;
-    if (st.status == SEQ_OK) {
-      double w[4];
-      double s = 0.0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int pos = 4 * lane + j;
-        w[j] = 0.0;
-        if (pos < ntop) {
-          const double z = static_cast<double>(comp_value(sm.sorted[pos]));
-          w[j] = exp((z - static_cast<double>(m)) * P.invT);
-        }
-        s += w[j];
-      }
-      const double incl = warp_incl_scan_f64(s, lane);
-      const double S = __shfl_sync(kFull, incl, 31);
-      int n_keep = ntop;
-      if (P.top_p < 1.0f) {
-        double acc = incl - s;
-        int first = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int pos = 4 * lane + j;
-          if (pos < ntop) {
-            acc += w[j];
-            if (first == 0x7fffffff && acc / S >= static_cast<double>(P.top_p)) first = pos;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(kFull, first, o));
-        n_keep = first == 0x7fffffff ? ntop : first + 1;
-      }
-      double part = 0.0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) part += (4 * lane + j < n_keep) ? w[j] : 0.0;
-      const double W = warp_sum_f64(part);
-      double ptok = 0.0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int pos = 4 * lane + j;
-        if (pos < n_keep) {
-          const int tok = static_cast<int>(comp_index(sm.sorted[pos]));
-          const double p = w[j] / W;
-          sm.list_tok[pos] = tok;
-          sm.list_p[pos] = p;
-          if (tok == dtok) ptok = p;
-        }
-      }
-      ptok = warp_sum_f64(ptok);
-      st.W = W;
-      st.p_tok = ptok;
-      st.n_list = n_keep;
-    }
-    if (lane == 0) sm.st = st;
-  }
-  __syncthreads();
-}
-
-// One HBM pass; leaves the kept list (descending order) in sm.list_tok/list_p.
-template <int DT>
-__device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = P.k;
-  uint64_t* buf = sm.u.s.wbuf[warp];
-  uint32_t* hist = sm.u.s.whist[warp];
-  WarpFilter f;
-  f.thr = 0;
-  f.thr_val = -__int_as_float(0x7f800000);
-  f.n = 0;
-  bool bad = false;
-  if (tid == 0) sm.shared_thr = 0ull;
-  __syncthreads();
-
-  for (int base = 0; base < row.nvec; base += kThreads * kUnroll) {
-    uint4 r[kUnroll];
-    int cnt[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) cnt[u] = load_vec<DT, true>(row, base + u * kThreads + tid, r[u]);
-    // adopt the CTA-wide threshold (warp-uniform: lane 0's read is broadcast)
-    const uint64_t s = shfl_u64(lane == 0 ? *reinterpret_cast<volatile unsigned long long*>(&sm.shared_thr) : 0ull, 0);
-    if (s > f.thr) {
-      f.thr = s;
-      f.thr_val = comp_value(s);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      bool vb = false;
-      const float vm = cnt[u] ? vec_max<DT>(r[u], cnt[u], vb) : -__int_as_float(0x7f800000);
-      bad |= vb;
-      const bool maybe = cnt[u] > 0 && vm >= f.thr_val;
-      if (__any_sync(kFull, maybe))
-        admit_vector<DT>(r[u], cnt[u], base + u * kThreads + tid, maybe, buf, hist, k, f, &sm.shared_thr, lane);
-    }
-  }
-  __syncwarp();
-  if (f.n > k) warp_refresh(buf, f.n, k, hist, lane, f.thr, f.thr_val);
-  if (lane == 0) sm.nw[warp] = f.n;
-  const int any_bad = block_or(bad ? 1 : 0, sm);   // also orders the nw writes
-  stream_finish<DT>(P, dtok, any_bad, sm);
 }
 
 // ------------------------------------------------------------------ PATH_FULL
@@ -944,6 +632,298 @@ __device__ void full_row(const Row& row, const RowParams& P, int dtok, Smem& sm)
   }
   if (tid == 0) sm.st = st;
   __syncthreads();
+}
+
+// ------------------------------------------------------------------ PATH_STREAM
+// k-th largest (1-based) composite of the contiguous shared buffer buf[0..n),
+// n > k, by a block-wide MSB-first radix select (counts in sm.u.f.cnt).
+__device__ __noinline__ uint64_t block_select_kth(const uint64_t* buf, int n, int k, Smem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t prefix = 0, mask = 0;
+  uint32_t need = static_cast<uint32_t>(k);
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    if (tid < 256) { sm.u.f.cnt[tid] = 0u; sm.u.f.mx[tid] = 0ull; }
+    __syncthreads();
+    for (int e = tid; e < n; e += kThreads) {
+      const uint64_t c = buf[e];
+      if ((c & mask) == prefix) {
+        const int d = static_cast<int>((c >> shift) & 255u);
+        atomicAdd(&sm.u.f.cnt[d], 1u);
+        atomicMax(&sm.u.f.mx[d], static_cast<unsigned long long>(c));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int digit;
+      uint32_t before;
+      pick_digit_count(sm.u.f.cnt, need, true, lane, digit, before);
+      if (lane == 0) {
+        sm.b_i32[0] = digit;
+        sm.b_i32[1] = static_cast<int>(before);
+        sm.b_i32[2] = static_cast<int>(sm.u.f.cnt[digit]);
+        sm.b_u64[0] = sm.u.f.mx[digit];
+      }
+    }
+    __syncthreads();
+    const int digit = sm.b_i32[0];
+    need -= static_cast<uint32_t>(sm.b_i32[1]);
+    const int cd = sm.b_i32[2];
+    const uint64_t mx = sm.b_u64[0];
+    prefix |= static_cast<uint64_t>(digit) << shift;
+    mask |= 0xffull << shift;
+    __syncthreads();
+    if (cd == 1) return mx;
+  }
+  return prefix;
+}
+
+// Appends every element of the row whose composite is >= lo into sm.cand
+// (a re-read of the whole row; used only when the candidate buffer overflowed).
+template <int DT>
+__device__ __noinline__ void collect_at_least(const Row& row, uint64_t lo, Smem& sm) {
+  constexpr int P = Elem<DT>::kPer;
+  if (threadIdx.x == 0) sm.ncand = 0;
+  __syncthreads();
+  for (int v = threadIdx.x; v < row.nvec; v += kThreads) {
+    uint4 r;
+    const int c = load_vec<DT, false>(row, v, r);
+    float x[P];
+    unpack<DT>(r, x);
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+      if (e >= c) continue;
+      const uint64_t cc = composite(fkey(x[e]), static_cast<uint32_t>(v * P + e));
+      if (cc >= lo) {
+        const int pos = atomicAdd(&sm.ncand, 1);
+        if (pos < kCandCap) sm.cand[pos] = cc;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// From the candidates in sm.cand (a superset of the row's top-k): the exact
+// top-k in descending order, then float64 softmax over them, the top-p cut
+// and the kept list [wrblog §7.2, §7.3].
+template <int DT>
+__device__ __noinline__ void stream_finish(const Row& row, const RowParams& P, const int dtok,
+                                           const int any_bad, float m_row, Smem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = P.k;
+  int n_c = sm.ncand;
+  if (!any_bad && n_c > kCandCap) {
+    // adversarial row (e.g. long runs of equal logits): exact selection by radix rounds
+    const uint64_t ck = full_select_topk<DT>(row, m_row, P.cT, k, sm);
+    collect_at_least<DT>(row, ck, sm);
+    n_c = min(sm.ncand, kCandCap);
+  }
+  int ntop = 0;
+  if (!any_bad) {
+    const uint64_t* src = sm.cand;
+    int nsrc = n_c;
+    if (n_c > kThreads) {       // narrow to exactly k before the quadratic rank sort
+      const uint64_t kth = block_select_kth(sm.cand, n_c, k, sm);
+      if (tid == 0) sm.b_i32[3] = 0;
+      __syncthreads();
+      for (int e = tid; e < n_c; e += kThreads) {
+        const uint64_t c = sm.cand[e];
+        if (c >= kth) sm.topk[atomicAdd(&sm.b_i32[3], 1)] = c;
+      }
+      __syncthreads();
+      src = sm.topk;
+      nsrc = sm.b_i32[3];
+    }
+    ntop = min(nsrc, k);
+    if (warp == 0) {            // rank sort, descending; keep ranks < k
+      for (int e = lane; e < nsrc; e += 32) {
+        const uint64_t c = src[e];
+        int rank = 0;
+        for (int j = 0; j < nsrc; ++j) rank += src[j] > c ? 1 : 0;
+        if (rank < k) sm.sorted[rank] = c;
+      }
+      __syncwarp();
+    }
+  }
+
+  // ---- softmax over the top-k, top-p cut, kept list (warp 0).  Each weight
+  // exp((z - m) / T) = 2^((z - m) cT) is evaluated from the exact difference
+  // z - m (two-sum) and a hi/lo split of the exponent, so its error is that of
+  // exp2f (2 ulp); sums, prefix sums and the normaliser are accumulated in
+  // float64 (additions only).
+  if (warp == 0) {
+    RowStat st;
+    st.path = PATH_STREAM;
+    st.cut = 0;
+    st.argmax = ntop ? static_cast<int>(comp_index(sm.sorted[0])) : -1;
+    const float m = ntop ? comp_value(sm.sorted[0]) : -__int_as_float(0x7f800000);
+    st.m = m;
+    st.status = any_bad ? SEQ_NONFINITE
+                        : ((ntop == 0 || !(m > -__int_as_float(0x7f800000))) ? SEQ_EMPTY_SUPPORT : SEQ_OK);
+    st.W = 0.0;
+    st.p_tok = 0.0;
+    st.n_list = 0;
+    if (st.status == SEQ_OK) {
+      float w[4];
+      double s = 0.0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int pos = 4 * lane + j;
+        w[j] = 0.0f;
+        if (pos < ntop) w[j] = exp2_diff(comp_value(sm.sorted[pos]), m, P.cT, P.cT_lo);
+        s += static_cast<double>(w[j]);
+      }
+      const double incl = warp_incl_scan_f64(s, lane);
+      const double S = __shfl_sync(kFull, incl, 31);
+      int n_keep = ntop;
+      if (P.top_p < 1.0f) {
+        const double target = static_cast<double>(P.top_p) * S;   // cum / S >= top_p
+        double acc = incl - s;
+        int first = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int pos = 4 * lane + j;
+          if (pos < ntop) {
+            acc += static_cast<double>(w[j]);
+            if (first == 0x7fffffff && acc >= target) first = pos;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(kFull, first, o));
+        n_keep = first == 0x7fffffff ? ntop : first + 1;
+      }
+      double part = 0.0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) part += (4 * lane + j < n_keep) ? static_cast<double>(w[j]) : 0.0;
+      const double W = warp_sum_f64(part);
+      const double invW = 1.0 / W;
+      double ptok = 0.0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int pos = 4 * lane + j;
+        if (pos < n_keep) {
+          const int tok = static_cast<int>(comp_index(sm.sorted[pos]));
+          const double p = static_cast<double>(w[j]) * invW;
+          sm.list_tok[pos] = tok;
+          sm.list_p[pos] = p;
+          if (tok == dtok) ptok = p;
+        }
+      }
+      st.W = W;
+      st.p_tok = warp_sum_f64(ptok);
+      st.n_list = n_keep;
+    }
+    if (lane == 0) sm.st = st;
+  }
+  __syncthreads();
+}
+
+// Appends the elements of vector v whose key is >= K to sm.cand (c = valid count).
+template <int DT>
+__device__ __forceinline__ void append_from_vector(const uint4& r, int c, int v, uint32_t K, Smem& sm) {
+  constexpr int P = Elem<DT>::kPer;
+  float x[P];
+  unpack<DT>(r, x);
+#pragma unroll
+  for (int e = 0; e < P; ++e) {
+    const uint32_t key = fkey(x[e]);
+    if (e < c && key >= K && !(x[e] != x[e])) {
+      const int pos = atomicAdd(&sm.ncand, 1);
+      if (pos < kCandCap) sm.cand[pos] = composite(key, static_cast<uint32_t>(v * P + e));
+    }
+  }
+}
+
+// PATH_STREAM row (1 <= k <= kSmallK).  Pass 1 streams the row from HBM once.
+// Each thread keeps the keys and positions of its four largest vector maxima
+// .  The k-th largest of the per-thread maxima is a lower bound K for
+// the row's k-th largest element (k distinct elements reach it), found bit by
+// bit with block-wide counts.  Only vectors whose maximum reaches K can hold a
+// top-k element: a thread re-reads its tracked ones in one round trip, or all
+// its groups when all four tracked vectors qualify (there may be more).  The
+// collected elements >= K are a small superset of the top-k.
+template <int DT>
+__device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& sm) {
+  const int tid = threadIdx.x;
+  constexpr int step = kThreads * kStreamUnroll;
+  const int iters = (row.nvec + step - 1) / step;
+  uint32_t mk0 = 0u, mk1 = 0u, mk2 = 0u, mk3 = 0u;      // four largest vector-max keys, descending
+  int mv0 = 0, mv1 = 0, mv2 = 0, mv3 = 0;               // their vector indices
+  bool bad = false;
+  for (int it = 0; it < iters; ++it) {
+    uint4 r[kStreamUnroll];
+    int cnt[kStreamUnroll];
+#pragma unroll
+    for (int u = 0; u < kStreamUnroll; ++u) cnt[u] = load_vec<DT, true>(row, it * step + u * kThreads + tid, r[u]);
+#pragma unroll
+    for (int u = 0; u < kStreamUnroll; ++u) {
+      if (cnt[u]) {
+        bool vb;
+        const uint32_t vk = fkey(vec_max<DT>(r[u], cnt[u], vb));
+        bad |= vb;
+        if (vk > mk3) {                                  // insert, keeping earlier vectors first on ties
+          const int v = it * step + u * kThreads + tid;
+          const bool g0 = vk > mk0, g1 = vk > mk1, g2 = vk > mk2;
+          mk3 = g2 ? mk2 : vk;                 mv3 = g2 ? mv2 : v;
+          mk2 = g2 ? (g1 ? mk1 : vk) : mk2;   mv2 = g2 ? (g1 ? mv1 : v) : mv2;
+          mk1 = g1 ? (g0 ? mk0 : vk) : mk1;   mv1 = g1 ? (g0 ? mv0 : v) : mv1;
+          mk0 = g0 ? vk : mk0;                 mv0 = g0 ? v : mv0;
+        }
+      }
+    }
+  }
+  sm.tmax[tid] = mk0;
+  const int any_bad = __syncthreads_or(bad ? 1 : 0);
+  if ((tid >> 5) == 0) {
+    // one warp searches the k-th largest of the kThreads maxima, bit by bit
+    const int lane = tid & 31;
+    uint32_t v[kThreads / 32];
+#pragma unroll
+    for (int j = 0; j < kThreads / 32; ++j) v[j] = sm.tmax[j * 32 + lane];
+    uint32_t K = 0u;
+    for (int bit = 31; bit >= (DT == DT_BF16 ? 16 : 0); --bit) {
+      const uint32_t c = K | (1u << bit);
+      uint32_t n = 0;
+#pragma unroll
+      for (int j = 0; j < kThreads / 32; ++j) n += v[j] >= c ? 1u : 0u;
+      if (__reduce_add_sync(kFull, n) >= static_cast<uint32_t>(P.k)) K = c;
+    }
+    if (lane == 0) {
+      sm.b_i32[4] = static_cast<int>(K);
+      sm.ncand = 0;
+      sm.nfull = 0;
+    }
+  }
+  __syncthreads();
+  const uint32_t K = static_cast<uint32_t>(sm.b_i32[4]);
+  if (!any_bad && mk3 != 0u && mk3 >= K) {
+    // every tracked vector qualifies and more may: the CTA re-reads all of them below
+    const int pos = atomicAdd(&sm.nfull, 1);
+    if (pos < kMaxFull) sm.full[pos] = tid;
+  } else if (!any_bad && mk0 != 0u && mk0 >= K) {
+    uint4 r0, r1, r2;
+    const int c0 = load_vec<DT, false>(row, mv0, r0);
+    const int c1 = (mk1 != 0u && mk1 >= K) ? load_vec<DT, false>(row, mv1, r1) : 0;
+    const int c2 = (mk2 != 0u && mk2 >= K) ? load_vec<DT, false>(row, mv2, r2) : 0;
+    append_from_vector<DT>(r0, c0, mv0, K, sm);
+    if (c1) append_from_vector<DT>(r1, c1, mv1, K, sm);
+    if (c2) append_from_vector<DT>(r2, c2, mv2, K, sm);
+  }
+  __syncthreads();
+  const int nfull = sm.nfull;
+  if (nfull > 0) {
+    // cooperative re-read: one vector per job, jobs spread over the whole CTA
+    const int per = (row.nvec + kThreads - 1) / kThreads;       // vectors per thread
+    const bool all = nfull > kMaxFull;                           // too many: re-read the whole row
+    const int jobs = all ? row.nvec : nfull * per;
+    for (int job = tid; job < jobs; job += kThreads) {
+      const int v = all ? job : sm.full[job / per] + (job % per) * kThreads;
+      uint4 r;
+      const int c = load_vec<DT, false>(row, v, r);
+      if (c) append_from_vector<DT>(r, c, v, K, sm);
+    }
+    __syncthreads();
+  }
+  stream_finish<DT>(row, P, dtok, any_bad, 0.0f, sm);
 }
 
 // Probability of token x under a PATH_FULL row given its logit z.

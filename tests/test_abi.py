@@ -99,6 +99,7 @@ def test_host_validation_before_any_launch(lib):
     assert call(tgt=fake + 1) == _lib.SPEC_ERR_MISALIGNED
     assert call(ws=fake + 16) == _lib.SPEC_ERR_MISALIGNED
     assert call(wsb=16) == _lib.SPEC_ERR_WORKSPACE
+    assert call(G=64) == _lib.SPEC_ERR_UNSUPPORTED        # sampling supports gamma_max <= 63
     assert _lib.spec_verify_greedy(None, 0, fake, None, 2, 3, 64, fake, 1 << 30, fake, fake, None, None) \
         == _lib.SPEC_ERR_INVALID_ARG
     assert _lib.spec_verify_greedy(fake, 0, fake, None, 2, 3, 64, fake, 8, fake, fake, None, None) \
