@@ -143,3 +143,40 @@ def transform_probs(logits: torch.Tensor, params: SamplingParams,
                                    _ptr(status), _stream(stream))
     _lib.check("spec_transform_probs", st)
     return probs.reshape(*logits.shape[:-1], V), status.reshape(logits.shape[:-1])
+
+
+class BoundSample:
+    """A spec_verify_sample call with its buffers marshalled once.
+
+    For serving loops that reuse the same device buffers every step: the
+    arguments are validated and converted at construction, and each call is one
+    C-ABI call on the stream current at construction (or the one given).
+    Writes into ``self.out``; raises on a non-zero status.
+    """
+
+    def __init__(self, target_logits, draft_logits, draft_tokens, u_accept, u_sample,
+                 target: SamplingParams, draft: SamplingParams, gamma_per_seq=None,
+                 draft_is_onehot=None, workspace=None, out=None, stream=None):
+        B, G1, V = target_logits.shape
+        G = G1 - 1
+        dev = target_logits.device
+        if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+            raise TypeError("target and draft logits must share a dtype")
+        self.workspace = workspace if workspace is not None else new_workspace(
+            workspace_size(B, G, V, target, draft), dev)
+        self.out = out if out is not None else alloc_outputs(B, G, dev)
+        self._keep = (target_logits, draft_logits, draft_tokens, u_accept, u_sample, gamma_per_seq,
+                      draft_is_onehot)
+        self._fn = _lib.load().spec_verify_sample
+        o = self.out
+        self._args = (_ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits),
+                      _ptr(draft_tokens), _ptr(gamma_per_seq), _ptr(draft_is_onehot), _ptr(u_accept),
+                      _ptr(u_sample), target.c(), draft.c(), B, G, V, _ptr(self.workspace),
+                      self.workspace.numel(), _ptr(o.tokens), _ptr(o.num_accepted), _ptr(o.accept_prob),
+                      _ptr(o.residual_z), _ptr(o.status), _stream(stream))
+
+    def __call__(self) -> VerifyOutput:
+        st = self._fn(*self._args)
+        if st:
+            _lib.check("spec_verify_sample", st)
+        return self.out

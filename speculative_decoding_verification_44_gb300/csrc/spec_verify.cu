@@ -15,6 +15,7 @@
 #include "sv_row.cuh"
 #include "spec_verify.h"
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -726,11 +727,21 @@ bool shape_ok(int B, int G, int V) {
   return static_cast<long long>(B) * slots <= 0x7fffffffLL;
 }
 
+// Raises a kernel's dynamic shared memory limit once per device (the attribute
+// is per device; later calls only read an atomic bit mask).
 template <typename K>
-cudaError_t prepare(K kernel) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(Smem)));
+cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(Smem)));
+  if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return err;
 }
+std::atomic<uint64_t> g_ready[6];   // sample, greedy, transform x {bf16, f32}
 
 }  // namespace
 
@@ -821,10 +832,10 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (dtype == SPEC_BF16) {
-    err = prepare(sample_kernel<DT_BF16>);
+    err = prepare(sample_kernel<DT_BF16>, g_ready[0]);
     if (err == cudaSuccess) sample_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
   } else {
-    err = prepare(sample_kernel<DT_F32>);
+    err = prepare(sample_kernel<DT_F32>, g_ready[1]);
     if (err == cudaSuccess) sample_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
@@ -868,10 +879,10 @@ spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (dtype == SPEC_BF16) {
-    err = prepare(greedy_kernel<DT_BF16>);
+    err = prepare(greedy_kernel<DT_BF16>, g_ready[2]);
     if (err == cudaSuccess) greedy_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
   } else {
-    err = prepare(greedy_kernel<DT_F32>);
+    err = prepare(greedy_kernel<DT_F32>, g_ready[3]);
     if (err == cudaSuccess) greedy_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
@@ -893,11 +904,11 @@ spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32
   const size_t rb = static_cast<size_t>(vocab) * es;
   cudaError_t err;
   if (dtype == SPEC_BF16) {
-    err = prepare(transform_kernel<DT_BF16>);
+    err = prepare(transform_kernel<DT_BF16>, g_ready[4]);
     if (err == cudaSuccess)
       transform_kernel<DT_BF16><<<rows, kThreads, sizeof(Smem), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
   } else {
-    err = prepare(transform_kernel<DT_F32>);
+    err = prepare(transform_kernel<DT_F32>, g_ready[5]);
     if (err == cudaSuccess)
       transform_kernel<DT_F32><<<rows, kThreads, sizeof(Smem), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
   }
