@@ -196,6 +196,37 @@ SPEC_API spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dty
                                    int32_t vocab, spec_sampling_params_t params,
                                    float* out_probs, int32_t* out_row_status, void* stream);
 
+/* spec_verify_sample without a caller-provided workspace: for callers that
+ * cannot allocate device memory themselves -- for example a plugin hosted by an
+ * inference server whose device memory belongs to the server's own allocator,
+ * or a latency-critical path that must not pay cudaMalloc's device-wide
+ * synchronisation.  This entry point has no counterpart in the method's
+ * description; it only changes where the scratch memory comes from.
+ *
+ * The scratch is a fixed 8 MiB array inside the library's device image; every
+ * GPU that loads the library holds it until the process exits.  Requests whose
+ * workspace (spec_verify_workspace_size) exceeds 8 MiB return
+ * SPEC_ERR_WORKSPACE and launch nothing.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library routine is called.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Each call
+ * clears the scratch's counters with cudaMemsetAsync on `stream`, then runs
+ * spec_verify_sample on it.  All calls share the one array, which keeps the
+ * last call's contents: calls that overlap on the GPU (other streams, other
+ * host threads) race and must not be issued.  Other arguments, outputs and
+ * errors are as for spec_verify_sample. */
+SPEC_API spec_status_t spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                                                  spec_dtype_t dtype, const int32_t* draft_tokens,
+                                                  const int32_t* gamma_per_seq,
+                                                  const uint8_t* draft_is_onehot,
+                                                  const float* u_accept, const float* u_sample,
+                                                  spec_sampling_params_t target_params,
+                                                  spec_sampling_params_t draft_params,
+                                                  int32_t batch, int32_t gamma_max, int32_t vocab,
+                                                  int32_t* out_tokens, int32_t* out_num_accepted,
+                                                  float* out_accept_prob, float* out_residual_z,
+                                                  int32_t* out_status, void* stream);
+
 /* Static, NUL-terminated description of a spec_status_t. */
 SPEC_API const char* spec_status_string(spec_status_t status);
 

@@ -33,7 +33,8 @@ SPEC_F32 = 1
 
 # Every symbol include/spec_verify.h declares.
 EXPORTED = ("spec_verify_workspace_size", "spec_verify_sample", "spec_greedy_workspace_size",
-            "spec_verify_greedy", "spec_transform_probs", "spec_status_string")
+            "spec_verify_greedy", "spec_transform_probs", "spec_status_string",
+            "spec_verify_sample_noalloc")
 
 
 class spec_sampling_params_t(ctypes.Structure):
@@ -71,6 +72,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_sample.restype = ctypes.c_int
     lib.spec_verify_sample.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, i32, i32, i32,
                                        vp, sz, vp, vp, vp, vp, vp, vp]
+    lib.spec_verify_sample_noalloc.restype = ctypes.c_int
+    lib.spec_verify_sample_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, i32, i32, i32,
+                                               vp, vp, vp, vp, vp, vp]
     lib.spec_verify_greedy.restype = ctypes.c_int
     lib.spec_verify_greedy.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, i32, vp, sz, vp, vp, vp, vp]
     lib.spec_transform_probs.restype = ctypes.c_int
@@ -106,6 +110,10 @@ def spec_greedy_workspace_size(batch: int, gamma_max: int) -> int:
 
 def spec_verify_sample(*args) -> int:
     return load().spec_verify_sample(*args)
+
+
+def spec_verify_sample_noalloc(*args) -> int:
+    return load().spec_verify_sample_noalloc(*args)
 
 
 def spec_verify_greedy(*args) -> int:

@@ -920,3 +920,57 @@ spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32
 
 // Five row CTAs must fit on one SM (228 KB of shared memory, 1 KB reserved per CTA).
 static_assert(5 * (sizeof(sv::Smem) + 1024) <= 228 * 1024, "row CTA shared memory too large for 5 CTAs per SM");
+
+// ====================================================================== allocation-free variant
+// Scratch for spec_verify_sample_noalloc: a fixed-size array in the library's
+// own device memory, present on every GPU that loads the library until the
+// process exits.  All calls share it.
+namespace {
+
+constexpr size_t kStaticScratchBytes = 8u << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (host code only sees a stand-in symbol, never a usable pointer).
+std::atomic<void*> g_scratch_addr[64];
+
+cudaError_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    err = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (err != cudaSuccess) return err;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" SPEC_API spec_status_t spec_verify_sample_noalloc(
+    const void* target_logits, const void* draft_logits, spec_dtype_t dtype, const int32_t* draft_tokens,
+    const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot, const float* u_accept,
+    const float* u_sample, spec_sampling_params_t target_params, spec_sampling_params_t draft_params,
+    int32_t batch, int32_t gamma_max, int32_t vocab, int32_t* out_tokens, int32_t* out_num_accepted,
+    float* out_accept_prob, float* out_residual_z, int32_t* out_status, void* stream) {
+  size_t need = 0;
+  const spec_status_t st = spec_verify_workspace_size(batch, gamma_max, vocab, target_params,
+                                                      draft_params, &need);
+  if (st != SPEC_OK) return st;
+  if (need > kStaticScratchBytes) return SPEC_ERR_WORKSPACE;   // beyond the 8 MiB static scratch
+  void* scratch = nullptr;
+  if (static_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
+  // The per-sequence counters at the start of the scratch must be zero when the
+  // kernel starts; clear them on the caller's stream.
+  const size_t counters = static_cast<size_t>(batch) * sizeof(uint32_t);
+  if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return spec_verify_sample(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
+                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, batch,
+                            gamma_max, vocab, scratch, kStaticScratchBytes, out_tokens,
+                            out_num_accepted, out_accept_prob, out_residual_z, out_status, stream);
+}
