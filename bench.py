@@ -183,6 +183,27 @@ def oracle_sample_time(w, seqs, budget_s=None):
     return positions, elapsed, n
 
 
+def replica_ids(rank: int, rotate: int = ROTATE) -> list[int]:
+    """Input sets of one rank: independent batches, disjoint across ranks (weak scaling)."""
+    return [rank * rotate + r for r in range(rotate)]
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over all ranks (timing: the slowest rank defines the step)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return units_per_rank * world / (ms_per_step / 1e3)
+
+
 def run_reference(args, rank):
     """Reference arm: the float64 oracle on the host cores, one sequence per step."""
     if rank != 0:
@@ -233,8 +254,7 @@ def main():
     from speculative_decoding_verification_44_gb300 import workloads
 
     # independent batches: replica = rank * ROTATE + r
-    sets = [workloads.make(WID, dev, draft_probs=gpu_draft_probs, replica=rank * ROTATE + r)
-            for r in range(ROTATE)]
+    sets = [workloads.make(WID, dev, draft_probs=gpu_draft_probs, replica=rep) for rep in replica_ids(rank)]
     w0 = sets[0]
     B, G, V = w0.B, w0.G, w0.V
     rt, rd = w0.rows_used()
@@ -274,13 +294,9 @@ def main():
             dist.barrier()
     total_ms = t_all0.elapsed_time(t_all1)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / K
-    positions_per_step = rt * world
-    value = positions_per_step / (ms_per_step / 1e3)
+    value = whole_job_rate(rt, world, ms_per_step)
 
     # outcome statistics of the last step (emitted tokens / s etc.)
     last = outs[(K - 1) % ROTATE]
@@ -331,11 +347,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / Ke
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": rt * world / (e_ms / 1e3), "unit": "positions/s", "h2d_bytes_per_step": h2d,
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": whole_job_rate(rt, world, e_ms), "unit": "positions/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
     cpu_baseline = None

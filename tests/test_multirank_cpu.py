@@ -1,0 +1,49 @@
+"""World-size-2 checks of the multi-GPU host logic on CPU (gloo): the step
+shards by sequence with no data-path collective, each rank times its own
+independent batch, and the slowest rank's time defines the whole-job rate."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = 10.0 + rank * 5.0                        # rank 1 is the slow one
+        out[rank] = (bench.replica_ids(rank), bench.max_over_ranks(mine, world))
+    finally:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def test_two_rank_sharding_and_timing():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    ids0, t0 = res[0]
+    ids1, t1 = res[1]
+    assert set(ids0).isdisjoint(ids1)                   # independent batches per rank
+    assert len(ids0) == len(ids1) == 4
+    assert t0 == t1 == 15.0                             # both see the slowest rank's time
+    import bench
+    assert bench.whole_job_rate(384, 2, 0.05) == pytest.approx(384 * 2 / 5e-5)
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.replica_ids(0) == [0, 1, 2, 3]
