@@ -91,31 +91,31 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const double* p
 
 // Inverse-CDF draw over a PATH_STREAM target row's kept list (warp 0 only).
 // Residual weights max(0, p - q) [wrblog §5], or p itself for the bonus draw;
-// the token is the smallest x (vocabulary order) with C(x) > u Z.
+// the token is the smallest x (vocabulary order) with C(x) > u Z.  Both kept
+// lists arrive in one round trip; entries are rank-sorted by token and the
+// running sums are double-float.
 template <int DT>
 __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
-                         const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
+                                      const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
   const int lane = threadIdx.x & 31;
   const int slots = 2 * a.G + 1;
   SmemEpi& E = sm.u.e;
-  const RowStat ts = E.rs[r];
-  const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
-  const int nt = ts.n_list;
-  // both kept lists are fetched in one round trip
+  const int nt = E.rs[r].n_list;
   const bool draft_list = residual && !onehot && ds.path == PATH_STREAM;
   const int nq = draft_list ? ds.n_list : 0;
+  const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
   const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
-  ListEntry te[kListCap / 32], qe[kListCap / 32];
+  ListEntry te[4], qe[4];
 #pragma unroll
-  for (int j = 0; j < kListCap / 32; ++j) {
-    const int e = lane + 32 * j;
+  for (int j = 0; j < 4; ++j) {             // entry e = 4*lane + j (blocked, as the sort)
+    const int e = 4 * lane + j;
     if (e < nt) te[j] = load_entry(tl + e);
     if (e < nq) qe[j] = load_entry(ql + e);
   }
-  if (draft_list) {
+  if (draft_list) {                          // token-sorted draft list for lookups
 #pragma unroll
-    for (int j = 0; j < kListCap / 32; ++j) {
-      const int e = lane + 32 * j;
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * lane + j;
       if (e < nq) {
         E.tok[e] = qe[j].token;
         E.w[e] = qe[j].p;
@@ -132,63 +132,61 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
   }
   const Row drow = seq_row<DT>(a, b, r, true);
   const float invWd = (residual && !onehot && ds.path == PATH_FULL) ? static_cast<float>(1.0 / ds.W) : 0.0f;
-  // target entries with their residual / bonus weights
 #pragma unroll
-  for (int j = 0; j < kListCap / 32; ++j) {
-    const int e = lane + 32 * j;
-    if (e >= nt) continue;
-    const ListEntry t = te[j];
-    double w = t.p;
-    if (residual) {
-      double q;
-      if (onehot) q = (t.token == dj) ? 1.0 : 0.0;
-      else if (ds.path == PATH_STREAM) q = list_lookup(E.qtok, E.qp, nq, t.token);
-      else q = full_prob(load_elem<DT>(drow.base, t.token), static_cast<uint32_t>(t.token), ds, a.dp.cT, invWd);
-      w = fmax(t.p - q, 0.0);
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * lane + j;
+    if (e < nt) {
+      const ListEntry t = te[j];
+      double w = t.p;
+      if (residual) {
+        double q;
+        if (onehot) q = (t.token == dj) ? 1.0 : 0.0;
+        else if (ds.path == PATH_STREAM) q = list_lookup(E.qtok, E.qp, nq, t.token);
+        else q = full_prob(load_elem<DT>(drow.base, t.token), static_cast<uint32_t>(t.token), ds, a.dp.cT, invWd);
+        w = fmax(t.p - q, 0.0);
+      }
+      E.tok[kListCap + e] = t.token;
+      E.w[kListCap + e] = w;
+      E.sw[e] = t.p;                         // p, for a Z == 0 fallback
     }
-    E.tok[kListCap + e] = t.token;
-    E.w[kListCap + e] = w;
-    E.sw[e] = t.p;   // keep p for a Z == 0 fallback
   }
   __syncwarp();
-  // sort by token (tokens of one list are distinct)
-  for (int e = lane; e < nt; e += 32) {
+  for (int e = lane; e < nt; e += 32) {      // rank sort by token (distinct within a list)
     int rank = 0;
-    const int te = E.tok[kListCap + e];
-    for (int j = 0; j < nt; ++j) rank += E.tok[kListCap + j] < te ? 1 : 0;
-    E.stok[rank] = te;
-    E.tok[rank] = e;   // original position, to fetch p for the fallback
+    const int tk = E.tok[kListCap + e];
+    for (int j = 0; j < nt; ++j) rank += E.tok[kListCap + j] < tk ? 1 : 0;
+    E.stok[rank] = tk;
+    E.tok[rank] = e;                         // original position
   }
   __syncwarp();
   for (int pass = 0; pass < 2; ++pass) {
-    double w[4];
-    double s = 0.0;
+    float w[4];
+    df s = df_from(0.0f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int pos = 4 * lane + j;
-      w[j] = 0.0;
-      if (pos < nt) {
-        const int orig = E.tok[pos];
-        w[j] = pass == 0 ? E.w[kListCap + orig] : E.sw[orig];
-      }
-      s += w[j];
+      const int e = pos < nt ? E.tok[pos] : 0;
+      w[j] = pos < nt ? static_cast<float>(pass == 0 ? E.w[kListCap + e] : E.sw[e]) : 0.0f;
+      s = df_add(s, df_from(w[j]));
     }
-    const double incl = warp_incl_scan_f64(s, lane);
-    const double Z = __shfl_sync(kFull, incl, 31);
-    if (pass == 0 && residual) Z_resid = Z;
-    if (!(Z > 0.0)) {
+    const df incl = warp_incl_scan_df(s, lane);
+    const df Z = df_shfl(incl, 31);
+    if (pass == 0 && residual) Z_resid = df_to_double(Z);
+    if (!(Z.hi > 0.0f)) {
       if (pass == 0 && residual) { flags |= SEQ_FLAG_Z_ZERO; continue; }
     }
-    const double t = u * Z;
-    double acc = incl - s;
+    const float uf = static_cast<float>(u);
+    const float th = uf * Z.hi;
+    const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
+    df acc = df_add(incl, {-s.hi, -s.lo});
     int found = 0x7fffffff, last = -1;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int pos = 4 * lane + j;
-      if (pos < nt && w[j] > 0.0) {
-        acc += w[j];
+      if (pos < nt && w[j] > 0.0f) {
+        acc = df_add(acc, df_from(w[j]));
         last = pos;
-        if (found == 0x7fffffff && acc > t) found = pos;
+        if (found == 0x7fffffff && !df_ge(t, acc)) found = pos;    // C(x) > t
       }
     }
 #pragma unroll
@@ -371,22 +369,36 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     E.uacc[t] = a.u_acc[tokb + t];
   }
   __syncthreads();
-  // status, in the documented order: tokens, uniforms, rows
-  if (tid == 0) {
-    int status = SEQ_OK;
-    for (int i = 0; i < gb && status == SEQ_OK; ++i)
-      if (E.dtok[i] < 0 || E.dtok[i] >= a.V) status = SEQ_BAD_TOKEN;
-    if (status == SEQ_OK) {
-      for (int i = 0; i < gb; ++i)
-        if (!(E.uacc[i] >= 0.0f && E.uacc[i] < 1.0f)) status = SEQ_BAD_UNIFORM;
+  // status, in the documented order: tokens, uniforms, rows (lane-parallel, warp 0)
+  if (warp == 0) {
+    bool bad_tok = false, bad_u = false;
+    for (int i = lane; i < gb; i += 32) {
+      bad_tok |= E.dtok[i] < 0 || E.dtok[i] >= a.V;
+      bad_u |= !(E.uacc[i] >= 0.0f && E.uacc[i] < 1.0f);
+    }
+    if (lane == 0) {
       const float us = a.u_samp[b];
-      if (!(us >= 0.0f && us < 1.0f)) status = SEQ_BAD_UNIFORM;
+      bad_u |= !(us >= 0.0f && us < 1.0f);
     }
-    for (int i = 0; i <= gb && status == SEQ_OK; ++i) {
-      status = E.rs[i].status;
-      if (status == SEQ_OK && i < gb && !onehot) status = E.rs[a.G + 1 + i].status;
+    int status = SEQ_OK;
+    if (__any_sync(kFull, bad_tok)) status = SEQ_BAD_TOKEN;
+    else if (__any_sync(kFull, bad_u)) status = SEQ_BAD_UNIFORM;
+    else {
+      // rows in order: target 0, draft 0, target 1, draft 1, ..., target gb
+      const int norder = 2 * gb + 1;
+      for (int base = 0; base < norder && status == SEQ_OK; base += 32) {
+        const int o = base + lane;
+        int st = SEQ_OK;
+        if (o < norder) {
+          const int i = o >> 1;
+          if ((o & 1) == 0) st = E.rs[i].status;
+          else if (!onehot) st = E.rs[a.G + 1 + i].status;
+        }
+        const unsigned bm = __ballot_sync(kFull, st != SEQ_OK);
+        if (bm) status = __shfl_sync(kFull, st, __ffs(bm) - 1);
+      }
     }
-    sm.b_i32[0] = status;
+    if (lane == 0) sm.b_i32[0] = status;
   }
   __syncthreads();
   if (sm.b_i32[0] != SEQ_OK) {

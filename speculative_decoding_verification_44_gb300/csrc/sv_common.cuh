@@ -245,3 +245,84 @@ __device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t v, int lane) {
 }
 
 }  // namespace sv
+
+namespace sv {
+
+// ---------------------------------------------------------------- warp sort
+// Bitonic sort of 128 64-bit keys held 4 per lane in blocked layout (lane l
+// holds positions 4l..4l+3), into descending order.  Pad with 0 to sort fewer.
+__device__ __forceinline__ void warp_sort128_desc(uint64_t (&v)[4], int lane) {
+#pragma unroll
+  for (int size = 2; size <= 128; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = 4 * lane + j;
+          const uint64_t o = shfl_xor_u64(v[j], stride >> 2);
+          const bool desc = (i & size) == 0;           // this block ends up descending
+          const bool lower = (i & stride) == 0;        // lower position of the pair
+          const bool keep_max = lower == desc;
+          v[j] = keep_max ? (o > v[j] ? o : v[j]) : (o < v[j] ? o : v[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if ((j & stride) == 0) {
+            const int jj = j | stride;
+            const bool desc = ((4 * lane + j) & size) == 0;
+            const uint64_t a = v[j], b = v[jj];
+            const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+            v[j] = desc ? hi : lo;
+            v[jj] = desc ? lo : hi;
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- double-float
+// A value carried as hi + lo (two floats), added with Knuth's two-sum: about
+// 48 significant bits with float-pipe latency only.
+struct df { float hi, lo; };
+__device__ __forceinline__ df df_from(float x) { return {x, 0.0f}; }
+__device__ __forceinline__ df df_add(df a, df b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  float e = (a.hi - (s - bb)) + (b.hi - bb);
+  e += a.lo + b.lo;
+  const float hi = s + e;
+  return {hi, e - (hi - s)};
+}
+__device__ __forceinline__ double df_to_double(df a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
+__device__ __forceinline__ df df_shfl_up(df a, int o) {
+  return {__shfl_up_sync(kFull, a.hi, o), __shfl_up_sync(kFull, a.lo, o)};
+}
+__device__ __forceinline__ df df_shfl_xor(df a, int m) {
+  return {__shfl_xor_sync(kFull, a.hi, m), __shfl_xor_sync(kFull, a.lo, m)};
+}
+__device__ __forceinline__ df df_shfl(df a, int src) {
+  return {__shfl_sync(kFull, a.hi, src), __shfl_sync(kFull, a.lo, src)};
+}
+__device__ __forceinline__ df warp_incl_scan_df(df v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const df t = df_shfl_up(v, o);
+    if (lane >= o) v = df_add(v, t);
+  }
+  return v;
+}
+__device__ __forceinline__ df warp_sum_df(df v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = df_add(v, df_shfl_xor(v, o));
+  return v;
+}
+// a >= b for double-float values (compares the exact sums' signs via df_add).
+__device__ __forceinline__ bool df_ge(df a, df b) {
+  const df d = df_add(a, {-b.hi, -b.lo});
+  return d.hi > 0.0f || (d.hi == 0.0f && d.lo >= 0.0f);
+}
+
+}  // namespace sv

@@ -89,8 +89,8 @@ struct __align__(16) Smem {
     SmemEpi e;
   } u;
   uint64_t cand[kCandCap];           // PATH_STREAM: candidates (composites >= the lower bound)
-  uint64_t sorted[kSmallK];          // PATH_STREAM: top-k in descending order
   uint64_t topk[kSmallK];
+  uint64_t sorted[kSmallK];          // PATH_STREAM: top-k in descending order
   int32_t list_tok[kListCap];
   double list_p[kListCap];
   int nw[kWarps];
@@ -718,44 +718,44 @@ __device__ __noinline__ void stream_finish(const Row& row, const RowParams& P, c
     n_c = min(sm.ncand, kCandCap);
   }
   int ntop = 0;
-  if (!any_bad) {
-    const uint64_t* src = sm.cand;
-    int nsrc = n_c;
-    if (n_c > kThreads) {       // narrow to exactly k before the quadratic rank sort
-      const uint64_t kth = block_select_kth(sm.cand, n_c, k, sm);
-      if (tid == 0) sm.b_i32[3] = 0;
-      __syncthreads();
-      for (int e = tid; e < n_c; e += kThreads) {
-        const uint64_t c = sm.cand[e];
-        if (c >= kth) sm.topk[atomicAdd(&sm.b_i32[3], 1)] = c;
-      }
-      __syncthreads();
-      src = sm.topk;
-      nsrc = sm.b_i32[3];
+  const uint64_t* src = sm.cand;
+  int nsrc = any_bad ? 0 : n_c;
+  if (nsrc > kListCap) {        // narrow to exactly k before the register sort
+    const uint64_t kth = block_select_kth(sm.cand, nsrc, k, sm);
+    if (tid == 0) sm.b_i32[3] = 0;
+    __syncthreads();
+    for (int e = tid; e < nsrc; e += kThreads) {
+      const uint64_t c = sm.cand[e];
+      if (c >= kth) sm.topk[atomicAdd(&sm.b_i32[3], 1)] = c;
     }
-    ntop = min(nsrc, k);
-    if (warp == 0) {            // rank sort, descending; keep ranks < k
-      for (int e = lane; e < nsrc; e += 32) {
-        const uint64_t c = src[e];
-        int rank = 0;
-        for (int j = 0; j < nsrc; ++j) rank += src[j] > c ? 1 : 0;
-        if (rank < k) sm.sorted[rank] = c;
-      }
-      __syncwarp();
-    }
+    __syncthreads();
+    src = sm.topk;
+    nsrc = sm.b_i32[3];
   }
+  ntop = min(nsrc, k);
 
-  // ---- softmax over the top-k, top-p cut, kept list (warp 0).  Each weight
-  // exp((z - m) / T) = 2^((z - m) cT) is evaluated from the exact difference
-  // z - m (two-sum) and a hi/lo split of the exponent, so its error is that of
-  // exp2f (2 ulp); sums, prefix sums and the normaliser are accumulated in
-  // float64 (additions only).
+  // ---- sort, softmax over the top-k, top-p cut, kept list (warp 0).
+  // Each weight exp((z - m) / T) = 2^((z - m) cT) is evaluated from the exact
+  // difference z - m (two-sum) and a hi/lo split of the exponent, so its error
+  // is exp2f's (2 ulp); sums, prefix sums and the normaliser are double-float.
   if (warp == 0) {
+    // rank sort (descending), then each lane takes positions 4*lane .. 4*lane+3
+    for (int e = lane; e < nsrc; e += 32) {
+      const uint64_t c = src[e];
+      int rank = 0;
+      for (int j = 0; j < nsrc; ++j) rank += src[j] > c ? 1 : 0;
+      if (rank < k) sm.sorted[rank] = c;
+    }
+    __syncwarp();
+    uint64_t v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = (4 * lane + j < ntop) ? sm.sorted[4 * lane + j] : 0ull;
+    const uint64_t top = ntop ? sm.sorted[0] : 0ull;
     RowStat st;
     st.path = PATH_STREAM;
     st.cut = 0;
-    st.argmax = ntop ? static_cast<int>(comp_index(sm.sorted[0])) : -1;
-    const float m = ntop ? comp_value(sm.sorted[0]) : -__int_as_float(0x7f800000);
+    st.argmax = ntop ? static_cast<int>(comp_index(top)) : -1;
+    const float m = ntop ? comp_value(top) : -__int_as_float(0x7f800000);
     st.m = m;
     st.status = any_bad ? SEQ_NONFINITE
                         : ((ntop == 0 || !(m > -__int_as_float(0x7f800000))) ? SEQ_EMPTY_SUPPORT : SEQ_OK);
@@ -764,52 +764,55 @@ __device__ __noinline__ void stream_finish(const Row& row, const RowParams& P, c
     st.n_list = 0;
     if (st.status == SEQ_OK) {
       float w[4];
-      double s = 0.0;
+      df s = df_from(0.0f);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int pos = 4 * lane + j;
-        w[j] = 0.0f;
-        if (pos < ntop) w[j] = exp2_diff(comp_value(sm.sorted[pos]), m, P.cT, P.cT_lo);
-        s += static_cast<double>(w[j]);
+        w[j] = (4 * lane + j < ntop) ? exp2_diff(comp_value(v[j]), m, P.cT, P.cT_lo) : 0.0f;
+        s = df_add(s, df_from(w[j]));
       }
-      const double incl = warp_incl_scan_f64(s, lane);
-      const double S = __shfl_sync(kFull, incl, 31);
+      const df incl = warp_incl_scan_df(s, lane);
       int n_keep = ntop;
       if (P.top_p < 1.0f) {
-        const double target = static_cast<double>(P.top_p) * S;   // cum / S >= top_p
-        double acc = incl - s;
+        const df S = df_shfl(incl, 31);
+        const float th = P.top_p * S.hi;                       // target = top_p * S, double-float
+        const df target = {th, fmaf(P.top_p, S.hi, -th) + P.top_p * S.lo};
+        df acc = df_add(incl, {-s.hi, -s.lo});                 // exclusive prefix
         int first = 0x7fffffff;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int pos = 4 * lane + j;
           if (pos < ntop) {
-            acc += static_cast<double>(w[j]);
-            if (first == 0x7fffffff && acc >= target) first = pos;
+            acc = df_add(acc, df_from(w[j]));
+            if (first == 0x7fffffff && df_ge(acc, target)) first = pos;
           }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(kFull, first, o));
         n_keep = first == 0x7fffffff ? ntop : first + 1;
       }
-      double part = 0.0;
+      df part = df_from(0.0f);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) part += (4 * lane + j < n_keep) ? static_cast<double>(w[j]) : 0.0;
-      const double W = warp_sum_f64(part);
+      for (int j = 0; j < 4; ++j)
+        if (4 * lane + j < n_keep) part = df_add(part, df_from(w[j]));
+      const double W = df_to_double(warp_sum_df(part));
       const double invW = 1.0 / W;
+      int hit = -1;
       double ptok = 0.0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int pos = 4 * lane + j;
         if (pos < n_keep) {
-          const int tok = static_cast<int>(comp_index(sm.sorted[pos]));
+          const int tok = static_cast<int>(comp_index(v[j]));
           const double p = static_cast<double>(w[j]) * invW;
           sm.list_tok[pos] = tok;
           sm.list_p[pos] = p;
-          if (tok == dtok) ptok = p;
+          if (tok == dtok) { hit = lane; ptok = p; }
         }
       }
+      const unsigned hb = __ballot_sync(kFull, hit >= 0);
+      if (hb) ptok = __shfl_sync(kFull, ptok, __ffs(hb) - 1);
       st.W = W;
-      st.p_tok = warp_sum_f64(ptok);
+      st.p_tok = hb ? ptok : 0.0;
       st.n_list = n_keep;
     }
     if (lane == 0) sm.st = st;
