@@ -205,7 +205,8 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
 // token-sorted list; 3: (p - delta_dj)+.
 struct ScanCtx {
   Row trow, drow;
-  RowStat ts, ds;
+  uint64_t cutt, cutd;   // kept iff composite >= cut
+  float mt, md;          // row maxima
   float cTt, cTd, invWt, invWd;
   int mode;
   int dj;
@@ -213,25 +214,29 @@ struct ScanCtx {
 };
 
 template <int DT>
-__device__ __forceinline__ float scan_vec(const ScanCtx& c, int v, const Smem& sm, float (&w)[Elem<DT>::kPer]) {
-  constexpr int P = Elem<DT>::kPer;
-  uint4 rt, rd;
+__device__ __forceinline__ int scan_load(const ScanCtx& c, int v, uint4& rt, uint4& rd) {
   const int n = load_vec<DT, false>(c.trow, v, rt);
+  rd = make_uint4(0u, 0u, 0u, 0u);
+  if (c.mode == 1 && n) load_vec<DT, false>(c.drow, v, rd);
+  return n;
+}
+
+template <int DT>
+__device__ __forceinline__ float scan_weights(const ScanCtx& c, int v, int n, const uint4& rt, const uint4& rd,
+                                              const Smem& sm, float (&w)[Elem<DT>::kPer]) {
+  constexpr int P = Elem<DT>::kPer;
   float zt[P], zd[P];
   unpack<DT>(rt, zt);
-  if (c.mode == 1) {
-    load_vec<DT, false>(c.drow, v, rd);
-    unpack<DT>(rd, zd);
-  }
+  unpack<DT>(rd, zd);
   float s = 0.0f;
 #pragma unroll
   for (int e = 0; e < P; ++e) {
     float we = 0.0f;
     if (e < n) {
       const uint32_t x = static_cast<uint32_t>(v * P + e);
-      const float p = full_prob(zt[e], x, c.ts, c.cTt, c.invWt);
+      const float p = full_prob(zt[e], x, c.cutt, c.mt, c.cTt, c.invWt);
       float q = 0.0f;
-      if (c.mode == 1) q = full_prob(zd[e], x, c.ds, c.cTd, c.invWd);
+      if (c.mode == 1) q = full_prob(zd[e], x, c.cutd, c.md, c.cTd, c.invWd);
       else if (c.mode == 2) q = list_lookup(sm.u.e.qtok, sm.u.e.qp, c.nq, static_cast<int>(x));
       else if (c.mode == 3) q = (static_cast<int>(x) == c.dj) ? 1.0f : 0.0f;
       we = c.mode == 0 ? p : fmaxf(p - q, 0.0f);
@@ -243,24 +248,46 @@ __device__ __forceinline__ float scan_vec(const ScanCtx& c, int v, const Smem& s
 }
 
 // Block-wide inverse-CDF draw over a full row in vocabulary order.  Each warp
-// owns a contiguous range of vectors; pass A sums the weights per warp, the
-// owning warp then re-scans its range with identical arithmetic to locate the
-// first x with C(x) > u Z.
+// owns a contiguous range of vectors, cut into chunks of cv vectors (a
+// multiple of 32 x kScanUnroll, at most kScanChunks per warp).  Pass A sums
+// the weights per chunk (float per lane, float64 across lanes) with
+// kScanUnroll loads in flight per lane; then the chunk holding u Z is found
+// from the sums, and one warp re-scans that chunk alone with identical
+// arithmetic to locate the first x with C(x) > u Z.
 template <int DT>
 __device__ __noinline__ int block_scan_draw(ScanCtx& c, double u, bool residual, double& Z_resid, int& flags, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
+  constexpr int kStep = 32 * kScanUnroll;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nv = c.trow.nvec;
   const int L = (nv + kWarps - 1) / kWarps;
   const int v0 = warp * L, v1 = min(nv, v0 + L);
+  const int per = (L + kScanChunks - 1) / kScanChunks;
+  const int cv = max(kStep, (per + kStep - 1) / kStep * kStep);
+  const int nch = (L + cv - 1) / cv;
+  double (*csum)[kScanChunks] = sm.u.e.csum;
   for (int attempt = 0; attempt < 2; ++attempt) {
     double acc = 0.0;
-    for (int s = v0; s < v1; s += 32) {
-      const int v = s + lane;
-      float w[P];
-      const float ls = v < v1 ? scan_vec<DT>(c, v, sm, w) : 0.0f;
-      const double incl = warp_incl_scan_f64(static_cast<double>(ls), lane);
-      acc += __shfl_sync(kFull, incl, 31);
+    for (int k = 0; k < nch; ++k) {
+      const int c0 = v0 + k * cv, c1 = min(v1, c0 + cv);
+      float ls = 0.0f;
+      for (int s = c0; s < c1; s += kStep) {
+        uint4 rt[kScanUnroll], rd[kScanUnroll];
+        int n[kScanUnroll];
+#pragma unroll
+        for (int q = 0; q < kScanUnroll; ++q) {
+          const int v = s + q * 32 + lane;
+          n[q] = v < c1 ? scan_load<DT>(c, v, rt[q], rd[q]) : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < kScanUnroll; ++q) {
+          float w[P];
+          if (n[q]) ls += scan_weights<DT>(c, s + q * 32 + lane, n[q], rt[q], rd[q], sm, w);
+        }
+      }
+      const double cs = warp_sum_f64(static_cast<double>(ls));
+      if (lane == 0) csum[warp][k] = cs;
+      acc += cs;
     }
     if (lane == 0) sm.u.e.wtot[warp] = acc;
     __syncthreads();
@@ -268,19 +295,25 @@ __device__ __noinline__ int block_scan_draw(ScanCtx& c, double u, bool residual,
       double Z = 0.0;
       for (int w = 0; w < kWarps; ++w) Z += sm.u.e.wtot[w];
       sm.b_f64[0] = Z;
+      // first chunk (warp-major, then chunk) whose range holds t = u Z; the last
+      // non-empty chunk if rounding leaves t at or above the total
       const double t = u * Z;
-      double start = 0.0;
-      int W = -1;
-      double tl = 0.0;
-      int lastW = -1;
-      double last_start = 0.0;
-      for (int w = 0; w < kWarps; ++w) {
-        if (sm.u.e.wtot[w] > 0.0) { lastW = w; last_start = start; }
-        if (W < 0 && sm.u.e.wtot[w] > 0.0 && start + sm.u.e.wtot[w] > t) { W = w; tl = t - start; }
-        start += sm.u.e.wtot[w];
+      double start = 0.0, tl = 0.0, last_start = 0.0;
+      int W = -1, K = -1, lastW = -1, lastK = -1;
+      for (int w = 0; w < kWarps && W < 0; ++w) {
+        const int nw = (w * L < nv) ? (min(nv, w * L + L) - w * L + cv - 1) / cv : 0;
+        for (int k = 0; k < nw; ++k) {
+          const double cs = csum[w][k];
+          if (cs > 0.0) {
+            lastW = w; lastK = k; last_start = start;
+            if (start + cs > t) { W = w; K = k; tl = t - start; break; }
+          }
+          start += cs;
+        }
       }
-      if (W < 0) { W = lastW; tl = t - last_start; }
+      if (W < 0) { W = lastW; K = lastK; tl = t - last_start; }
       sm.b_i32[4] = W;
+      sm.b_i32[5] = K;
       sm.b_f64[1] = tl;
       sm.b_i32[6] = -1;
     }
@@ -298,12 +331,19 @@ __device__ __noinline__ int block_scan_draw(ScanCtx& c, double u, bool residual,
     }
     if (warp == sm.b_i32[4]) {
       const double tl = sm.b_f64[1];
+      const int c0 = v0 + sm.b_i32[5] * cv, c1 = min(v1, c0 + cv);
       double running = 0.0;
       int last_tok = -1;
-      for (int s = v0; s < v1; s += 32) {
+      for (int s = c0; s < c1; s += 32) {
         const int v = s + lane;
         float w[P];
-        const float ls = v < v1 ? scan_vec<DT>(c, v, sm, w) : 0.0f;
+        uint4 rt, rd;
+        const int n = v < c1 ? scan_load<DT>(c, v, rt, rd) : 0;
+        const float ls = n ? scan_weights<DT>(c, v, n, rt, rd, sm, w) : 0.0f;
+        if (!n) {
+#pragma unroll
+          for (int e = 0; e < P; ++e) w[e] = 0.0f;
+        }
         const double incl = warp_incl_scan_f64(static_cast<double>(ls), lane);
         const double excl_prev = __shfl_up_sync(kFull, incl, 1);
         const unsigned bal = __ballot_sync(kFull, ls > 0.0f && running + incl > tl);
@@ -474,8 +514,10 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     ScanCtx c;
     c.trow = seq_row<DT>(a, b, r, false);
     c.drow = (residual && !onehot) ? seq_row<DT>(a, b, r, true) : c.trow;
-    c.ts = ts;
-    c.ds = ds;
+    c.cutt = ts.cut;
+    c.mt = ts.m;
+    c.cutd = ds.cut;
+    c.md = ds.m;
     c.cTt = a.tp.cT;
     c.cTd = a.dp.cT;
     c.invWt = static_cast<float>(1.0 / ts.W);
@@ -749,11 +791,18 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
   const uint64_t bit = 1ull << (dev & 63);
   if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
   err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(Smem)));
+                             static_cast<int>(sizeof(Smem) + sizeof(FullExtra)));
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
 std::atomic<uint64_t> g_ready[6];   // sample, greedy, transform x {bf16, f32}
+
+// Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
+// needs FullExtra after Smem; launches without such rows keep their occupancy.
+size_t smem_for(const RowParams& a, const RowParams& b) {
+  const bool topp_full = (a.path == PATH_FULL && a.top_p < 1.0f) || (b.path == PATH_FULL && b.top_p < 1.0f);
+  return sizeof(Smem) + (topp_full ? sizeof(FullExtra) : 0);
+}
 
 }  // namespace
 
@@ -845,10 +894,10 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   cudaError_t err;
   if (dtype == SPEC_BF16) {
     err = prepare(sample_kernel<DT_BF16>, g_ready[0]);
-    if (err == cudaSuccess) sample_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess) sample_kernel<DT_BF16><<<grid, kThreads, smem_for(a.tp, a.dp), s>>>(a);
   } else {
     err = prepare(sample_kernel<DT_F32>, g_ready[1]);
-    if (err == cudaSuccess) sample_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess) sample_kernel<DT_F32><<<grid, kThreads, smem_for(a.tp, a.dp), s>>>(a);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
@@ -918,11 +967,11 @@ spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32
   if (dtype == SPEC_BF16) {
     err = prepare(transform_kernel<DT_BF16>, g_ready[4]);
     if (err == cudaSuccess)
-      transform_kernel<DT_BF16><<<rows, kThreads, sizeof(Smem), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
+      transform_kernel<DT_BF16><<<rows, kThreads, smem_for(P, P), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
   } else {
     err = prepare(transform_kernel<DT_F32>, g_ready[5]);
     if (err == cudaSuccess)
-      transform_kernel<DT_F32><<<rows, kThreads, sizeof(Smem), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
+      transform_kernel<DT_F32><<<rows, kThreads, smem_for(P, P), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

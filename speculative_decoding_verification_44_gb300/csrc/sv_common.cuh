@@ -22,6 +22,8 @@ constexpr int kStreamUnroll = 4;            // streaming top-k path: 16-byte loa
 constexpr int kListCap = kSmallK;           // kept-list entries stored per row
 constexpr int kMaxGamma = 63;               // largest gamma_max the sampling verifier accepts
 constexpr int kUnroll = 4;                  // 16-byte loads in flight per thread
+constexpr int kScanUnroll = 2;              // inverse-CDF scan: 16-byte loads in flight per lane
+constexpr int kScanChunks = 64;             // inverse-CDF scan: chunk sums kept per warp
 
 enum { DT_BF16 = 0, DT_F32 = 1 };
 enum { PATH_STREAM = 0, PATH_FULL = 1 };
@@ -75,6 +77,35 @@ __device__ __forceinline__ float exp2_diff(float z, float m, float cT_hi, float 
   const float t_lo = fmaf(d, cT_hi, -t) + fmaf(d, cT_lo, d_lo * cT_hi);
   const float e = exp2f(t);
   return fmaf(e, t_lo * 0.6931471805599453f, e);
+}
+
+// ---------------------------------------------------------------- shared memory by address
+// Explicit shared-window accesses for code that only holds a generic pointer
+// (out-of-line functions): no generic-to-shared resolution per access, and
+// red.shared returns nothing, so the issuing thread does not wait on it.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_volatile_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t atoms_cas_u32(uint32_t a, uint32_t cmp, uint32_t val) {
+  uint32_t old;
+  asm volatile("atom.shared.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "r"(a), "r"(cmp), "r"(val) : "memory");
+  return old;
+}
+__device__ __forceinline__ void reds_add_u32(uint32_t a, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- loads

@@ -17,12 +17,12 @@
 //     top-k.  The block then merges the warps' top-k, sorts the k survivors
 //     and evaluates softmax and the top-p cut over them in float64.
 //   PATH_FULL (top_k off or large): pass 1 streams the row once for the
-//     maximum and the softmax denominator (per-thread online rescaling,
-//     Kahan-compensated float sums, float64 across threads).  A top-k or
-//     top-p cut is then found by MSB-first radix selection over re-reads of
-//     the row (L2-resident after pass 1): digit histograms of counts (top-k)
-//     or of exact 64-bit fixed-point probability masses (top-p), the first
-//     top-p round bucketed by log-probability so that hot buckets spread.
+//     maximum (and, with no cut at all, the softmax denominator: per-thread
+//     online rescaling, Kahan-compensated float sums, float64 across
+//     threads).  A large top-k is found by MSB-first radix selection over
+//     re-reads of the row (digit histograms of counts); a top-p cut by
+//     bracketing (see "PATH_FULL top-p by bracketing" below), with radix
+//     selection over exact 64-bit fixed-point masses as its fallback.
 //
 // Sources: [wrblog] "推测解码：草稿模型、接受率、正确性与加速边界" (wrblog.cn).
 #pragma once
@@ -79,6 +79,7 @@ struct __align__(16) SmemEpi {
   int32_t qtok[kListCap];            // draft kept list sorted by token (binary search)
   double qp[kListCap];
   double wtot[kWarps];               // per-warp segment totals of the block scan
+  double csum[kWarps][kScanChunks];  // per-chunk totals of the block scan
   RowStat rs[2 * kMaxGamma + 1];     // the sequence's row summaries
   int32_t dtok[kMaxGamma];
   float uacc[kMaxGamma];
@@ -364,67 +365,99 @@ __device__ __noinline__ double full_sum_kept(const Row& row, float m, float cT, 
   return block_sum_d(static_cast<double>(s), sm);
 }
 
-// Index of the n-th (1-based) element, in index order, whose key equals K.
+// Warp segments: warp w owns the contiguous vectors [w L, (w + 1) L) of a row,
+// so counts per warp are counts per index range.
+__device__ __forceinline__ int seg_len(const Row& row) { return (row.nvec + kWarps - 1) / kWarps; }
+
+// Raw element bits that carry order key K: the value's own bits and, for a
+// zero, those of -0 as well (keys fold -0 onto +0).
 template <int DT>
-__device__ __noinline__ int find_nth_with_key(const Row& row, uint32_t K, uint32_t n, Smem& sm) {
+struct KeyBits {
+  uint32_t a, b;
+  __device__ __forceinline__ explicit KeyBits(uint32_t K) {
+    const uint32_t v = __float_as_uint(key_value(K));
+    a = DT == DT_BF16 ? (v >> 16) : v;
+    b = (v & 0x7fffffffu) == 0u ? (DT == DT_BF16 ? 0x8000u : 0x80000000u) : a;
+  }
+  __device__ __forceinline__ bool hit(uint32_t x) const { return x == a || x == b; }
+  // Elements e < c of vector q that carry the key, as a bit mask.
+  __device__ __forceinline__ uint32_t mask(const uint4& q, int c) const {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < Elem<DT>::kPer; ++e) {
+      const uint32_t x = DT == DT_BF16 ? ((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu)) : w[e];
+      m |= (e < c && hit(x)) ? (1u << e) : 0u;
+    }
+    return m;
+  }
+};
+
+// Index of the r-th (1-based) element with key K in vectors [v0, v1), in
+// index order; -1 if there are fewer.  Block-wide: while the range is long,
+// every warp counts K in one eighth of it (kUnroll loads in flight per lane)
+// and the range shrinks to the eighth holding the r-th; one warp then scans.
+template <int DT>
+__device__ __noinline__ int range_find_nth(const Row& row, uint32_t K, int v0, int v1, uint32_t r, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int L = (row.nvec + kWarps - 1) / kWarps;
-  const int v0 = warp * L, v1 = min(row.nvec, v0 + L);
-  uint32_t my = 0;
-  for (int s = v0; s < v1; s += 32) {
-    const int v = s + lane;
-    uint4 r;
-    const int c = v < v1 ? load_vec<DT, false>(row, v, r) : 0;
-    if (c) {
-      float x[P];
-      unpack<DT>(r, x);
+  const KeyBits<DT> kb(K);
+  while (v1 - v0 > 32 * kWarps) {
+    const int sub = (v1 - v0 + kWarps - 1) / kWarps;
+    const int a0 = v0 + warp * sub, a1 = min(v1, a0 + sub);
+    uint32_t my = 0;
+    for (int s = a0; s < a1; s += 32 * kUnroll) {
+      uint4 q[kUnroll];
+      int c[kUnroll];
 #pragma unroll
-      for (int e = 0; e < P; ++e) my += (e < c && fkey(x[e]) == K) ? 1u : 0u;
-    }
-  }
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = s + u * 32 + lane;
+        c[u] = v < a1 ? load_vec<DT, false>(row, v, q[u]) : 0;
+      }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) my += __shfl_xor_sync(kFull, my, o);
-  if (lane == 0) sm.u.f.wcnt[warp] = my;
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t acc = 0;
-    int W = kWarps - 1;
-    uint32_t r = n;
-    for (int w = 0; w < kWarps; ++w) {
-      if (acc + sm.u.f.wcnt[w] >= n) { W = w; r = n - acc; break; }
-      acc += sm.u.f.wcnt[w];
+      for (int u = 0; u < kUnroll; ++u) my += __popc(kb.mask(q[u], c[u]));
     }
-    sm.b_i32[4] = W;
-    sm.b_i32[5] = static_cast<int>(r);
-    sm.b_i32[6] = -1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) my += __shfl_xor_sync(kFull, my, o);
+    if (lane == 0) sm.u.f.wcnt[warp] = my;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t acc = 0;
+      int W = -1;
+      for (int w = 0; w < kWarps; ++w) {
+        if (acc + sm.u.f.wcnt[w] >= r) { W = w; break; }
+        acc += sm.u.f.wcnt[w];
+      }
+      sm.b_i32[4] = W;
+      sm.b_i32[5] = static_cast<int>(r - acc);
+    }
+    __syncthreads();
+    const int W = sm.b_i32[4];
+    r = static_cast<uint32_t>(sm.b_i32[5]);
+    __syncthreads();
+    if (W < 0) return -1;                   // same in every thread
+    v0 = v0 + W * sub;
+    v1 = min(v1, v0 + sub);
   }
+  if (tid == 0) sm.b_i32[6] = -1;
   __syncthreads();
-  if (warp == sm.b_i32[4]) {
-    const uint32_t r = static_cast<uint32_t>(sm.b_i32[5]);
+  if (warp == 0) {
     uint32_t running = 0;
     for (int s = v0; s < v1; s += 32) {
       const int v = s + lane;
-      uint4 rr;
-      const int c = v < v1 ? load_vec<DT, false>(row, v, rr) : 0;
-      float x[P];
-      unpack<DT>(rr, x);
-      uint32_t mine = 0;
-#pragma unroll
-      for (int e = 0; e < P; ++e) mine += (e < c && fkey(x[e]) == K) ? 1u : 0u;
+      uint4 q;
+      const int c = v < v1 ? load_vec<DT, false>(row, v, q) : 0;
+      const uint32_t hits = kb.mask(q, c);
+      const uint32_t mine = __popc(hits);
       const uint32_t incl = warp_incl_scan_u32(mine, lane);
       const unsigned bal = __ballot_sync(kFull, running + incl >= r && mine > 0);
       if (bal) {
         const int Lw = __ffs(bal) - 1;
         if (lane == Lw) {
-          uint32_t cur = running + incl - mine;
-#pragma unroll
-          for (int e = 0; e < P; ++e) {
-            if (e < c && fkey(x[e]) == K) {
-              ++cur;
-              if (cur == r) { sm.b_i32[6] = v * P + e; break; }
-            }
-          }
+          // the (r - before)-th set bit of this lane's hit mask
+          uint32_t h = hits;
+          for (uint32_t k = running + incl - mine + 1; k < r; ++k) h &= h - 1;
+          sm.b_i32[6] = v * P + (__ffs(h) - 1);
         }
         break;
       }
@@ -433,6 +466,12 @@ __device__ __noinline__ int find_nth_with_key(const Row& row, uint32_t K, uint32
   }
   __syncthreads();
   return sm.b_i32[6];
+}
+
+// Index of the n-th (1-based) element, in index order, whose key equals K.
+template <int DT>
+__device__ __forceinline__ int find_nth_with_key(const Row& row, uint32_t K, uint32_t n, Smem& sm) {
+  return range_find_nth<DT>(row, K, 0, row.nvec, n, sm);
 }
 
 // One radix round over a re-read of the row.  Elements taking part: composite
@@ -596,13 +635,618 @@ __device__ __noinline__ uint64_t full_select_topp(const Row& row, float m, float
   return composite(K, static_cast<uint32_t>(idx));
 }
 
+// ------------------------------------------------------------------ PATH_FULL top-p by bracketing
+// The top-p cut of a full row without radix rounds.  An element's mass
+// depends on its value only, so masses can be counted per distinct key:
+//   1. bucket pass: the kept masses summed per log-probability class -- kNB
+//      buckets of one width below a level top, plus one class above and one
+//      below -- in per-thread private float columns of shared memory (no
+//      atomics, no bank conflicts).  The class where the cumulative mass
+//      (largest first) reaches top_p, widened to its neighbours when the float
+//      sums leave the crossing within a margin of a class edge, is the bracket.
+//   2. exact pass: the masses above and below the bracket are summed per
+//      thread (Kahan float; float64 across threads), and every element inside
+//      the bracket is counted per distinct key in a small hash table, one
+//      count per warp segment.  A key's mass is its count times its weight.
+//   3. resolve: the bracket's keys in descending order give the crossing key
+//      K*, how many of its ties the prefix takes, and W; the per-warp counts
+//      name the warp segment holding the last tie taken, and one warp scans
+//      that eighth of the row for its index.
+// A bracket holding more distinct keys than the table is refined by another
+// bucket pass over its own range (float32 rows, whose values rarely repeat,
+// need this); after kMaxLevels levels the radix rounds above take over.
+constexpr int kNB = 32;                 // buckets per level
+constexpr int kNC = kNB + 2;            // classes: above, kNB buckets, below
+constexpr float kLevel0Width = 1.5f;    // log2 units; level 0 spans 48 below the maximum
+constexpr int kNTBits = 8;
+constexpr int kNT = 1 << kNTBits;       // bracket key table slots (one per thread)
+constexpr int kProbe = 8;               // linear probes before a key counts as overflow
+constexpr int kMaxLevels = 3;
+constexpr uint32_t kNoKey = 0xffffffffu;  // the key of a NaN: never a key of a finite row
+static_assert(kNT == kThreads, "one table slot per thread");
+
+// ------------------------------------------------------------------ PATH_FULL top-p by key counts (bf16)
+// A bf16 row has at most 65536 distinct values and usually a few hundred to
+// a few thousand; an element's probability depends on its value alone.  So
+// the streaming pass that takes the maximum also counts the elements per
+// distinct value, with no exponential per element:
+//   * values with |z| in [2^-3, 2^5) -- the bulk of a logits row -- index a
+//     direct table by (sign, binade, 7 mantissa bits): one red.shared per
+//     element, no key check;
+//   * any other value goes to a small open-addressing table keyed by its
+//     16-bit order key; -inf is skipped (probability 0).
+// Counts are kept per warp pair (each pair streams its own quarter of the
+// row).  The cut then follows from the tables:
+//   * per value: weight 2^((z - m) cT) as a 64-bit fixed-point mass, times
+//     its count, summed into 256 log-probability bins (exact integer sums);
+//   * the bin where the cumulative mass (largest first) reaches
+//     ceil(top_p x total) -- the same tau as the radix rounds -- and, inside
+//     it, the values in descending order give the crossing value K* and how
+//     many of its ties the prefix takes;
+//   * the per-pair counts of K* name the quarter of the row holding the last
+//     tie taken, and a hierarchical count over that quarter finds its index.
+// An overflow of the small table (too many distinct values outside the
+// window) hands the row to bracketing, which reuses the maximum.
+constexpr int kKCDirect = 2048;         // 2 signs x 8 binades x 128 mantissas
+constexpr int kKCExpLo = 124;           // biased exponent of 2^-3
+constexpr int kKHBits = 8;
+constexpr int kKH = 1 << kKHBits;       // small table slots
+constexpr int kKHProbe = 16;            // linear probes before overflow
+constexpr int kKCSlots = kKCDirect + kKH;
+constexpr int kKCList = kCandCap / 2;   // values of the crossing bin (unsorted, then sorted, in sm.cand)
+constexpr int kPairs = kWarps / 2;
+static_assert(kWarps % 2 == 0, "rows are counted per warp pair");
+
+struct KeyCount {
+  uint32_t cnt[kPairs][kKCSlots];       // direct slots, then small-table slots
+  uint32_t keys[kKH];                   // 16-bit order keys of the small table
+};
+
+struct __align__(16) FullExtra {
+  union {
+    float priv[kNC][kThreads];          // bucket pass: column tid is thread tid's
+    struct {
+      uint32_t keys[kNT];
+      uint32_t cnt[kWarps][kNT];        // per warp segment
+      uint32_t skey[kNT];               // bracket keys, descending
+      uint32_t scnt[kNT];
+      float sw[kNT];
+      double smass[kNT];
+      int16_t sslot[kNT];
+    } t;
+    KeyCount kc;                        // bf16 key counts
+  } u;
+  float csum[kNC];
+  int bi[8];
+  double bd[2];
+};
+
+// Bytes of dynamic shared memory this launch was given.
+__device__ __forceinline__ unsigned dyn_smem_bytes() {
+  unsigned r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
+struct Level {
+  float top;    // log2-probability at the top of bucket 1
+  float inv_w;  // 1 / bucket width
+};
+// Class of log-probability t: 0 above the level's range, 1..kNB its buckets
+// from the top, kNB + 1 below.  Non-increasing in t, and one function for
+// every pass, so each class is a contiguous range of keys.
+__device__ __forceinline__ int class_of(float t, const Level& L) {
+  float f = fmaf(L.top - t, L.inv_w, 1.0f);
+  f = fminf(fmaxf(f, 0.0f), static_cast<float>(kNB + 1));
+  return __float_as_int(__fadd_rz(f, 8388608.0f)) - 0x4b000000;   // floor(f), f in [0, 2^23)
+}
+
+__device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
+  const float y = v - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+}
+
+// Pass 1: row maximum and the NaN / +inf flag only.
+template <int DT>
+__device__ void full_max(const Row& row, Smem& sm, float& m_out, int& bad_out) {
+  const int tid = threadIdx.x;
+  float m = -__int_as_float(0x7f800000);
+  bool bad = false;
+  for (int base = 0; base < row.nvec; base += kThreads * kUnroll) {
+    uint4 r[kUnroll];
+    int cnt[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) cnt[u] = load_vec<DT, false>(row, base + u * kThreads + tid, r[u]);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (cnt[u] == 0) continue;
+      bool vb;
+      m = fmaxf(m, vec_max<DT>(r[u], cnt[u], vb));
+      bad |= vb;
+    }
+  }
+  m_out = block_max_f(m, sm);
+  bad_out = block_or(bad ? 1 : 0, sm);
+}
+
+// Step 1: approximate kept mass per class into fx.csum.
+template <int DT>
+__device__ __noinline__ void topp_bucket_pass(const Row& row, float m, float cT, uint64_t ck, Level L,
+                                              Smem& sm, FullExtra& fx) {
+  constexpr int P = Elem<DT>::kPer;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t col = smem_u32(&fx.u.priv[0][tid]);   // this thread's column, stride kThreads floats
+#pragma unroll
+  for (int c = 0; c < kNC; ++c) sts_f32(col + c * kThreads * 4, 0.0f);
+  for (int base = 0; base < row.nvec; base += kThreads * kUnroll) {
+    uint4 r[kUnroll];
+    int cnt[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) cnt[u] = load_vec<DT, false>(row, base + u * kThreads + tid, r[u]);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (cnt[u] == 0) continue;
+      float x[P];
+      unpack<DT>(r[u], x);
+      const int v = base + u * kThreads + tid;
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        if (e >= cnt[u]) continue;
+        if (ck != 0ull && composite(fkey(x[e]), static_cast<uint32_t>(v * P + e)) < ck) continue;
+        const float t = (x[e] - m) * cT;
+        const uint32_t a = col + static_cast<uint32_t>(class_of(t, L)) * (kThreads * 4);
+        sts_f32(a, lds_f32(a) + fast_exp2(t));
+      }
+    }
+  }
+  __syncthreads();
+  for (int c = warp; c < kNC; c += kWarps) {
+    float s = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kThreads / 32; ++q) s += fx.u.priv[c][lane + 32 * q];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if (lane == 0) fx.csum[c] = s;
+  }
+  __syncthreads();
+}
+
+// Bracket [lo, hi] of classes around the crossing of top_p in the class sums.
+// Every thread computes the same answer from the same shared values.
+__device__ __forceinline__ void choose_bracket(const float* cs, float top_p, int& lo, int& hi) {
+  float tot = 0.0f;
+  for (int c = 0; c < kNC; ++c) tot += cs[c];
+  const float tau = top_p * tot, eps = 2e-4f * tot;
+  float before = 0.0f;
+  int c = 0;
+  for (; c < kNC - 1; ++c) {
+    if (before + cs[c] >= tau) break;
+    before += cs[c];
+  }
+  lo = hi = c;
+  float b_lo = before;                      // approximate mass above class lo
+  while (lo > 0 && b_lo >= tau - eps) { --lo; b_lo -= cs[lo]; }
+  float a_hi = before + cs[c];              // approximate mass through class hi
+  while (hi < kNC - 1 && a_hi < tau + eps) { ++hi; a_hi += cs[hi]; }
+}
+
+// Counts key K in the bracket table (per-warp count row cntw); false when the
+// probe sequence is full of other keys.
+// keys: shared address of the key array; cntw: of this warp's count row.
+__device__ __forceinline__ bool table_count(uint32_t keys, uint32_t cntw, uint32_t K) {
+  const uint32_t h = ((K ^ (K >> 15)) * 0x9e3779b1u) >> (32 - kNTBits);
+  for (int p = 0; p < kProbe; ++p) {
+    const uint32_t s = (h + p) & (kNT - 1);
+    uint32_t cur = lds_volatile_u32(keys + 4 * s);
+    if (cur == kNoKey) cur = atoms_cas_u32(keys + 4 * s, kNoKey, K);
+    if (cur == kNoKey || cur == K) {
+      reds_add_u32(cntw + 4 * s, 1u);
+      return true;
+    }
+  }
+  return false;
+}
+
+// Step 2: exact mass above and below classes [lo, hi]; keys inside counted.
+// Returns 1 if the table overflowed.
+template <int DT>
+__device__ __noinline__ int topp_exact_pass(const Row& row, float m, float cT, uint64_t ck, Level L, int lo,
+                                            int hi, Smem& sm, FullExtra& fx, double& above, double& below) {
+  constexpr int P = Elem<DT>::kPer;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  fx.u.t.keys[tid] = kNoKey;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) fx.u.t.cnt[w][tid] = 0u;
+  if (tid == 0) fx.bi[0] = 0;
+  __syncthreads();
+  volatile int* ovf = &fx.bi[0];
+  const uint32_t keys = smem_u32(fx.u.t.keys), cntw = smem_u32(fx.u.t.cnt[warp]);
+  float sa = 0.0f, ca = 0.0f, sb = 0.0f, cb = 0.0f;
+  const int Ls = seg_len(row);
+  const int v0 = warp * Ls, v1 = min(row.nvec, v0 + Ls);
+  for (int s = v0; s < v1; s += 32 * kUnroll) {
+    if (*ovf) break;
+    uint4 r[kUnroll];
+    int c[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = s + u * 32 + lane;
+      c[u] = v < v1 ? load_vec<DT, false>(row, v, r[u]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (c[u] == 0) continue;
+      float x[P];
+      unpack<DT>(r[u], x);
+      const int v = s + u * 32 + lane;
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        if (e >= c[u]) continue;
+        const uint32_t K = fkey(x[e]);
+        if (ck != 0ull && composite(K, static_cast<uint32_t>(v * P + e)) < ck) continue;
+        const float t = (x[e] - m) * cT;
+        const int cl = class_of(t, L);
+        const float w = fast_exp2(t);
+        const bool up = cl < lo, down = cl > hi;
+        kahan_add(sa, ca, up ? w : 0.0f);      // branch-free: both sums see every element
+        kahan_add(sb, cb, down ? w : 0.0f);
+        if (!up && !down && !table_count(keys, cntw, K)) *ovf = 1;
+      }
+    }
+  }
+  above = block_sum_d(static_cast<double>(sa) - static_cast<double>(ca), sm);
+  below = block_sum_d(static_cast<double>(sb) - static_cast<double>(cb), sm);
+  return fx.bi[0];
+}
+
+// Step 3: crossing key, ties taken and W from the table; the cut's index from
+// one warp segment.  False if the bracket does not hold the crossing.
+template <int DT>
+__device__ __noinline__ bool topp_resolve(const Row& row, float m, float cT, float top_p, double above,
+                                          double below, Smem& sm, FullExtra& fx, uint64_t& cut, double& W) {
+  auto& T = fx.u.t;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t K = T.keys[tid];
+  const bool valid = K != kNoKey;
+  double mass = 0.0;
+  if (valid) {
+    uint32_t count = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) count += T.cnt[w][tid];
+    const float wK = fast_exp2((key_value(K) - m) * cT);   // the weight every element of key K got
+    mass = static_cast<double>(count) * static_cast<double>(wK);
+    int rank = 0;
+    for (int s = 0; s < kNT; ++s) {
+      const uint32_t o = T.keys[s];
+      rank += (o != kNoKey && o > K) ? 1 : 0;
+    }
+    T.skey[rank] = K;
+    T.scnt[rank] = count;
+    T.sw[rank] = wK;
+    T.smass[rank] = mass;
+    T.sslot[rank] = static_cast<int16_t>(tid);
+  }
+  const int nk = __syncthreads_count(valid);
+  const double inb = block_sum_d(mass, sm);
+  const double tau = static_cast<double>(top_p) * (above + below + inb);
+  if (!(nk > 0 && above < tau && tau <= above + inb)) return false;   // same values in every thread
+  if (warp == 0) {
+    double run = above, before = 0.0;
+    int pos = -1;
+    for (int base = 0; base < nk; base += 32) {
+      const int i = base + lane;
+      const double ms = i < nk ? T.smass[i] : 0.0;
+      const double incl = warp_incl_scan_f64(ms, lane);
+      const unsigned bal = __ballot_sync(kFull, i < nk && run + incl >= tau);
+      if (bal) {
+        const int Lb = __ffs(bal) - 1;
+        pos = base + Lb;
+        before = run + __shfl_sync(kFull, incl - ms, Lb);
+        break;
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    if (pos < 0) {                          // rounding left tau just above the scanned total
+      pos = nk - 1;
+      before = run - T.smass[pos];
+    }
+    if (lane == 0) {
+      const double wk = static_cast<double>(T.sw[pos]);
+      double need = ceil((tau - before) / wk);
+      if (!(need >= 1.0)) need = 1.0;
+      if (need > static_cast<double>(T.scnt[pos])) need = static_cast<double>(T.scnt[pos]);
+      const uint32_t n = static_cast<uint32_t>(need);
+      fx.bd[0] = before + need * wk;
+      const int slot = T.sslot[pos];
+      uint32_t acc = 0, r = n;
+      int Wn = kWarps - 1;
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t cw = T.cnt[w][slot];
+        if (acc + cw >= n) { Wn = w; r = n - acc; break; }
+        acc += cw;
+      }
+      fx.bi[1] = static_cast<int>(T.skey[pos]);
+      fx.bi[2] = Wn;
+      fx.bi[3] = static_cast<int>(r);
+    }
+  }
+  __syncthreads();
+  const uint32_t Ks = static_cast<uint32_t>(fx.bi[1]);
+  const int Ls = seg_len(row), v0 = min(row.nvec, fx.bi[2] * Ls);
+  const int idx = range_find_nth<DT>(row, Ks, v0, min(row.nvec, v0 + Ls), static_cast<uint32_t>(fx.bi[3]), sm);
+  if (idx < 0) return false;
+  cut = composite(Ks, static_cast<uint32_t>(idx));
+  W = fx.bd[0];
+  return true;
+}
+
+// The top-p cut among {composite >= ck} by bracketing; false if it gave up.
+template <int DT>
+__device__ __noinline__ bool topp_bracketed(const Row& row, float m, float cT, uint64_t ck, float top_p,
+                                            Smem& sm, FullExtra& fx, uint64_t& cut, double& W) {
+  Level L;
+  L.top = 0.0f;
+  float w = kLevel0Width;
+  L.inv_w = 1.0f / w;
+  for (int level = 0; level < kMaxLevels; ++level) {
+    topp_bucket_pass<DT>(row, m, cT, ck, L, sm, fx);
+    int lo, hi;
+    choose_bracket(fx.csum, top_p, lo, hi);
+    double above, below;
+    const int overflow = topp_exact_pass<DT>(row, m, cT, ck, L, lo, hi, sm, fx, above, below);
+    if (!overflow) return topp_resolve<DT>(row, m, cT, top_p, above, below, sm, fx, cut, W);
+    if (lo == 0) return false;              // nothing above the range to refine into
+    L.top = L.top - static_cast<float>(lo - 1) * w;
+    if (hi <= kNB) w = w * static_cast<float>(hi - lo + 1) / static_cast<float>(kNB);
+    L.inv_w = 1.0f / w;
+  }
+  return false;
+}
+
+// 16-bit order key of bf16 bits b (-0 folded onto +0), and back.
+__device__ __forceinline__ uint32_t bf16_key(uint32_t b) {
+  b = (b == 0x8000u) ? 0u : b;
+  return (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+}
+__device__ __forceinline__ float bf16_key_value(uint32_t k) {
+  const uint32_t b = (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu);
+  return __uint_as_float(b << 16);
+}
+// bf16 bits of key-count slot s (direct window or small table).
+__device__ __forceinline__ uint32_t kc_slot_bits(const KeyCount& T, int s) {
+  if (s < kKCDirect) {
+    const uint32_t sign = static_cast<uint32_t>(s) >> 10, rel = (static_cast<uint32_t>(s) >> 7) & 7u;
+    return (sign << 15) | ((rel + kKCExpLo) << 7) | (static_cast<uint32_t>(s) & 127u);
+  }
+  const uint32_t k = T.keys[s - kKCDirect];
+  return (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu);
+}
+
+// Counts one bf16 element (bits b) into the pair's count row cnt (shared
+// address); keys is the small table's key array.  False on overflow.
+__device__ __forceinline__ bool kc_count(uint32_t keys, uint32_t cnt, uint32_t b) {
+  const uint32_t rel = ((b >> 7) & 0xffu) - kKCExpLo;
+  if (rel < 8u) {
+    reds_add_u32(cnt + 4 * (((b >> 15) << 10) | (rel << 7) | (b & 127u)), 1u);
+    return true;
+  }
+  if (b == 0xff80u) return true;                       // -inf: probability 0, never kept mass
+  const uint32_t k = bf16_key(b);
+  const uint32_t h = (k * 0x9e3779b1u) >> (32 - kKHBits);
+  for (int p = 0; p < kKHProbe; ++p) {
+    const uint32_t s = (h + p) & (kKH - 1);
+    uint32_t cur = lds_volatile_u32(keys + 4 * s);
+    if (cur == kNoKey) cur = atoms_cas_u32(keys + 4 * s, kNoKey, k);
+    if (cur == kNoKey || cur == k) {
+      reds_add_u32(cnt + 4 * (kKCDirect + s), 1u);
+      return true;
+    }
+  }
+  return false;
+}
+
+// Pass 1 of a bf16 top-p row: maximum, NaN / +inf flag and the value counts,
+// warp pair j over its own quarter of the row.  Returns 1 if the small table
+// overflowed (the maximum and flag are complete either way).
+__device__ __noinline__ int kc_pass(const Row& row, Smem& sm, FullExtra& fx, float& m_out, int& bad_out) {
+  constexpr int P = Elem<DT_BF16>::kPer;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int s = tid; s < kKH; s += kThreads) fx.u.kc.keys[s] = kNoKey;
+  for (int s = tid; s < kPairs * kKCSlots; s += kThreads) (&fx.u.kc.cnt[0][0])[s] = 0u;
+  if (tid == 0) fx.bi[0] = 0;
+  __syncthreads();
+  volatile int* ovf = &fx.bi[0];
+  const uint32_t keys = smem_u32(fx.u.kc.keys), cnt = smem_u32(fx.u.kc.cnt[warp >> 1]);
+  float m = -__int_as_float(0x7f800000);
+  bool bad = false, counting = true;
+  const int Ls = seg_len(row);
+  const int v0 = warp * Ls, v1 = min(row.nvec, v0 + Ls);
+  for (int s = v0; s < v1; s += 32 * kUnroll) {
+    if (counting && *ovf) counting = false;
+    uint4 r[kUnroll];
+    int c[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = s + u * 32 + lane;
+      c[u] = v < v1 ? load_vec<DT_BF16, false>(row, v, r[u]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (c[u] == 0) continue;
+      bool vb;
+      m = fmaxf(m, vec_max<DT_BF16>(r[u], c[u], vb));
+      bad |= vb;
+      if (!counting) continue;
+      const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        if (e >= c[u]) continue;
+        const uint32_t b = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu);
+        if (!kc_count(keys, cnt, b)) {
+          *ovf = 1;
+          counting = false;
+          break;
+        }
+      }
+    }
+  }
+  m_out = block_max_f(m, sm);
+  bad_out = block_or(bad ? 1 : 0, sm);
+  return fx.bi[0];
+}
+
+// The cut from the value counts; false when the crossing bin holds more
+// values than the list (the caller then brackets).
+__device__ __noinline__ bool kc_resolve(const Row& row, float m, float cT, float scale, float top_p, Smem& sm,
+                                        FullExtra& fx, uint64_t& cut, double& W) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const KeyCount& T = fx.u.kc;
+  auto count_of = [&](int s) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j) c += T.cnt[j][s];
+    return c;
+  };
+  auto used = [&](int s) { return s < kKCDirect ? count_of(s) != 0u : T.keys[s - kKCDirect] != kNoKey; };
+  if (tid < 256) {
+    sm.u.f.mass[tid] = 0ull;
+    sm.u.f.cnt[tid] = 0u;
+  }
+  if (tid == 0) sm.ncand = 0;
+  __syncthreads();
+  for (int s = tid; s < kKCSlots; s += kThreads) {
+    if (!used(s)) continue;
+    const float t = (__uint_as_float(kc_slot_bits(T, s) << 16) - m) * cT;
+    const unsigned long long wf = fixed_mass(fast_exp2(t), scale);
+    const int b = tbin_of(t);
+    atomicAdd(&sm.u.f.mass[b], static_cast<unsigned long long>(count_of(s)) * wf);
+    atomicAdd(&sm.u.f.cnt[b], 1u);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t tot = 0;
+    for (int j = lane; j < 256; j += 32) tot += sm.u.f.mass[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += shfl_xor_u64(tot, o);
+    const double tf = ceil(static_cast<double>(top_p) * static_cast<double>(tot));
+    uint64_t tau = tf >= static_cast<double>(tot) ? tot : static_cast<uint64_t>(tf);
+    if (tau == 0) tau = 1;
+    int digit;
+    uint64_t before;
+    pick_digit_mass(sm.u.f.mass, 0ull, tau, false, lane, digit, before);
+    if (lane == 0) {
+      sm.b_u64[0] = tau;
+      sm.b_u64[1] = before;
+      sm.b_i32[0] = digit;
+    }
+  }
+  __syncthreads();
+  const uint64_t tau = sm.b_u64[0], above = sm.b_u64[1];
+  const int tb = sm.b_i32[0];
+  if (sm.u.f.cnt[tb] > static_cast<uint32_t>(kKCList)) return false;   // same in every thread
+  // the crossing bin's values, as (key << 48 | slot << 32 | count), then sorted descending
+  for (int s = tid; s < kKCSlots; s += kThreads) {
+    if (!used(s)) continue;
+    const uint32_t b = kc_slot_bits(T, s);
+    if (tbin_of((__uint_as_float(b << 16) - m) * cT) != tb) continue;
+    const int pos = atomicAdd(&sm.ncand, 1);
+    sm.cand[pos] = (static_cast<uint64_t>(bf16_key(b)) << 48) | (static_cast<uint64_t>(s) << 32) | count_of(s);
+  }
+  __syncthreads();
+  const int n = sm.ncand;
+  for (int e = tid; e < n; e += kThreads) {
+    const uint64_t c = sm.cand[e];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += sm.cand[j] > c ? 1 : 0;
+    sm.cand[kKCList + rank] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint64_t* srt = sm.cand + kKCList;
+    uint64_t run = above, before = 0;
+    int pos = -1;
+    auto mass_of = [&](uint64_t e, unsigned long long& wf) {
+      wf = fixed_mass(fast_exp2((bf16_key_value(static_cast<uint32_t>(e >> 48)) - m) * cT), scale);
+      return static_cast<uint64_t>(static_cast<uint32_t>(e)) * wf;
+    };
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      unsigned long long wf;
+      const uint64_t ms = i < n ? mass_of(srt[i], wf) : 0ull;
+      uint64_t incl = ms;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t t = shfl_u64(incl, (lane - o) & 31);
+        if (lane >= o) incl += t;
+      }
+      const unsigned bal = __ballot_sync(kFull, i < n && ms != 0 && run + incl >= tau);
+      if (bal) {
+        const int Lb = __ffs(bal) - 1;
+        pos = base + Lb;
+        before = run + shfl_u64(incl - ms, Lb);
+        break;
+      }
+      run += shfl_u64(incl, 31);
+    }
+    if (pos < 0) {                                  // rounding: take the last value with mass
+      pos = n - 1;
+      unsigned long long wf;
+      while (pos > 0 && mass_of(srt[pos], wf) == 0) --pos;
+      before = run - mass_of(srt[pos], wf);
+    }
+    if (lane == 0) {
+      const uint64_t e = srt[pos];
+      unsigned long long wf;
+      mass_of(e, wf);
+      const uint32_t c = static_cast<uint32_t>(e);
+      uint64_t need = (wf && tau > before) ? (tau - before + wf - 1) / wf : 1;
+      if (need < 1) need = 1;
+      if (need > c) need = c;
+      const int slot = static_cast<int>((e >> 32) & 0xffffu);
+      uint32_t acc = 0, r = static_cast<uint32_t>(need);
+      int Q = kPairs - 1;
+      for (int j = 0; j < kPairs; ++j) {
+        const uint32_t cj = T.cnt[j][slot];
+        if (acc + cj >= need) { Q = j; r = static_cast<uint32_t>(need) - acc; break; }
+        acc += cj;
+      }
+      sm.b_u64[2] = before + need * wf;
+      sm.b_i32[1] = static_cast<int>(fkey(bf16_key_value(static_cast<uint32_t>(e >> 48))));
+      sm.b_i32[2] = Q;
+      sm.b_i32[3] = static_cast<int>(r);
+    }
+  }
+  __syncthreads();
+  const uint32_t K32 = static_cast<uint32_t>(sm.b_i32[1]);
+  const unsigned long long Wf = sm.b_u64[2];
+  const int Ls = seg_len(row), Q = sm.b_i32[2];
+  const uint32_t r = static_cast<uint32_t>(sm.b_i32[3]);
+  __syncthreads();
+  const int v0 = min(row.nvec, 2 * Q * Ls), v1 = min(row.nvec, v0 + 2 * Ls);
+  const int idx = range_find_nth<DT_BF16>(row, K32, v0, v1, r, sm);
+  if (idx < 0) return false;
+  cut = composite(K32, static_cast<uint32_t>(idx));
+  W = static_cast<double>(Wf) / static_cast<double>(scale);
+  return true;
+}
+
 template <int DT>
 __device__ void full_row(const Row& row, const RowParams& P, int dtok, Smem& sm) {
   const int tid = threadIdx.x;
   float m;
-  double S;
+  double S = 0.0;
   int bad;
-  full_pass1<DT>(row, P.cT, sm, m, S, bad);
+  // top-p needs the launch's extra shared memory for key counts or bracketing
+  const bool extra = dyn_smem_bytes() >= sizeof(Smem) + sizeof(FullExtra);
+  FullExtra& fx = *reinterpret_cast<FullExtra*>(reinterpret_cast<unsigned char*>(&sm) + sizeof(Smem));
+  const bool keycount = DT == DT_BF16 && extra && P.k == 0 && P.top_p < 1.0f;
+  int kc_overflow = 1;
+  if (keycount) kc_overflow = kc_pass(row, sm, fx, m, bad);
+  // the softmax denominator of the whole row is W only with neither cut
+  else if (P.k > 0 || P.top_p < 1.0f) full_max<DT>(row, sm, m, bad);
+  else full_pass1<DT>(row, P.cT, sm, m, S, bad);
   RowStat st;
   st.path = PATH_FULL;
   st.m = m;
@@ -617,9 +1261,15 @@ __device__ void full_row(const Row& row, const RowParams& P, int dtok, Smem& sm)
     uint64_t ck = 0;
     if (P.k > 0) ck = full_select_topk<DT>(row, m, P.cT, P.k, sm);
     if (P.top_p < 1.0f) {
-      unsigned long long Wf = 0;
-      st.cut = full_select_topp<DT>(row, m, P.cT, scale, ck, P.top_p, sm, Wf);
-      st.W = static_cast<double>(Wf) / static_cast<double>(scale);
+      // key counts, else bracketing, else the radix rounds (which need no extra memory)
+      bool done = false;
+      if (keycount && !kc_overflow) done = kc_resolve(row, m, P.cT, scale, P.top_p, sm, fx, st.cut, st.W);
+      if (!done && extra) done = topp_bracketed<DT>(row, m, P.cT, ck, P.top_p, sm, fx, st.cut, st.W);
+      if (!done) {
+        unsigned long long Wf = 0;
+        st.cut = full_select_topp<DT>(row, m, P.cT, scale, ck, P.top_p, sm, Wf);
+        st.W = static_cast<double>(Wf) / static_cast<double>(scale);
+      }
     } else if (ck) {
       st.cut = ck;
       st.W = full_sum_kept<DT>(row, m, P.cT, ck, sm);
@@ -930,9 +1580,12 @@ __device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& s
 }
 
 // Probability of token x under a PATH_FULL row given its logit z.
+__device__ __forceinline__ float full_prob(float z, uint32_t x, uint64_t cut, float m, float cT, float invW) {
+  if (cut != 0ull && composite(fkey(z), x) < cut) return 0.0f;
+  return fast_exp2((z - m) * cT) * invW;
+}
 __device__ __forceinline__ float full_prob(float z, uint32_t x, const RowStat& st, float cT, float invW) {
-  if (st.cut != 0ull && composite(fkey(z), x) < st.cut) return 0.0f;
-  return fast_exp2((z - st.m) * cT) * invW;
+  return full_prob(z, x, st.cut, st.m, cT, invW);
 }
 
 }  // namespace sv

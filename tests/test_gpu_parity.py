@@ -60,6 +60,48 @@ def test_transform_probs_match_oracle(dtype, params, V):
     assert checked >= rows - 2
 
 
+def _full_rows(kind, rows, V, g):
+    from speculative_decoding_verification_44_gb300.workloads import _zipf_rows
+    if kind == "flat":                 # every element ties: the cut is an index among equals
+        return torch.zeros(rows, V)
+    if kind == "few_values":           # four values, thousands of ties each
+        return 0.5 * torch.randint(0, 4, (rows, V), generator=g).float()
+    if kind == "near_zero":            # bf16 keys spread over many binades near 0
+        return 1e-3 * torch.randn(rows, V, generator=g)
+    if kind == "randn":
+        return 3.0 * torch.randn(rows, V, generator=g)
+    return _zipf_rows(rows, V, g, 0.5, "cpu")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("kind,T", [("flat", 1.0), ("few_values", 1.0), ("near_zero", 1.0), ("randn", 1.0),
+                                    ("zipf", 0.05), ("zipf", 1.0), ("zipf", 5.0)])
+@pytest.mark.parametrize("top_p", [0.001, 0.37, 0.95, 0.9999])
+@pytest.mark.parametrize("V", [8192, 6007])
+def test_full_row_top_p_cut(dtype, kind, T, top_p, V):
+    """Top-p without top-k over whole rows: ties at the cut, many distinct keys
+    near the cut, unique float32 values, and cold / hot temperatures."""
+    import speculative_decoding_verification_44_gb300 as sv
+    g = torch.Generator().manual_seed(V + int(1000 * top_p) + int(100 * T))
+    rows = 8
+    z = _full_rows(kind, rows, V, g).to(dtype)
+    p = sv.SamplingParams(T, 0, top_p)
+    probs, status = sv.transform_probs(z.cuda(), p)
+    detail = oracle.transform_rows_detail(to_f64(z), *params_tuple(p))
+    assert (status.cpu() == 0).all()
+    got = probs.cpu().double().numpy()
+    checked = 0
+    for r, rd in enumerate(detail):
+        if rd.ambiguous_mass > TOL_PROB:
+            continue
+        np.testing.assert_allclose(got[r], rd.probs, atol=TOL_PROB, rtol=0, err_msg=f"row {r}")
+        clear = np.ones(V, dtype=bool)
+        clear[rd.ambiguous] = False
+        assert ((got[r] > 0) == (rd.probs > 0))[clear].all(), r
+        checked += 1
+    assert checked >= rows // 2
+
+
 def test_transform_textbook_softmax_third_opinion():
     import speculative_decoding_verification_44_gb300 as sv
     z = torch.randn(8, 32000, generator=torch.Generator().manual_seed(5)) * 3
