@@ -41,6 +41,21 @@ struct SampleArgs {
   float* out_aprob;
   float* out_Z;
   int32_t* out_status;
+  // full-row draws deferred to draw_kernel (target rows on PATH_FULL)
+  int defer;
+  int chunk_vecs;       // vectors per draw chunk
+  int nchunk;           // chunks per row
+  uint32_t* dcount;     // [B] chunk CTAs finished (self-cleaning)
+  struct DrawRec* drec; // [B]
+  double* dsum;         // [B][nchunk] weight sum per chunk
+};
+
+// What draw_kernel needs from the sequence epilogue; j < 0: nothing to draw.
+struct DrawRec {
+  int32_t j;       // position drawn at (the rejected draft, or gamma for the bonus)
+  int32_t flags;   // sequence status flags so far
+  int32_t mode;    // ScanCtx mode
+  int32_t dj;      // the rejected draft token (mode 3)
 };
 
 __device__ __forceinline__ RowStat load_stat(const RowStat* p) {
@@ -67,6 +82,7 @@ __device__ void write_error(const SampleArgs& a, int b, int status) {
     a.out_nacc[b] = -1;
     if (a.out_Z) a.out_Z[b] = -1.0f;
     if (a.out_status) a.out_status[b] = status;
+    if (a.defer) a.drec[b].j = -1;
   }
 }
 
@@ -89,15 +105,19 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const double* p
   return 0.0f;
 }
 
-// Inverse-CDF draw over a PATH_STREAM target row's kept list (warp 0 only).
+// Inverse-CDF draw over a PATH_STREAM target row's kept list, block-wide.
 // Residual weights max(0, p - q) [wrblog §5], or p itself for the bonus draw;
-// the token is the smallest x (vocabulary order) with C(x) > u Z.  Both kept
-// lists arrive in one round trip; entries are rank-sorted by token and the
-// running sums are double-float.
+// the token is the smallest x (vocabulary order) with C(x) > u Z.  No sort:
+// both lists arrive in one round trip, thread e takes target entry e, finds
+// q by scanning the draft list, then sums -- in double-float, in list order
+// -- Z and its own prefix C(x_e-) over the entries with smaller tokens.  The
+// draw is the smallest token whose C(x_e-) + w_e exceeds u Z (the largest
+// token with weight if rounding leaves none).
 template <int DT>
 __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
                                       const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
-  const int lane = threadIdx.x & 31;
+  static_assert(kThreads >= 2 * kListCap, "one thread per entry of both lists");
+  const int tid = threadIdx.x;
   const int slots = 2 * a.G + 1;
   SmemEpi& E = sm.u.e;
   const int nt = E.rs[r].n_list;
@@ -105,97 +125,73 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
   const int nq = draft_list ? ds.n_list : 0;
   const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
   const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
-  ListEntry te[4], qe[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {             // entry e = 4*lane + j (blocked, as the sort)
-    const int e = 4 * lane + j;
-    if (e < nt) te[j] = load_entry(tl + e);
-    if (e < nq) qe[j] = load_entry(ql + e);
+  if (tid < nt) {
+    const ListEntry t = load_entry(tl + tid);
+    E.tok[tid] = t.token;
+    E.w[tid] = t.p;
+  } else if (tid >= kListCap && tid - kListCap < nq) {
+    const ListEntry q = load_entry(ql + tid - kListCap);
+    E.qtok[tid - kListCap] = q.token;
+    E.qp[tid - kListCap] = q.p;
   }
-  if (draft_list) {                          // token-sorted draft list for lookups
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = 4 * lane + j;
-      if (e < nq) {
-        E.tok[e] = qe[j].token;
-        E.w[e] = qe[j].p;
+  if (tid == 0) {
+    sm.b_i32[3] = 0x7fffffff;
+    sm.b_i32[6] = -1;
+  }
+  __syncthreads();
+  int mytok = 0;
+  if (tid < nt) {
+    mytok = E.tok[tid];
+    const double p = E.w[tid];
+    double w = p;
+    if (residual) {
+      double q = 0.0;
+      if (onehot) q = (mytok == dj) ? 1.0 : 0.0;
+      else if (draft_list) {
+        for (int f = 0; f < nq; ++f)
+          if (E.qtok[f] == mytok) q = E.qp[f];
+      } else {
+        const Row drow = seq_row<DT>(a, b, r, true);
+        q = full_prob(load_elem<DT>(drow.base, mytok), static_cast<uint32_t>(mytok), cut_test(ds.cut), ds.m,
+                      a.dp.cT, static_cast<float>(1.0 / ds.W));
       }
+      w = fmax(p - q, 0.0);
     }
-    __syncwarp();
-    for (int e = lane; e < nq; e += 32) {
-      int rank = 0;
-      for (int j = 0; j < nq; ++j) rank += E.tok[j] < E.tok[e] ? 1 : 0;
-      E.qtok[rank] = E.tok[e];
-      E.qp[rank] = E.w[e];
-    }
-    __syncwarp();
+    const float wh = static_cast<float>(w), ph = static_cast<float>(p);
+    E.wh[tid] = wh;
+    E.wl[tid] = static_cast<float>(w - static_cast<double>(wh));
+    E.ph[tid] = ph;
+    E.pl[tid] = static_cast<float>(p - static_cast<double>(ph));
   }
-  const Row drow = seq_row<DT>(a, b, r, true);
-  const float invWd = (residual && !onehot && ds.path == PATH_FULL) ? static_cast<float>(1.0 / ds.W) : 0.0f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int e = 4 * lane + j;
-    if (e < nt) {
-      const ListEntry t = te[j];
-      double w = t.p;
-      if (residual) {
-        double q;
-        if (onehot) q = (t.token == dj) ? 1.0 : 0.0;
-        else if (ds.path == PATH_STREAM) q = list_lookup(E.qtok, E.qp, nq, t.token);
-        else q = full_prob(load_elem<DT>(drow.base, t.token), static_cast<uint32_t>(t.token), ds, a.dp.cT, invWd);
-        w = fmax(t.p - q, 0.0);
-      }
-      E.tok[kListCap + e] = t.token;
-      E.w[kListCap + e] = w;
-      E.sw[e] = t.p;                         // p, for a Z == 0 fallback
-    }
-  }
-  __syncwarp();
-  for (int e = lane; e < nt; e += 32) {      // rank sort by token (distinct within a list)
-    int rank = 0;
-    const int tk = E.tok[kListCap + e];
-    for (int j = 0; j < nt; ++j) rank += E.tok[kListCap + j] < tk ? 1 : 0;
-    E.stok[rank] = tk;
-    E.tok[rank] = e;                         // original position
-  }
-  __syncwarp();
+  __syncthreads();
   for (int pass = 0; pass < 2; ++pass) {
-    float w[4];
-    df s = df_from(0.0f);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int pos = 4 * lane + j;
-      const int e = pos < nt ? E.tok[pos] : 0;
-      w[j] = pos < nt ? static_cast<float>(pass == 0 ? E.w[kListCap + e] : E.sw[e]) : 0.0f;
-      s = df_add(s, df_from(w[j]));
+    const float* H = pass == 0 ? E.wh : E.ph;
+    const float* Lo = pass == 0 ? E.wl : E.pl;
+    df Z = df_from(0.0f), pre = df_from(0.0f);
+    for (int f = 0; f < nt; ++f) {               // every thread: the same Z, in the same order
+      const df wf = {H[f], Lo[f]};
+      Z = df_add(Z, wf);
+      if (tid < nt && E.tok[f] < mytok) pre = df_add(pre, wf);
     }
-    const df incl = warp_incl_scan_df(s, lane);
-    const df Z = df_shfl(incl, 31);
     if (pass == 0 && residual) Z_resid = df_to_double(Z);
     if (!(Z.hi > 0.0f)) {
-      if (pass == 0 && residual) { flags |= SEQ_FLAG_Z_ZERO; continue; }
+      if (pass == 0 && residual) {               // Z == 0 after a rejection: draw from p instead
+        flags |= SEQ_FLAG_Z_ZERO;
+        continue;
+      }
+      return -1;
     }
     const float uf = static_cast<float>(u);
     const float th = uf * Z.hi;
     const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
-    df acc = df_add(incl, {-s.hi, -s.lo});
-    int found = 0x7fffffff, last = -1;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int pos = 4 * lane + j;
-      if (pos < nt && w[j] > 0.0f) {
-        acc = df_add(acc, df_from(w[j]));
-        last = pos;
-        if (found == 0x7fffffff && !df_ge(t, acc)) found = pos;    // C(x) > t
-      }
+    if (tid < nt && H[tid] > 0.0f) {
+      if (!df_ge(t, df_add(pre, {H[tid], Lo[tid]}))) atomicMin(&sm.b_i32[3], mytok);   // C(x) > t
+      atomicMax(&sm.b_i32[6], mytok);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      found = min(found, __shfl_xor_sync(kFull, found, o));
-      last = max(last, __shfl_xor_sync(kFull, last, o));
-    }
-    const int pos = found != 0x7fffffff ? found : last;
-    return pos >= 0 ? E.stok[pos] : -1;
+    __syncthreads();
+    const int sel = sm.b_i32[3] != 0x7fffffff ? sm.b_i32[3] : sm.b_i32[6];
+    __syncthreads();
+    return sel;
   }
   return -1;
 }
@@ -205,7 +201,7 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
 // token-sorted list; 3: (p - delta_dj)+.
 struct ScanCtx {
   Row trow, drow;
-  uint64_t cutt, cutd;   // kept iff composite >= cut
+  CutTest ctt, ctd;      // kept sets of the target and draft rows
   float mt, md;          // row maxima
   float cTt, cTd, invWt, invWd;
   int mode;
@@ -234,9 +230,9 @@ __device__ __forceinline__ float scan_weights(const ScanCtx& c, int v, int n, co
     float we = 0.0f;
     if (e < n) {
       const uint32_t x = static_cast<uint32_t>(v * P + e);
-      const float p = full_prob(zt[e], x, c.cutt, c.mt, c.cTt, c.invWt);
+      const float p = full_prob(zt[e], x, c.ctt, c.mt, c.cTt, c.invWt);
       float q = 0.0f;
-      if (c.mode == 1) q = full_prob(zd[e], x, c.cutd, c.md, c.cTd, c.invWd);
+      if (c.mode == 1) q = full_prob(zd[e], x, c.ctd, c.md, c.cTd, c.invWd);
       else if (c.mode == 2) q = list_lookup(sm.u.e.qtok, sm.u.e.qp, c.nq, static_cast<int>(x));
       else if (c.mode == 3) q = (static_cast<int>(x) == c.dj) ? 1.0f : 0.0f;
       we = c.mode == 0 ? p : fmaxf(p - q, 0.0f);
@@ -255,7 +251,7 @@ __device__ __forceinline__ float scan_weights(const ScanCtx& c, int v, int n, co
 // from the sums, and one warp re-scans that chunk alone with identical
 // arithmetic to locate the first x with C(x) > u Z.
 template <int DT>
-__device__ __noinline__ int block_scan_draw(ScanCtx& c, double u, bool residual, double& Z_resid, int& flags, Smem& sm) {
+__device__ __noinline__ int block_scan_draw(ScanCtx c, double u, bool residual, double& Z_resid, int& flags, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   constexpr int kStep = 32 * kScanUnroll;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -383,6 +379,47 @@ __device__ __noinline__ int block_scan_draw(ScanCtx& c, double u, bool residual,
   return -1;
 }
 
+// Scan context of a full-row draw at position r.  Block-wide: mode 2 stages
+// the draft's kept list, sorted by token, in shared memory.
+template <int DT>
+__device__ ScanCtx make_scan(const SampleArgs& a, int b, int r, int mode, bool onehot, const RowStat& ts,
+                             const RowStat& ds, int dj, Smem& sm) {
+  const int tid = threadIdx.x;
+  const int slots = 2 * a.G + 1;
+  ScanCtx c;
+  c.trow = seq_row<DT>(a, b, r, false);
+  c.drow = (mode != 0 && !onehot) ? seq_row<DT>(a, b, r, true) : c.trow;
+  c.ctt = cut_test(ts.cut);
+  c.mt = ts.m;
+  c.ctd = cut_test(ds.cut);
+  c.md = ds.m;
+  c.cTt = a.tp.cT;
+  c.cTd = a.dp.cT;
+  c.invWt = static_cast<float>(1.0 / ts.W);
+  c.invWd = static_cast<float>(1.0 / ds.W);
+  c.dj = dj;
+  c.nq = 0;
+  c.mode = mode;
+  if (mode == 2) {
+    const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
+    c.nq = ds.n_list;
+    if (tid < c.nq) {
+      const ListEntry q = load_entry(ql + tid);
+      sm.u.e.tok[tid] = q.token;
+      sm.u.e.w[tid] = q.p;
+    }
+    __syncthreads();
+    if (tid < c.nq) {
+      int rank = 0;
+      for (int jj = 0; jj < c.nq; ++jj) rank += sm.u.e.tok[jj] < sm.u.e.tok[tid] ? 1 : 0;
+      sm.u.e.qtok[rank] = sm.u.e.tok[tid];
+      sm.u.e.qp[rank] = sm.u.e.w[tid];
+    }
+    __syncthreads();
+  }
+  return c;
+}
+
 // Sequence epilogue, run by the CTA that analysed the sequence's last row.
 template <int DT>
 __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb, bool onehot, Smem& sm) {
@@ -497,51 +534,24 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   const double u = static_cast<double>(a.u_samp[b]);
   double Z_resid = -1.0;
   int tok = -1;
+  bool deferred = false;
   if (ts.path == PATH_STREAM) {
-    if (warp == 0) {
-      tok = list_draw<DT>(a, b, r, residual, onehot, dj, ds, u, Z_resid, flags, sm);
-      if (lane == 0) {
-        sm.b_i32[3] = tok;
-        sm.b_i32[5] = flags;
-        sm.b_f64[2] = Z_resid;
-      }
+    tok = list_draw<DT>(a, b, r, residual, onehot, dj, ds, u, Z_resid, flags, sm);
+  } else if (a.defer) {
+    // a full-row draw: draw_kernel does it, chunk-parallel, and writes the drawn
+    // token, residual_Z and status
+    if (tid == 0) {
+      DrawRec rec;
+      rec.j = j;
+      rec.flags = flags;
+      rec.mode = !residual ? 0 : (onehot ? 3 : (ds.path == PATH_FULL ? 1 : 2));
+      rec.dj = dj;
+      a.drec[b] = rec;
     }
-    __syncthreads();
-    tok = sm.b_i32[3];
-    flags = sm.b_i32[5];
-    Z_resid = sm.b_f64[2];
+    deferred = true;
   } else {
-    ScanCtx c;
-    c.trow = seq_row<DT>(a, b, r, false);
-    c.drow = (residual && !onehot) ? seq_row<DT>(a, b, r, true) : c.trow;
-    c.cutt = ts.cut;
-    c.mt = ts.m;
-    c.cutd = ds.cut;
-    c.md = ds.m;
-    c.cTt = a.tp.cT;
-    c.cTd = a.dp.cT;
-    c.invWt = static_cast<float>(1.0 / ts.W);
-    c.invWd = static_cast<float>(1.0 / ds.W);
-    c.dj = dj;
-    c.nq = 0;
-    c.mode = !residual ? 0 : (onehot ? 3 : (ds.path == PATH_FULL ? 1 : 2));
-    if (c.mode == 2) {   // token-sorted draft list in shared memory
-      const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
-      c.nq = ds.n_list;
-      if (tid < c.nq) {
-        const ListEntry q = load_entry(ql + tid);
-        sm.u.e.tok[tid] = q.token;
-        sm.u.e.w[tid] = q.p;
-      }
-      __syncthreads();
-      if (tid < c.nq) {
-        int rank = 0;
-        for (int jj = 0; jj < c.nq; ++jj) rank += sm.u.e.tok[jj] < sm.u.e.tok[tid] ? 1 : 0;
-        sm.u.e.qtok[rank] = sm.u.e.tok[tid];
-        sm.u.e.qp[rank] = sm.u.e.w[tid];
-      }
-      __syncthreads();
-    }
+    const int mode = !residual ? 0 : (onehot ? 3 : (ds.path == PATH_FULL ? 1 : 2));
+    ScanCtx c = make_scan<DT>(a, b, r, mode, onehot, ts, ds, dj, sm);
     tok = block_scan_draw<DT>(c, u, residual, Z_resid, flags, sm);
   }
 
@@ -551,12 +561,14 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     int v = -1;
     if (t < j) v = a.tokens[tokb + t];
     else if (t == j) v = tok;
-    a.out_tokens[ob + t] = v;
+    if (t != j || !deferred) a.out_tokens[ob + t] = v;
   }
   if (tid == 0) {
     a.out_nacc[b] = j;
-    if (a.out_Z) a.out_Z[b] = residual ? static_cast<float>(Z_resid) : -1.0f;
-    if (a.out_status) a.out_status[b] = flags;
+    if (!deferred) {
+      if (a.out_Z) a.out_Z[b] = residual ? static_cast<float>(Z_resid) : -1.0f;
+      if (a.out_status) a.out_status[b] = flags;
+    }
   }
 }
 
@@ -578,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   if (!is_draft && i > gb) return;
   if (is_draft && (onehot || i >= gb)) return;
 
-  const RowParams& P = is_draft ? a.dp : a.tp;
+  const RowParams P = is_draft ? a.dp : a.tp;
   const Row row = seq_row<DT>(a, b, i, is_draft);
   int dtok = -1;
   if (i < gb) {
@@ -613,6 +625,173 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   sample_epilogue<DT>(a, b, gb, onehot, sm);
   __syncthreads();
   if (threadIdx.x == 0) a.counters[b] = 0u;   // leave the workspace reusable
+}
+
+// ------------------------------------------------------------------ chunk-parallel full-row draw
+// The residual or bonus draw over a PATH_FULL target row reads up to two whole
+// rows; one CTA doing it alone is latency-bound.  Here every sequence with a
+// pending draw gets nchunk CTAs: CTA (b, c) sums the draw weights of chunk c
+// (chunk_vecs vectors of the row, in vocabulary order) into dsum[b][c]; the
+// last of them to finish forms Z = sum_c dsum[b][c] in chunk order, finds the
+// chunk whose range of the cumulative sum holds u Z, and re-scans that chunk
+// block-wide with identical per-element arithmetic for the first x with
+// C(x) > u Z [wrblog §5, §6].  Z == 0 after a rejection falls back to the
+// draw from p, over the whole row, as the sequence epilogue did.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
+  constexpr int P = Elem<DT>::kPer;
+  constexpr int kVPT = 4;   // vectors per thread in a chunk (chunk_vecs == kVPT * kThreads)
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int b = blockIdx.x, ch = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const DrawRec rec = a.drec[b];
+  if (rec.j < 0) return;
+  const int slots = 2 * a.G + 1;
+  const bool onehot = a.dft == nullptr || (a.onehot != nullptr && a.onehot[b] != 0);
+  const bool residual = rec.mode != 0;
+  const RowStat* S = a.stats + static_cast<size_t>(b) * slots;
+  const RowStat ts = load_stat(S + rec.j);
+  RowStat ds;
+  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0;
+  if (residual && !onehot) ds = load_stat(S + a.G + 1 + rec.j);
+  ScanCtx c = make_scan<DT>(a, b, rec.j, rec.mode, onehot, ts, ds, rec.dj, sm);
+  const int nv = c.trow.nvec;
+
+  // 1. this chunk's weight sum
+  {
+    const int v0 = ch * a.chunk_vecs;
+    uint4 rt[kVPT], rd[kVPT];
+    int n[kVPT];
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+      const int v = v0 + i * kThreads + tid;
+      n[i] = v < nv ? scan_load<DT>(c, v, rt[i], rd[i]) : 0;
+    }
+    float ls = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+      float w[P];
+      if (n[i]) ls += scan_weights<DT>(c, v0 + i * kThreads + tid, n[i], rt[i], rd[i], sm, w);
+    }
+    const double cs = block_sum_d(static_cast<double>(ls), sm);
+    if (tid == 0) {
+      a.dsum[static_cast<size_t>(b) * a.nchunk + ch] = cs;
+      __threadfence();
+      const unsigned prev = atomicAdd(&a.dcount[b], 1u);
+      sm.b_i32[7] = (prev + 1u == static_cast<unsigned>(a.nchunk)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!sm.b_i32[7]) return;
+    __threadfence();
+  }
+
+  // 2. the last chunk CTA: Z, the chunk holding u Z, the element inside it
+  const double* D = a.dsum + static_cast<size_t>(b) * a.nchunk;
+  const double u = static_cast<double>(a.u_samp[b]);
+  int flags = rec.flags;
+  if (warp == 0) {
+    double Z = 0.0;
+    for (int base = 0; base < a.nchunk; base += 32) {
+      const int k = base + lane;
+      Z += warp_sum_f64(k < a.nchunk ? __ldcg(D + k) : 0.0);
+    }
+    const double t = u * Z;
+    double run = 0.0, tl = 0.0, last_start = 0.0;
+    int K = -1, lastK = -1;
+    for (int base = 0; base < a.nchunk && K < 0; base += 32) {
+      const int k = base + lane;
+      const double cs = k < a.nchunk ? __ldcg(D + k) : 0.0;
+      const double incl = warp_incl_scan_f64(cs, lane);
+      const unsigned hit = __ballot_sync(kFull, cs > 0.0 && run + incl > t);
+      const unsigned pos = __ballot_sync(kFull, cs > 0.0);
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        K = base + L;
+        tl = t - (run + __shfl_sync(kFull, incl - cs, L));
+      } else if (pos) {
+        const int L = 31 - __clz(pos);
+        lastK = base + L;
+        last_start = run + __shfl_sync(kFull, incl - cs, L);
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+    if (K < 0) { K = lastK; tl = t - last_start; }     // rounding: the last chunk with weight
+    if (lane == 0) {
+      sm.b_f64[0] = Z;
+      sm.b_f64[1] = tl;
+      sm.b_i32[4] = K;
+    }
+  }
+  __syncthreads();
+  const double Z = sm.b_f64[0];
+  int tok = -1;
+  if (!(Z > 0.0) || sm.b_i32[4] < 0) {
+    // no weight at all: after a rejection draw from p over the whole row
+    if (residual) {
+      flags |= SEQ_FLAG_Z_ZERO;
+      c.mode = 0;
+      double Zp;
+      tok = block_scan_draw<DT>(c, u, false, Zp, flags, sm);
+    }
+  } else {
+    // block-wide re-scan of chunk K: thread t takes kVPT consecutive vectors
+    const double tl = sm.b_f64[1];
+    const int v0 = sm.b_i32[4] * a.chunk_vecs + tid * kVPT;
+    float w[kVPT][P];
+    float ts_sum = 0.0f;
+    int last_pos = -1;
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+      const int v = v0 + i;
+      uint4 rt, rd;
+      const int n = v < nv ? scan_load<DT>(c, v, rt, rd) : 0;
+      if (n) ts_sum += scan_weights<DT>(c, v, n, rt, rd, sm, w[i]);
+      else {
+#pragma unroll
+        for (int e = 0; e < P; ++e) w[i][e] = 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < P; ++e) if (w[i][e] > 0.0f) last_pos = v * P + e;
+    }
+    // exclusive prefix of the per-thread sums, in thread (= vocabulary) order
+    const double incl = warp_incl_scan_f64(static_cast<double>(ts_sum), lane);
+    if (lane == 31) sm.u.e.wtot[warp] = incl;
+    if (tid == 0) { sm.b_i32[5] = -1; sm.b_i32[6] = -1; }
+    __syncthreads();
+    double wbase = 0.0;
+    for (int k = 0; k < warp; ++k) wbase += sm.u.e.wtot[k];
+    const double base = wbase + incl - static_cast<double>(ts_sum);
+    const bool mine = ts_sum > 0.0f && base + static_cast<double>(ts_sum) > tl;
+    if (mine) atomicMin(reinterpret_cast<unsigned*>(&sm.b_i32[5]), static_cast<unsigned>(tid));
+    if (last_pos >= 0) atomicMax(&sm.b_i32[6], last_pos);
+    __syncthreads();
+    if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
+      float c32 = 0.0f;
+      int found = -1, lastp = -1;
+#pragma unroll
+      for (int i = 0; i < kVPT; ++i) {
+#pragma unroll
+        for (int e = 0; e < P; ++e) {
+          if (w[i][e] > 0.0f) {
+            c32 += w[i][e];
+            lastp = (v0 + i) * P + e;
+            if (found < 0 && base + static_cast<double>(c32) > tl) found = lastp;
+          }
+        }
+      }
+      sm.b_i32[7] = found >= 0 ? found : lastp;
+    }
+    if (tid == 0 && sm.b_i32[5] == -1) sm.b_i32[7] = sm.b_i32[6];   // rounding: last weighted element
+    __syncthreads();
+    tok = sm.b_i32[7];
+  }
+  if (tid == 0) {
+    a.out_tokens[static_cast<size_t>(b) * (a.G + 1) + rec.j] = tok;
+    if (a.out_Z) a.out_Z[b] = residual ? static_cast<float>(Z) : -1.0f;
+    if (a.out_status) a.out_status[b] = flags;
+    a.dcount[b] = 0u;   // leave the workspace reusable
+  }
 }
 
 // ------------------------------------------------------------------ greedy
@@ -713,8 +892,9 @@ __global__ void __launch_bounds__(kThreads, 5) transform_kernel(const char* logi
       for (int e = threadIdx.x; e < st.n_list; e += kThreads) o[sm.list_tok[e]] = static_cast<float>(sm.list_p[e]);
   } else {
     const float invW = static_cast<float>(1.0 / st.W);
+    const CutTest ct = cut_test(st.cut);
     for (int x = threadIdx.x; x < V; x += kThreads)
-      o[x] = full_prob(load_elem<DT>(row.base, x), static_cast<uint32_t>(x), st, P.cT, invW);
+      o[x] = full_prob(load_elem<DT>(row.base, x), static_cast<uint32_t>(x), ct, st.m, P.cT, invW);
   }
   if (out_status && threadIdx.x == 0) out_status[r] = st.status;
 }
@@ -761,17 +941,32 @@ bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t elem_bytes(spec_dtype_t dt) { return dt == SPEC_BF16 ? 2 : 4; }
 int elems_per_vec(spec_dtype_t dt) { return dt == SPEC_BF16 ? 8 : 4; }
 
+constexpr int kChunkVecs = 4 * kThreads;   // draw_kernel: vectors per chunk (four per thread)
+
+// Chunks per row of the full-row draw (float32 rows have the most vectors).
+int draw_chunks(int V, spec_dtype_t dt) {
+  const long long nvec = (static_cast<long long>(V) + elems_per_vec(dt) - 1) / elems_per_vec(dt);
+  return static_cast<int>((nvec + kChunkVecs - 1) / kChunkVecs);
+}
+
+// Workspace: the two per-sequence counter arrays come first -- the only part
+// that must be zero when a call starts (kernels leave them zero again).
 struct SampleLayout {
-  size_t counters, stats, lists, total;
+  size_t counters, dcount, stats, lists, drec, dsum, total;
 };
-SampleLayout sample_layout(int B, int G, const RowParams& tp, const RowParams& dp) {
+size_t zero_region_bytes(int B) { return 2 * round_up(static_cast<size_t>(B) * sizeof(uint32_t)); }
+SampleLayout sample_layout(int B, int G, int V, const RowParams& tp, const RowParams& dp) {
   SampleLayout L;
   const size_t slots = static_cast<size_t>(2 * G + 1);
   L.counters = 0;
-  L.stats = round_up(static_cast<size_t>(B) * sizeof(uint32_t));
+  L.dcount = round_up(static_cast<size_t>(B) * sizeof(uint32_t));
+  L.stats = zero_region_bytes(B);
   L.lists = L.stats + round_up(static_cast<size_t>(B) * slots * sizeof(RowStat));
   const bool need_lists = tp.path == PATH_STREAM || dp.path == PATH_STREAM;
-  L.total = L.lists + (need_lists ? round_up(static_cast<size_t>(B) * slots * kListCap * sizeof(ListEntry)) : 0);
+  L.drec = L.lists + (need_lists ? round_up(static_cast<size_t>(B) * slots * kListCap * sizeof(ListEntry)) : 0);
+  const bool defer = tp.path == PATH_FULL;
+  L.dsum = L.drec + (defer ? round_up(static_cast<size_t>(B) * sizeof(DrawRec)) : 0);
+  L.total = L.dsum + (defer ? round_up(static_cast<size_t>(B) * draw_chunks(V, SPEC_F32) * sizeof(double)) : 0);
   return L;
 }
 
@@ -795,7 +990,7 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
-std::atomic<uint64_t> g_ready[6];   // sample, greedy, transform x {bf16, f32}
+std::atomic<uint64_t> g_ready[8];   // sample, greedy, transform, draw x {bf16, f32}
 
 // Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
 // needs FullExtra after Smem; launches without such rows keep their occupancy.
@@ -826,7 +1021,7 @@ spec_status_t spec_verify_workspace_size(int32_t batch, int32_t gamma_max, int32
   if (!bytes || !shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
     return SPEC_ERR_INVALID_ARG;
   if (gamma_max > kMaxGamma) return SPEC_ERR_UNSUPPORTED;
-  *bytes = sample_layout(batch, gamma_max, make_row_params(target_params, vocab, SPEC_BF16),
+  *bytes = sample_layout(batch, gamma_max, vocab, make_row_params(target_params, vocab, SPEC_BF16),
                          make_row_params(draft_params, vocab, SPEC_BF16)).total;
   return SPEC_OK;
 }
@@ -865,7 +1060,7 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   SampleArgs a;
   a.tp = make_row_params(target_params, vocab, dtype);
   a.dp = make_row_params(draft_params, vocab, dtype);
-  const SampleLayout L = sample_layout(batch, gamma_max, a.tp, a.dp);
+  const SampleLayout L = sample_layout(batch, gamma_max, vocab, a.tp, a.dp);
   if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   a.tgt = static_cast<const char*>(target_logits);
@@ -889,15 +1084,26 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   a.out_aprob = out_accept_prob;
   a.out_Z = out_residual_z;
   a.out_status = out_status;
+  a.defer = a.tp.path == PATH_FULL ? 1 : 0;
+  a.chunk_vecs = kChunkVecs;
+  a.nchunk = draw_chunks(vocab, dtype);
+  a.dcount = reinterpret_cast<uint32_t*>(ws + L.dcount);
+  a.drec = reinterpret_cast<DrawRec*>(ws + L.drec);
+  a.dsum = reinterpret_cast<double*>(ws + L.dsum);
   const unsigned grid = static_cast<unsigned>(batch) * static_cast<unsigned>(2 * gamma_max + 1);
+  const dim3 dgrid(static_cast<unsigned>(batch), static_cast<unsigned>(a.nchunk));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (dtype == SPEC_BF16) {
     err = prepare(sample_kernel<DT_BF16>, g_ready[0]);
     if (err == cudaSuccess) sample_kernel<DT_BF16><<<grid, kThreads, smem_for(a.tp, a.dp), s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6]);
+    if (err == cudaSuccess && a.defer) draw_kernel<DT_BF16><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
   } else {
     err = prepare(sample_kernel<DT_F32>, g_ready[1]);
     if (err == cudaSuccess) sample_kernel<DT_F32><<<grid, kThreads, smem_for(a.tp, a.dp), s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_F32>, g_ready[7]);
+    if (err == cudaSuccess && a.defer) draw_kernel<DT_F32><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
@@ -1026,9 +1232,8 @@ extern "C" SPEC_API spec_status_t spec_verify_sample_noalloc(
   void* scratch = nullptr;
   if (static_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
   // The per-sequence counters at the start of the scratch must be zero when the
-  // kernel starts; clear them on the caller's stream.
-  const size_t counters = static_cast<size_t>(batch) * sizeof(uint32_t);
-  if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // kernels start; clear them on the caller's stream.
+  if (cudaMemsetAsync(scratch, 0, zero_region_bytes(batch), static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return spec_verify_sample(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
                             draft_is_onehot, u_accept, u_sample, target_params, draft_params, batch,

@@ -107,6 +107,12 @@ __device__ __forceinline__ uint32_t atoms_cas_u32(uint32_t a, uint32_t cmp, uint
 __device__ __forceinline__ void reds_add_u32(uint32_t a, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
+// red.shared only where pred holds: a predicated instruction, no branch.
+__device__ __forceinline__ void reds_add_u32_if(uint32_t a, uint32_t v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p red.shared.add.u32 [%0], %1;\n\t}"
+      ::"r"(a), "r"(v), "r"(static_cast<uint32_t>(pred)) : "memory");
+}
 
 // ---------------------------------------------------------------- loads
 // Streaming 16-byte load: read once, do not keep in L1, ask L2 to fetch 256 B.
@@ -147,7 +153,7 @@ __device__ __forceinline__ Row make_row(const void* base, int V, bool aligned) {
 
 // Loads virtual vector v; returns the number of valid elements (0 if v is past the end).
 template <int DT, bool kStream>
-__device__ __forceinline__ int load_vec(const Row& row, int v, uint4& out) {
+__device__ __forceinline__ int load_vec(const Row row, int v, uint4& out) {
   constexpr int P = Elem<DT>::kPer;
   out = make_uint4(0u, 0u, 0u, 0u);
   if (v >= row.nvec) return 0;
@@ -170,6 +176,18 @@ __device__ __forceinline__ int load_vec(const Row& row, int v, uint4& out) {
     out = make_uint4(w[0], w[1], w[2], w[3]);
   }
   return n;
+}
+
+// load_vec for a caller that has already branched on row.aligned and
+// guarantees v < row.nvec: the aligned case is one load and no branches.
+template <int DT, bool kStream, bool kAligned>
+__device__ __forceinline__ int load_vec_as(const Row row, int v, uint4& out) {
+  if (kAligned) {
+    const void* p = row.base + static_cast<size_t>(v) * 16;
+    out = kStream ? ld_stream(p) : ld_reread(p);
+    return Elem<DT>::kPer;
+  }
+  return load_vec<DT, kStream>(row, v, out);
 }
 
 // One element by index (scalar load).

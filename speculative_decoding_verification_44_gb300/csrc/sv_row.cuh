@@ -72,12 +72,12 @@ struct __align__(16) SmemFull {
   uint32_t wcnt[kWarps];
 };
 struct __align__(16) SmemEpi {
-  double w[2 * kListCap];            // candidate weights (list-based draw)
+  double w[2 * kListCap];            // kept-list entries (list draw; draft list staging)
   int32_t tok[2 * kListCap];
-  double sw[2 * kListCap];           // sorted by token
-  int32_t stok[2 * kListCap];
-  int32_t qtok[kListCap];            // draft kept list sorted by token (binary search)
+  int32_t qtok[kListCap];            // draft kept list (sorted by token for the block scan's lookups)
   double qp[kListCap];
+  float wh[kListCap], wl[kListCap];  // list draw: weights and p as double-float
+  float ph[kListCap], pl[kListCap];
   double wtot[kWarps];               // per-warp segment totals of the block scan
   double csum[kWarps][kScanChunks];  // per-chunk totals of the block scan
   RowStat rs[2 * kMaxGamma + 1];     // the sequence's row summaries
@@ -236,7 +236,7 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, Smem& sm) {
 // ------------------------------------------------------------------ greedy row
 // argmax_x z(x), lowest index on ties [wrblog §7.1]; status for NaN / +inf / all -inf.
 template <int DT>
-__device__ void greedy_row(const Row& row, Smem& sm, int& argmax, int& status) {
+__device__ void greedy_row(const Row row, Smem& sm, int& argmax, int& status) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x;
   float best = -__int_as_float(0x7f800000);
@@ -285,7 +285,7 @@ __device__ __forceinline__ int tbin_of(float t) {
 
 // Pass 1: maximum and softmax denominator of the whole row.
 template <int DT>
-__device__ void full_pass1(const Row& row, float cT, Smem& sm, float& m_out, double& S_out, int& bad_out) {
+__device__ void full_pass1(const Row row, float cT, Smem& sm, float& m_out, double& S_out, int& bad_out) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x;
   const float NEG_INF = -__int_as_float(0x7f800000);
@@ -335,7 +335,7 @@ __device__ void full_pass1(const Row& row, float cT, Smem& sm, float& m_out, dou
 
 // Sum over the kept set {composite >= cut} of 2^((z - m) cT), float64 across threads.
 template <int DT>
-__device__ __noinline__ double full_sum_kept(const Row& row, float m, float cT, uint64_t cut, Smem& sm) {
+__device__ __noinline__ double full_sum_kept(const Row row, float m, float cT, uint64_t cut, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x;
   float s = 0.0f, comp = 0.0f;
@@ -367,7 +367,7 @@ __device__ __noinline__ double full_sum_kept(const Row& row, float m, float cT, 
 
 // Warp segments: warp w owns the contiguous vectors [w L, (w + 1) L) of a row,
 // so counts per warp are counts per index range.
-__device__ __forceinline__ int seg_len(const Row& row) { return (row.nvec + kWarps - 1) / kWarps; }
+__device__ __forceinline__ int seg_len(const Row row) { return (row.nvec + kWarps - 1) / kWarps; }
 
 // Raw element bits that carry order key K: the value's own bits and, for a
 // zero, those of -0 as well (keys fold -0 onto +0).
@@ -398,7 +398,7 @@ struct KeyBits {
 // every warp counts K in one eighth of it (kUnroll loads in flight per lane)
 // and the range shrinks to the eighth holding the r-th; one warp then scans.
 template <int DT>
-__device__ __noinline__ int range_find_nth(const Row& row, uint32_t K, int v0, int v1, uint32_t r, Smem& sm) {
+__device__ __noinline__ int range_find_nth(const Row row, uint32_t K, int v0, int v1, uint32_t r, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const KeyBits<DT> kb(K);
@@ -470,7 +470,7 @@ __device__ __noinline__ int range_find_nth(const Row& row, uint32_t K, int v0, i
 
 // Index of the n-th (1-based) element, in index order, whose key equals K.
 template <int DT>
-__device__ __forceinline__ int find_nth_with_key(const Row& row, uint32_t K, uint32_t n, Smem& sm) {
+__device__ __forceinline__ int find_nth_with_key(const Row row, uint32_t K, uint32_t n, Smem& sm) {
   return range_find_nth<DT>(row, K, 0, row.nvec, n, sm);
 }
 
@@ -480,7 +480,7 @@ __device__ __forceinline__ int find_nth_with_key(const Row& row, uint32_t K, uin
 // composite byte at `shift`.  Accumulates counts, fixed-point masses (when
 // with_mass) and the largest composite per digit.
 template <int DT>
-__device__ __noinline__ void full_round(const Row& row, float m, float cT, float scale, uint64_t ck, int tb,
+__device__ __noinline__ void full_round(const Row row, float m, float cT, float scale, uint64_t ck, int tb,
                            uint64_t prefix, uint64_t mask, int kind, int shift, bool with_mass,
                            Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
@@ -522,7 +522,7 @@ __device__ __noinline__ void full_round(const Row& row, float m, float cT, float
 
 // k-th largest composite of the row (count-based radix select).
 template <int DT>
-__device__ __noinline__ uint64_t full_select_topk(const Row& row, float m, float cT, int k, Smem& sm) {
+__device__ __noinline__ uint64_t full_select_topk(const Row row, float m, float cT, int k, Smem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint64_t prefix = 0, mask = 0;
   uint32_t need = static_cast<uint32_t>(k);
@@ -562,7 +562,7 @@ __device__ __noinline__ uint64_t full_select_topk(const Row& row, float m, float
 // cumulative mass (descending order) reaches top_p of the kept mass.  Returns
 // c* and the fixed-point kept mass through c*.
 template <int DT>
-__device__ __noinline__ uint64_t full_select_topp(const Row& row, float m, float cT, float scale, uint64_t ck,
+__device__ __noinline__ uint64_t full_select_topp(const Row row, float m, float cT, float scale, uint64_t ck,
                                      float top_p, Smem& sm, unsigned long long& Wfixed) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // round 0: log-probability buckets, ascending = descending probability
@@ -750,7 +750,7 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
 
 // Pass 1: row maximum and the NaN / +inf flag only.
 template <int DT>
-__device__ void full_max(const Row& row, Smem& sm, float& m_out, int& bad_out) {
+__device__ void full_max(const Row row, Smem& sm, float& m_out, int& bad_out) {
   const int tid = threadIdx.x;
   float m = -__int_as_float(0x7f800000);
   bool bad = false;
@@ -773,7 +773,7 @@ __device__ void full_max(const Row& row, Smem& sm, float& m_out, int& bad_out) {
 
 // Step 1: approximate kept mass per class into fx.csum.
 template <int DT>
-__device__ __noinline__ void topp_bucket_pass(const Row& row, float m, float cT, uint64_t ck, Level L,
+__device__ __noinline__ void topp_bucket_pass(const Row row, float m, float cT, uint64_t ck, Level L,
                                               Smem& sm, FullExtra& fx) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -852,7 +852,7 @@ __device__ __forceinline__ bool table_count(uint32_t keys, uint32_t cntw, uint32
 // Step 2: exact mass above and below classes [lo, hi]; keys inside counted.
 // Returns 1 if the table overflowed.
 template <int DT>
-__device__ __noinline__ int topp_exact_pass(const Row& row, float m, float cT, uint64_t ck, Level L, int lo,
+__device__ __noinline__ int topp_exact_pass(const Row row, float m, float cT, uint64_t ck, Level L, int lo,
                                             int hi, Smem& sm, FullExtra& fx, double& above, double& below) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -904,7 +904,7 @@ __device__ __noinline__ int topp_exact_pass(const Row& row, float m, float cT, u
 // Step 3: crossing key, ties taken and W from the table; the cut's index from
 // one warp segment.  False if the bracket does not hold the crossing.
 template <int DT>
-__device__ __noinline__ bool topp_resolve(const Row& row, float m, float cT, float top_p, double above,
+__device__ __noinline__ bool topp_resolve(const Row row, float m, float cT, float top_p, double above,
                                           double below, Smem& sm, FullExtra& fx, uint64_t& cut, double& W) {
   auto& T = fx.u.t;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -984,7 +984,7 @@ __device__ __noinline__ bool topp_resolve(const Row& row, float m, float cT, flo
 
 // The top-p cut among {composite >= ck} by bracketing; false if it gave up.
 template <int DT>
-__device__ __noinline__ bool topp_bracketed(const Row& row, float m, float cT, uint64_t ck, float top_p,
+__device__ __noinline__ bool topp_bracketed(const Row row, float m, float cT, uint64_t ck, float top_p,
                                             Smem& sm, FullExtra& fx, uint64_t& cut, double& W) {
   Level L;
   L.top = 0.0f;
@@ -1024,82 +1024,119 @@ __device__ __forceinline__ uint32_t kc_slot_bits(const KeyCount& T, int s) {
   return (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu);
 }
 
-// Counts one bf16 element (bits b) into the pair's count row cnt (shared
-// address); keys is the small table's key array.  False on overflow.
-__device__ __forceinline__ bool kc_count(uint32_t keys, uint32_t cnt, uint32_t b) {
-  const uint32_t rel = ((b >> 7) & 0xffu) - kKCExpLo;
-  if (rel < 8u) {
-    reds_add_u32(cnt + 4 * (((b >> 15) << 10) | (rel << 7) | (b & 127u)), 1u);
-    return true;
-  }
-  if (b == 0xff80u) return true;                       // -inf: probability 0, never kept mass
-  const uint32_t k = bf16_key(b);
-  const uint32_t h = (k * 0x9e3779b1u) >> (32 - kKHBits);
-  for (int p = 0; p < kKHProbe; ++p) {
-    const uint32_t s = (h + p) & (kKH - 1);
-    uint32_t cur = lds_volatile_u32(keys + 4 * s);
-    if (cur == kNoKey) cur = atoms_cas_u32(keys + 4 * s, kNoKey, k);
-    if (cur == kNoKey || cur == k) {
-      reds_add_u32(cnt + 4 * (kKCDirect + s), 1u);
-      return true;
-    }
-  }
-  return false;
+// Direct-window slot of bf16 bits b (only bits 0..15 are read): with
+// t = (exponent - kKCExpLo) * 128 + mantissa, in the window iff t < 1024, at
+// slot sign * 1024 + t.  Returns t; *off = the sign's byte offset (4 * 1024).
+__device__ __forceinline__ uint32_t kc_direct(uint32_t b, uint32_t& off) {
+  off = (b >> 3) & 0x1000u;
+  return (b & 0x7fffu) - (static_cast<uint32_t>(kKCExpLo) << 7);
 }
 
-// Pass 1 of a bf16 top-p row: maximum, NaN / +inf flag and the value counts,
-// warp pair j over its own quarter of the row.  Returns 1 if the small table
-// overflowed (the maximum and flag are complete either way).
-__device__ __noinline__ int kc_pass(const Row& row, Smem& sm, FullExtra& fx, float& m_out, int& bad_out) {
+// Counts the elements of vector words q selected by mask in the small table
+// (keys: its key array); NaN / +inf set *bad, -inf is skipped (probability
+// 0).  Inline, but only reached for the rare values outside the direct
+// window.  False on overflow.
+__device__ __forceinline__ bool kc_count_table(uint32_t keys, uint32_t cnt, uint4 q, uint32_t mask,
+                                               volatile int* bad) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  while (mask) {
+    const int e = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const uint32_t b = ((e & 1) ? (w[e >> 1] >> 16) : w[e >> 1]) & 0xffffu;
+    if ((b & 0x7f80u) == 0x7f80u) {                     // inf or NaN
+      if (b != 0xff80u) *bad = 1;
+      continue;
+    }
+    const uint32_t k = bf16_key(b);
+    const uint32_t h = (k * 0x9e3779b1u) >> (32 - kKHBits);
+    bool done = false;
+    for (int p = 0; p < kKHProbe && !done; ++p) {
+      const uint32_t s = (h + p) & (kKH - 1);
+      uint32_t cur = lds_volatile_u32(keys + 4 * s);
+      if (cur == kNoKey) cur = atoms_cas_u32(keys + 4 * s, kNoKey, k);
+      if (cur == kNoKey || cur == k) {
+        reds_add_u32(cnt + 4 * (kKCDirect + s), 1u);
+        done = true;
+      }
+    }
+    if (!done) return false;
+  }
+  return true;
+}
+
+// The counting loop of kc_pass, for aligned or element-wise rows.
+template <bool kAligned>
+__device__ __forceinline__ void kc_loop(const Row row, int v0, int v1, uint32_t keys, uint32_t cnt,
+                                        volatile int* ovf, volatile int* bad) {
   constexpr int P = Elem<DT_BF16>::kPer;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int s = tid; s < kKH; s += kThreads) fx.u.kc.keys[s] = kNoKey;
-  for (int s = tid; s < kPairs * kKCSlots; s += kThreads) (&fx.u.kc.cnt[0][0])[s] = 0u;
-  if (tid == 0) fx.bi[0] = 0;
-  __syncthreads();
-  volatile int* ovf = &fx.bi[0];
-  const uint32_t keys = smem_u32(fx.u.kc.keys), cnt = smem_u32(fx.u.kc.cnt[warp >> 1]);
-  float m = -__int_as_float(0x7f800000);
-  bool bad = false, counting = true;
-  const int Ls = seg_len(row);
-  const int v0 = warp * Ls, v1 = min(row.nvec, v0 + Ls);
-  for (int s = v0; s < v1; s += 32 * kUnroll) {
-    if (counting && *ovf) counting = false;
+  const int lane = threadIdx.x & 31;
+  bool counting = true;   // this thread's; an overflow anywhere discards the counts
+  for (int s = v0; s < v1 && counting; s += 32 * kUnroll) {
     uint4 r[kUnroll];
     int c[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int v = s + u * 32 + lane;
-      c[u] = v < v1 ? load_vec<DT_BF16, false>(row, v, r[u]) : 0;
+      r[u] = make_uint4(0u, 0u, 0u, 0u);
+      c[u] = v < v1 ? load_vec_as<DT_BF16, false, kAligned>(row, v, r[u]) : 0;
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (c[u] == 0) continue;
-      bool vb;
-      m = fmaxf(m, vec_max<DT_BF16>(r[u], c[u], vb));
-      bad |= vb;
-      if (!counting) continue;
       const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+      uint32_t rest = 0;
 #pragma unroll
       for (int e = 0; e < P; ++e) {
-        if (e >= c[u]) continue;
-        const uint32_t b = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu);
-        if (!kc_count(keys, cnt, b)) {
-          *ovf = 1;
-          counting = false;
-          break;
-        }
+        const uint32_t b = (e & 1) ? (w[e >> 1] >> 16) : w[e >> 1];
+        uint32_t off;
+        const uint32_t t = kc_direct(b, off);
+        const bool valid = e < c[u], in = t < 1024u;
+        reds_add_u32_if(cnt + off + 4 * t, 1u, valid && in);
+        rest |= (valid && !in) ? (1u << e) : 0u;
+      }
+      if (__builtin_expect(rest != 0u, 0) && !kc_count_table(keys, cnt, r[u], rest, bad)) {
+        *ovf = 1;
+        counting = false;
       }
     }
   }
+}
+
+// Pass 1 of a bf16 top-p row: the value counts, warp pair j over its own
+// quarter of the row; then the maximum (the largest value counted) and the
+// NaN / +inf flag.  Returns 1 if the small table overflowed -- the maximum is
+// then incomplete and the caller takes it with full_max.
+__device__ __noinline__ int kc_pass(const Row row, Smem& sm, FullExtra& fx, float& m_out, int& bad_out) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int s = tid; s < kKH; s += kThreads) fx.u.kc.keys[s] = kNoKey;
+  for (int s = tid; s < kPairs * kKCSlots; s += kThreads) (&fx.u.kc.cnt[0][0])[s] = 0u;
+  if (tid == 0) {
+    fx.bi[0] = 0;
+    fx.bi[1] = 0;
+  }
+  __syncthreads();
+  const uint32_t keys = smem_u32(fx.u.kc.keys), cnt = smem_u32(fx.u.kc.cnt[warp >> 1]);
+  const int Ls = seg_len(row);
+  const int v0 = warp * Ls, v1 = min(row.nvec, v0 + Ls);
+  if (row.aligned) kc_loop<true>(row, v0, v1, keys, cnt, &fx.bi[0], &fx.bi[1]);
+  else kc_loop<false>(row, v0, v1, keys, cnt, &fx.bi[0], &fx.bi[1]);
+  __syncthreads();
+  // the maximum is the largest value with a count
+  const KeyCount& T = fx.u.kc;
+  float m = -__int_as_float(0x7f800000);
+  for (int s = tid; s < kKCSlots; s += kThreads) {
+    const bool used = s < kKCDirect ? (T.cnt[0][s] | T.cnt[1][s] | T.cnt[2][s] | T.cnt[3][s]) != 0u
+                                    : T.keys[s - kKCDirect] != kNoKey;
+    if (used) m = fmaxf(m, __uint_as_float(kc_slot_bits(T, s) << 16));
+  }
+  static_assert(kPairs == 4, "the used-slot test reads four count rows");
   m_out = block_max_f(m, sm);
-  bad_out = block_or(bad ? 1 : 0, sm);
+  bad_out = fx.bi[1];
   return fx.bi[0];
 }
 
 // The cut from the value counts; false when the crossing bin holds more
 // values than the list (the caller then brackets).
-__device__ __noinline__ bool kc_resolve(const Row& row, float m, float cT, float scale, float top_p, Smem& sm,
+__device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float scale, float top_p, Smem& sm,
                                         FullExtra& fx, uint64_t& cut, double& W) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const KeyCount& T = fx.u.kc;
@@ -1233,7 +1270,7 @@ __device__ __noinline__ bool kc_resolve(const Row& row, float m, float cT, float
 }
 
 template <int DT>
-__device__ void full_row(const Row& row, const RowParams& P, int dtok, Smem& sm) {
+__device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
   const int tid = threadIdx.x;
   float m;
   double S = 0.0;
@@ -1243,7 +1280,10 @@ __device__ void full_row(const Row& row, const RowParams& P, int dtok, Smem& sm)
   FullExtra& fx = *reinterpret_cast<FullExtra*>(reinterpret_cast<unsigned char*>(&sm) + sizeof(Smem));
   const bool keycount = DT == DT_BF16 && extra && P.k == 0 && P.top_p < 1.0f;
   int kc_overflow = 1;
-  if (keycount) kc_overflow = kc_pass(row, sm, fx, m, bad);
+  if (keycount) {
+    kc_overflow = kc_pass(row, sm, fx, m, bad);
+    if (kc_overflow) full_max<DT>(row, sm, m, bad);
+  }
   // the softmax denominator of the whole row is W only with neither cut
   else if (P.k > 0 || P.top_p < 1.0f) full_max<DT>(row, sm, m, bad);
   else full_pass1<DT>(row, P.cT, sm, m, S, bad);
@@ -1330,7 +1370,7 @@ __device__ __noinline__ uint64_t block_select_kth(const uint64_t* buf, int n, in
 // Appends every element of the row whose composite is >= lo into sm.cand
 // (a re-read of the whole row; used only when the candidate buffer overflowed).
 template <int DT>
-__device__ __noinline__ void collect_at_least(const Row& row, uint64_t lo, Smem& sm) {
+__device__ __noinline__ void collect_at_least(const Row row, uint64_t lo, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
   if (threadIdx.x == 0) sm.ncand = 0;
   __syncthreads();
@@ -1356,7 +1396,7 @@ __device__ __noinline__ void collect_at_least(const Row& row, uint64_t lo, Smem&
 // top-k in descending order, then float64 softmax over them, the top-p cut
 // and the kept list [wrblog §7.2, §7.3].
 template <int DT>
-__device__ __noinline__ void stream_finish(const Row& row, const RowParams& P, const int dtok,
+__device__ __noinline__ void stream_finish(const Row row, const RowParams P, const int dtok,
                                            const int any_bad, float m_row, Smem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k;
@@ -1495,7 +1535,7 @@ __device__ __forceinline__ void append_from_vector(const uint4& r, int c, int v,
 // its groups when all four tracked vectors qualify (there may be more).  The
 // collected elements >= K are a small superset of the top-k.
 template <int DT>
-__device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& sm) {
+__device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
   const int tid = threadIdx.x;
   constexpr int step = kThreads * kStreamUnroll;
   const int iters = (row.nvec + step - 1) / step;
@@ -1580,12 +1620,26 @@ __device__ void stream_row(const Row& row, const RowParams& P, int dtok, Smem& s
 }
 
 // Probability of token x under a PATH_FULL row given its logit z.
-__device__ __forceinline__ float full_prob(float z, uint32_t x, uint64_t cut, float m, float cT, float invW) {
-  if (cut != 0ull && composite(fkey(z), x) < cut) return 0.0f;
-  return fast_exp2((z - m) * cT) * invW;
+// The kept-set test composite(key(z), x) >= cut as float and index compares:
+// kept iff z > v, or z == v and x <= i (cut 0 keeps everything).
+struct CutTest {
+  float v;
+  uint32_t i;
+};
+__device__ __forceinline__ CutTest cut_test(uint64_t cut) {
+  CutTest c;
+  if (cut == 0ull) {
+    c.v = -__int_as_float(0x7f800000);
+    c.i = 0xffffffffu;
+  } else {
+    c.v = key_value(static_cast<uint32_t>(cut >> 32));
+    c.i = ~static_cast<uint32_t>(cut);
+  }
+  return c;
 }
-__device__ __forceinline__ float full_prob(float z, uint32_t x, const RowStat& st, float cT, float invW) {
-  return full_prob(z, x, st.cut, st.m, cT, invW);
+__device__ __forceinline__ float full_prob(float z, uint32_t x, const CutTest& ct, float m, float cT, float invW) {
+  const bool kept = z > ct.v || (z == ct.v && x <= ct.i);
+  return kept ? fast_exp2((z - m) * cT) * invW : 0.0f;
 }
 
 }  // namespace sv

@@ -88,6 +88,19 @@ def test_workspace_reuse_and_counters_reset():
     o2 = gpu_sample(wc, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(o1.tokens, o2.tokens) and torch.equal(o1.num_accepted, o2.num_accepted)
+    # full-row target rows: the draw runs chunk-parallel in a second kernel with
+    # its own per-sequence counters, right after the row counters
+    f = workload(5, B=8, V=9000)
+    fc = f.to("cuda")
+    fws = sv.new_workspace(sv.workspace_size(f.B, f.G, f.V, f.target_params, f.draft_params), "cuda")
+    zero = 2 * ((4 * f.B + 255) // 256 * 256)
+    f1 = gpu_sample(fc, workspace=fws)
+    torch.cuda.synchronize()
+    assert (fws[:zero] == 0).all()
+    f2 = gpu_sample(fc, workspace=fws)
+    torch.cuda.synchronize()
+    assert torch.equal(f1.tokens, f2.tokens) and torch.equal(f1.status, f2.status)
+    assert torch.equal(f1.residual_z, f2.residual_z)
     g = workload(4, B=8, V=4096).to("cuda")
     gws = sv.new_workspace(sv.greedy_workspace_size(g.B, g.G), "cuda")
     for _ in range(3):
