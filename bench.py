@@ -34,7 +34,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "verified positions/s and logits HBM GB/s (% of peak), B=64 g=5 V=128256 bf16"
-WID = 3
+WID = 3             # the serving workload: the default, and the one METRIC names
+SAMPLING_WIDS = (2, 3, 5)
 L2_BYTES = 126 * 2 ** 20
 ROTATE = 4
 KERNEL_SOURCES = ["speculative_decoding_verification_44_gb300/csrc/spec_verify.cu",
@@ -51,7 +52,18 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="serving-zipf-topk-topp",
+                    help="sampling workload to time (default: the serving workload); the others "
+                         "exist for profiling the full-row and small-vocabulary paths")
     return ap.parse_args()
+
+
+def workload_id(name: str) -> int:
+    from speculative_decoding_verification_44_gb300 import workloads
+    for wid in SAMPLING_WIDS:
+        if workloads.NAMES[wid] == name:
+            return wid
+    raise SystemExit(f"--workload must be one of {[workloads.NAMES[w] for w in SAMPLING_WIDS]}")
 
 
 def kernel_source_sha() -> str:
@@ -166,6 +178,8 @@ def oracle_sample_time(w, seqs, budget_s=None):
           float(np.float32(w.target_params.top_p)))
     dp = (float(np.float32(w.draft_params.temperature)), int(w.draft_params.top_k),
           float(np.float32(w.draft_params.top_p)))
+    gam = w.gamma_per_seq.cpu().numpy() if w.gamma_per_seq is not None else None
+    oh = w.draft_is_onehot.cpu().numpy() if w.draft_is_onehot is not None else None
     positions, elapsed, n = 0, 0.0, 0
     for b in seqs:
         tl = f64(w.target_logits[b:b + 1])
@@ -173,10 +187,12 @@ def oracle_sample_time(w, seqs, budget_s=None):
         toks = w.draft_tokens[b:b + 1].cpu().numpy()
         ua = w.u_accept[b:b + 1].cpu().double().numpy()
         us = w.u_sample[b:b + 1].cpu().double().numpy()
+        g = gam[b:b + 1] if gam is not None else None
+        o = oh[b:b + 1] if oh is not None else None
         t0 = time.perf_counter()
-        oracle.verify_sample(tl, dl, toks, ua, us, tp, dp)
+        oracle.verify_sample(tl, dl, toks, ua, us, tp, dp, gamma_per_seq=g, one_hot=o)
         elapsed += time.perf_counter() - t0
-        positions += w.G + 1
+        positions += (int(g[0]) if g is not None else w.G) + 1
         n += 1
         if budget_s is not None and elapsed >= budget_s:
             break
@@ -204,26 +220,39 @@ def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float
     return units_per_rank * world / (ms_per_step / 1e3)
 
 
+def params_of(w) -> dict:
+    p = w.target_params
+    return {"temperature": round(float(p.temperature), 6), "top_k": int(p.top_k), "top_p": round(float(p.top_p), 6)}
+
+
+def metric_of(wid: int, w) -> str:
+    if wid == WID:
+        return METRIC
+    dt = "bf16" if w.dtype.itemsize == 2 else "f32"
+    return f"verified positions/s and logits HBM GB/s (% of peak), {w.name} B={w.B} g<={w.G} V={w.V} {dt}"
+
+
 def run_reference(args, rank):
     """Reference arm: the float64 oracle on the host cores, one sequence per step."""
     if rank != 0:
         return
     from speculative_decoding_verification_44_gb300 import workloads
-    w = workloads.make(WID, "cpu", draft_probs=cpu_oracle_probs)
+    wid = workload_id(args.workload)
+    w = workloads.make(wid, "cpu", draft_probs=cpu_oracle_probs)
     order = [s % w.B for s in range(args.warmup + args.steps)]
     oracle_sample_time(w, order[: args.warmup])
     pos, secs, n = oracle_sample_time(w, order[args.warmup:])
     value = pos / secs
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+        "impl": "reference", "metric": metric_of(wid, w), "value": value, "unit": "positions/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / max(1, n), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workloads.NAMES[WID], "B": w.B, "gamma": w.G, "V": w.V, "dtype": "bf16",
-                   "temperature": 0.7, "top_k": 50, "top_p": 0.9,
-                   "step": "one sequence (gamma+1 = 6 verified positions) per step"},
+        "config": {"workload": workloads.NAMES[wid], "B": w.B, "gamma": w.G, "V": w.V,
+                   "dtype": "bf16" if w.dtype.itemsize == 2 else "f32", **params_of(w),
+                   "step": "one sequence (gamma_b + 1 verified positions) per step"},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} sequences of the serving workload, one per step"},
+                         "sample": f"{n} sequences of the {workloads.NAMES[wid]} workload, one per step"},
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -254,11 +283,15 @@ def main():
     from speculative_decoding_verification_44_gb300 import workloads
 
     # independent batches: replica = rank * ROTATE + r
-    sets = [workloads.make(WID, dev, draft_probs=gpu_draft_probs, replica=rep) for rep in replica_ids(rank)]
+    wid = workload_id(args.workload)
+    sets = [workloads.make(wid, dev, draft_probs=gpu_draft_probs, replica=rep) for rep in replica_ids(rank)]
     w0 = sets[0]
     B, G, V = w0.B, w0.G, w0.V
     rt, rd = w0.rows_used()
-    logits_bytes = (rt + rd) * V * 2
+    esize = w0.target_logits.element_size()
+    logits_bytes = (rt + rd) * V * esize
+    # a target row without a small top-k takes the full-row path; its draw is a second kernel
+    full_target = not (1 <= w0.target_params.top_k <= 128 and w0.target_params.top_k < V)
     io_bytes = B * G * 4 * 2 + B * 4 + B * (G + 1) * 4 + B * 4 * 3 + B * G * 4
     alg_bytes = logits_bytes + io_bytes
     ws = sv.new_workspace(sv.workspace_size(B, G, V, w0.target_params, w0.draft_params), dev)
@@ -266,7 +299,8 @@ def main():
     stream = torch.cuda.current_stream()
 
     calls = [sv.BoundSample(w.target_logits, w.draft_logits, w.draft_tokens, w.u_accept, w.u_sample,
-                            w.target_params, w.draft_params, workspace=ws, out=outs[r])
+                            w.target_params, w.draft_params, gamma_per_seq=w.gamma_per_seq,
+                            draft_is_onehot=w.draft_is_onehot, workspace=ws, out=outs[r])
              for r, w in enumerate(sets)]
 
     def step(i):
@@ -305,10 +339,12 @@ def main():
     peak, peak_kind = measured_peaks()
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     achieved = alg_bytes / avg_launch_s / 1e9
-    traffic = profile_traffic()
+    traffic = profile_traffic() if wid == WID else None
+    dname = "bf16" if esize == 2 else "f32"
+    kname = f"sv::sample_kernel<{dname}>" + (f" + sv::draw_kernel<{dname}>" if full_target else "")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_kind": f"of {peak_kind}",
-                "kernel": "sv::sample_kernel<bf16>", "algorithmic_bytes_per_launch": alg_bytes,
+                "kernel": kname, "algorithmic_bytes_per_launch": alg_bytes,
                 "launch_ms_median": statistics.median(launch_ms),
                 "frac_of_nominal_8TBps": achieved / 8000.0}
 
@@ -316,8 +352,9 @@ def main():
     e2e = None
     if not args.no_e2e:
         w = sets[0]
-        host = {k: getattr(w, k).cpu().pin_memory() for k in
-                ("target_logits", "draft_logits", "draft_tokens", "u_accept", "u_sample")}
+        names = ["target_logits", "draft_logits", "draft_tokens", "u_accept", "u_sample"]
+        names += [k for k in ("gamma_per_seq", "draft_is_onehot") if getattr(w, k) is not None]
+        host = {k: getattr(w, k).cpu().pin_memory() for k in names}
         dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         hout = {"tokens": torch.empty(B, G + 1, dtype=torch.int32).pin_memory(),
                 "num_accepted": torch.empty(B, dtype=torch.int32).pin_memory(),
@@ -331,6 +368,7 @@ def main():
                 dbuf[k].copy_(host[k], non_blocking=True)
             sv.verify_sample(dbuf["target_logits"], dbuf["draft_logits"], dbuf["draft_tokens"],
                              dbuf["u_accept"], dbuf["u_sample"], w.target_params, w.draft_params,
+                             gamma_per_seq=dbuf.get("gamma_per_seq"), draft_is_onehot=dbuf.get("draft_is_onehot"),
                              workspace=ws, out=dout)
             hout["tokens"].copy_(dout.tokens, non_blocking=True)
             hout["num_accepted"].copy_(dout.num_accepted, non_blocking=True)
@@ -360,11 +398,11 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": K,
+            "metric": metric_of(wid, w0), "value": value, "unit": "positions/s", "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workloads.NAMES[WID], "B": B, "gamma": G, "V": V,
-                       "temperature": 0.7, "top_k": 50, "top_p": 0.9, "batches_per_gpu": 1,
+            "scaling": "weak", "vs_baseline": None, "dtype": dname, "data": "synthetic",
+            "config": {"workload": workloads.NAMES[wid], "B": B, "gamma": G, "V": V,
+                       **params_of(w0), "batches_per_gpu": 1,
                        "l2": f"inputs rotate over {ROTATE} independent sets of {logits_bytes / 1e6:.1f} MB "
                              f"(each larger than the {L2_BYTES / 2**20:.0f} MiB L2)",
                        "parallelism": f"replicas x{world} (one batch per GPU, no data-path collective)"},
@@ -373,7 +411,7 @@ def main():
             "emitted_tokens_per_s_last_step": emitted * world / (ms_per_step / 1e3),
             "logits_bytes_per_verified_position": logits_bytes / rt,
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
-            "gpu_launches": K,
+            "gpu_launches": K * (2 if full_target else 1),
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
