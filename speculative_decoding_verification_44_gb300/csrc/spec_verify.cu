@@ -475,50 +475,50 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
         if (bm) status = __shfl_sync(kFull, st, __ffs(bm) - 1);
       }
     }
-    if (lane == 0) sm.b_i32[0] = status;
+
+    // 2. a_i = min(1, p_i(d_i) / q_i(d_i)); accept iff u_i < a_i; stop at the
+    //    first rejection -- in the same warp pass, once the status is clean
+    int j = gb, flags = 0;
+    if (status == SEQ_OK) {
+      for (int base = 0; base < a.G; base += 32) {
+        const int i = base + lane;
+        bool rej = false, zq = false;
+        if (i < gb) {
+          const float p = static_cast<float>(E.rs[i].p_tok);
+          const float q = onehot ? 1.0f : static_cast<float>(E.rs[a.G + 1 + i].p_tok);
+          float ai;
+          if (q > 0.0f) ai = fminf(1.0f, p / q);
+          else { ai = p > 0.0f ? 1.0f : 0.0f; zq = true; }
+          rej = !(E.uacc[i] < ai);
+          if (a.out_aprob) a.out_aprob[tokb + i] = ai;
+        } else if (i < a.G && a.out_aprob) {
+          a.out_aprob[tokb + i] = -1.0f;
+        }
+        if (j == gb) {
+          const unsigned rm = __ballot_sync(kFull, rej);
+          const unsigned zm = __ballot_sync(kFull, zq);
+          if (rm) {
+            const int f = __ffs(rm) - 1;
+            j = base + f;
+            const unsigned upto = (f == 31) ? kFull : ((2u << f) - 1u);
+            if (zm & upto) flags |= SEQ_FLAG_ZERO_Q;
+          } else if (zm) {
+            flags |= SEQ_FLAG_ZERO_Q;
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+      sm.b_i32[0] = status;
+      sm.b_i32[1] = j;
+      sm.b_i32[2] = flags;
+    }
   }
   __syncthreads();
   if (sm.b_i32[0] != SEQ_OK) {
     write_error(a, b, sm.b_i32[0]);
     return;
   }
-
-  // 2. a_i = min(1, p_i(d_i) / q_i(d_i)); accept iff u_i < a_i; stop at the first rejection
-  if (warp == 0) {
-    int j = gb, flags = 0;
-    for (int base = 0; base < a.G; base += 32) {
-      const int i = base + lane;
-      bool rej = false, zq = false;
-      if (i < gb) {
-        const float p = static_cast<float>(E.rs[i].p_tok);
-        const float q = onehot ? 1.0f : static_cast<float>(E.rs[a.G + 1 + i].p_tok);
-        float ai;
-        if (q > 0.0f) ai = fminf(1.0f, p / q);
-        else { ai = p > 0.0f ? 1.0f : 0.0f; zq = true; }
-        rej = !(E.uacc[i] < ai);
-        if (a.out_aprob) a.out_aprob[tokb + i] = ai;
-      } else if (i < a.G && a.out_aprob) {
-        a.out_aprob[tokb + i] = -1.0f;
-      }
-      if (j == gb) {
-        const unsigned rm = __ballot_sync(kFull, rej);
-        const unsigned zm = __ballot_sync(kFull, zq);
-        if (rm) {
-          const int f = __ffs(rm) - 1;
-          j = base + f;
-          const unsigned upto = (f == 31) ? kFull : ((2u << f) - 1u);
-          if (zm & upto) flags |= SEQ_FLAG_ZERO_Q;
-        } else if (zm) {
-          flags |= SEQ_FLAG_ZERO_Q;
-        }
-      }
-    }
-    if (lane == 0) {
-      sm.b_i32[1] = j;
-      sm.b_i32[2] = flags;
-    }
-  }
-  __syncthreads();
   const int j = sm.b_i32[1];
   int flags = sm.b_i32[2];
   __syncthreads();

@@ -1424,19 +1424,22 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
   }
   ntop = min(nsrc, k);
 
-  // ---- sort, softmax over the top-k, top-p cut, kept list (warp 0).
-  // Each weight exp((z - m) / T) = 2^((z - m) cT) is evaluated from the exact
-  // difference z - m (two-sum) and a hi/lo split of the exponent, so its error
-  // is exp2f's (2 ulp); sums, prefix sums and the normaliser are double-float.
+  // rank sort (descending), one candidate per thread (nsrc <= kListCap <= kThreads)
+  static_assert(kListCap <= kThreads, "one thread per candidate");
+  if (tid < nsrc) {
+    const uint64_t c = src[tid];
+    int rank = 0;
+    for (int j = 0; j < nsrc; ++j) rank += src[j] > c ? 1 : 0;
+    if (rank < k) sm.sorted[rank] = c;
+  }
+  __syncthreads();
+
+  // ---- softmax over the top-k, top-p cut, kept list (warp 0; lane takes
+  // positions 4*lane .. 4*lane+3).  Each weight exp((z - m) / T) = 2^((z - m) cT)
+  // is evaluated from the exact difference z - m (two-sum) and a hi/lo split of
+  // the exponent, so its error is exp2f's (2 ulp); sums, prefix sums and the
+  // normaliser are double-float.
   if (warp == 0) {
-    // rank sort (descending), then each lane takes positions 4*lane .. 4*lane+3
-    for (int e = lane; e < nsrc; e += 32) {
-      const uint64_t c = src[e];
-      int rank = 0;
-      for (int j = 0; j < nsrc; ++j) rank += src[j] > c ? 1 : 0;
-      if (rank < k) sm.sorted[rank] = c;
-    }
-    __syncwarp();
     uint64_t v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] = (4 * lane + j < ntop) ? sm.sorted[4 * lane + j] : 0ull;
