@@ -44,6 +44,10 @@ Readings where the pages are silent (each is named where it is used):
 * R10 a NaN or +inf logit in any row the sequence uses, or a row whose logits
       are all -inf, fails the whole sequence: nothing is committed
       ([wrblog §15]).  -inf marks a banned token ([wrblog §2.3]).
+* R11 early-exit greedy: the rows are read in position order and reading
+      stops at the first draft that differs from the target's argmax -- the
+      sequential verifier of [wrblog §6], which never looks past the first
+      rejection.  "The rows the sequence uses" in R10 are then the rows read.
 
 Pins (tests/test_oracle_*.py): the worked examples of [wrblog §4.3, §5, §7.1]
 and [baisen §2, §4, §6]; the identities Z = sum (p-q)+ = sum (q-p)+ =
@@ -247,6 +251,7 @@ class SeqResult:
     sample_lo: float = np.nan
     sample_hi: float = np.nan
     sample_cdf: np.ndarray | None = field(default=None, repr=False)  # normalised CDF drawn from
+    rows_read: int = -1             # early-exit greedy: target rows read (R11)
 
 
 def _error_result(status: int, gamma_max: int) -> SeqResult:
@@ -379,6 +384,35 @@ def verify_greedy_sequence(target: np.ndarray, tokens: np.ndarray, gamma_b: int,
     return SeqResult(out, n_acc, SEQ_OK, np.full(gamma_max, -1.0), -1.0)
 
 
+def verify_greedy_sequence_early(target: np.ndarray, tokens: np.ndarray, gamma_b: int,
+                                 gamma_max: int) -> SeqResult:
+    """Greedy verification that stops reading rows at the first mismatch (R11).
+
+    [wrblog §6] verifies position by position and stops at the first rejection;
+    [wrblog §7.1] makes the greedy test d_i == argmax p_i.  Row i is read only
+    once d_1..d_{i-1} all matched, so rows after the stop point are never read
+    and their contents cannot fail the sequence.
+    """
+    V = target.shape[1]
+    if not 0 <= gamma_b <= gamma_max:
+        return _error_result(SEQ_BAD_LENGTH, gamma_max)
+    d = [int(t) for t in tokens[:gamma_b]]
+    if any(not 0 <= t < V for t in d):
+        return _error_result(SEQ_BAD_TOKEN, gamma_max)
+    out = np.full(gamma_max + 1, -1, dtype=np.int64)
+    for i in range(gamma_b + 1):
+        gi, st = greedy_row(target[i])
+        if st != SEQ_OK:
+            res = _error_result(st, gamma_max)
+            res.rows_read = i + 1
+            return res
+        if i == gamma_b or d[i] != gi:
+            out[:i] = d[:i]
+            out[i] = gi
+            return SeqResult(out, i, SEQ_OK, np.full(gamma_max, -1.0), -1.0, rows_read=i + 1)
+    raise AssertionError("unreachable: the loop returns at i == gamma_b")
+
+
 # --------------------------------------------------------------------------
 # Batches  [aiqz "加速收益与工程" -- requests verified together as one batch]
 # --------------------------------------------------------------------------
@@ -436,6 +470,20 @@ def verify_greedy(target: np.ndarray, tokens: np.ndarray,
     for b in seqs:
         g = gamma_max if gamma_per_seq is None else int(gamma_per_seq[b])
         out.append(verify_greedy_sequence(target[b], tokens[b], g, gamma_max))
+    return _collect(out)
+
+
+def verify_greedy_early(target: np.ndarray, tokens: np.ndarray,
+                        gamma_per_seq: np.ndarray | None = None,
+                        seqs: list[int] | None = None) -> BatchResult:
+    """Batched early-exit greedy verification (R11), one sequence at a time."""
+    B, G1, _ = target.shape
+    gamma_max = G1 - 1
+    seqs = range(B) if seqs is None else seqs
+    out = []
+    for b in seqs:
+        g = gamma_max if gamma_per_seq is None else int(gamma_per_seq[b])
+        out.append(verify_greedy_sequence_early(target[b], tokens[b], g, gamma_max))
     return _collect(out)
 
 
