@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "verified positions/s and logits HBM GB/s (% of peak), B=64 g=5 V=128256 bf16"
 WID = 3             # the serving workload: the default, and the one METRIC names
 SAMPLING_WIDS = (2, 3, 5)
+GREEDY_WID = 4
 L2_BYTES = 126 * 2 ** 20
 ROTATE = 4
 KERNEL_SOURCES = ["speculative_decoding_verification_44_gb300/csrc/spec_verify.cu",
@@ -53,17 +54,19 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default="serving-zipf-topk-topp",
-                    help="sampling workload to time (default: the serving workload); the others "
-                         "exist for profiling the full-row and small-vocabulary paths")
+                    help="workload to time (default: the serving workload); the others exist for "
+                         "profiling the full-row, small-vocabulary and greedy paths")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="greedy workload only: spec_verify_greedy_early instead of spec_verify_greedy")
     return ap.parse_args()
 
 
 def workload_id(name: str) -> int:
     from speculative_decoding_verification_44_gb300 import workloads
-    for wid in SAMPLING_WIDS:
+    for wid in SAMPLING_WIDS + (GREEDY_WID,):
         if workloads.NAMES[wid] == name:
             return wid
-    raise SystemExit(f"--workload must be one of {[workloads.NAMES[w] for w in SAMPLING_WIDS]}")
+    raise SystemExit(f"--workload must be one of {[workloads.NAMES[w] for w in SAMPLING_WIDS + (GREEDY_WID,)]}")
 
 
 def kernel_source_sha() -> str:
@@ -238,6 +241,8 @@ def run_reference(args, rank):
         return
     from speculative_decoding_verification_44_gb300 import workloads
     wid = workload_id(args.workload)
+    if wid == GREEDY_WID:
+        raise SystemExit("the reference arm times the sampling oracle; use a sampling workload")
     w = workloads.make(wid, "cpu", draft_probs=cpu_oracle_probs)
     order = [s % w.B for s in range(args.warmup + args.steps)]
     oracle_sample_time(w, order[: args.warmup])
@@ -256,6 +261,74 @@ def run_reference(args, rank):
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def run_greedy(args, rank, world, dev, sv, workloads):
+    """Greedy workload (all rows, or early exit): device-timed steps over rotating inputs."""
+    import torch
+    sets = [workloads.make(GREEDY_WID, dev, replica=rep) for rep in replica_ids(rank)]
+    w0 = sets[0]
+    B, G, V = w0.B, w0.G, w0.V
+    rt, _ = w0.rows_used()
+    ws = sv.new_workspace(sv.greedy_workspace_size(B, G), dev)
+    outs = [sv.alloc_outputs(B, G, dev, accept_prob=False, residual_z=False) for _ in range(ROTATE)]
+    rows = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(ROTATE)]
+
+    def step(i):
+        w, r = sets[i % ROTATE], i % ROTATE
+        if args.early_exit:
+            sv.verify_greedy_early(w.target_logits, w.draft_tokens, w.gamma_per_seq, workspace=ws, out=outs[r],
+                                   rows_read=rows[r])
+        else:
+            sv.verify_greedy(w.target_logits, w.draft_tokens, w.gamma_per_seq, workspace=ws, out=outs[r])
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(K):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms_per_step = max_over_ranks(t0.elapsed_time(t1), world, dev) / K
+    row_bytes = V * w0.target_logits.element_size()
+    read = [int(r.sum().item()) for r in rows] if args.early_exit else [rt] * ROTATE
+    needed = [int((o.num_accepted.clamp(min=0) + 1).sum().item()) for o in outs]
+    peak, peak_kind = measured_peaks()
+    # algorithmic rows: every row for the all-rows verifier (it checks them all), the rows
+    # up to each sequence's stop for early exit (speculative extra reads are waste)
+    alg_rows = statistics.mean(needed) if args.early_exit else rt
+    achieved = alg_rows * row_bytes / (ms_per_step / 1e3) / 1e9
+    if rank == 0:
+        line = {
+            "metric": f"verified positions/s, {w0.name} B={B} g={G} V={V} bf16"
+                      + (" (early exit)" if args.early_exit else ""),
+            "value": whole_job_rate(rt, world, ms_per_step), "unit": "positions/s", "n_gpus": world,
+            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w0.name, "B": B, "gamma": G, "V": V, "early_exit": bool(args.early_exit),
+                       "l2": f"inputs rotate over {ROTATE} independent sets of {rt * row_bytes / 1e6:.1f} MB"},
+            "rows_read_per_step": statistics.mean(read), "rows_needed_per_step": statistics.mean(needed),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": f"of {peak_kind}",
+                         "kernel": "sv::greedy_early_kernel<bf16>" if args.early_exit else "sv::greedy_kernel<bf16>",
+                         "algorithmic_bytes_per_launch": alg_rows * row_bytes,
+                         "bytes_read_per_launch": statistics.mean(read) * row_bytes},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": K, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
 
 
 def main():
@@ -284,6 +357,9 @@ def main():
 
     # independent batches: replica = rank * ROTATE + r
     wid = workload_id(args.workload)
+    if wid == GREEDY_WID:
+        run_greedy(args, rank, world, dev, sv, workloads)
+        return
     sets = [workloads.make(wid, dev, draft_probs=gpu_draft_probs, replica=rep) for rep in replica_ids(rank)]
     w0 = sets[0]
     B, G, V = w0.B, w0.G, w0.V

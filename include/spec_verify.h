@@ -189,6 +189,29 @@ SPEC_API spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_
                                  int32_t* out_tokens, int32_t* out_num_accepted,
                                  int32_t* out_status, void* stream);
 
+/* Early-exit greedy verification [wrblog §6, §7.1]: the same outputs as
+ * spec_verify_greedy on valid inputs, but a row is read only while the
+ * sequence has not yet been decided: once row s of a sequence fails or
+ * mismatches (d_s != g_s), rows after s are skipped, and the result depends
+ * on rows 0..s alone.  The checks of a sequence run in the order length,
+ * draft tokens, then rows 0..s; a NaN / +inf / all -inf row after the stop
+ * does not fail the sequence (it would fail spec_verify_greedy).
+ *
+ * One launch over (position, sequence) pairs, positions first, so a row's
+ * predecessors have usually finished when it starts; no CTA waits for
+ * another.  A row whose predecessors are still running is read
+ * speculatively: out_rows_read can exceed (the stop + 1).
+ * workspace     spec_greedy_workspace_size() bytes, same zero-fill rule
+ *               (the kernel leaves it reusable).
+ * out_rows_read [batch] int32: target rows read (0 for a length or token
+ *               error), or NULL.  Other arguments as for spec_verify_greedy. */
+SPEC_API spec_status_t spec_verify_greedy_early(const void* target_logits, spec_dtype_t dtype,
+                                       const int32_t* draft_tokens, const int32_t* gamma_per_seq,
+                                       int32_t batch, int32_t gamma_max, int32_t vocab,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* out_tokens, int32_t* out_num_accepted,
+                                       int32_t* out_status, int32_t* out_rows_read, void* stream);
+
 /* The transform step alone [wrblog §7.2, §7.3]: writes the full probability
  * rows p = top_p(top_k(softmax(z / T))) the verifier samples from.
  * logits [rows][vocab] of dtype; out_probs [rows][vocab] float;

@@ -34,7 +34,7 @@ SPEC_F32 = 1
 # Every symbol include/spec_verify.h declares.
 EXPORTED = ("spec_verify_workspace_size", "spec_verify_sample", "spec_greedy_workspace_size",
             "spec_verify_greedy", "spec_transform_probs", "spec_status_string",
-            "spec_verify_sample_noalloc")
+            "spec_verify_sample_noalloc", "spec_verify_greedy_early")
 
 
 class spec_sampling_params_t(ctypes.Structure):
@@ -77,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                vp, vp, vp, vp, vp, vp]
     lib.spec_verify_greedy.restype = ctypes.c_int
     lib.spec_verify_greedy.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, i32, vp, sz, vp, vp, vp, vp]
+    lib.spec_verify_greedy_early.restype = ctypes.c_int
+    lib.spec_verify_greedy_early.argtypes = [vp, ctypes.c_int, vp, vp, i32, i32, i32, vp, sz, vp, vp, vp, vp, vp]
     lib.spec_transform_probs.restype = ctypes.c_int
     lib.spec_transform_probs.argtypes = [vp, ctypes.c_int, i32, i32, P, vp, vp, vp]
     if path == LIB_PATH:
@@ -118,6 +120,10 @@ def spec_verify_sample_noalloc(*args) -> int:
 
 def spec_verify_greedy(*args) -> int:
     return load().spec_verify_greedy(*args)
+
+
+def spec_verify_greedy_early(*args) -> int:
+    return load().spec_verify_greedy_early(*args)
 
 
 def spec_transform_probs(*args) -> int:

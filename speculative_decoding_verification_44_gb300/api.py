@@ -132,6 +132,28 @@ def verify_greedy(target_logits: torch.Tensor, draft_tokens: torch.Tensor,
     return out
 
 
+def verify_greedy_early(target_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                        gamma_per_seq: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, out: VerifyOutput | None = None,
+                        rows_read: torch.Tensor | None = None,
+                        stream: torch.cuda.Stream | None = None) -> VerifyOutput:
+    """spec_verify_greedy_early on torch tensors: rows after the first mismatch are
+    skipped.  ``rows_read`` ([B] int32), if given, receives the rows read."""
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    if workspace is None:
+        workspace = new_workspace(greedy_workspace_size(B, G), dev)
+    if out is None:
+        out = alloc_outputs(B, G, dev, accept_prob=False, residual_z=False)
+    st = _lib.spec_verify_greedy_early(
+        _ptr(target_logits), _dtype_code(target_logits), _ptr(draft_tokens), _ptr(gamma_per_seq),
+        B, G, V, _ptr(workspace), workspace.numel(), _ptr(out.tokens), _ptr(out.num_accepted),
+        _ptr(out.status), _ptr(rows_read), _stream(stream))
+    _lib.check("spec_verify_greedy_early", st)
+    return out
+
+
 def transform_probs(logits: torch.Tensor, params: SamplingParams,
                     stream: torch.cuda.Stream | None = None) -> tuple[torch.Tensor, torch.Tensor]:
     """spec_transform_probs: full probability rows of a [rows, V] logits tensor."""

@@ -104,6 +104,20 @@ def test_host_validation_before_any_launch(lib):
         == _lib.SPEC_ERR_INVALID_ARG
     assert _lib.spec_verify_greedy(fake, 0, fake, None, 2, 3, 64, fake, 8, fake, fake, None, None) \
         == _lib.SPEC_ERR_WORKSPACE
+    early = _lib.spec_verify_greedy_early
+
+    def ecall(tgt=fake, dtype=0, tok=fake, B=2, G=3, ws=fake, wsb=1 << 30, rows=None):
+        return early(tgt, dtype, tok, None, B, G, 64, ws, wsb, fake, fake, None, rows, None)
+
+    assert ecall(tgt=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert ecall(dtype=5) == _lib.SPEC_ERR_INVALID_ARG
+    assert ecall(tok=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert ecall(B=0) == _lib.SPEC_ERR_INVALID_ARG
+    assert ecall(ws=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert ecall(tgt=fake + 1) == _lib.SPEC_ERR_MISALIGNED
+    assert ecall(rows=fake + 2) == _lib.SPEC_ERR_MISALIGNED
+    assert ecall(ws=fake + 16) == _lib.SPEC_ERR_MISALIGNED
+    assert ecall(wsb=8) == _lib.SPEC_ERR_WORKSPACE
     assert _lib.spec_transform_probs(fake, 0, 0, 64, P, fake, None, None) == _lib.SPEC_ERR_INVALID_ARG
     assert _lib.spec_transform_probs(fake + 2, 1, 1, 64, P, fake, None, None) == _lib.SPEC_ERR_MISALIGNED
 
