@@ -48,6 +48,13 @@ Readings where the pages are silent (each is named where it is used):
       stops at the first draft that differs from the target's argmax -- the
       sequential verifier of [wrblog §6], which never looks past the first
       rejection.  "The rows the sequence uses" in R10 are then the rows read.
+* R12 lenience beta in (0, 1] [magicnet §8]: the page shrinks the draft
+      distribution to beta q and then compares it with the target; here beta q
+      stands in for q throughout -- acceptance min(1, p / (beta q)) and, on a
+      rejection, the residual (p - beta q)+ / Z_beta.  beta = 1 is the lossless
+      path.  The page states only the acceptance rule and the guarantee that no
+      token is drawn with more than 1 / beta times its true probability; the
+      residual is this reading (it meets that guarantee, as the tests check).
 
 Pins (tests/test_oracle_*.py): the worked examples of [wrblog §4.3, §5, §7.1]
 and [baisen §2, §4, §6]; the identities Z = sum (p-q)+ = sum (q-p)+ =
@@ -196,10 +203,11 @@ def one_hot_row(V: int, token: int) -> RowDist:
 # --------------------------------------------------------------------------
 # Step 2: acceptance   [wrblog §4.1, §4.2, §6]
 # --------------------------------------------------------------------------
-def acceptance_probability(p_x: float, q_x: float) -> tuple[float, bool]:
-    """a(x) = min(1, p(x)/q(x)) [wrblog §4.1]; returns (a, q_was_zero) (R6)."""
+def acceptance_probability(p_x: float, q_x: float, lenience: float = 1.0) -> tuple[float, bool]:
+    """a(x) = min(1, p(x) / (beta q(x))) [wrblog §4.1; magicnet §8 (R12)], beta = 1 by
+    default; returns (a, q_was_zero) (R6)."""
     if q_x > 0.0:
-        return min(1.0, p_x / q_x), False
+        return min(1.0, p_x / (lenience * q_x)), False
     return (1.0 if p_x > 0.0 else 0.0), True
 
 
@@ -208,9 +216,9 @@ def acceptance_rate(p: np.ndarray, q: np.ndarray) -> float:
     return float(np.minimum(p, q).sum())
 
 
-def residual_weights(p: np.ndarray, q: np.ndarray) -> np.ndarray:
-    """Unnormalised residual (p - q)+  [wrblog §5]."""
-    return np.maximum(p - q, 0.0)
+def residual_weights(p: np.ndarray, q: np.ndarray, lenience: float = 1.0) -> np.ndarray:
+    """Unnormalised residual (p - beta q)+  [wrblog §5; magicnet §8 (R12)], beta = 1 by default."""
+    return np.maximum(p - lenience * q, 0.0)
 
 
 # --------------------------------------------------------------------------
@@ -268,7 +276,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
                            target_params: tuple[float, int, float],
                            draft_params: tuple[float, int, float],
                            gamma_b: int, gamma_max: int, one_hot: bool,
-                           keep_cdf: bool = False) -> SeqResult:
+                           keep_cdf: bool = False, lenience: float = 1.0) -> SeqResult:
     """Verify one sequence in sampling mode  [wrblog §6; rainlin §1].
 
     target: (gamma_max+1, V) float64 logits; rows 0..gamma_b are used.
@@ -276,6 +284,8 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
     tokens: (gamma_max,) draft tokens d_1..d_gamma (0-based positions).
     """
     V = target.shape[1]
+    if not 0.0 < lenience <= 1.0:                                   # [magicnet §8]: 0 < beta <= 1
+        raise ValueError("lenience must lie in (0, 1]")
     if not 0 <= gamma_b <= gamma_max:
         return _error_result(SEQ_BAD_LENGTH, gamma_max)
     d = [int(t) for t in tokens[:gamma_b]]
@@ -301,7 +311,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
     a = np.full(gamma_max, -1.0)
     zero_q = np.zeros(gamma_max, dtype=bool)
     for i in range(gamma_b):
-        a[i], zero_q[i] = acceptance_probability(p_rows[i].probs[d[i]], q_rows[i].probs[d[i]])
+        a[i], zero_q[i] = acceptance_probability(p_rows[i].probs[d[i]], q_rows[i].probs[d[i]], lenience)
     status = SEQ_OK
     rejected_at = None
     accept_margin = np.inf
@@ -317,7 +327,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
     residual_Z = -1.0
     if rejected_at is not None:
         j = rejected_at
-        w = residual_weights(p_rows[j].probs, q_rows[j].probs)     # [wrblog §5]
+        w = residual_weights(p_rows[j].probs, q_rows[j].probs, lenience)   # [wrblog §5] (R12)
         residual_Z = float(w.sum())
         if not residual_Z > 0:                                      # R7
             w = p_rows[j].probs
@@ -439,7 +449,8 @@ def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarr
                   u_accept: np.ndarray, u_sample: np.ndarray,
                   target_params: tuple[float, int, float], draft_params: tuple[float, int, float],
                   gamma_per_seq: np.ndarray | None = None, one_hot: np.ndarray | None = None,
-                  seqs: list[int] | None = None, keep_cdf: bool = False) -> BatchResult:
+                  seqs: list[int] | None = None, keep_cdf: bool = False,
+                  lenience: float = 1.0) -> BatchResult:
     """Batched sampling verification, one sequence at a time.
 
     target (B, gamma_max+1, V), draft (B, gamma_max, V) or None (all one-hot),
@@ -455,7 +466,7 @@ def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarr
         oh = draft is None or (one_hot is not None and bool(one_hot[b]))
         out.append(verify_sample_sequence(target[b], None if oh else draft[b], tokens[b],
                                           u_accept[b], float(u_sample[b]), target_params,
-                                          draft_params, g, gamma_max, oh, keep_cdf))
+                                          draft_params, g, gamma_max, oh, keep_cdf, lenience))
     return _collect(out)
 
 
