@@ -41,6 +41,8 @@
  *   [wrblog]  "推测解码：草稿模型、接受率、正确性与加速边界" (wrblog.cn)
  *   [rainlin] "投机解码" (rainlin-net.pages.dev, llm-inference/speculative-decoding)
  *   [baisen]  "投机采样 / 投机解码（Speculative Decoding）" (baisen.site)
+ *   [magicnet] "投机解码到底能加速多少：把接受率、草稿成本与墙钟收益算清楚"
+ *             (magicnetworld.com)
  *
  * Conventions common to every entry point
  * ----------------------------------------
@@ -172,6 +174,32 @@ SPEC_API spec_status_t spec_verify_sample(const void* target_logits, const void*
                                  int32_t* out_tokens, int32_t* out_num_accepted,
                                  float* out_accept_prob, float* out_residual_z,
                                  int32_t* out_status, void* stream);
+
+/* Lenient sampling verification [magicnet §8]: spec_verify_sample with the
+ * draft's distribution shrunk to lenience * q before it is compared with the
+ * target, so draft token d_i is accepted with probability
+ * a_i = min(1, p_i(d_i) / (lenience * q_i(d_i))), and at the first rejection
+ * j the replacement is drawn from (p_j - lenience * q_j)+ / Z (the page gives
+ * the acceptance rule; using lenience * q in the residual too is this
+ * library's reading).  0 < lenience <= 1; lenience = 1 is spec_verify_sample
+ * exactly.  Below 1 the output no longer follows the target's distribution:
+ * the page's guarantee is that no token is emitted with more than
+ * 1 / lenience times its target probability.  out_residual_z reports
+ * Z = sum (p_j - lenience * q_j)+.  A lenience outside (0, 1] or NaN returns
+ * SPEC_ERR_INVALID_ARG; everything else (arguments, workspace -- the same
+ * spec_verify_workspace_size -- outputs, errors, launches) is as for
+ * spec_verify_sample. */
+SPEC_API spec_status_t spec_verify_sample_lenient(const void* target_logits, const void* draft_logits,
+                                         spec_dtype_t dtype, const int32_t* draft_tokens,
+                                         const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                         const float* u_accept, const float* u_sample,
+                                         spec_sampling_params_t target_params,
+                                         spec_sampling_params_t draft_params, float lenience,
+                                         int32_t batch, int32_t gamma_max, int32_t vocab,
+                                         void* workspace, size_t workspace_bytes,
+                                         int32_t* out_tokens, int32_t* out_num_accepted,
+                                         float* out_accept_prob, float* out_residual_z,
+                                         int32_t* out_status, void* stream);
 
 /* Bytes of workspace spec_verify_greedy needs (same zero-fill rule). */
 SPEC_API spec_status_t spec_greedy_workspace_size(int32_t batch, int32_t gamma_max, size_t* bytes);

@@ -34,7 +34,7 @@ SPEC_F32 = 1
 # Every symbol include/spec_verify.h declares.
 EXPORTED = ("spec_verify_workspace_size", "spec_verify_sample", "spec_greedy_workspace_size",
             "spec_verify_greedy", "spec_transform_probs", "spec_status_string",
-            "spec_verify_sample_noalloc", "spec_verify_greedy_early")
+            "spec_verify_sample_noalloc", "spec_verify_greedy_early", "spec_verify_sample_lenient")
 
 
 class spec_sampling_params_t(ctypes.Structure):
@@ -72,6 +72,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_sample.restype = ctypes.c_int
     lib.spec_verify_sample.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, i32, i32, i32,
                                        vp, sz, vp, vp, vp, vp, vp, vp]
+    lib.spec_verify_sample_lenient.restype = ctypes.c_int
+    lib.spec_verify_sample_lenient.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, ctypes.c_float,
+                                               i32, i32, i32, vp, sz, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_sample_noalloc.restype = ctypes.c_int
     lib.spec_verify_sample_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, i32, i32, i32,
                                                vp, vp, vp, vp, vp, vp]
@@ -112,6 +115,10 @@ def spec_greedy_workspace_size(batch: int, gamma_max: int) -> int:
 
 def spec_verify_sample(*args) -> int:
     return load().spec_verify_sample(*args)
+
+
+def spec_verify_sample_lenient(*args) -> int:
+    return load().spec_verify_sample_lenient(*args)
 
 
 def spec_verify_sample_noalloc(*args) -> int:

@@ -86,12 +86,14 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
                   gamma_per_seq: torch.Tensor | None = None,
                   draft_is_onehot: torch.Tensor | None = None,
                   workspace: torch.Tensor | None = None, out: VerifyOutput | None = None,
-                  stream: torch.cuda.Stream | None = None) -> VerifyOutput:
-    """spec_verify_sample on torch tensors.
+                  stream: torch.cuda.Stream | None = None,
+                  lenience: float | None = None) -> VerifyOutput:
+    """spec_verify_sample on torch tensors (spec_verify_sample_lenient when
+    ``lenience`` is given).
 
     target_logits [B, G+1, V] and draft_logits [B, G, V] (or None: all one-hot) of
     bfloat16 / float32; draft_tokens [B, G] int32; u_accept [B, G] and u_sample [B]
-    float32; gamma_per_seq [B] int32; draft_is_onehot [B] uint8.
+    float32; gamma_per_seq [B] int32; draft_is_onehot [B] uint8; lenience in (0, 1].
     """
     B, G1, V = target_logits.shape
     G = G1 - 1
@@ -102,13 +104,17 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
         workspace = new_workspace(workspace_size(B, G, V, target, draft), dev)
     if out is None:
         out = alloc_outputs(B, G, dev)
-    st = _lib.spec_verify_sample(
-        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
-        _ptr(gamma_per_seq), _ptr(draft_is_onehot), _ptr(u_accept), _ptr(u_sample),
-        target.c(), draft.c(), B, G, V, _ptr(workspace), workspace.numel(),
-        _ptr(out.tokens), _ptr(out.num_accepted), _ptr(out.accept_prob), _ptr(out.residual_z),
-        _ptr(out.status), _stream(stream))
-    _lib.check("spec_verify_sample", st)
+    head = (_ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
+            _ptr(gamma_per_seq), _ptr(draft_is_onehot), _ptr(u_accept), _ptr(u_sample),
+            target.c(), draft.c())
+    tail = (B, G, V, _ptr(workspace), workspace.numel(),
+            _ptr(out.tokens), _ptr(out.num_accepted), _ptr(out.accept_prob), _ptr(out.residual_z),
+            _ptr(out.status), _stream(stream))
+    if lenience is None:
+        _lib.check("spec_verify_sample", _lib.spec_verify_sample(*head, *tail))
+    else:
+        _lib.check("spec_verify_sample_lenient",
+                   _lib.spec_verify_sample_lenient(*head, float(lenience), *tail))
     return out
 
 

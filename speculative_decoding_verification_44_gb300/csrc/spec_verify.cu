@@ -31,6 +31,7 @@ struct SampleArgs {
   const float* u_acc;
   const float* u_samp;
   RowParams tp, dp;
+  float beta;           // lenience: beta q stands in for q (1 = the lossless rule)
   int B, G, V;
   int aligned;
   size_t row_bytes;
@@ -107,18 +108,19 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const double* p
 }
 
 // Inverse-CDF draw over a PATH_STREAM target row's kept list, block-wide.
-// Residual weights max(0, p - q) [wrblog §5], or p itself for the bonus draw;
-// the token is the smallest x (vocabulary order) with C(x) > u Z.  No sort:
-// both lists arrive in one round trip, thread e takes target entry e, finds
-// q by scanning the draft list, then sums -- in double-float, in list order
-// -- Z and its own prefix C(x_e-) over the entries with smaller tokens.  The
-// draw is the smallest token whose C(x_e-) + w_e exceeds u Z (the largest
-// token with weight if rounding leaves none).
+// Residual weights max(0, p - beta q) [wrblog §5; magicnet §8], or p itself for
+// the bonus draw; the token is the smallest x (vocabulary order) with
+// C(x) > u Z.  Kept lists are stored in token order, so thread e takes target
+// entry e (one round trip for both lists), looks q up by binary search in the
+// draft list, and a block scan in double-float gives every C(x) and Z at once.
+// The draw is the first entry whose C(x) exceeds u Z (the last entry with
+// weight if rounding leaves none).
 template <int DT>
 __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
                                       const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
   static_assert(kThreads >= 2 * kListCap, "one thread per entry of both lists");
-  const int tid = threadIdx.x;
+  constexpr int kScanWarps = kListCap / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slots = 2 * a.G + 1;
   SmemEpi& E = sm.u.e;
   const int nt = E.rs[r].n_list;
@@ -126,10 +128,12 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
   const int nq = draft_list ? ds.n_list : 0;
   const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
   const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
+  ListEntry te;
+  te.p = 0.0;
+  te.token = 0x7fffffff;
   if (tid < nt) {
-    const ListEntry t = load_entry(tl + tid);
-    E.tok[tid] = t.token;
-    E.w[tid] = t.p;
+    te = load_entry(tl + tid);
+    E.tok[tid] = te.token;
   } else if (tid >= kListCap && tid - kListCap < nq) {
     const ListEntry q = load_entry(ql + tid - kListCap);
     E.qtok[tid - kListCap] = q.token;
@@ -140,42 +144,50 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
     sm.b_i32[6] = -1;
   }
   __syncthreads();
-  int mytok = 0;
-  if (tid < nt) {
-    mytok = E.tok[tid];
-    const double p = E.w[tid];
-    double w = p;
-    if (residual) {
-      double q = 0.0;
-      if (onehot) q = (mytok == dj) ? 1.0 : 0.0;
-      else if (draft_list) {
-        for (int f = 0; f < nq; ++f)
-          if (E.qtok[f] == mytok) q = E.qp[f];
-      } else {
-        const Row drow = seq_row<DT>(a, b, r, true);
-        q = full_prob(load_elem<DT>(drow.base, mytok), static_cast<uint32_t>(mytok), cut_test(ds.cut), ds.m,
-                      a.dp.cT, static_cast<float>(1.0 / ds.W));
+  double w = te.p;
+  if (residual && tid < nt) {
+    double q = 0.0;
+    if (onehot) {
+      q = (te.token == dj) ? 1.0 : 0.0;
+    } else if (draft_list) {
+      int lo = 0, hi = nq - 1;
+      while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int t = E.qtok[mid];
+        if (t == te.token) { q = E.qp[mid]; break; }
+        if (t < te.token) lo = mid + 1; else hi = mid - 1;
       }
-      w = fmax(p - q, 0.0);
+    } else {
+      const Row drow = seq_row<DT>(a, b, r, true);
+      q = full_prob(load_elem<DT>(drow.base, te.token), static_cast<uint32_t>(te.token), cut_test(ds.cut), ds.m,
+                    a.dp.cT, static_cast<float>(1.0 / ds.W));
     }
-    const float wh = static_cast<float>(w), ph = static_cast<float>(p);
-    E.wh[tid] = wh;
-    E.wl[tid] = static_cast<float>(w - static_cast<double>(wh));
-    E.ph[tid] = ph;
-    E.pl[tid] = static_cast<float>(p - static_cast<double>(ph));
+    w = fmax(te.p - static_cast<double>(a.beta) * q, 0.0);
   }
-  __syncthreads();
   for (int pass = 0; pass < 2; ++pass) {
-    const float* H = pass == 0 ? E.wh : E.ph;
-    const float* Lo = pass == 0 ? E.wl : E.pl;
-    df Z = df_from(0.0f), pre = df_from(0.0f);
-    for (int f = 0; f < nt; ++f) {               // every thread: the same Z, in the same order
-      const df wf = {H[f], Lo[f]};
-      Z = df_add(Z, wf);
-      if (tid < nt && E.tok[f] < mytok) pre = df_add(pre, wf);
+    const double x = pass == 0 ? w : te.p;
+    const float xh = static_cast<float>(x);
+    const df xd = {xh, static_cast<float>(x - static_cast<double>(xh))};
+    df incl = df_from(0.0f);
+    if (warp < kScanWarps) {
+      incl = warp_incl_scan_df(xd, lane);
+      if (lane == 31) {
+        E.wh[warp] = incl.hi;
+        E.wl[warp] = incl.lo;
+      }
     }
+    __syncthreads();
+    df Z = df_from(0.0f), base = df_from(0.0f);
+#pragma unroll
+    for (int k = 0; k < kScanWarps; ++k) {       // every thread: the same Z, in the same order
+      const df s = {E.wh[k], E.wl[k]};
+      if (k < warp) base = df_add(base, s);
+      Z = df_add(Z, s);
+    }
+    incl = df_add(base, incl);
     if (pass == 0 && residual) Z_resid = df_to_double(Z);
     if (!(Z.hi > 0.0f)) {
+      __syncthreads();                           // E.wh / E.wl are rewritten by the next pass
       if (pass == 0 && residual) {               // Z == 0 after a rejection: draw from p instead
         flags |= SEQ_FLAG_Z_ZERO;
         continue;
@@ -185,12 +197,13 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
     const float uf = static_cast<float>(u);
     const float th = uf * Z.hi;
     const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
-    if (tid < nt && H[tid] > 0.0f) {
-      if (!df_ge(t, df_add(pre, {H[tid], Lo[tid]}))) atomicMin(&sm.b_i32[3], mytok);   // C(x) > t
-      atomicMax(&sm.b_i32[6], mytok);
+    if (tid < nt && xh > 0.0f) {
+      if (!df_ge(t, incl)) atomicMin(&sm.b_i32[3], tid);     // C(x) > u Z
+      atomicMax(&sm.b_i32[6], tid);
     }
     __syncthreads();
-    const int sel = sm.b_i32[3] != 0x7fffffff ? sm.b_i32[3] : sm.b_i32[6];
+    const int e = sm.b_i32[3] != 0x7fffffff ? sm.b_i32[3] : sm.b_i32[6];
+    const int sel = e >= 0 ? E.tok[e] : -1;
     __syncthreads();
     return sel;
   }
@@ -198,13 +211,14 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
 }
 
 // Per-element weight for the block scan over a PATH_FULL target row.
-// mode 0: p; 1: (p - q)+ with q a PATH_FULL draft row; 2: (p - q)+ with q a
-// token-sorted list; 3: (p - delta_dj)+.
+// mode 0: p; 1: (p - beta q)+ with q a PATH_FULL draft row; 2: (p - beta q)+
+// with q a token-sorted list; 3: (p - beta delta_dj)+.
 struct ScanCtx {
   Row trow, drow;
   CutTest ctt, ctd;      // kept sets of the target and draft rows
   float mt, md;          // row maxima
   float cTt, cTd, invWt, invWd;
+  float beta;            // lenience factor on q
   int mode;
   int dj;
   int nq;
@@ -236,7 +250,7 @@ __device__ __forceinline__ float scan_weights(const ScanCtx& c, int v, int n, co
       if (c.mode == 1) q = full_prob(zd[e], x, c.ctd, c.md, c.cTd, c.invWd);
       else if (c.mode == 2) q = list_lookup(sm.u.e.qtok, sm.u.e.qp, c.nq, static_cast<int>(x));
       else if (c.mode == 3) q = (static_cast<int>(x) == c.dj) ? 1.0f : 0.0f;
-      we = c.mode == 0 ? p : fmaxf(p - q, 0.0f);
+      we = c.mode == 0 ? p : fmaxf(p - c.beta * q, 0.0f);
     }
     w[e] = we;
     s += we;
@@ -399,22 +413,16 @@ __device__ ScanCtx make_scan(const SampleArgs& a, int b, int r, int mode, bool o
   c.invWt = static_cast<float>(1.0 / ts.W);
   c.invWd = static_cast<float>(1.0 / ds.W);
   c.dj = dj;
+  c.beta = a.beta;
   c.nq = 0;
   c.mode = mode;
-  if (mode == 2) {
+  if (mode == 2) {                 // kept lists are stored in token order
     const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
     c.nq = ds.n_list;
     if (tid < c.nq) {
       const ListEntry q = load_entry(ql + tid);
-      sm.u.e.tok[tid] = q.token;
-      sm.u.e.w[tid] = q.p;
-    }
-    __syncthreads();
-    if (tid < c.nq) {
-      int rank = 0;
-      for (int jj = 0; jj < c.nq; ++jj) rank += sm.u.e.tok[jj] < sm.u.e.tok[tid] ? 1 : 0;
-      sm.u.e.qtok[rank] = sm.u.e.tok[tid];
-      sm.u.e.qp[rank] = sm.u.e.w[tid];
+      sm.u.e.qtok[tid] = q.token;
+      sm.u.e.qp[tid] = q.p;
     }
     __syncthreads();
   }
@@ -446,6 +454,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     E.dtok[t] = a.tokens[tokb + t];
     E.uacc[t] = a.u_acc[tokb + t];
   }
+  if (tid == kThreads - 1) sm.b_f64[2] = static_cast<double>(a.u_samp[b]);
   __syncthreads();
   // status, in the documented order: tokens, uniforms, rows (lane-parallel, warp 0)
   if (warp == 0) {
@@ -455,8 +464,8 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
       bad_u |= !(E.uacc[i] >= 0.0f && E.uacc[i] < 1.0f);
     }
     if (lane == 0) {
-      const float us = a.u_samp[b];
-      bad_u |= !(us >= 0.0f && us < 1.0f);
+      const double us = sm.b_f64[2];
+      bad_u |= !(us >= 0.0 && us < 1.0);
     }
     int status = SEQ_OK;
     if (__any_sync(kFull, bad_tok)) status = SEQ_BAD_TOKEN;
@@ -488,7 +497,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
           const float p = static_cast<float>(E.rs[i].p_tok);
           const float q = onehot ? 1.0f : static_cast<float>(E.rs[a.G + 1 + i].p_tok);
           float ai;
-          if (q > 0.0f) ai = fminf(1.0f, p / q);
+          if (q > 0.0f) ai = fminf(1.0f, p / (a.beta * q));   // [magicnet §8]; beta = 1: p / q
           else { ai = p > 0.0f ? 1.0f : 0.0f; zq = true; }
           rej = !(E.uacc[i] < ai);
           if (a.out_aprob) a.out_aprob[tokb + i] = ai;
@@ -532,7 +541,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0;
   if (residual && !onehot) ds = E.rs[a.G + 1 + r];
   const int dj = residual ? E.dtok[j] : -1;
-  const double u = static_cast<double>(a.u_samp[b]);
+  const double u = sm.b_f64[2];
   double Z_resid = -1.0;
   int tok = -1;
   bool deferred = false;
@@ -604,13 +613,18 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   // publish the row summary, then count this row in
   if (threadIdx.x == 0) a.stats[static_cast<size_t>(b) * slots + slot] = sm.st;
   if (P.path == PATH_STREAM) {
+    // the kept list, stored in token order (entry e goes to its token's rank)
+    static_assert(kListCap <= kThreads, "one thread per kept entry");
     ListEntry* dst = a.lists + (static_cast<size_t>(b) * slots + slot) * kListCap;
-    for (int e = threadIdx.x; e < sm.st.n_list; e += kThreads) {
+    const int n = sm.st.n_list;
+    if (threadIdx.x < n) {
       ListEntry le;
-      le.p = sm.list_p[e];
-      le.token = sm.list_tok[e];
+      le.p = sm.list_p[threadIdx.x];
+      le.token = sm.list_tok[threadIdx.x];
       le.pad = 0;
-      dst[e] = le;
+      int rank = 0;
+      for (int f = 0; f < n; ++f) rank += sm.list_tok[f] < le.token ? 1 : 0;
+      dst[rank] = le;
     }
   }
   __threadfence();
@@ -1143,18 +1157,20 @@ spec_status_t spec_greedy_workspace_size(int32_t batch, int32_t gamma_max, size_
   return SPEC_OK;
 }
 
-spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
-                                 spec_dtype_t dtype, const int32_t* draft_tokens,
-                                 const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
-                                 const float* u_accept, const float* u_sample,
-                                 spec_sampling_params_t target_params,
-                                 spec_sampling_params_t draft_params,
-                                 int32_t batch, int32_t gamma_max, int32_t vocab,
-                                 void* workspace, size_t workspace_bytes,
-                                 int32_t* out_tokens, int32_t* out_num_accepted,
-                                 float* out_accept_prob, float* out_residual_z,
-                                 int32_t* out_status, void* stream) {
+// spec_verify_sample and spec_verify_sample_lenient: one body, beta = lenience.
+static spec_status_t verify_sample_impl(const void* target_logits, const void* draft_logits,
+                                        spec_dtype_t dtype, const int32_t* draft_tokens,
+                                        const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                        const float* u_accept, const float* u_sample,
+                                        spec_sampling_params_t target_params,
+                                        spec_sampling_params_t draft_params, float lenience,
+                                        int32_t batch, int32_t gamma_max, int32_t vocab,
+                                        void* workspace, size_t workspace_bytes,
+                                        int32_t* out_tokens, int32_t* out_num_accepted,
+                                        float* out_accept_prob, float* out_residual_z,
+                                        int32_t* out_status, void* stream) {
   if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  if (!(lenience > 0.0f && lenience <= 1.0f)) return SPEC_ERR_INVALID_ARG;
   if (!shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
     return SPEC_ERR_INVALID_ARG;
   if (gamma_max > kMaxGamma) return SPEC_ERR_UNSUPPORTED;
@@ -1180,6 +1196,7 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   a.onehot = draft_is_onehot;
   a.u_acc = u_accept;
   a.u_samp = u_sample;
+  a.beta = lenience;
   a.B = batch;
   a.G = gamma_max;
   a.V = vocab;
@@ -1217,6 +1234,40 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
+                                 spec_dtype_t dtype, const int32_t* draft_tokens,
+                                 const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                 const float* u_accept, const float* u_sample,
+                                 spec_sampling_params_t target_params,
+                                 spec_sampling_params_t draft_params,
+                                 int32_t batch, int32_t gamma_max, int32_t vocab,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* out_tokens, int32_t* out_num_accepted,
+                                 float* out_accept_prob, float* out_residual_z,
+                                 int32_t* out_status, void* stream) {
+  return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
+                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, 1.0f,
+                            batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,
+                            out_num_accepted, out_accept_prob, out_residual_z, out_status, stream);
+}
+
+spec_status_t spec_verify_sample_lenient(const void* target_logits, const void* draft_logits,
+                                         spec_dtype_t dtype, const int32_t* draft_tokens,
+                                         const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                         const float* u_accept, const float* u_sample,
+                                         spec_sampling_params_t target_params,
+                                         spec_sampling_params_t draft_params, float lenience,
+                                         int32_t batch, int32_t gamma_max, int32_t vocab,
+                                         void* workspace, size_t workspace_bytes,
+                                         int32_t* out_tokens, int32_t* out_num_accepted,
+                                         float* out_accept_prob, float* out_residual_z,
+                                         int32_t* out_status, void* stream) {
+  return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
+                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, lenience,
+                            batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,
+                            out_num_accepted, out_accept_prob, out_residual_z, out_status, stream);
 }
 
 spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,

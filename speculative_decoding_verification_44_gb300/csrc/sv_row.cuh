@@ -72,12 +72,10 @@ struct __align__(16) SmemFull {
   uint32_t wcnt[kWarps];
 };
 struct __align__(16) SmemEpi {
-  double w[2 * kListCap];            // kept-list entries (list draw; draft list staging)
-  int32_t tok[2 * kListCap];
-  int32_t qtok[kListCap];            // draft kept list (sorted by token for the block scan's lookups)
+  int32_t tok[kListCap];             // list draw: the target kept list's tokens
+  int32_t qtok[kListCap];            // draft kept list (token order, for lookups)
   double qp[kListCap];
-  float wh[kListCap], wl[kListCap];  // list draw: weights and p as double-float
-  float ph[kListCap], pl[kListCap];
+  float wh[kWarps], wl[kWarps];      // list draw: per-warp scan totals, double-float
   double wtot[kWarps];               // per-warp segment totals of the block scan
   double csum[kWarps][kScanChunks];  // per-chunk totals of the block scan
   RowStat rs[2 * kMaxGamma + 1];     // the sequence's row summaries

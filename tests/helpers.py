@@ -37,7 +37,7 @@ def oracle_probs(rows: torch.Tensor, params) -> torch.Tensor:
     return torch.from_numpy(p)
 
 
-def run_oracle_sample(w, seqs=None, keep_cdf=True):
+def run_oracle_sample(w, seqs=None, keep_cdf=True, lenience=1.0):
     tl = to_f64(w.target_logits) if seqs is None else to_f64(w.target_logits[seqs])
     dl = None
     if w.draft_logits is not None:
@@ -49,7 +49,8 @@ def run_oracle_sample(w, seqs=None, keep_cdf=True):
     gam = None if w.gamma_per_seq is None else w.gamma_per_seq.cpu().numpy()[sel]
     oh = None if w.draft_is_onehot is None else w.draft_is_onehot.cpu().numpy()[sel]
     return oracle.verify_sample(tl, dl, toks, ua, us, params_tuple(w.target_params),
-                                params_tuple(w.draft_params), gam, oh, keep_cdf=keep_cdf)
+                                params_tuple(w.draft_params), gam, oh, keep_cdf=keep_cdf,
+                                lenience=lenience)
 
 
 def run_oracle_greedy(w, seqs=None):
@@ -141,3 +142,11 @@ def compare_greedy(out, ref, w, seqs=None):
         assert nacc[b] == r.num_accepted, (b, nacc[b], r.num_accepted)
         assert (toks[b] == r.tokens).all(), (b, toks[b], r.tokens)
     return len(seqs)
+
+
+def check_sample_counts(out, ref, w, seqs=None, min_exact=0.9):
+    """compare_sample plus the parity bar: few flagged / boundary sequences, the rest exact."""
+    c = compare_sample(out, ref, w, seqs)
+    assert c["flagged"] + c["boundary"] <= max(2, 0.02 * c["n"]), c
+    assert c["exact"] >= min_exact * (c["n"] - c["flagged"] - c["errors"]), c
+    return c

@@ -118,6 +118,15 @@ def test_host_validation_before_any_launch(lib):
     assert ecall(rows=fake + 2) == _lib.SPEC_ERR_MISALIGNED
     assert ecall(ws=fake + 16) == _lib.SPEC_ERR_MISALIGNED
     assert ecall(wsb=8) == _lib.SPEC_ERR_WORKSPACE
+    lenient = _lib.spec_verify_sample_lenient
+
+    def lcall(beta, wsb=1 << 30):
+        return lenient(fake, fake, 0, fake, None, None, fake, fake, P, P, beta, 2, 3, 64, fake, wsb,
+                       fake, fake, None, None, None, None)
+
+    for beta in (0.0, -1.0, 1.0000001, float("nan"), float("inf")):
+        assert lcall(beta) == _lib.SPEC_ERR_INVALID_ARG, beta
+    assert lcall(0.5, wsb=16) == _lib.SPEC_ERR_WORKSPACE     # a valid lenience reaches the later checks
     assert _lib.spec_transform_probs(fake, 0, 0, 64, P, fake, None, None) == _lib.SPEC_ERR_INVALID_ARG
     assert _lib.spec_transform_probs(fake + 2, 1, 1, 64, P, fake, None, None) == _lib.SPEC_ERR_MISALIGNED
 
