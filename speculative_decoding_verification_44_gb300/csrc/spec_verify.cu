@@ -96,12 +96,12 @@ __device__ __forceinline__ Row seq_row(const SampleArgs& a, int b, int i, bool d
 }
 
 // Probability q(x) of a PATH_STREAM draft row: lookup in its token-sorted list.
-__device__ __forceinline__ float list_lookup(const int32_t* tok, const double* p, int n, int x) {
+__device__ __forceinline__ float list_lookup(const int32_t* tok, const float* p, int n, int x) {
   int lo = 0, hi = n - 1;
   while (lo <= hi) {
     const int mid = (lo + hi) >> 1;
     const int t = tok[mid];
-    if (t == x) return static_cast<float>(p[mid]);
+    if (t == x) return p[mid];
     if (t < x) lo = mid + 1; else hi = mid - 1;
   }
   return 0.0f;
@@ -117,7 +117,7 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const double* p
 // weight if rounding leaves none).
 template <int DT>
 __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
-                                      const RowStat& ds, double u, double& Z_resid, int& flags, Smem& sm) {
+                                      const RowStat& ds, float uf, double& Z_resid, int& flags, Smem& sm) {
   static_assert(kThreads >= 2 * kListCap, "one thread per entry of both lists");
   constexpr int kScanWarps = kListCap / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -129,7 +129,8 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
   const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
   const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
   ListEntry te;
-  te.p = 0.0;
+  te.p = 0.0f;
+  te.p_lo = 0.0f;
   te.token = 0x7fffffff;
   if (tid < nt) {
     te = load_entry(tl + tid);
@@ -137,18 +138,20 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
   } else if (tid >= kListCap && tid - kListCap < nq) {
     const ListEntry q = load_entry(ql + tid - kListCap);
     E.qtok[tid - kListCap] = q.token;
-    E.qp[tid - kListCap] = q.p;
+    E.qp[tid - kListCap] = q.p + q.p_lo;
   }
   if (tid == 0) {
     sm.b_i32[3] = 0x7fffffff;
     sm.b_i32[6] = -1;
   }
   __syncthreads();
-  double w = te.p;
+  // weights as double-float (no float64 arithmetic: that pipe is slow here)
+  const df pw = {te.p, te.p_lo};
+  df w = pw;
   if (residual && tid < nt) {
-    double q = 0.0;
+    float q = 0.0f;
     if (onehot) {
-      q = (te.token == dj) ? 1.0 : 0.0;
+      q = (te.token == dj) ? 1.0f : 0.0f;
     } else if (draft_list) {
       int lo = 0, hi = nq - 1;
       while (lo <= hi) {
@@ -162,12 +165,13 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
       q = full_prob(load_elem<DT>(drow.base, te.token), static_cast<uint32_t>(te.token), cut_test(ds.cut), ds.m,
                     a.dp.cT, static_cast<float>(1.0 / ds.W));
     }
-    w = fmax(te.p - static_cast<double>(a.beta) * q, 0.0);
+    const float bq = a.beta * q;                      // beta q exactly, as hi + lo
+    const df d = df_add(pw, {-bq, -fmaf(a.beta, q, -bq)});
+    w = d.hi > 0.0f ? d : df_from(0.0f);
   }
   for (int pass = 0; pass < 2; ++pass) {
-    const double x = pass == 0 ? w : te.p;
-    const float xh = static_cast<float>(x);
-    const df xd = {xh, static_cast<float>(x - static_cast<double>(xh))};
+    const df xd = pass == 0 ? w : pw;
+    const float xh = xd.hi;
     df incl = df_from(0.0f);
     if (warp < kScanWarps) {
       incl = warp_incl_scan_df(xd, lane);
@@ -185,7 +189,7 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
       Z = df_add(Z, s);
     }
     incl = df_add(base, incl);
-    if (pass == 0 && residual) Z_resid = df_to_double(Z);
+    if (pass == 0 && residual && tid == 0) Z_resid = Z.hi;   // only thread 0 reports it
     if (!(Z.hi > 0.0f)) {
       __syncthreads();                           // E.wh / E.wl are rewritten by the next pass
       if (pass == 0 && residual) {               // Z == 0 after a rejection: draw from p instead
@@ -194,7 +198,6 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
       }
       return -1;
     }
-    const float uf = static_cast<float>(u);
     const float th = uf * Z.hi;
     const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
     if (tid < nt && xh > 0.0f) {
@@ -422,7 +425,7 @@ __device__ ScanCtx make_scan(const SampleArgs& a, int b, int r, int mode, bool o
     if (tid < c.nq) {
       const ListEntry q = load_entry(ql + tid);
       sm.u.e.qtok[tid] = q.token;
-      sm.u.e.qp[tid] = q.p;
+      sm.u.e.qp[tid] = q.p + q.p_lo;
     }
     __syncthreads();
   }
@@ -444,7 +447,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     const bool used = t <= gb || (t > a.G && !onehot && t - a.G - 1 < gb);
     RowStat rs;
     rs.status = SEQ_OK;
-    rs.p_tok = 0.0;
+    rs.p_tok = 0.0f;
     rs.path = PATH_FULL;
     rs.n_list = 0;
     if (used) rs = load_stat(S + t);
@@ -454,7 +457,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     E.dtok[t] = a.tokens[tokb + t];
     E.uacc[t] = a.u_acc[tokb + t];
   }
-  if (tid == kThreads - 1) sm.b_f64[2] = static_cast<double>(a.u_samp[b]);
+  if (tid == kThreads - 1) sm.b_f32[0] = a.u_samp[b];
   __syncthreads();
   // status, in the documented order: tokens, uniforms, rows (lane-parallel, warp 0)
   if (warp == 0) {
@@ -464,8 +467,8 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
       bad_u |= !(E.uacc[i] >= 0.0f && E.uacc[i] < 1.0f);
     }
     if (lane == 0) {
-      const double us = sm.b_f64[2];
-      bad_u |= !(us >= 0.0 && us < 1.0);
+      const float us = sm.b_f32[0];
+      bad_u |= !(us >= 0.0f && us < 1.0f);
     }
     int status = SEQ_OK;
     if (__any_sync(kFull, bad_tok)) status = SEQ_BAD_TOKEN;
@@ -494,8 +497,8 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
         const int i = base + lane;
         bool rej = false, zq = false;
         if (i < gb) {
-          const float p = static_cast<float>(E.rs[i].p_tok);
-          const float q = onehot ? 1.0f : static_cast<float>(E.rs[a.G + 1 + i].p_tok);
+          const float p = E.rs[i].p_tok;
+          const float q = onehot ? 1.0f : E.rs[a.G + 1 + i].p_tok;
           float ai;
           if (q > 0.0f) ai = fminf(1.0f, p / (a.beta * q));   // [magicnet §8]; beta = 1: p / q
           else { ai = p > 0.0f ? 1.0f : 0.0f; zq = true; }
@@ -541,12 +544,12 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0;
   if (residual && !onehot) ds = E.rs[a.G + 1 + r];
   const int dj = residual ? E.dtok[j] : -1;
-  const double u = sm.b_f64[2];
+  const float uf = sm.b_f32[0];
   double Z_resid = -1.0;
   int tok = -1;
   bool deferred = false;
   if (ts.path == PATH_STREAM) {
-    tok = list_draw<DT>(a, b, r, residual, onehot, dj, ds, u, Z_resid, flags, sm);
+    tok = list_draw<DT>(a, b, r, residual, onehot, dj, ds, uf, Z_resid, flags, sm);
   } else if (a.defer) {
     // a full-row draw: draw_kernel does it, chunk-parallel, and writes the drawn
     // token, residual_Z and status
@@ -562,14 +565,14 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   } else {
     const int mode = !residual ? 0 : (onehot ? 3 : (ds.path == PATH_FULL ? 1 : 2));
     ScanCtx c = make_scan<DT>(a, b, r, mode, onehot, ts, ds, dj, sm);
-    tok = block_scan_draw<DT>(c, u, residual, Z_resid, flags, sm);
+    tok = block_scan_draw<DT>(c, static_cast<double>(uf), residual, Z_resid, flags, sm);
   }
 
   // 4. outputs: accepted drafts, the drawn token, then -1
   const size_t ob = static_cast<size_t>(b) * (a.G + 1);
   for (int t = tid; t <= a.G; t += kThreads) {
     int v = -1;
-    if (t < j) v = a.tokens[tokb + t];
+    if (t < j) v = E.dtok[t];
     else if (t == j) v = tok;
     if (t != j || !deferred) a.out_tokens[ob + t] = v;
   }
@@ -619,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
     const int n = sm.st.n_list;
     if (threadIdx.x < n) {
       ListEntry le;
-      le.p = sm.list_p[threadIdx.x];
+      le.p = sm.list_ph[threadIdx.x];
+      le.p_lo = sm.list_pl[threadIdx.x];
       le.token = sm.list_tok[threadIdx.x];
       le.pad = 0;
       int rank = 0;
@@ -999,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 5) transform_kernel(const char* logi
     for (int x = threadIdx.x; x < V; x += kThreads) o[x] = 0.0f;
     __syncthreads();
     if (st.status == SEQ_OK)
-      for (int e = threadIdx.x; e < st.n_list; e += kThreads) o[sm.list_tok[e]] = static_cast<float>(sm.list_p[e]);
+      for (int e = threadIdx.x; e < st.n_list; e += kThreads) o[sm.list_tok[e]] = sm.list_ph[e];
   } else {
     const float invW = static_cast<float>(1.0 / st.W);
     const CutTest ct = cut_test(st.cut);

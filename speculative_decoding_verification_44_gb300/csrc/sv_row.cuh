@@ -46,20 +46,20 @@ struct RowParams {
 
 // Per-row result, mirrored into the workspace for the sequence epilogue.
 struct __align__(16) RowStat {
-  double W;        // normaliser: sum over the kept set of exp((z - m) / T)
-  double p_tok;    // probability of the draft token this row scores (0 if none)
+  double W;        // PATH_FULL: normaliser, sum over the kept set of exp((z - m) / T)
   uint64_t cut;    // PATH_FULL: token kept iff composite >= cut (0 keeps all)
   float m;         // row maximum
+  float p_tok;     // probability of the draft token this row scores (0 if none)
   int32_t status;  // SEQ_OK, SEQ_NONFINITE or SEQ_EMPTY_SUPPORT
   int32_t n_list;  // PATH_STREAM: kept-list length
   int32_t path;
   int32_t argmax;  // greedy rows: argmax token
-  int32_t pad;
+  int32_t pad[2];
 };
 static_assert(sizeof(RowStat) == 48, "RowStat layout");
 
 struct __align__(16) ListEntry {  // one kept token of a PATH_STREAM row
-  double p;
+  float p, p_lo;                  // its probability as a double-float (hi, lo)
   int32_t token;
   int32_t pad;
 };
@@ -74,7 +74,7 @@ struct __align__(16) SmemFull {
 struct __align__(16) SmemEpi {
   int32_t tok[kListCap];             // list draw: the target kept list's tokens
   int32_t qtok[kListCap];            // draft kept list (token order, for lookups)
-  double qp[kListCap];
+  float qp[kListCap];
   float wh[kWarps], wl[kWarps];      // list draw: per-warp scan totals, double-float
   double wtot[kWarps];               // per-warp segment totals of the block scan
   double csum[kWarps][kScanChunks];  // per-chunk totals of the block scan
@@ -86,17 +86,17 @@ struct __align__(16) Smem {
   union {
     SmemFull f;
     SmemEpi e;
+    uint32_t khist[4][256];          // PATH_STREAM: digit histograms of the per-thread maxima
   } u;
   uint64_t cand[kCandCap];           // PATH_STREAM: candidates (composites >= the lower bound)
   uint64_t topk[kSmallK];
   uint64_t sorted[kSmallK];          // PATH_STREAM: top-k in descending order
   int32_t list_tok[kListCap];
-  double list_p[kListCap];
+  float list_ph[kListCap], list_pl[kListCap];   // kept probabilities, double-float
   int nw[kWarps];
   int ncand;
   int nfull;                         // PATH_STREAM: threads whose vectors need a full re-read
   int16_t full[kMaxFull];
-  uint32_t tmax[kThreads];           // PATH_STREAM: per-thread maxima (keys)
   float red_f[kWarps];
   double red_d[kWarps];
   uint64_t red_u[kWarps];
@@ -105,6 +105,7 @@ struct __align__(16) Smem {
   // broadcast slots
   uint64_t b_u64[4];
   double b_f64[4];
+  float b_f32[2];
   int b_i32[8];
   RowStat st;
 };
@@ -1292,7 +1293,7 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm) 
   st.n_list = 0;
   st.argmax = -1;
   st.W = S;
-  st.p_tok = 0.0;
+  st.p_tok = 0.0f;
   st.status = bad ? SEQ_NONFINITE : (m > -__int_as_float(0x7f800000) ? SEQ_OK : SEQ_EMPTY_SUPPORT);
   if (st.status == SEQ_OK) {
     const float scale = __int_as_float((127 + P.fixed_shift) << 23);   // 2^fixed_shift
@@ -1315,7 +1316,7 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm) 
     if (dtok >= 0) {
       const float z = load_elem<DT>(row.base, dtok);
       if (composite(fkey(z), static_cast<uint32_t>(dtok)) >= st.cut)
-        st.p_tok = static_cast<double>(fast_exp2((z - m) * P.cT)) / st.W;
+        st.p_tok = static_cast<float>(static_cast<double>(fast_exp2((z - m) * P.cT)) / st.W);
     }
   }
   if (tid == 0) sm.st = st;
@@ -1450,8 +1451,8 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
     st.m = m;
     st.status = any_bad ? SEQ_NONFINITE
                         : ((ntop == 0 || !(m > -__int_as_float(0x7f800000))) ? SEQ_EMPTY_SUPPORT : SEQ_OK);
-    st.W = 0.0;
-    st.p_tok = 0.0;
+    st.W = 0.0;                                               // PATH_FULL rows only
+    st.p_tok = 0.0f;
     st.n_list = 0;
     if (st.status == SEQ_OK) {
       float w[4];
@@ -1485,25 +1486,30 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (4 * lane + j < n_keep) part = df_add(part, df_from(w[j]));
-      const double W = df_to_double(warp_sum_df(part));
-      const double invW = 1.0 / W;
+      // 1 / W as a double-float: a float reciprocal refined by one Newton step
+      // (the float64 pipe is far slower than the float pipe on this part)
+      const df W = warp_sum_df(part);
+      const float r = __frcp_rn(W.hi);
+      const float r_lo = r * (fmaf(-W.hi, r, 1.0f) - W.lo * r);
       int hit = -1;
-      double ptok = 0.0;
+      float ptok = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int pos = 4 * lane + j;
         if (pos < n_keep) {
           const int tok = static_cast<int>(comp_index(v[j]));
-          const double p = static_cast<double>(w[j]) * invW;
+          const float ph = w[j] * r;                            // p = w / W, double-float
+          const float pl = fmaf(w[j], r, -ph) + w[j] * r_lo;
+          const float hi = ph + pl;
           sm.list_tok[pos] = tok;
-          sm.list_p[pos] = p;
-          if (tok == dtok) { hit = lane; ptok = p; }
+          sm.list_ph[pos] = hi;
+          sm.list_pl[pos] = pl - (hi - ph);
+          if (tok == dtok) { hit = lane; ptok = hi; }
         }
       }
       const unsigned hb = __ballot_sync(kFull, hit >= 0);
       if (hb) ptok = __shfl_sync(kFull, ptok, __ffs(hb) - 1);
-      st.W = W;
-      st.p_tok = hb ? ptok : 0.0;
+      st.p_tok = hb ? ptok : 0.0f;
       st.n_list = n_keep;
     }
     if (lane == 0) sm.st = st;
@@ -1543,6 +1549,8 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
   uint32_t mk0 = 0u, mk1 = 0u, mk2 = 0u, mk3 = 0u;      // four largest vector-max keys, descending
   int mv0 = 0, mv1 = 0, mv2 = 0, mv3 = 0;               // their vector indices
   bool bad = false;
+#pragma unroll
+  for (int rd = 0; rd < 4; ++rd) sm.u.khist[rd][tid] = 0u;  // visible after the barrier below
   for (int it = 0; it < iters; ++it) {
     uint4 r[kStreamUnroll];
     int cnt[kStreamUnroll];
@@ -1565,30 +1573,36 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
       }
     }
   }
-  sm.tmax[tid] = mk0;
   const int any_bad = __syncthreads_or(bad ? 1 : 0);
-  if ((tid >> 5) == 0) {
-    // one warp searches the k-th largest of the kThreads maxima, bit by bit
-    const int lane = tid & 31;
-    uint32_t v[kThreads / 32];
+  // K = the k-th largest of the kThreads maxima: MSB-first radix select, one
+  // 8-bit digit per round (bf16 keys: the top 16 bits, two rounds)
+  constexpr int kRounds = DT == DT_BF16 ? 2 : 4;
+  uint32_t prefix = 0u;
+  uint32_t need = static_cast<uint32_t>(P.k);
 #pragma unroll
-    for (int j = 0; j < kThreads / 32; ++j) v[j] = sm.tmax[j * 32 + lane];
-    uint32_t K = 0u;
-    for (int bit = 31; bit >= (DT == DT_BF16 ? 16 : 0); --bit) {
-      const uint32_t c = K | (1u << bit);
-      uint32_t n = 0;
-#pragma unroll
-      for (int j = 0; j < kThreads / 32; ++j) n += v[j] >= c ? 1u : 0u;
-      if (__reduce_add_sync(kFull, n) >= static_cast<uint32_t>(P.k)) K = c;
+  for (int rd = 0; rd < kRounds; ++rd) {
+    const int sh = 24 - 8 * rd;
+    if (rd == 0 || (mk0 >> (sh + 8)) == prefix) atomicAdd(&sm.u.khist[rd][(mk0 >> sh) & 0xffu], 1u);
+    __syncthreads();
+    if ((tid >> 5) == 0) {
+      int digit;
+      uint32_t before;
+      pick_digit_count(sm.u.khist[rd], need, true, tid & 31, digit, before);
+      if (tid == 0) {
+        sm.b_i32[4] = static_cast<int>((prefix << 8) | static_cast<uint32_t>(digit));
+        sm.b_i32[5] = static_cast<int>(need - before);
+      }
     }
-    if (lane == 0) {
-      sm.b_i32[4] = static_cast<int>(K);
-      sm.ncand = 0;
-      sm.nfull = 0;
-    }
+    __syncthreads();
+    prefix = static_cast<uint32_t>(sm.b_i32[4]);
+    need = static_cast<uint32_t>(sm.b_i32[5]);
+  }
+  const uint32_t K = prefix << (32 - 8 * kRounds);
+  if (tid == 0) {
+    sm.ncand = 0;
+    sm.nfull = 0;
   }
   __syncthreads();
-  const uint32_t K = static_cast<uint32_t>(sm.b_i32[4]);
   if (!any_bad && mk3 != 0u && mk3 >= K) {
     // every tracked vector qualifies and more may: the CTA re-reads all of them below
     const int pos = atomicAdd(&sm.nfull, 1);
