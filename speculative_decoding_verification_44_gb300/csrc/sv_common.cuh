@@ -19,6 +19,7 @@ constexpr int kSmallK = 128;                // streaming top-k path handles 1 <=
 constexpr int kCandCap = 1024;              // streaming top-k path: candidate buffer (entries)
 constexpr int kMaxFull = 32;                // streaming top-k path: threads re-read cooperatively
 constexpr int kStreamUnroll = 4;            // streaming top-k path: 16-byte loads in flight per thread
+constexpr int kRing = 4;                    // streaming top-k path, aligned rows: cp.async ring slots per thread
 constexpr int kListCap = kSmallK;           // kept-list entries stored per row
 constexpr int kMaxGamma = 63;               // largest gamma_max the sampling verifier accepts
 constexpr int kUnroll = 4;                  // 16-byte loads in flight per thread
@@ -122,6 +123,15 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
+// Asynchronous 16-byte global -> shared copy (L1 bypassed, L2 fetches 256 B).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" :: "r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
 // Re-read load (second pass over a row that should still sit in L2).
 __device__ __forceinline__ uint4 ld_reread(const void* p) {
   uint4 r;

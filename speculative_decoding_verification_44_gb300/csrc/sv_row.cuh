@@ -86,8 +86,9 @@ struct __align__(16) Smem {
   union {
     SmemFull f;
     SmemEpi e;
-    uint32_t khist[4][256];          // PATH_STREAM: digit histograms of the per-thread maxima
+    uint4 ring[kRing][kThreads];     // PATH_STREAM pass 1: each thread's cp.async ring of vectors
   } u;
+  uint32_t khist[2][256];            // PATH_STREAM: digit histograms of the per-thread maxima
   uint64_t cand[kCandCap];           // PATH_STREAM: candidates (composites >= the lower bound)
   uint64_t topk[kSmallK];
   uint64_t sorted[kSmallK];          // PATH_STREAM: top-k in descending order
@@ -1550,28 +1551,51 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
   int mv0 = 0, mv1 = 0, mv2 = 0, mv3 = 0;               // their vector indices
   bool bad = false;
 #pragma unroll
-  for (int rd = 0; rd < 4; ++rd) sm.u.khist[rd][tid] = 0u;  // visible after the barrier below
-  for (int it = 0; it < iters; ++it) {
+  for (int h = 0; h < 2; ++h) sm.khist[h][tid] = 0u;   // visible after the barrier below
+  // One vector's contribution: its maximum, and an insertion among the four tracked.
+  const auto take = [&](const uint4& r, int c, int v) {
+    bool vb;
+    const uint32_t vk = fkey(vec_max<DT>(r, c, vb));
+    bad |= vb;
+    if (vk > mk3) {                                  // insert, keeping earlier vectors first on ties
+      const bool g0 = vk > mk0, g1 = vk > mk1, g2 = vk > mk2;
+      mk3 = g2 ? mk2 : vk;                 mv3 = g2 ? mv2 : v;
+      mk2 = g2 ? (g1 ? mk1 : vk) : mk2;   mv2 = g2 ? (g1 ? mv1 : v) : mv2;
+      mk1 = g1 ? (g0 ? mk0 : vk) : mk1;   mv1 = g1 ? (g0 ? mv0 : v) : mv1;
+      mk0 = g0 ? vk : mk0;                 mv0 = g0 ? v : mv0;
+    }
+  };
+  if (row.aligned) {
+    // Aligned rows: thread t takes vectors t, t + kThreads, ... through a ring of
+    // kRing shared-memory slots filled by cp.async, kRing - 1 copies in flight.
+    const int nk = (row.nvec - tid + kThreads - 1) / kThreads;
+    const char* src = row.base + static_cast<size_t>(tid) * 16;
+    constexpr size_t kStride = static_cast<size_t>(kThreads) * 16;
+#pragma unroll
+    for (int s = 0; s < kRing - 1; ++s) {
+      if (s < nk) cp_async16(&sm.u.ring[s][tid], src + s * kStride);
+      cp_async_commit();
+    }
+    int slot = 0, fill = kRing - 1;
+    for (int k = 0; k < nk; ++k) {
+      if (k + kRing - 1 < nk) cp_async16(&sm.u.ring[fill][tid], src + (k + kRing - 1) * kStride);
+      cp_async_commit();
+      cp_async_wait<kRing - 1>();                    // the copy of vector k has landed
+      const uint4 r = sm.u.ring[slot][tid];
+      slot = slot + 1 == kRing ? 0 : slot + 1;
+      fill = fill + 1 == kRing ? 0 : fill + 1;
+      take(r, Elem<DT>::kPer, tid + k * kThreads);
+    }
+    cp_async_wait<0>();
+  }
+  for (int it = 0; !row.aligned && it < iters; ++it) {
     uint4 r[kStreamUnroll];
     int cnt[kStreamUnroll];
 #pragma unroll
     for (int u = 0; u < kStreamUnroll; ++u) cnt[u] = load_vec<DT, true>(row, it * step + u * kThreads + tid, r[u]);
 #pragma unroll
-    for (int u = 0; u < kStreamUnroll; ++u) {
-      if (cnt[u]) {
-        bool vb;
-        const uint32_t vk = fkey(vec_max<DT>(r[u], cnt[u], vb));
-        bad |= vb;
-        if (vk > mk3) {                                  // insert, keeping earlier vectors first on ties
-          const int v = it * step + u * kThreads + tid;
-          const bool g0 = vk > mk0, g1 = vk > mk1, g2 = vk > mk2;
-          mk3 = g2 ? mk2 : vk;                 mv3 = g2 ? mv2 : v;
-          mk2 = g2 ? (g1 ? mk1 : vk) : mk2;   mv2 = g2 ? (g1 ? mv1 : v) : mv2;
-          mk1 = g1 ? (g0 ? mk0 : vk) : mk1;   mv1 = g1 ? (g0 ? mv0 : v) : mv1;
-          mk0 = g0 ? vk : mk0;                 mv0 = g0 ? v : mv0;
-        }
-      }
-    }
+    for (int u = 0; u < kStreamUnroll; ++u)
+      if (cnt[u]) take(r[u], cnt[u], it * step + u * kThreads + tid);
   }
   const int any_bad = __syncthreads_or(bad ? 1 : 0);
   // K = the k-th largest of the kThreads maxima: MSB-first radix select, one
@@ -1582,12 +1606,13 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
 #pragma unroll
   for (int rd = 0; rd < kRounds; ++rd) {
     const int sh = 24 - 8 * rd;
-    if (rd == 0 || (mk0 >> (sh + 8)) == prefix) atomicAdd(&sm.u.khist[rd][(mk0 >> sh) & 0xffu], 1u);
+    uint32_t* hist = sm.khist[rd & 1];
+    if (rd == 0 || (mk0 >> (sh + 8)) == prefix) atomicAdd(&hist[(mk0 >> sh) & 0xffu], 1u);
     __syncthreads();
     if ((tid >> 5) == 0) {
       int digit;
       uint32_t before;
-      pick_digit_count(sm.u.khist[rd], need, true, tid & 31, digit, before);
+      pick_digit_count(hist, need, true, tid & 31, digit, before);
       if (tid == 0) {
         sm.b_i32[4] = static_cast<int>((prefix << 8) | static_cast<uint32_t>(digit));
         sm.b_i32[5] = static_cast<int>(need - before);
@@ -1596,6 +1621,7 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
     __syncthreads();
     prefix = static_cast<uint32_t>(sm.b_i32[4]);
     need = static_cast<uint32_t>(sm.b_i32[5]);
+    if (rd + 2 < kRounds) hist[tid] = 0u;           // reused two rounds later, after a barrier
   }
   const uint32_t K = prefix << (32 - 8 * kRounds);
   if (tid == 0) {
