@@ -1648,6 +1648,10 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
     // cooperative re-read: one vector per job, jobs spread over the whole CTA
     const int per = (row.nvec + kThreads - 1) / kThreads;       // vectors per thread
     const bool all = nfull > kMaxFull;                           // too many: re-read the whole row
+    if (all) {                       // the whole row is re-read: drop what the tracked vectors added
+      if (tid == 0) sm.ncand = 0;
+      __syncthreads();
+    }
     const int jobs = all ? row.nvec : nfull * per;
     for (int job = tid; job < jobs; job += kThreads) {
       const int v = all ? job : sm.full[job / per] + (job % per) * kThreads;

@@ -102,6 +102,37 @@ def test_full_row_top_p_cut(dtype, kind, T, top_p, V):
     assert checked >= rows // 2
 
 
+def test_stream_rows_where_many_threads_pass_the_threshold():
+    """Streaming top-k rows built so that more than 32 of a CTA's threads have all
+    four of their best vectors at or above the candidate threshold: the row is
+    then re-read whole, and the candidates collected before must not be counted
+    twice.  (V = 8192 bf16 is 1024 vectors of eight: four per thread when each of
+    256 threads takes every 256th vector.)"""
+    import speculative_decoding_verification_44_gb300 as sv
+    V = 8192
+    z = torch.full((2, V), -10.0)
+    for t in range(20):                       # one very large logit in the thread's first vector
+        z[:, 8 * t] = 10.0
+    for t in range(20, 60):                   # all four of the thread's vectors hold 5.0
+        for j in range(4):
+            z[:, 8 * (t + 256 * j) + 3] = 5.0
+    for t in range(60, 70):                   # one moderate logit
+        z[:, 8 * t + 1] = 1.0
+    z[1, 5000:5100] = 4.0                     # second row: more ties below the top block
+    zb = z.to(torch.bfloat16)
+    for params in ((1.0, 64, 1.0), (0.8, 64, 0.9), (1.0, 100, 1.0), (2.0, 128, 0.999)):
+        p = sv.SamplingParams(*params)
+        probs, status = sv.transform_probs(zb.cuda(), p)
+        detail = oracle.transform_rows_detail(to_f64(zb), *params_tuple(p))
+        assert (status.cpu() == 0).all()
+        got = probs.cpu().double().numpy()
+        for r, rd in enumerate(detail):
+            assert np.isfinite(got[r]).all(), (params, r)
+            if rd.ambiguous_mass > TOL_PROB:
+                continue
+            np.testing.assert_allclose(got[r], rd.probs, atol=TOL_PROB, rtol=0, err_msg=f"{params} row {r}")
+
+
 def test_transform_textbook_softmax_third_opinion():
     import speculative_decoding_verification_44_gb300 as sv
     z = torch.randn(8, 32000, generator=torch.Generator().manual_seed(5)) * 3
