@@ -48,6 +48,18 @@ Readings where the pages are silent (each is named where it is used):
       stops at the first draft that differs from the target's argmax -- the
       sequential verifier of [wrblog §6], which never looks past the first
       rejection.  "The rows the sequence uses" in R10 are then the rows read.
+* R13 per-sequence sampling rules [wrblog §15]: requests in one batch keep their
+      own temperature / top-k / top-p, so each sequence may carry its own target
+      and draft rules.  A rule outside its domain (temperature not finite or
+      <= 0, top_k < 0, top_p outside (0, 1]) fails that sequence only, checked
+      after the uniforms; a one-hot sequence's draft rule is not used, so not
+      checked.
+* R14 end-of-sequence commit [wrblog §14.3]: no token is committed after the
+      end-of-sequence token.  The emitted block (accepted drafts, then the
+      replacement or bonus token) is cut just after its first EOS; when an
+      accepted draft is the EOS, the committed drafts end there and no
+      replacement or bonus token follows.  The scan and the draw are unchanged
+      (the same uniforms decide them); only the commit is cut.
 * R12 lenience beta in (0, 1] [magicnet §8]: the page shrinks the draft
       distribution to beta q and then compares it with the target; here beta q
       stands in for q throughout -- acceptance min(1, p / (beta q)) and, on a
@@ -76,7 +88,7 @@ Sources:
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import numpy as np
 
@@ -88,9 +100,11 @@ SEQ_BAD_TOKEN = 2       # a draft token outside [0, V)
 SEQ_BAD_UNIFORM = 3     # a uniform outside [0, 1) or NaN
 SEQ_NONFINITE = 4       # NaN or +inf logit in a row the sequence uses
 SEQ_EMPTY_SUPPORT = 5   # a row whose logits are all -inf
+SEQ_BAD_PARAMS = 6      # a sampling rule the sequence uses is outside its domain (R13)
 SEQ_ERROR_MASK = 0xFF
 SEQ_FLAG_ZERO_Q = 0x100  # an evaluated draft token had q(d) == 0 (R6)
 SEQ_FLAG_Z_ZERO = 0x200  # residual mass was 0 after a rejection (R7)
+SEQ_FLAG_EOS = 0x400     # the committed block ends at the end-of-sequence token (R14)
 
 
 # --------------------------------------------------------------------------
@@ -260,6 +274,7 @@ class SeqResult:
     sample_hi: float = np.nan
     sample_cdf: np.ndarray | None = field(default=None, repr=False)  # normalised CDF drawn from
     rows_read: int = -1             # early-exit greedy: target rows read (R11)
+    num_emitted: int = -1           # tokens committed: num_accepted + 1, or fewer after an EOS cut (R14)
 
 
 def _error_result(status: int, gamma_max: int) -> SeqResult:
@@ -269,6 +284,12 @@ def _error_result(status: int, gamma_max: int) -> SeqResult:
 
 def _valid_uniform(u: float) -> bool:
     return bool(0.0 <= u < 1.0)
+
+
+def valid_params(params: tuple[float, int, float]) -> bool:
+    """The domain of a sampling rule (R13): temperature finite and > 0, top_k >= 0, top_p in (0, 1]."""
+    T, k, p = params
+    return bool(np.isfinite(T) and T > 0.0 and k >= 0 and 0.0 < p <= 1.0)
 
 
 def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarray,
@@ -293,6 +314,8 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
         return _error_result(SEQ_BAD_TOKEN, gamma_max)
     if not all(_valid_uniform(float(u)) for u in u_accept[:gamma_b]) or not _valid_uniform(float(u_sample)):
         return _error_result(SEQ_BAD_UNIFORM, gamma_max)
+    if not valid_params(target_params) or (not one_hot and not valid_params(draft_params)):    # R13
+        return _error_result(SEQ_BAD_PARAMS, gamma_max)
 
     # Step 1: p_1..p_{gamma+1} and q_1..q_gamma, each with its own transform [wrblog §7.2].
     p_rows, q_rows = [], []
@@ -350,11 +373,30 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
     sample_amb = np.unique(np.concatenate([r.ambiguous for r in sample_rows]))
     res = SeqResult(out, n_acc, status, a, residual_Z, accept_margin, top_p_margin,
                     draft_ambiguous=draft_amb, sample_ambiguous=sample_amb,
-                    sample_u=float(u_sample), sample_lo=lo, sample_hi=hi)
+                    sample_u=float(u_sample), sample_lo=lo, sample_hi=hi, num_emitted=n_acc + 1)
     if keep_cdf:
         C = np.cumsum(w)
         res.sample_cdf = C / C[-1]
     return res
+
+
+def commit_at_eos(res: SeqResult, eos_token: int) -> SeqResult:
+    """Cut a sequence's committed block just after its first end-of-sequence token
+    [wrblog §14.3] (R14).  eos_token < 0 and failed sequences are left unchanged."""
+    if eos_token < 0 or res.num_accepted < 0:
+        return res
+    block = res.tokens[: res.num_accepted + 1]
+    hits = np.flatnonzero(block == eos_token)
+    if hits.size == 0:
+        return res
+    t = int(hits[0])
+    tokens = res.tokens.copy()
+    tokens[t + 1:] = -1
+    cut = replace(res, tokens=tokens, status=res.status | SEQ_FLAG_EOS)
+    if t < res.num_accepted:        # an accepted draft is the EOS: no replacement / bonus token
+        cut.num_accepted = t + 1
+        cut.num_emitted = t + 1
+    return cut
 
 
 def greedy_row(z: np.ndarray) -> tuple[int, int]:
@@ -450,12 +492,16 @@ def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarr
                   target_params: tuple[float, int, float], draft_params: tuple[float, int, float],
                   gamma_per_seq: np.ndarray | None = None, one_hot: np.ndarray | None = None,
                   seqs: list[int] | None = None, keep_cdf: bool = False,
-                  lenience: float = 1.0) -> BatchResult:
+                  lenience: float = 1.0, params_per_seq: list | None = None,
+                  eos_token: int = -1) -> BatchResult:
     """Batched sampling verification, one sequence at a time.
 
     target (B, gamma_max+1, V), draft (B, gamma_max, V) or None (all one-hot),
     tokens / u_accept (B, gamma_max), u_sample (B,), all float64 / int.
     ``seqs`` restricts the work to a subset of sequence indices.
+    ``params_per_seq``: per sequence b, the pair (target rule, draft rule)
+    replacing target_params / draft_params (R13).  ``eos_token`` >= 0 cuts
+    each committed block after its first end-of-sequence token (R14).
     """
     B, G1, _ = target.shape
     gamma_max = G1 - 1
@@ -464,9 +510,11 @@ def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarr
     for b in seqs:
         g = gamma_max if gamma_per_seq is None else int(gamma_per_seq[b])
         oh = draft is None or (one_hot is not None and bool(one_hot[b]))
-        out.append(verify_sample_sequence(target[b], None if oh else draft[b], tokens[b],
-                                          u_accept[b], float(u_sample[b]), target_params,
-                                          draft_params, g, gamma_max, oh, keep_cdf, lenience))
+        tp, dp = (target_params, draft_params) if params_per_seq is None else params_per_seq[b]
+        res = verify_sample_sequence(target[b], None if oh else draft[b], tokens[b],
+                                     u_accept[b], float(u_sample[b]), tp, dp, g, gamma_max, oh,
+                                     keep_cdf, lenience)
+        out.append(commit_at_eos(res, eos_token))
     return _collect(out)
 
 
