@@ -104,12 +104,17 @@ enum {
     SPEC_SEQ_BAD_UNIFORM = 3,     /* a used uniform outside [0, 1) or NaN             */
     SPEC_SEQ_NONFINITE = 4,       /* NaN or +inf logit in a row the sequence uses     */
     SPEC_SEQ_EMPTY_SUPPORT = 5,   /* a used row whose logits are all -inf             */
+    SPEC_SEQ_BAD_PARAMS = 6,      /* spec_verify_sample_ex: a per-sequence sampling
+                                     rule the sequence uses is outside its domain     */
     SPEC_SEQ_ERROR_MASK = 0xFF,
     SPEC_SEQ_FLAG_ZERO_Q = 0x100, /* an evaluated draft token had q(d) == 0           */
-    SPEC_SEQ_FLAG_Z_ZERO = 0x200  /* residual mass was 0 after a rejection            */
+    SPEC_SEQ_FLAG_Z_ZERO = 0x200, /* residual mass was 0 after a rejection            */
+    SPEC_SEQ_FLAG_EOS = 0x400     /* spec_verify_sample_ex: the committed block ends
+                                     with the end-of-sequence token                   */
 };
 /* Checks run in this order and the first failure is reported: length, draft
- * tokens, uniforms, then rows i = 0..gamma_b (target row i, then draft row i). */
+ * tokens, uniforms, per-sequence rules (spec_verify_sample_ex), then rows
+ * i = 0..gamma_b (target row i, then draft row i). */
 
 typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
 
@@ -200,6 +205,63 @@ SPEC_API spec_status_t spec_verify_sample_lenient(const void* target_logits, con
                                          int32_t* out_tokens, int32_t* out_num_accepted,
                                          float* out_accept_prob, float* out_residual_z,
                                          int32_t* out_status, void* stream);
+
+/* Options of spec_verify_sample_ex.  {1.0f, -1, NULL, NULL} is
+ * spec_verify_sample exactly.
+ *
+ * lenience           (0, 1]: as for spec_verify_sample_lenient [magicnet §8].
+ * eos_token          -1, or an end-of-sequence token in [0, vocab): no token is
+ *                    committed after it [wrblog §14.3].  When an accepted draft
+ *                    d_t is the EOS, the sequence commits d_1..d_t only (no
+ *                    replacement or bonus token; out_residual_z = -1);
+ *                    SPEC_SEQ_FLAG_EOS marks a committed block that ends with
+ *                    the EOS (also when the drawn token is the EOS).  The
+ *                    acceptance scan and the draw are unchanged.
+ * target_params_seq  [batch] DEVICE array of per-sequence target rules, or NULL
+ * draft_params_seq   [batch] DEVICE array of per-sequence draft rules, or NULL:
+ *                    requests batched together keep their own temperature,
+ *                    top-k and top-p [wrblog §15].  When given, that side's
+ *                    scalar rule is not used for sampling (it must still be
+ *                    valid: it sizes nothing and is checked like the others).
+ *                    A per-sequence rule outside its domain fails only its
+ *                    sequence (SPEC_SEQ_BAD_PARAMS); a one-hot sequence's draft
+ *                    rule is not used and not checked.  With per-sequence rules
+ *                    the launch reserves the full-row path's extra shared
+ *                    memory and the draw kernel always runs (its CTAs exit at
+ *                    once for sequences with kept-list targets). */
+typedef struct {
+    float lenience;
+    int32_t eos_token;
+    const spec_sampling_params_t* target_params_seq;
+    const spec_sampling_params_t* draft_params_seq;
+} spec_verify_options_t;
+
+/* Bytes of workspace spec_verify_sample_ex needs with these options (per-
+ * sequence rules reserve room for both row paths).  options may be NULL. */
+SPEC_API spec_status_t spec_verify_workspace_size_ex(int32_t batch, int32_t gamma_max, int32_t vocab,
+                                            spec_sampling_params_t target_params,
+                                            spec_sampling_params_t draft_params,
+                                            const spec_verify_options_t* options, size_t* bytes);
+
+/* spec_verify_sample with options (host pointer; NULL = the defaults):
+ * lenience, the end-of-sequence commit and per-sequence sampling rules.
+ * out_num_emitted [batch] int32, or NULL: tokens committed -- num_accepted + 1,
+ * num_accepted when the block ends at an accepted EOS draft, -1 on error.
+ * The workspace is spec_verify_workspace_size_ex() bytes.  An eos_token
+ * outside [-1, vocab) or a lenience outside (0, 1] returns
+ * SPEC_ERR_INVALID_ARG; everything else is as for spec_verify_sample. */
+SPEC_API spec_status_t spec_verify_sample_ex(const void* target_logits, const void* draft_logits,
+                                    spec_dtype_t dtype, const int32_t* draft_tokens,
+                                    const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                    const float* u_accept, const float* u_sample,
+                                    spec_sampling_params_t target_params,
+                                    spec_sampling_params_t draft_params,
+                                    const spec_verify_options_t* options,
+                                    int32_t batch, int32_t gamma_max, int32_t vocab,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* out_tokens, int32_t* out_num_accepted,
+                                    float* out_accept_prob, float* out_residual_z,
+                                    int32_t* out_status, int32_t* out_num_emitted, void* stream);
 
 /* Bytes of workspace spec_verify_greedy needs (same zero-fill rule). */
 SPEC_API spec_status_t spec_greedy_workspace_size(int32_t batch, int32_t gamma_max, size_t* bytes);

@@ -24,9 +24,11 @@ SPEC_SEQ_BAD_TOKEN = 2
 SPEC_SEQ_BAD_UNIFORM = 3
 SPEC_SEQ_NONFINITE = 4
 SPEC_SEQ_EMPTY_SUPPORT = 5
+SPEC_SEQ_BAD_PARAMS = 6
 SPEC_SEQ_ERROR_MASK = 0xFF
 SPEC_SEQ_FLAG_ZERO_Q = 0x100
 SPEC_SEQ_FLAG_Z_ZERO = 0x200
+SPEC_SEQ_FLAG_EOS = 0x400
 
 SPEC_BF16 = 0
 SPEC_F32 = 1
@@ -34,11 +36,17 @@ SPEC_F32 = 1
 # Every symbol include/spec_verify.h declares.
 EXPORTED = ("spec_verify_workspace_size", "spec_verify_sample", "spec_greedy_workspace_size",
             "spec_verify_greedy", "spec_transform_probs", "spec_status_string",
-            "spec_verify_sample_noalloc", "spec_verify_greedy_early", "spec_verify_sample_lenient")
+            "spec_verify_sample_noalloc", "spec_verify_greedy_early", "spec_verify_sample_lenient",
+            "spec_verify_workspace_size_ex", "spec_verify_sample_ex")
 
 
 class spec_sampling_params_t(ctypes.Structure):
     _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
+
+class spec_verify_options_t(ctypes.Structure):
+    _fields_ = [("lenience", ctypes.c_float), ("eos_token", ctypes.c_int32),
+                ("target_params_seq", ctypes.c_void_p), ("draft_params_seq", ctypes.c_void_p)]
 
 
 class SpecError(RuntimeError):
@@ -72,6 +80,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_sample.restype = ctypes.c_int
     lib.spec_verify_sample.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, i32, i32, i32,
                                        vp, sz, vp, vp, vp, vp, vp, vp]
+    O = ctypes.POINTER(spec_verify_options_t)
+    lib.spec_verify_workspace_size_ex.restype = ctypes.c_int
+    lib.spec_verify_workspace_size_ex.argtypes = [i32, i32, i32, P, P, O, ctypes.POINTER(sz)]
+    lib.spec_verify_sample_ex.restype = ctypes.c_int
+    lib.spec_verify_sample_ex.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, O,
+                                          i32, i32, i32, vp, sz, vp, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_sample_lenient.restype = ctypes.c_int
     lib.spec_verify_sample_lenient.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, ctypes.c_float,
                                                i32, i32, i32, vp, sz, vp, vp, vp, vp, vp, vp]
@@ -107,6 +121,16 @@ def spec_verify_workspace_size(batch: int, gamma_max: int, vocab: int, target_pa
     return out.value
 
 
+def spec_verify_workspace_size_ex(batch: int, gamma_max: int, vocab: int, target_params, draft_params,
+                                  options) -> int:
+    out = sz(0)
+    check("spec_verify_workspace_size_ex",
+          load().spec_verify_workspace_size_ex(batch, gamma_max, vocab, target_params, draft_params,
+                                               ctypes.byref(options) if options is not None else None,
+                                               ctypes.byref(out)))
+    return out.value
+
+
 def spec_greedy_workspace_size(batch: int, gamma_max: int) -> int:
     out = sz(0)
     check("spec_greedy_workspace_size", load().spec_greedy_workspace_size(batch, gamma_max, ctypes.byref(out)))
@@ -115,6 +139,10 @@ def spec_greedy_workspace_size(batch: int, gamma_max: int) -> int:
 
 def spec_verify_sample(*args) -> int:
     return load().spec_verify_sample(*args)
+
+
+def spec_verify_sample_ex(*args) -> int:
+    return load().spec_verify_sample_ex(*args)
 
 
 def spec_verify_sample_lenient(*args) -> int:

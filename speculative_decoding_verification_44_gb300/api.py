@@ -6,6 +6,7 @@ device, contiguous, with the layouts include/spec_verify.h documents.
 """
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass
 
 import torch
@@ -31,6 +32,7 @@ class VerifyOutput:
     status: torch.Tensor          # [B] int32 SPEC_SEQ_* codes
     accept_prob: torch.Tensor | None = None   # [B, gamma_max] float32
     residual_z: torch.Tensor | None = None    # [B] float32
+    num_emitted: torch.Tensor | None = None   # [B] int32 tokens committed (spec_verify_sample_ex)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -57,8 +59,20 @@ def _stream(stream: torch.cuda.Stream | None) -> int:
 
 
 def workspace_size(batch: int, gamma_max: int, vocab: int, target: SamplingParams,
-                   draft: SamplingParams) -> int:
-    return _lib.spec_verify_workspace_size(batch, gamma_max, vocab, target.c(), draft.c())
+                   draft: SamplingParams, per_sequence: bool = False) -> int:
+    """Workspace bytes; ``per_sequence``: sized for per-sequence rules (spec_verify_workspace_size_ex)."""
+    if not per_sequence:
+        return _lib.spec_verify_workspace_size(batch, gamma_max, vocab, target.c(), draft.c())
+    opt = _lib.spec_verify_options_t(1.0, -1, 1, 1)        # non-null per-sequence pointers: both sides
+    return _lib.spec_verify_workspace_size_ex(batch, gamma_max, vocab, target.c(), draft.c(), opt)
+
+
+def rules_tensor(rules, device) -> torch.Tensor:
+    """Per-sequence sampling rules as the [B] spec_sampling_params_t array the C ABI reads
+    (int32 [B, 3]: temperature bits, top_k, top_p bits) on ``device``."""
+    t = torch.tensor([[r.temperature, 0.0, r.top_p] for r in rules], dtype=torch.float32).view(torch.int32)
+    t[:, 1] = torch.tensor([int(r.top_k) for r in rules], dtype=torch.int32)
+    return t.contiguous().to(device)
 
 
 def greedy_workspace_size(batch: int, gamma_max: int) -> int:
@@ -87,30 +101,48 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
                   draft_is_onehot: torch.Tensor | None = None,
                   workspace: torch.Tensor | None = None, out: VerifyOutput | None = None,
                   stream: torch.cuda.Stream | None = None,
-                  lenience: float | None = None) -> VerifyOutput:
-    """spec_verify_sample on torch tensors (spec_verify_sample_lenient when
-    ``lenience`` is given).
+                  lenience: float | None = None, eos_token: int | None = None,
+                  target_rules=None, draft_rules=None) -> VerifyOutput:
+    """spec_verify_sample on torch tensors; spec_verify_sample_lenient when only
+    ``lenience`` is given; spec_verify_sample_ex when ``eos_token`` or per-sequence
+    rules are given.
 
     target_logits [B, G+1, V] and draft_logits [B, G, V] (or None: all one-hot) of
     bfloat16 / float32; draft_tokens [B, G] int32; u_accept [B, G] and u_sample [B]
-    float32; gamma_per_seq [B] int32; draft_is_onehot [B] uint8; lenience in (0, 1].
+    float32; gamma_per_seq [B] int32; draft_is_onehot [B] uint8; lenience in (0, 1];
+    target_rules / draft_rules: per-sequence rules, a list of SamplingParams or a
+    tensor from rules_tensor() (the scalar ``target`` / ``draft`` then only size the call).
     """
     B, G1, V = target_logits.shape
     G = G1 - 1
     if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
         raise TypeError("target and draft logits must share a dtype")
     dev = target_logits.device
+    ex = eos_token is not None or target_rules is not None or draft_rules is not None
+    if isinstance(target_rules, (list, tuple)):
+        target_rules = rules_tensor(target_rules, dev)
+    if isinstance(draft_rules, (list, tuple)):
+        draft_rules = rules_tensor(draft_rules, dev)
     if workspace is None:
-        workspace = new_workspace(workspace_size(B, G, V, target, draft), dev)
+        workspace = new_workspace(workspace_size(B, G, V, target, draft,
+                                                 per_sequence=target_rules is not None or draft_rules is not None), dev)
     if out is None:
         out = alloc_outputs(B, G, dev)
+    if ex and out.num_emitted is None:
+        out.num_emitted = torch.empty(B, dtype=torch.int32, device=dev)
     head = (_ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
             _ptr(gamma_per_seq), _ptr(draft_is_onehot), _ptr(u_accept), _ptr(u_sample),
             target.c(), draft.c())
     tail = (B, G, V, _ptr(workspace), workspace.numel(),
             _ptr(out.tokens), _ptr(out.num_accepted), _ptr(out.accept_prob), _ptr(out.residual_z),
             _ptr(out.status), _stream(stream))
-    if lenience is None:
+    if ex:
+        opt = _lib.spec_verify_options_t(1.0 if lenience is None else float(lenience),
+                                         -1 if eos_token is None else int(eos_token),
+                                         _ptr(target_rules), _ptr(draft_rules))
+        _lib.check("spec_verify_sample_ex",
+                   _lib.spec_verify_sample_ex(*head, ctypes.byref(opt), *tail[:-1], _ptr(out.num_emitted), tail[-1]))
+    elif lenience is None:
         _lib.check("spec_verify_sample", _lib.spec_verify_sample(*head, *tail))
     else:
         _lib.check("spec_verify_sample_lenient",

@@ -22,6 +22,30 @@
 
 namespace sv {
 
+// A sampling rule's domain [wrblog §2.3, §7.2-§7.3]: temperature finite and > 0,
+// top_k >= 0, top_p in (0, 1].
+__host__ __device__ inline bool rule_ok(const spec_sampling_params_t& p) {
+  return isfinite(p.temperature) && p.temperature > 0.0f && p.top_k >= 0 && p.top_p > 0.0f && p.top_p <= 1.0f;
+}
+
+// A rule prepared for the row kernels (the same arithmetic on host and device).
+__host__ __device__ inline RowParams row_params_of(const spec_sampling_params_t& p, int V) {
+  RowParams r;
+  r.T = p.temperature;
+  const double cT = 1.4426950408889634 / static_cast<double>(p.temperature);  // log2(e) / T
+  r.cT = static_cast<float>(cT);
+  r.cT_lo = static_cast<float>(cT - static_cast<double>(r.cT));
+  r.invT = 1.0 / static_cast<double>(p.temperature);
+  r.k = (p.top_k >= V) ? 0 : p.top_k;
+  r.top_p = p.top_p;
+  r.path = (r.k >= 1 && r.k <= kSmallK) ? PATH_STREAM : PATH_FULL;
+  int bits = 0;
+  for (uint32_t v = static_cast<uint32_t>(V); v; v >>= 1) ++bits;
+  const int sh = 62 - bits;
+  r.fixed_shift = sh < 24 ? 24 : (sh > 40 ? 40 : sh);
+  return r;
+}
+
 struct SampleArgs {
   const char* tgt;
   const char* dft;
@@ -31,7 +55,10 @@ struct SampleArgs {
   const float* u_acc;
   const float* u_samp;
   RowParams tp, dp;
+  const spec_sampling_params_t* tps;   // [B] per-sequence target rules (device), or null
+  const spec_sampling_params_t* dps;   // [B] per-sequence draft rules (device), or null
   float beta;           // lenience: beta q stands in for q (1 = the lossless rule)
+  int eos;              // end-of-sequence token (-1: none): nothing is committed after it
   int B, G, V;
   int aligned;
   size_t row_bytes;
@@ -43,6 +70,7 @@ struct SampleArgs {
   float* out_aprob;
   float* out_Z;
   int32_t* out_status;
+  int32_t* out_nemit;   // tokens committed, or null
   // full-row draws deferred to draw_kernel (target rows on PATH_FULL)
   int defer;
   int chunk_vecs;       // vectors per draw chunk
@@ -82,6 +110,7 @@ __device__ void write_error(const SampleArgs& a, int b, int status) {
     for (int t = threadIdx.x; t < a.G; t += blockDim.x) a.out_aprob[static_cast<size_t>(b) * a.G + t] = -1.0f;
   if (threadIdx.x == 0) {
     a.out_nacc[b] = -1;
+    if (a.out_nemit) a.out_nemit[b] = -1;
     if (a.out_Z) a.out_Z[b] = -1.0f;
     if (a.out_status) a.out_status[b] = status;
     if (a.defer) a.drec[b].j = -1;
@@ -163,7 +192,7 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
     } else {
       const Row drow = seq_row<DT>(a, b, r, true);
       q = full_prob(load_elem<DT>(drow.base, te.token), static_cast<uint32_t>(te.token), cut_test(ds.cut), ds.m,
-                    a.dp.cT, static_cast<float>(1.0 / ds.W));
+                    ds.cT, static_cast<float>(1.0 / ds.W));
     }
     const float bq = a.beta * q;                      // beta q exactly, as hi + lo
     const df d = df_add(pw, {-bq, -fmaf(a.beta, q, -bq)});
@@ -411,8 +440,8 @@ __device__ ScanCtx make_scan(const SampleArgs& a, int b, int r, int mode, bool o
   c.mt = ts.m;
   c.ctd = cut_test(ds.cut);
   c.md = ds.m;
-  c.cTt = a.tp.cT;
-  c.cTd = a.dp.cT;
+  c.cTt = ts.cT;
+  c.cTd = ds.cT;
   c.invWt = static_cast<float>(1.0 / ts.W);
   c.invWd = static_cast<float>(1.0 / ds.W);
   c.dj = dj;
@@ -433,7 +462,7 @@ __device__ ScanCtx make_scan(const SampleArgs& a, int b, int r, int mode, bool o
 }
 
 // Sequence epilogue, run by the CTA that analysed the sequence's last row.
-template <int DT>
+template <int DT, bool EX>
 __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb, bool onehot, Smem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slots = 2 * a.G + 1;
@@ -458,6 +487,12 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     E.uacc[t] = a.u_acc[tokb + t];
   }
   if (tid == kThreads - 1) sm.b_f32[0] = a.u_samp[b];
+  if (EX && tid == kThreads - 2) {              // per-sequence rules the sequence uses
+    bool ok = true;
+    if (a.tps) ok = rule_ok(a.tps[b]);
+    if (a.dps && !onehot) ok = ok && rule_ok(a.dps[b]);
+    sm.b_i32[8] = ok ? 1 : 0;
+  }
   __syncthreads();
   // status, in the documented order: tokens, uniforms, rows (lane-parallel, warp 0)
   if (warp == 0) {
@@ -473,6 +508,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     int status = SEQ_OK;
     if (__any_sync(kFull, bad_tok)) status = SEQ_BAD_TOKEN;
     else if (__any_sync(kFull, bad_u)) status = SEQ_BAD_UNIFORM;
+    else if (EX && !sm.b_i32[8]) status = SEQ_BAD_PARAMS;
     else {
       // rows in order: target 0, draft 0, target 1, draft 1, ..., target gb
       const int norder = 2 * gb + 1;
@@ -521,10 +557,19 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
         }
       }
     }
+    // end-of-sequence commit [wrblog §14.3]: the first accepted draft equal to eos ends the block
+    int cut = -1;
+    if (EX && status == SEQ_OK && a.eos >= 0) {
+      for (int base = 0; base < j && cut < 0; base += 32) {
+        const unsigned m = __ballot_sync(kFull, base + lane < j && E.dtok[base + lane] == a.eos);
+        if (m) cut = base + __ffs(m) - 1;
+      }
+    }
     if (lane == 0) {
       sm.b_i32[0] = status;
       sm.b_i32[1] = j;
       sm.b_i32[2] = flags;
+      sm.b_i32[9] = cut;
     }
   }
   __syncthreads();
@@ -534,14 +579,29 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   }
   const int j = sm.b_i32[1];
   int flags = sm.b_i32[2];
+  const int cut = EX ? sm.b_i32[9] : -1;
   __syncthreads();
+  const size_t ob = static_cast<size_t>(b) * (a.G + 1);
+  if (EX && cut >= 0) {
+    // an accepted draft is the end-of-sequence token: the committed block ends
+    // there, with no replacement or bonus token (so no draw)
+    for (int t = tid; t <= a.G; t += kThreads) a.out_tokens[ob + t] = t <= cut ? E.dtok[t] : -1;
+    if (tid == 0) {
+      a.out_nacc[b] = cut + 1;
+      if (a.out_nemit) a.out_nemit[b] = cut + 1;
+      if (a.out_Z) a.out_Z[b] = -1.0f;
+      if (a.out_status) a.out_status[b] = flags | SEQ_FLAG_EOS;
+      if (a.defer) a.drec[b].j = -1;
+    }
+    return;
+  }
 
   // 3. residual draw at the rejected position, or the bonus draw [wrblog §5, §6]
   const bool residual = j < gb;
   const int r = j;   // == gb when every draft was accepted
   const RowStat ts = E.rs[r];
   RowStat ds;
-  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0;
+  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f;
   if (residual && !onehot) ds = E.rs[a.G + 1 + r];
   const int dj = residual ? E.dtok[j] : -1;
   const float uf = sm.b_f32[0];
@@ -550,6 +610,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   bool deferred = false;
   if (ts.path == PATH_STREAM) {
     tok = list_draw<DT>(a, b, r, residual, onehot, dj, ds, uf, Z_resid, flags, sm);
+    if (a.defer && tid == 0) a.drec[b].j = -1;   // per-sequence rules: nothing for draw_kernel
   } else if (a.defer) {
     // a full-row draw: draw_kernel does it, chunk-parallel, and writes the drawn
     // token, residual_Z and status
@@ -569,7 +630,6 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   }
 
   // 4. outputs: accepted drafts, the drawn token, then -1
-  const size_t ob = static_cast<size_t>(b) * (a.G + 1);
   for (int t = tid; t <= a.G; t += kThreads) {
     int v = -1;
     if (t < j) v = E.dtok[t];
@@ -578,14 +638,18 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   }
   if (tid == 0) {
     a.out_nacc[b] = j;
+    if (EX && a.out_nemit) a.out_nemit[b] = j + 1;
     if (!deferred) {
       if (a.out_Z) a.out_Z[b] = residual ? static_cast<float>(Z_resid) : -1.0f;
+      if (EX && a.eos >= 0 && tok == a.eos) flags |= SEQ_FLAG_EOS;
       if (a.out_status) a.out_status[b] = flags;
     }
   }
 }
 
-template <int DT>
+// EX: the spec_verify_sample_ex features (per-sequence rules, end-of-sequence
+// commit, emitted counts) are compiled in; the plain instantiation omits them.
+template <int DT, bool EX>
 __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
@@ -603,19 +667,43 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   if (!is_draft && i > gb) return;
   if (is_draft && (onehot || i >= gb)) return;
 
-  const RowParams P = is_draft ? a.dp : a.tp;
+  RowParams P = is_draft ? a.dp : a.tp;
+  const spec_sampling_params_t* rules = EX ? (is_draft ? a.dps : a.tps) : nullptr;
+  bool rule_valid = true;
+  if (EX && rules) {                             // this sequence's own rule [wrblog §15]
+    if (threadIdx.x == 0) {
+      const spec_sampling_params_t sp = rules[b];
+      const bool ok = rule_ok(sp);
+      sm.b_i32[6] = ok ? 1 : 0;
+      if (ok) sm.rowp = row_params_of(sp, a.V);
+    }
+    __syncthreads();
+    rule_valid = sm.b_i32[6] != 0;
+    if (rule_valid) P = sm.rowp;
+  }
   const Row row = seq_row<DT>(a, b, i, is_draft);
   int dtok = -1;
   if (i < gb) {
     const int t = a.tokens[static_cast<size_t>(b) * a.G + i];
     dtok = (t >= 0 && t < a.V) ? t : -1;
   }
-  if (P.path == PATH_STREAM) stream_row<DT>(row, P, dtok, sm);
-  else full_row<DT>(row, P, dtok, sm);
+  if (EX && !rule_valid) {                       // the epilogue reports the sequence's bad rule
+    if (threadIdx.x == 0) {
+      RowStat st;
+      st.W = 1.0; st.cut = 0; st.m = 0.0f; st.p_tok = 0.0f; st.status = SEQ_OK; st.n_list = 0;
+      st.path = PATH_FULL; st.argmax = -1; st.cT = 0.0f; st.pad = 0;
+      sm.st = st;
+    }
+    __syncthreads();
+  } else if (P.path == PATH_STREAM) {
+    stream_row<DT>(row, P, dtok, sm);
+  } else {
+    full_row<DT>(row, P, dtok, sm);
+  }
 
   // publish the row summary, then count this row in
   if (threadIdx.x == 0) a.stats[static_cast<size_t>(b) * slots + slot] = sm.st;
-  if (P.path == PATH_STREAM) {
+  if ((!EX || rule_valid) && P.path == PATH_STREAM) {
     // the kept list, stored in token order (entry e goes to its token's rank)
     static_assert(kListCap <= kThreads, "one thread per kept entry");
     ListEntry* dst = a.lists + (static_cast<size_t>(b) * slots + slot) * kListCap;
@@ -641,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   __syncthreads();
   if (!sm.b_i32[7]) return;
   __threadfence();
-  sample_epilogue<DT>(a, b, gb, onehot, sm);
+  sample_epilogue<DT, EX>(a, b, gb, onehot, sm);
   __syncthreads();
   if (threadIdx.x == 0) a.counters[b] = 0u;   // leave the workspace reusable
 }
@@ -672,7 +760,7 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   const RowStat* S = a.stats + static_cast<size_t>(b) * slots;
   const RowStat ts = load_stat(S + rec.j);
   RowStat ds;
-  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0;
+  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f;
   if (residual && !onehot) ds = load_stat(S + a.G + 1 + rec.j);
   ScanCtx c = make_scan<DT>(a, b, rec.j, rec.mode, onehot, ts, ds, rec.dj, sm);
   const int nv = c.trow.nvec;
@@ -808,6 +896,7 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   if (tid == 0) {
     a.out_tokens[static_cast<size_t>(b) * (a.G + 1) + rec.j] = tok;
     if (a.out_Z) a.out_Z[b] = residual ? static_cast<float>(Z) : -1.0f;
+    if (a.eos >= 0 && tok == a.eos) flags |= SEQ_FLAG_EOS;
     if (a.out_status) a.out_status[b] = flags;
     a.dcount[b] = 0u;   // leave the workspace reusable
   }
@@ -1023,32 +1112,9 @@ using namespace sv;
 constexpr size_t kAlign = 256;
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-bool params_ok(const spec_sampling_params_t& p) {
-  return std::isfinite(p.temperature) && p.temperature > 0.0f && p.top_k >= 0 &&
-         p.top_p > 0.0f && p.top_p <= 1.0f;
-}
+bool params_ok(const spec_sampling_params_t& p) { return rule_ok(p); }
 
-int bit_length(uint32_t v) {
-  int n = 0;
-  while (v) { ++n; v >>= 1; }
-  return n;
-}
-
-RowParams make_row_params(const spec_sampling_params_t& p, int V, spec_dtype_t dt) {
-  RowParams r;
-  r.T = p.temperature;
-  const double cT = 1.4426950408889634 / static_cast<double>(p.temperature);  // log2(e) / T
-  r.cT = static_cast<float>(cT);
-  r.cT_lo = static_cast<float>(cT - static_cast<double>(r.cT));
-  r.invT = 1.0 / static_cast<double>(p.temperature);
-  r.k = (p.top_k >= V) ? 0 : p.top_k;
-  r.top_p = p.top_p;
-  (void)dt;
-  r.path = (r.k >= 1 && r.k <= kSmallK) ? PATH_STREAM : PATH_FULL;
-  int sh = 62 - bit_length(static_cast<uint32_t>(V));
-  r.fixed_shift = sh < 24 ? 24 : (sh > 40 ? 40 : sh);
-  return r;
-}
+RowParams make_row_params(const spec_sampling_params_t& p, int V, spec_dtype_t) { return row_params_of(p, V); }
 
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -1069,16 +1135,18 @@ struct SampleLayout {
   size_t counters, dcount, stats, lists, drec, dsum, total;
 };
 size_t zero_region_bytes(int B) { return 2 * round_up(static_cast<size_t>(B) * sizeof(uint32_t)); }
-SampleLayout sample_layout(int B, int G, int V, const RowParams& tp, const RowParams& dp) {
+// tps / dps: that side's rules come per sequence, so its rows may take either path.
+SampleLayout sample_layout(int B, int G, int V, const RowParams& tp, const RowParams& dp, bool tps = false,
+                           bool dps = false) {
   SampleLayout L;
   const size_t slots = static_cast<size_t>(2 * G + 1);
   L.counters = 0;
   L.dcount = round_up(static_cast<size_t>(B) * sizeof(uint32_t));
   L.stats = zero_region_bytes(B);
   L.lists = L.stats + round_up(static_cast<size_t>(B) * slots * sizeof(RowStat));
-  const bool need_lists = tp.path == PATH_STREAM || dp.path == PATH_STREAM;
+  const bool need_lists = tps || dps || tp.path == PATH_STREAM || dp.path == PATH_STREAM;
   L.drec = L.lists + (need_lists ? round_up(static_cast<size_t>(B) * slots * kListCap * sizeof(ListEntry)) : 0);
-  const bool defer = tp.path == PATH_FULL;
+  const bool defer = tps || tp.path == PATH_FULL;
   L.dsum = L.drec + (defer ? round_up(static_cast<size_t>(B) * sizeof(DrawRec)) : 0);
   L.total = L.dsum + (defer ? round_up(static_cast<size_t>(B) * draw_chunks(V, SPEC_F32) * sizeof(double)) : 0);
   return L;
@@ -1119,7 +1187,7 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
-std::atomic<uint64_t> g_ready[10];  // sample, greedy, transform, draw, greedy-early x {bf16, f32}
+std::atomic<uint64_t> g_ready[12];  // sample, greedy, transform, draw, greedy-early, sample-ex x {bf16, f32}
 
 // Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
 // needs FullExtra after Smem; launches without such rows keep their occupancy.
@@ -1155,6 +1223,19 @@ spec_status_t spec_verify_workspace_size(int32_t batch, int32_t gamma_max, int32
   return SPEC_OK;
 }
 
+spec_status_t spec_verify_workspace_size_ex(int32_t batch, int32_t gamma_max, int32_t vocab,
+                                            spec_sampling_params_t target_params,
+                                            spec_sampling_params_t draft_params,
+                                            const spec_verify_options_t* options, size_t* bytes) {
+  if (!bytes || !shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
+    return SPEC_ERR_INVALID_ARG;
+  if (gamma_max > kMaxGamma) return SPEC_ERR_UNSUPPORTED;
+  const bool tps = options && options->target_params_seq, dps = options && options->draft_params_seq;
+  *bytes = sample_layout(batch, gamma_max, vocab, make_row_params(target_params, vocab, SPEC_BF16),
+                         make_row_params(draft_params, vocab, SPEC_BF16), tps, dps).total;
+  return SPEC_OK;
+}
+
 spec_status_t spec_greedy_workspace_size(int32_t batch, int32_t gamma_max, size_t* bytes) {
   if (!bytes || !shape_ok(batch, gamma_max, 1)) return SPEC_ERR_INVALID_ARG;
   *bytes = greedy_layout(batch, gamma_max).total;
@@ -1167,14 +1248,21 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
                                         const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
                                         const float* u_accept, const float* u_sample,
                                         spec_sampling_params_t target_params,
-                                        spec_sampling_params_t draft_params, float lenience,
+                                        spec_sampling_params_t draft_params,
+                                        const spec_verify_options_t* options,
                                         int32_t batch, int32_t gamma_max, int32_t vocab,
                                         void* workspace, size_t workspace_bytes,
                                         int32_t* out_tokens, int32_t* out_num_accepted,
                                         float* out_accept_prob, float* out_residual_z,
-                                        int32_t* out_status, void* stream) {
+                                        int32_t* out_status, int32_t* out_num_emitted, void* stream) {
   if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  const float lenience = options ? options->lenience : 1.0f;
+  const int32_t eos = options ? options->eos_token : -1;
+  const spec_sampling_params_t* tps = options ? options->target_params_seq : nullptr;
+  const spec_sampling_params_t* dps = options ? options->draft_params_seq : nullptr;
   if (!(lenience > 0.0f && lenience <= 1.0f)) return SPEC_ERR_INVALID_ARG;
+  if (eos < -1 || eos >= vocab) return SPEC_ERR_INVALID_ARG;
+  if (!aligned_to(tps, 4) || !aligned_to(dps, 4) || !aligned_to(out_num_emitted, 4)) return SPEC_ERR_MISALIGNED;
   if (!shape_ok(batch, gamma_max, vocab) || !params_ok(target_params) || !params_ok(draft_params))
     return SPEC_ERR_INVALID_ARG;
   if (gamma_max > kMaxGamma) return SPEC_ERR_UNSUPPORTED;
@@ -1190,9 +1278,13 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   SampleArgs a;
   a.tp = make_row_params(target_params, vocab, dtype);
   a.dp = make_row_params(draft_params, vocab, dtype);
-  const SampleLayout L = sample_layout(batch, gamma_max, vocab, a.tp, a.dp);
+  const SampleLayout L = sample_layout(batch, gamma_max, vocab, a.tp, a.dp, tps != nullptr, dps != nullptr);
   if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
+  a.tps = tps;
+  a.dps = dps;
+  a.eos = eos;
+  a.out_nemit = out_num_emitted;
   a.tgt = static_cast<const char*>(target_logits);
   a.dft = static_cast<const char*>(draft_logits);
   a.tokens = draft_tokens;
@@ -1215,7 +1307,9 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   a.out_aprob = out_accept_prob;
   a.out_Z = out_residual_z;
   a.out_status = out_status;
-  a.defer = a.tp.path == PATH_FULL ? 1 : 0;
+  a.defer = (tps != nullptr || a.tp.path == PATH_FULL) ? 1 : 0;
+  // per-sequence rules: any row may take the full-row path with a top-p cut
+  const size_t smem = (tps || dps) ? sizeof(Smem) + sizeof(FullExtra) : smem_for(a.tp, a.dp);
   a.chunk_vecs = kChunkVecs;
   a.nchunk = draw_chunks(vocab, dtype);
   a.dcount = reinterpret_cast<uint32_t*>(ws + L.dcount);
@@ -1225,14 +1319,25 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   const dim3 dgrid(static_cast<unsigned>(batch), static_cast<unsigned>(a.nchunk));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (dtype == SPEC_BF16) {
-    err = prepare(sample_kernel<DT_BF16>, g_ready[0]);
-    if (err == cudaSuccess) sample_kernel<DT_BF16><<<grid, kThreads, smem_for(a.tp, a.dp), s>>>(a);
+  const bool ex = tps || dps || eos >= 0 || out_num_emitted;
+  if (dtype == SPEC_BF16 && ex) {
+    err = prepare(sample_kernel<DT_BF16, true>, g_ready[10]);
+    if (err == cudaSuccess) sample_kernel<DT_BF16, true><<<grid, kThreads, smem, s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6]);
+    if (err == cudaSuccess && a.defer) draw_kernel<DT_BF16><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
+  } else if (ex) {
+    err = prepare(sample_kernel<DT_F32, true>, g_ready[11]);
+    if (err == cudaSuccess) sample_kernel<DT_F32, true><<<grid, kThreads, smem, s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_F32>, g_ready[7]);
+    if (err == cudaSuccess && a.defer) draw_kernel<DT_F32><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
+  } else if (dtype == SPEC_BF16) {
+    err = prepare(sample_kernel<DT_BF16, false>, g_ready[0]);
+    if (err == cudaSuccess) sample_kernel<DT_BF16, false><<<grid, kThreads, smem, s>>>(a);
     if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6]);
     if (err == cudaSuccess && a.defer) draw_kernel<DT_BF16><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
   } else {
-    err = prepare(sample_kernel<DT_F32>, g_ready[1]);
-    if (err == cudaSuccess) sample_kernel<DT_F32><<<grid, kThreads, smem_for(a.tp, a.dp), s>>>(a);
+    err = prepare(sample_kernel<DT_F32, false>, g_ready[1]);
+    if (err == cudaSuccess) sample_kernel<DT_F32, false><<<grid, kThreads, smem, s>>>(a);
     if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_F32>, g_ready[7]);
     if (err == cudaSuccess && a.defer) draw_kernel<DT_F32><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
   }
@@ -1252,9 +1357,9 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
                                  float* out_accept_prob, float* out_residual_z,
                                  int32_t* out_status, void* stream) {
   return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
-                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, 1.0f,
+                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, nullptr,
                             batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,
-                            out_num_accepted, out_accept_prob, out_residual_z, out_status, stream);
+                            out_num_accepted, out_accept_prob, out_residual_z, out_status, nullptr, stream);
 }
 
 spec_status_t spec_verify_sample_lenient(const void* target_logits, const void* draft_logits,
@@ -1268,10 +1373,34 @@ spec_status_t spec_verify_sample_lenient(const void* target_logits, const void* 
                                          int32_t* out_tokens, int32_t* out_num_accepted,
                                          float* out_accept_prob, float* out_residual_z,
                                          int32_t* out_status, void* stream) {
+  spec_verify_options_t opt;
+  opt.lenience = lenience;
+  opt.eos_token = -1;
+  opt.target_params_seq = nullptr;
+  opt.draft_params_seq = nullptr;
   return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
-                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, lenience,
+                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, &opt,
                             batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,
-                            out_num_accepted, out_accept_prob, out_residual_z, out_status, stream);
+                            out_num_accepted, out_accept_prob, out_residual_z, out_status, nullptr, stream);
+}
+
+spec_status_t spec_verify_sample_ex(const void* target_logits, const void* draft_logits,
+                                    spec_dtype_t dtype, const int32_t* draft_tokens,
+                                    const int32_t* gamma_per_seq, const uint8_t* draft_is_onehot,
+                                    const float* u_accept, const float* u_sample,
+                                    spec_sampling_params_t target_params,
+                                    spec_sampling_params_t draft_params,
+                                    const spec_verify_options_t* options,
+                                    int32_t batch, int32_t gamma_max, int32_t vocab,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* out_tokens, int32_t* out_num_accepted,
+                                    float* out_accept_prob, float* out_residual_z,
+                                    int32_t* out_status, int32_t* out_num_emitted, void* stream) {
+  return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
+                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, options,
+                            batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,
+                            out_num_accepted, out_accept_prob, out_residual_z, out_status, out_num_emitted,
+                            stream);
 }
 
 spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,

@@ -54,7 +54,8 @@ struct __align__(16) RowStat {
   int32_t n_list;  // PATH_STREAM: kept-list length
   int32_t path;
   int32_t argmax;  // greedy rows: argmax token
-  int32_t pad[2];
+  float cT;        // the row's log2(e) / T (its sampling rule, for the draw)
+  int32_t pad;
 };
 static_assert(sizeof(RowStat) == 48, "RowStat layout");
 
@@ -107,7 +108,8 @@ struct __align__(16) Smem {
   uint64_t b_u64[4];
   double b_f64[4];
   float b_f32[2];
-  int b_i32[8];
+  int b_i32[10];
+  RowParams rowp;                    // a row's sampling rule when it is given per sequence
   RowStat st;
 };
 
@@ -1295,6 +1297,7 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm) 
   st.argmax = -1;
   st.W = S;
   st.p_tok = 0.0f;
+  st.cT = P.cT;
   st.status = bad ? SEQ_NONFINITE : (m > -__int_as_float(0x7f800000) ? SEQ_OK : SEQ_EMPTY_SUPPORT);
   if (st.status == SEQ_OK) {
     const float scale = __int_as_float((127 + P.fixed_shift) << 23);   // 2^fixed_shift
@@ -1455,6 +1458,7 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
     st.W = 0.0;                                               // PATH_FULL rows only
     st.p_tok = 0.0f;
     st.n_list = 0;
+    st.cT = P.cT;
     if (st.status == SEQ_OK) {
       float w[4];
       df s = df_from(0.0f);

@@ -37,7 +37,8 @@ def oracle_probs(rows: torch.Tensor, params) -> torch.Tensor:
     return torch.from_numpy(p)
 
 
-def run_oracle_sample(w, seqs=None, keep_cdf=True, lenience=1.0):
+def run_oracle_sample(w, seqs=None, keep_cdf=True, lenience=1.0, rules=None, eos_token=-1):
+    """The oracle on workload ``w``; ``rules``: per sequence (target SamplingParams, draft SamplingParams)."""
     tl = to_f64(w.target_logits) if seqs is None else to_f64(w.target_logits[seqs])
     dl = None
     if w.draft_logits is not None:
@@ -48,9 +49,14 @@ def run_oracle_sample(w, seqs=None, keep_cdf=True, lenience=1.0):
     us = w.u_sample.cpu().double().numpy()[sel]
     gam = None if w.gamma_per_seq is None else w.gamma_per_seq.cpu().numpy()[sel]
     oh = None if w.draft_is_onehot is None else w.draft_is_onehot.cpu().numpy()[sel]
+    per = None
+    if rules is not None:
+        per = [(params_tuple(t), params_tuple(d)) for t, d in rules]
+        if seqs is not None:
+            per = [per[b] for b in seqs]
     return oracle.verify_sample(tl, dl, toks, ua, us, params_tuple(w.target_params),
                                 params_tuple(w.draft_params), gam, oh, keep_cdf=keep_cdf,
-                                lenience=lenience)
+                                lenience=lenience, params_per_seq=per, eos_token=eos_token)
 
 
 def run_oracle_greedy(w, seqs=None):
@@ -95,6 +101,15 @@ def compare_sample(out, ref, w, seqs=None):
         assert (status[b] & 0xFF) == 0, (b, status[b])
         n = int(nacc[b])
         assert 0 <= n <= gb, (b, n, gb)
+        if r.num_emitted == r.num_accepted:         # the oracle's block ends at an accepted EOS draft
+            if r.accept_margin < TOL_BOUNDARY or r.draft_ambiguous:
+                c["flagged"] += 1
+                continue
+            assert n == r.num_accepted and (toks[b] == r.tokens).all(), (b, toks[b], r.tokens)
+            assert status[b] & oracle.SEQ_FLAG_EOS, (b, status[b])
+            c["eos_cut"] = c.get("eos_cut", 0) + 1
+            c["exact"] += 1
+            continue
         assert 0 <= toks[b, n] < w.V, (b, toks[b])
         assert (toks[b, n + 1:] == -1).all(), (b, toks[b])
         if aprob is not None:
