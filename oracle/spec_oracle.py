@@ -60,6 +60,20 @@ Readings where the pages are silent (each is named where it is used):
       accepted draft is the EOS, the committed drafts end there and no
       replacement or bonus token follows.  The scan and the draw are unchanged
       (the same uniforms decide them); only the commit is cut.
+* R15 greedy tree verification [aiqz tree speculation; magicnet §7 tree attention]:
+      the draft is a tree; node 0 is the root (the position after the
+      committed prefix) and node i > 0 carries a draft token and a parent
+      node p_i < i; the target row of node i scores the token after the path
+      root..i.  The pages say the tree is verified in one forward and the best
+      path is accepted, not how.  Greedy reading: from the root, move to the
+      child whose token is the target's argmax at the current node -- the
+      first such child in index order when siblings repeat a token -- until no
+      child matches, then emit the argmax there (the correction, or the bonus
+      at a leaf).  With distinct sibling tokens this is the deepest node whose
+      whole path matches the argmaxes, and a chain (p_i = i - 1) is the linear
+      greedy verifier.  Every node row is read, so any failed row fails the
+      sequence (R10).  No multi-path acceptance rule for sampling mode is given
+      on the pages; none is built.
 * R12 lenience beta in (0, 1] [magicnet §8]: the page shrinks the draft
       distribution to beta q and then compares it with the target; here beta q
       stands in for q throughout -- acceptance min(1, p / (beta q)) and, on a
@@ -101,6 +115,7 @@ SEQ_BAD_UNIFORM = 3     # a uniform outside [0, 1) or NaN
 SEQ_NONFINITE = 4       # NaN or +inf logit in a row the sequence uses
 SEQ_EMPTY_SUPPORT = 5   # a row whose logits are all -inf
 SEQ_BAD_PARAMS = 6      # a sampling rule the sequence uses is outside its domain (R13)
+SEQ_BAD_TREE = 7        # a draft-tree node whose parent is not an earlier node (R15)
 SEQ_ERROR_MASK = 0xFF
 SEQ_FLAG_ZERO_Q = 0x100  # an evaluated draft token had q(d) == 0 (R6)
 SEQ_FLAG_Z_ZERO = 0x200  # residual mass was 0 after a rejection (R7)
@@ -275,6 +290,7 @@ class SeqResult:
     sample_cdf: np.ndarray | None = field(default=None, repr=False)  # normalised CDF drawn from
     rows_read: int = -1             # early-exit greedy: target rows read (R11)
     num_emitted: int = -1           # tokens committed: num_accepted + 1, or fewer after an EOS cut (R14)
+    path: list | None = None        # greedy tree verification: the accepted path's nodes, root first (R15)
 
 
 def _error_result(status: int, gamma_max: int) -> SeqResult:
@@ -434,6 +450,56 @@ def verify_greedy_sequence(target: np.ndarray, tokens: np.ndarray, gamma_b: int,
     out[:n_acc] = d[:n_acc]
     out[n_acc] = g[n_acc]
     return SeqResult(out, n_acc, SEQ_OK, np.full(gamma_max, -1.0), -1.0)
+
+
+def verify_greedy_tree_sequence(target: np.ndarray, tokens: np.ndarray, parents: np.ndarray,
+                                n_nodes: int, max_nodes: int) -> SeqResult:
+    """Greedy verification of a draft tree (R15).
+
+    target: (max_nodes, V) float64 logits, row i for node i (rows 0..n_nodes-1 used);
+    tokens / parents: (max_nodes,) node tokens and parent indices (entry 0, the root, unused).
+    Returns tokens = the accepted path's draft tokens then the correction / bonus token,
+    num_accepted = the path length L, and the path's nodes (root first) in ``path``.
+    """
+    V = target.shape[1]
+    if not 1 <= n_nodes <= max_nodes:
+        return _error_result(SEQ_BAD_LENGTH, max_nodes - 1)
+    if any(not 0 <= int(tokens[i]) < V for i in range(1, n_nodes)):
+        return _error_result(SEQ_BAD_TOKEN, max_nodes - 1)
+    if any(not 0 <= int(parents[i]) < i for i in range(1, n_nodes)):
+        return _error_result(SEQ_BAD_TREE, max_nodes - 1)
+    g = []
+    for i in range(n_nodes):
+        gi, st = greedy_row(target[i])
+        if st != SEQ_OK:
+            return _error_result(st, max_nodes - 1)
+        g.append(gi)
+    path = [0]
+    while True:
+        cur = path[-1]
+        nxt = next((c for c in range(cur + 1, n_nodes)
+                    if int(parents[c]) == cur and int(tokens[c]) == g[cur]), None)
+        if nxt is None:
+            break
+        path.append(nxt)
+    L = len(path) - 1
+    out = np.full(max_nodes, -1, dtype=np.int64)
+    out[:L] = [int(tokens[c]) for c in path[1:]]
+    out[L] = g[path[-1]]
+    res = SeqResult(out, L, SEQ_OK, np.full(max_nodes - 1, -1.0), -1.0, num_emitted=L + 1)
+    res.path = path
+    return res
+
+
+def verify_greedy_tree(target: np.ndarray, tokens: np.ndarray, parents: np.ndarray,
+                       nodes_per_seq: np.ndarray | None = None) -> BatchResult:
+    """Batched greedy tree verification (R15), one sequence at a time."""
+    B, N, _ = target.shape
+    out = []
+    for b in range(B):
+        n = N if nodes_per_seq is None else int(nodes_per_seq[b])
+        out.append(verify_greedy_tree_sequence(target[b], tokens[b], parents[b], n, N))
+    return _collect(out)
 
 
 def verify_greedy_sequence_early(target: np.ndarray, tokens: np.ndarray, gamma_b: int,
