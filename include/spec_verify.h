@@ -43,6 +43,7 @@
  *   [baisen]  "投机采样 / 投机解码（Speculative Decoding）" (baisen.site)
  *   [magicnet] "投机解码到底能加速多少：把接受率、草稿成本与墙钟收益算清楚"
  *             (magicnetworld.com)
+ *   [baisen]'s §8 and [magicnet]'s §7 describe draft trees verified in one forward.
  *
  * Conventions common to every entry point
  * ----------------------------------------
@@ -106,6 +107,8 @@ enum {
     SPEC_SEQ_EMPTY_SUPPORT = 5,   /* a used row whose logits are all -inf             */
     SPEC_SEQ_BAD_PARAMS = 6,      /* spec_verify_sample_ex: a per-sequence sampling
                                      rule the sequence uses is outside its domain     */
+    SPEC_SEQ_BAD_TREE = 7,        /* spec_verify_greedy_tree: a node whose parent is
+                                     not an earlier node                              */
     SPEC_SEQ_ERROR_MASK = 0xFF,
     SPEC_SEQ_FLAG_ZERO_Q = 0x100, /* an evaluated draft token had q(d) == 0           */
     SPEC_SEQ_FLAG_Z_ZERO = 0x200, /* residual mass was 0 after a rejection            */
@@ -301,6 +304,43 @@ SPEC_API spec_status_t spec_verify_greedy_early(const void* target_logits, spec_
                                        void* workspace, size_t workspace_bytes,
                                        int32_t* out_tokens, int32_t* out_num_accepted,
                                        int32_t* out_status, int32_t* out_rows_read, void* stream);
+
+/* Workspace bytes spec_verify_greedy_tree needs (same zero-fill rule). */
+SPEC_API spec_status_t spec_tree_workspace_size(int32_t batch, int32_t max_nodes, size_t* bytes);
+
+/* Greedy verification of a draft tree per sequence [baisen §8; magicnet §7]:
+ * several candidate continuations sharing prefixes, verified by one target
+ * forward with tree attention.  Node 0 is the root (the position after the
+ * committed prefix; its token is unused); node i > 0 carries draft token
+ * tree_tokens[b][i] and parent tree_parents[b][i] < i.  Row i of target_logits
+ * ([batch][max_nodes][vocab]) is the target's next-token logits after the path
+ * root..i.  The accepted path starts at the root and moves to the child whose
+ * token is the target's argmax at the current node (lowest index on argmax
+ * ties; the first such child in node order if siblings repeat a token) until
+ * no child matches; the argmax there is emitted (the correction, or the bonus
+ * token at a leaf).  A chain tree (parent i - 1) is spec_verify_greedy.  The
+ * pages give no multi-path acceptance rule for sampling mode; this library
+ * has none.
+ *
+ * nodes_per_seq [batch] int32 in [1, max_nodes], or NULL (= max_nodes); nodes
+ *               at or beyond it are never read.  Every node row below it is
+ *               read, and a NaN / +inf / all -inf row fails the sequence.
+ * out_tokens    [batch][max_nodes] int32: the accepted path's draft tokens, the
+ *               emitted argmax, then -1.
+ * out_num_accepted [batch]: accepted path length L (L + 1 tokens emitted), -1
+ *               on error.
+ * out_path      [batch][max_nodes] int32: the path's nodes, root first (L + 1
+ *               entries), then -1; or NULL.
+ * out_status    [batch] SPEC_SEQ_* (checks in order: length, node tokens,
+ *               parents -> SPEC_SEQ_BAD_TREE, rows in node order), or NULL.
+ * workspace     spec_tree_workspace_size() bytes, zero-filled before first use
+ *               (left reusable).  One launch; other conventions as above. */
+SPEC_API spec_status_t spec_verify_greedy_tree(const void* target_logits, spec_dtype_t dtype,
+                                      const int32_t* tree_tokens, const int32_t* tree_parents,
+                                      const int32_t* nodes_per_seq, int32_t batch, int32_t max_nodes,
+                                      int32_t vocab, void* workspace, size_t workspace_bytes,
+                                      int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_path,
+                                      int32_t* out_status, void* stream);
 
 /* The transform step alone [wrblog §7.2, §7.3]: writes the full probability
  * rows p = top_p(top_k(softmax(z / T))) the verifier samples from.

@@ -60,7 +60,7 @@ Readings where the pages are silent (each is named where it is used):
       accepted draft is the EOS, the committed drafts end there and no
       replacement or bonus token follows.  The scan and the draw are unchanged
       (the same uniforms decide them); only the commit is cut.
-* R15 greedy tree verification [aiqz tree speculation; magicnet §7 tree attention]:
+* R15 greedy tree verification [baisen §8; magicnet §7]:
       the draft is a tree; node 0 is the root (the position after the
       committed prefix) and node i > 0 carries a draft token and a parent
       node p_i < i; the target row of node i scores the token after the path

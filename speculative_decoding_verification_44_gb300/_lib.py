@@ -25,6 +25,7 @@ SPEC_SEQ_BAD_UNIFORM = 3
 SPEC_SEQ_NONFINITE = 4
 SPEC_SEQ_EMPTY_SUPPORT = 5
 SPEC_SEQ_BAD_PARAMS = 6
+SPEC_SEQ_BAD_TREE = 7
 SPEC_SEQ_ERROR_MASK = 0xFF
 SPEC_SEQ_FLAG_ZERO_Q = 0x100
 SPEC_SEQ_FLAG_Z_ZERO = 0x200
@@ -37,7 +38,8 @@ SPEC_F32 = 1
 EXPORTED = ("spec_verify_workspace_size", "spec_verify_sample", "spec_greedy_workspace_size",
             "spec_verify_greedy", "spec_transform_probs", "spec_status_string",
             "spec_verify_sample_noalloc", "spec_verify_greedy_early", "spec_verify_sample_lenient",
-            "spec_verify_workspace_size_ex", "spec_verify_sample_ex")
+            "spec_verify_workspace_size_ex", "spec_verify_sample_ex", "spec_tree_workspace_size",
+            "spec_verify_greedy_tree")
 
 
 class spec_sampling_params_t(ctypes.Structure):
@@ -86,6 +88,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_sample_ex.restype = ctypes.c_int
     lib.spec_verify_sample_ex.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, O,
                                           i32, i32, i32, vp, sz, vp, vp, vp, vp, vp, vp, vp]
+    lib.spec_tree_workspace_size.restype = ctypes.c_int
+    lib.spec_tree_workspace_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
+    lib.spec_verify_greedy_tree.restype = ctypes.c_int
+    lib.spec_verify_greedy_tree.argtypes = [vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, vp, sz,
+                                            vp, vp, vp, vp, vp]
     lib.spec_verify_sample_lenient.restype = ctypes.c_int
     lib.spec_verify_sample_lenient.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, ctypes.c_float,
                                                i32, i32, i32, vp, sz, vp, vp, vp, vp, vp, vp]
@@ -129,6 +136,16 @@ def spec_verify_workspace_size_ex(batch: int, gamma_max: int, vocab: int, target
                                                ctypes.byref(options) if options is not None else None,
                                                ctypes.byref(out)))
     return out.value
+
+
+def spec_tree_workspace_size(batch: int, max_nodes: int) -> int:
+    out = sz(0)
+    check("spec_tree_workspace_size", load().spec_tree_workspace_size(batch, max_nodes, ctypes.byref(out)))
+    return out.value
+
+
+def spec_verify_greedy_tree(*args) -> int:
+    return load().spec_verify_greedy_tree(*args)
 
 
 def spec_greedy_workspace_size(batch: int, gamma_max: int) -> int:

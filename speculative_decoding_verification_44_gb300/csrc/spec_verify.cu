@@ -980,6 +980,124 @@ __global__ void __launch_bounds__(kThreads, 5) greedy_kernel(const GreedyArgs a)
   }
 }
 
+// ------------------------------------------------------------------ greedy tree
+// Greedy verification of a draft tree [baisen §8; magicnet §7]: node 0 is the
+// root, node i > 0 carries a draft token and a parent p_i < i, and target row
+// i scores the token after the path root..i.  One CTA per node row computes
+// its argmax; the last CTA of the sequence walks from the root, moving to the
+// first child (in index order) whose token is the current node's argmax, and
+// emits the argmax where no child matches.  Warp 0 does the checks and the
+// walk: every step scans the candidate children 32 at a time with a ballot.
+struct TreeArgs {
+  const char* tgt;
+  const int32_t* tokens;    // [B][N]
+  const int32_t* parents;   // [B][N]
+  const int32_t* nodes;     // [B] or null (N everywhere)
+  int B, N, V;
+  int aligned;
+  size_t row_bytes;
+  uint32_t* counters;       // [B]
+  int2* rows;               // [B][N] (argmax, status)
+  int32_t* out_tokens;      // [B][N]
+  int32_t* out_nacc;        // [B]
+  int32_t* out_path;        // [B][N] or null
+  int32_t* out_status;      // [B] or null
+};
+
+__device__ void tree_fail(const TreeArgs& a, int b, int status, int lane) {
+  const size_t ob = static_cast<size_t>(b) * a.N;
+  for (int t = lane; t < a.N; t += 32) {
+    a.out_tokens[ob + t] = -1;
+    if (a.out_path) a.out_path[ob + t] = -1;
+  }
+  if (lane == 0) {
+    a.out_nacc[b] = -1;
+    if (a.out_status) a.out_status[b] = status;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 5) greedy_tree_kernel(const TreeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int b = blockIdx.x / a.N;
+  const int i = blockIdx.x - b * a.N;
+  const int n = a.nodes ? a.nodes[b] : a.N;
+  const int lane = threadIdx.x & 31;
+  if (n < 1 || n > a.N) {
+    if (i == 0 && threadIdx.x < 32) tree_fail(a, b, SEQ_BAD_LENGTH, lane);
+    return;
+  }
+  if (i >= n) return;
+  const Row row = make_row<DT>(a.tgt + (static_cast<size_t>(b) * a.N + i) * a.row_bytes, a.V, a.aligned != 0);
+  int g, st;
+  greedy_row<DT>(row, sm, g, st);
+  if (threadIdx.x == 0) a.rows[static_cast<size_t>(b) * a.N + i] = make_int2(g, st);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&a.counters[b], 1u);
+    sm.b_i32[7] = (prev + 1u == static_cast<unsigned>(n)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sm.b_i32[7] || threadIdx.x >= 32) return;
+  __threadfence();
+  const size_t ob = static_cast<size_t>(b) * a.N;
+  const int32_t* T = a.tokens + ob;
+  const int32_t* Pa = a.parents + ob;
+  const int2* R = a.rows + ob;
+  // checks in the documented order: node tokens, parents, then the rows in node order
+  int status = SEQ_OK;
+  bool bad_tok = false, bad_par = false;
+  for (int c = 1 + lane; c < n; c += 32) {
+    bad_tok |= T[c] < 0 || T[c] >= a.V;
+    bad_par |= Pa[c] < 0 || Pa[c] >= c;
+  }
+  if (__any_sync(kFull, bad_tok)) status = SEQ_BAD_TOKEN;
+  else if (__any_sync(kFull, bad_par)) status = SEQ_BAD_TREE;
+  for (int base = 0; base < n && status == SEQ_OK; base += 32) {
+    const int st2 = base + lane < n ? __ldcg(&R[base + lane].y) : SEQ_OK;
+    const unsigned m = __ballot_sync(kFull, st2 != SEQ_OK);
+    if (m) status = __shfl_sync(kFull, st2, __ffs(m) - 1);
+  }
+  if (status != SEQ_OK) {
+    tree_fail(a, b, status, lane);
+    if (lane == 0) a.counters[b] = 0u;
+    return;
+  }
+  // the walk: the first child of cur (index order) whose token is cur's argmax
+  int cur = 0, L = 0;
+  if (lane == 0 && a.out_path) a.out_path[ob] = 0;
+  while (true) {
+    const int gcur = __ldcg(&R[cur].x);
+    int next = -1;
+    for (int base = cur + 1; base < n && next < 0; base += 32) {
+      const int c = base + lane;
+      const unsigned m = __ballot_sync(kFull, c < n && Pa[c] == cur && T[c] == gcur);
+      if (m) next = base + __ffs(m) - 1;
+    }
+    if (next < 0) {
+      if (lane == 0) a.out_tokens[ob + L] = gcur;           // the correction, or the bonus at a leaf
+      break;
+    }
+    if (lane == 0) {
+      a.out_tokens[ob + L] = T[next];
+      if (a.out_path) a.out_path[ob + L + 1] = next;
+    }
+    cur = next;
+    ++L;
+  }
+  for (int t = L + 1 + lane; t < a.N; t += 32) {
+    a.out_tokens[ob + t] = -1;
+    if (a.out_path && t > L) a.out_path[ob + t] = -1;
+  }
+  if (lane == 0) {
+    a.out_nacc[b] = L;
+    if (a.out_status) a.out_status[b] = SEQ_OK;
+    a.counters[b] = 0u;                                     // leave the workspace reusable
+  }
+}
+
 // ------------------------------------------------------------------ early-exit greedy
 // Greedy verification that stops at the first mismatch [wrblog §6, §7.1],
 // without making any CTA wait for another.  The grid is position-major: CTA
@@ -1187,7 +1305,7 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
-std::atomic<uint64_t> g_ready[12];  // sample, greedy, transform, draw, greedy-early, sample-ex x {bf16, f32}
+std::atomic<uint64_t> g_ready[14];  // sample, greedy, transform, draw, greedy-early, sample-ex, tree x {bf16, f32}
 
 // Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
 // needs FullExtra after Smem; launches without such rows keep their occupancy.
@@ -1401,6 +1519,62 @@ spec_status_t spec_verify_sample_ex(const void* target_logits, const void* draft
                             batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,
                             out_num_accepted, out_accept_prob, out_residual_z, out_status, out_num_emitted,
                             stream);
+}
+
+spec_status_t spec_tree_workspace_size(int32_t batch, int32_t max_nodes, size_t* bytes) {
+  if (!bytes || max_nodes < 1 || !shape_ok(batch, max_nodes - 1, 1)) return SPEC_ERR_INVALID_ARG;
+  *bytes = greedy_layout(batch, max_nodes - 1).total;     // counters, then [B][N] (argmax, status)
+  return SPEC_OK;
+}
+
+spec_status_t spec_verify_greedy_tree(const void* target_logits, spec_dtype_t dtype,
+                                      const int32_t* tree_tokens, const int32_t* tree_parents,
+                                      const int32_t* nodes_per_seq, int32_t batch, int32_t max_nodes,
+                                      int32_t vocab, void* workspace, size_t workspace_bytes,
+                                      int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_path,
+                                      int32_t* out_status, void* stream) {
+  if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  if (max_nodes < 1 || vocab < 1 || !shape_ok(batch, max_nodes - 1, vocab)) return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !tree_tokens || !tree_parents || !out_tokens || !out_num_accepted || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype);
+  if (!aligned_to(target_logits, es) || !aligned_to(tree_tokens, 4) || !aligned_to(tree_parents, 4) ||
+      !aligned_to(nodes_per_seq, 4) || !aligned_to(out_tokens, 4) || !aligned_to(out_num_accepted, 4) ||
+      !aligned_to(out_path, 4) || !aligned_to(out_status, 4) || !aligned_to(workspace, kAlign))
+    return SPEC_ERR_MISALIGNED;
+  size_t need = 0;
+  spec_tree_workspace_size(batch, max_nodes, &need);
+  if (workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  const GreedyLayout L = greedy_layout(batch, max_nodes - 1);
+  TreeArgs a;
+  a.tgt = static_cast<const char*>(target_logits);
+  a.tokens = tree_tokens;
+  a.parents = tree_parents;
+  a.nodes = nodes_per_seq;
+  a.B = batch;
+  a.N = max_nodes;
+  a.V = vocab;
+  a.aligned = (vocab % elems_per_vec(dtype) == 0) && aligned_to(target_logits, 16);
+  a.row_bytes = static_cast<size_t>(vocab) * es;
+  a.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  a.rows = reinterpret_cast<int2*>(ws + L.rows);
+  a.out_tokens = out_tokens;
+  a.out_nacc = out_num_accepted;
+  a.out_path = out_path;
+  a.out_status = out_status;
+  const unsigned grid = static_cast<unsigned>(batch) * static_cast<unsigned>(max_nodes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (dtype == SPEC_BF16) {
+    err = prepare(greedy_tree_kernel<DT_BF16>, g_ready[12]);
+    if (err == cudaSuccess) greedy_tree_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
+  } else {
+    err = prepare(greedy_tree_kernel<DT_F32>, g_ready[13]);
+    if (err == cudaSuccess) greedy_tree_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
+  }
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,

@@ -31,7 +31,7 @@ enum { PATH_STREAM = 0, PATH_FULL = 1 };
 
 enum {
   SEQ_OK = 0, SEQ_BAD_LENGTH = 1, SEQ_BAD_TOKEN = 2, SEQ_BAD_UNIFORM = 3,
-  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6,
+  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6, SEQ_BAD_TREE = 7,
   SEQ_FLAG_ZERO_Q = 0x100, SEQ_FLAG_Z_ZERO = 0x200, SEQ_FLAG_EOS = 0x400
 };
 

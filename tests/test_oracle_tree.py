@@ -1,7 +1,7 @@
 """Oracle pins for greedy draft-tree verification (reading R15 of the oracle).
 
 The pages say a tree of candidate paths is verified in one forward and the
-best path is accepted [aiqz tree speculation; magicnet §7, tree attention];
+best path is accepted [baisen §8; magicnet §7];
 greedy verification of a tree is then pinned by:
 
 * a chain tree (every node's parent is the node before it) is exactly the
