@@ -53,6 +53,14 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--lenience", type=float, default=None,
+                    help="sampling workloads: spec_verify_sample_lenient with this beta")
+    ap.add_argument("--eos", type=int, default=None,
+                    help="sampling workloads: spec_verify_sample_ex with this end-of-sequence token")
+    ap.add_argument("--per-seq-rules", action="store_true",
+                    help="sampling workloads: spec_verify_sample_ex with the workload's rules given per sequence")
+    ap.add_argument("--tree", action="store_true",
+                    help="greedy workload: spec_verify_greedy_tree over draft trees of the same rows")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the steps as eager launches instead of one CUDA-graph replay")
     ap.add_argument("--workload", default="serving-zipf-topk-topp",
@@ -230,6 +238,18 @@ def params_of(w) -> dict:
     return {"temperature": round(float(p.temperature), 6), "top_k": int(p.top_k), "top_p": round(float(p.top_p), 6)}
 
 
+def variant_of(args) -> str:
+    """Metric suffix naming a non-default call (empty for the plain call)."""
+    parts = []
+    if args.lenience is not None:
+        parts.append(f"lenience {args.lenience}")
+    if args.eos is not None:
+        parts.append(f"eos {args.eos}")
+    if args.per_seq_rules:
+        parts.append("per-sequence rules")
+    return f" ({', '.join(parts)})" if parts else ""
+
+
 def metric_of(wid: int, w) -> str:
     if wid == WID:
         return METRIC
@@ -275,10 +295,33 @@ def run_greedy(args, rank, world, dev, sv, workloads):
     ws = sv.new_workspace(sv.greedy_workspace_size(B, G), dev)
     outs = [sv.alloc_outputs(B, G, dev, accept_prob=False, residual_z=False) for _ in range(ROTATE)]
     rows = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(ROTATE)]
+    trees = []
+    if args.tree:
+        # draft trees over the same G + 1 rows: node i's parent is random among the earlier
+        # nodes, its token the parent row's argmax with probability 0.8 (the workload's rate)
+        import numpy as np
+        ws = sv.new_workspace(sv.tree_workspace_size(B, G + 1), dev)
+        for r, w in enumerate(sets):
+            rng = np.random.default_rng(5000 + r)
+            arg = w.target_logits.float().argmax(dim=-1).cpu().numpy()
+            tok = np.zeros((B, G + 1), dtype=np.int32)
+            par = np.full((B, G + 1), -1, dtype=np.int32)
+            for b in range(B):
+                for i in range(1, G + 1):
+                    par[b, i] = rng.integers(0, i)
+                    tok[b, i] = arg[b, par[b, i]] if rng.random() < 0.8 else rng.integers(0, V)
+            trees.append((torch.from_numpy(tok).to(dev), torch.from_numpy(par).to(dev),
+                          torch.empty(B, G + 1, dtype=torch.int32, device=dev)))
+            outs[r] = sv.VerifyOutput(tokens=torch.empty(B, G + 1, dtype=torch.int32, device=dev),
+                                      num_accepted=torch.empty(B, dtype=torch.int32, device=dev),
+                                      status=torch.empty(B, dtype=torch.int32, device=dev))
 
     def step(i):
         w, r = sets[i % ROTATE], i % ROTATE
-        if args.early_exit:
+        if args.tree:
+            tok, par, path = trees[r]
+            sv.verify_greedy_tree(w.target_logits, tok, par, workspace=ws, out=outs[r], path=path)
+        elif args.early_exit:
             sv.verify_greedy_early(w.target_logits, w.draft_tokens, w.gamma_per_seq, workspace=ws, out=outs[r],
                                    rows_read=rows[r])
         else:
@@ -302,26 +345,28 @@ def run_greedy(args, rank, world, dev, sv, workloads):
         torch.cuda.synchronize()
     ms_per_step = max_over_ranks(t0.elapsed_time(t1), world, dev) / K
     row_bytes = V * w0.target_logits.element_size()
-    read = [int(r.sum().item()) for r in rows] if args.early_exit else [rt] * ROTATE
+    read = [int(r.sum().item()) for r in rows] if (args.early_exit and not args.tree) else [rt] * ROTATE
     needed = [int((o.num_accepted.clamp(min=0) + 1).sum().item()) for o in outs]
     peak, peak_kind = measured_peaks()
     # algorithmic rows: every row for the all-rows verifier (it checks them all), the rows
     # up to each sequence's stop for early exit (speculative extra reads are waste)
-    alg_rows = statistics.mean(needed) if args.early_exit else rt
+    alg_rows = statistics.mean(needed) if (args.early_exit and not args.tree) else rt
     achieved = alg_rows * row_bytes / (ms_per_step / 1e3) / 1e9
     if rank == 0:
         line = {
             "metric": f"verified positions/s, {w0.name} B={B} g={G} V={V} bf16"
-                      + (" (early exit)" if args.early_exit else ""),
+                      + (" (draft trees of the same rows)" if args.tree else
+                         " (early exit)" if args.early_exit else ""),
             "value": whole_job_rate(rt, world, ms_per_step), "unit": "positions/s", "n_gpus": world,
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w0.name, "B": B, "gamma": G, "V": V, "early_exit": bool(args.early_exit),
+            "config": {"workload": w0.name, "B": B, "gamma": G, "V": V, "early_exit": bool(args.early_exit), "tree": bool(args.tree),
                        "l2": f"inputs rotate over {ROTATE} independent sets of {rt * row_bytes / 1e6:.1f} MB"},
             "rows_read_per_step": statistics.mean(read), "rows_needed_per_step": statistics.mean(needed),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None, "peak_kind": f"of {peak_kind}",
-                         "kernel": "sv::greedy_early_kernel<bf16>" if args.early_exit else "sv::greedy_kernel<bf16>",
+                         "kernel": "sv::greedy_tree_kernel<bf16>" if args.tree else
+                                   "sv::greedy_early_kernel<bf16>" if args.early_exit else "sv::greedy_kernel<bf16>",
                          "algorithmic_bytes_per_launch": alg_rows * row_bytes,
                          "bytes_read_per_launch": statistics.mean(read) * row_bytes},
             "cpu_baseline": None, "e2e": None, "gpu_launches": K, "clocks": clk.summary(),
@@ -372,13 +417,22 @@ def main():
     full_target = not (1 <= w0.target_params.top_k <= 128 and w0.target_params.top_k < V)
     io_bytes = B * G * 4 * 2 + B * 4 + B * (G + 1) * 4 + B * 4 * 3 + B * G * 4
     alg_bytes = logits_bytes + io_bytes
-    ws = sv.new_workspace(sv.workspace_size(B, G, V, w0.target_params, w0.draft_params), dev)
+    # optional paths: lenience, end-of-sequence commit, per-sequence rules (the workload's own
+    # rule for every sequence; promised kept-list when that rule is on the kept-list path)
+    kept = not full_target and 1 <= w0.draft_params.top_k <= 128
+    opts = dict(lenience=args.lenience, eos_token=args.eos)
+    if args.per_seq_rules:
+        opts.update(target_rules=[w0.target_params] * B, draft_rules=[w0.draft_params] * B, kept_list_only=kept)
+        if not kept:
+            full_target = True
+    ws = sv.new_workspace(sv.workspace_size(B, G, V, w0.target_params, w0.draft_params,
+                                            per_sequence=args.per_seq_rules, kept_list_only=kept), dev)
     outs = [sv.alloc_outputs(B, G, dev) for _ in range(ROTATE)]
     stream = torch.cuda.current_stream()
 
     calls = [sv.BoundSample(w.target_logits, w.draft_logits, w.draft_tokens, w.u_accept, w.u_sample,
                             w.target_params, w.draft_params, gamma_per_seq=w.gamma_per_seq,
-                            draft_is_onehot=w.draft_is_onehot, workspace=ws, out=outs[r])
+                            draft_is_onehot=w.draft_is_onehot, workspace=ws, out=outs[r], **opts)
              for r, w in enumerate(sets)]
 
     def step(i):
@@ -396,7 +450,8 @@ def main():
         gstream = torch.cuda.Stream()
         gcalls = [sv.BoundSample(w.target_logits, w.draft_logits, w.draft_tokens, w.u_accept, w.u_sample,
                                  w.target_params, w.draft_params, gamma_per_seq=w.gamma_per_seq,
-                                 draft_is_onehot=w.draft_is_onehot, workspace=ws, out=outs[r], stream=gstream)
+                                 draft_is_onehot=w.draft_is_onehot, workspace=ws, out=outs[r], stream=gstream,
+                                 **opts)
                   for r, w in enumerate(sets)]
         gstream.wait_stream(stream)
         with torch.cuda.stream(gstream):
@@ -508,7 +563,8 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": metric_of(wid, w0), "value": value, "unit": "positions/s", "n_gpus": world, "steps": K,
+            "metric": metric_of(wid, w0) + variant_of(args), "value": value, "unit": "positions/s",
+            "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dname, "data": "synthetic",
             "config": {"workload": workloads.NAMES[wid], "B": B, "gamma": G, "V": V,

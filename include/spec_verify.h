@@ -209,7 +209,7 @@ SPEC_API spec_status_t spec_verify_sample_lenient(const void* target_logits, con
                                          float* out_accept_prob, float* out_residual_z,
                                          int32_t* out_status, void* stream);
 
-/* Options of spec_verify_sample_ex.  {1.0f, -1, NULL, NULL} is
+/* Options of spec_verify_sample_ex.  {1.0f, -1, NULL, NULL, 0} is
  * spec_verify_sample exactly.
  *
  * lenience           (0, 1]: as for spec_verify_sample_lenient [magicnet §8].
@@ -230,13 +230,21 @@ SPEC_API spec_status_t spec_verify_sample_lenient(const void* target_logits, con
  *                    sequence (SPEC_SEQ_BAD_PARAMS); a one-hot sequence's draft
  *                    rule is not used and not checked.  With per-sequence rules
  *                    the launch reserves the full-row path's extra shared
- *                    memory and the draw kernel always runs (its CTAs exit at
- *                    once for sequences with kept-list targets). */
+ *                    memory (fewer row CTAs per SM) and the draw kernel always
+ *                    runs (its CTAs exit at once for sequences with kept-list
+ *                    targets) -- unless kept_list_only is set.
+ * kept_list_only     non-zero: the caller promises every per-sequence rule has
+ *                    1 <= top_k <= 128 (top_k < vocab), the library's kept-list
+ *                    path; the launch then keeps the plain call's occupancy and
+ *                    workspace.  A per-sequence rule outside the promise fails
+ *                    its sequence with SPEC_SEQ_BAD_PARAMS.  The scalar rules
+ *                    must keep it too.  Ignored without per-sequence rules. */
 typedef struct {
     float lenience;
     int32_t eos_token;
     const spec_sampling_params_t* target_params_seq;
     const spec_sampling_params_t* draft_params_seq;
+    int32_t kept_list_only;
 } spec_verify_options_t;
 
 /* Bytes of workspace spec_verify_sample_ex needs with these options (per-

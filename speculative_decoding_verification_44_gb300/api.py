@@ -59,11 +59,12 @@ def _stream(stream: torch.cuda.Stream | None) -> int:
 
 
 def workspace_size(batch: int, gamma_max: int, vocab: int, target: SamplingParams,
-                   draft: SamplingParams, per_sequence: bool = False) -> int:
-    """Workspace bytes; ``per_sequence``: sized for per-sequence rules (spec_verify_workspace_size_ex)."""
+                   draft: SamplingParams, per_sequence: bool = False, kept_list_only: bool = False) -> int:
+    """Workspace bytes; ``per_sequence``: sized for per-sequence rules (spec_verify_workspace_size_ex),
+    ``kept_list_only``: with the caller's kept-list promise."""
     if not per_sequence:
         return _lib.spec_verify_workspace_size(batch, gamma_max, vocab, target.c(), draft.c())
-    opt = _lib.spec_verify_options_t(1.0, -1, 1, 1)        # non-null per-sequence pointers: both sides
+    opt = _lib.spec_verify_options_t(1.0, -1, 1, 1, int(kept_list_only))   # non-null per-sequence pointers
     return _lib.spec_verify_workspace_size_ex(batch, gamma_max, vocab, target.c(), draft.c(), opt)
 
 
@@ -102,7 +103,7 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
                   workspace: torch.Tensor | None = None, out: VerifyOutput | None = None,
                   stream: torch.cuda.Stream | None = None,
                   lenience: float | None = None, eos_token: int | None = None,
-                  target_rules=None, draft_rules=None) -> VerifyOutput:
+                  target_rules=None, draft_rules=None, kept_list_only: bool = False) -> VerifyOutput:
     """spec_verify_sample on torch tensors; spec_verify_sample_lenient when only
     ``lenience`` is given; spec_verify_sample_ex when ``eos_token`` or per-sequence
     rules are given.
@@ -111,7 +112,8 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
     bfloat16 / float32; draft_tokens [B, G] int32; u_accept [B, G] and u_sample [B]
     float32; gamma_per_seq [B] int32; draft_is_onehot [B] uint8; lenience in (0, 1];
     target_rules / draft_rules: per-sequence rules, a list of SamplingParams or a
-    tensor from rules_tensor() (the scalar ``target`` / ``draft`` then only size the call).
+    tensor from rules_tensor() (the scalar ``target`` / ``draft`` then only size the call);
+    kept_list_only: the promise that every per-sequence rule has 1 <= top_k <= 128.
     """
     B, G1, V = target_logits.shape
     G = G1 - 1
@@ -125,7 +127,8 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
         draft_rules = rules_tensor(draft_rules, dev)
     if workspace is None:
         workspace = new_workspace(workspace_size(B, G, V, target, draft,
-                                                 per_sequence=target_rules is not None or draft_rules is not None), dev)
+                                                 per_sequence=target_rules is not None or draft_rules is not None,
+                                                 kept_list_only=kept_list_only), dev)
     if out is None:
         out = alloc_outputs(B, G, dev)
     if ex and out.num_emitted is None:
@@ -139,7 +142,7 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
     if ex:
         opt = _lib.spec_verify_options_t(1.0 if lenience is None else float(lenience),
                                          -1 if eos_token is None else int(eos_token),
-                                         _ptr(target_rules), _ptr(draft_rules))
+                                         _ptr(target_rules), _ptr(draft_rules), int(kept_list_only))
         _lib.check("spec_verify_sample_ex",
                    _lib.spec_verify_sample_ex(*head, ctypes.byref(opt), *tail[:-1], _ptr(out.num_emitted), tail[-1]))
     elif lenience is None:
@@ -245,27 +248,48 @@ class BoundSample:
 
     def __init__(self, target_logits, draft_logits, draft_tokens, u_accept, u_sample,
                  target: SamplingParams, draft: SamplingParams, gamma_per_seq=None,
-                 draft_is_onehot=None, workspace=None, out=None, stream=None):
+                 draft_is_onehot=None, workspace=None, out=None, stream=None, lenience=None,
+                 eos_token=None, target_rules=None, draft_rules=None, kept_list_only=False):
         B, G1, V = target_logits.shape
         G = G1 - 1
         dev = target_logits.device
         if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
             raise TypeError("target and draft logits must share a dtype")
+        if isinstance(target_rules, (list, tuple)):
+            target_rules = rules_tensor(target_rules, dev)
+        if isinstance(draft_rules, (list, tuple)):
+            draft_rules = rules_tensor(draft_rules, dev)
+        per = target_rules is not None or draft_rules is not None
+        ex = per or eos_token is not None
         self.workspace = workspace if workspace is not None else new_workspace(
-            workspace_size(B, G, V, target, draft), dev)
+            workspace_size(B, G, V, target, draft, per_sequence=per, kept_list_only=kept_list_only), dev)
         self.out = out if out is not None else alloc_outputs(B, G, dev)
+        if ex and self.out.num_emitted is None:
+            self.out.num_emitted = torch.empty(B, dtype=torch.int32, device=dev)
         self._keep = (target_logits, draft_logits, draft_tokens, u_accept, u_sample, gamma_per_seq,
-                      draft_is_onehot)
-        self._fn = _lib.load().spec_verify_sample
+                      draft_is_onehot, target_rules, draft_rules)
         o = self.out
-        self._args = (_ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits),
-                      _ptr(draft_tokens), _ptr(gamma_per_seq), _ptr(draft_is_onehot), _ptr(u_accept),
-                      _ptr(u_sample), target.c(), draft.c(), B, G, V, _ptr(self.workspace),
-                      self.workspace.numel(), _ptr(o.tokens), _ptr(o.num_accepted), _ptr(o.accept_prob),
-                      _ptr(o.residual_z), _ptr(o.status), _stream(stream))
+        head = (_ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits),
+                _ptr(draft_tokens), _ptr(gamma_per_seq), _ptr(draft_is_onehot), _ptr(u_accept),
+                _ptr(u_sample), target.c(), draft.c())
+        tail = (B, G, V, _ptr(self.workspace), self.workspace.numel(), _ptr(o.tokens), _ptr(o.num_accepted),
+                _ptr(o.accept_prob), _ptr(o.residual_z), _ptr(o.status))
+        lib = _lib.load()
+        if ex:
+            self._opt = _lib.spec_verify_options_t(1.0 if lenience is None else float(lenience),
+                                                   -1 if eos_token is None else int(eos_token),
+                                                   _ptr(target_rules), _ptr(draft_rules), int(kept_list_only))
+            self._fn, self._name = lib.spec_verify_sample_ex, "spec_verify_sample_ex"
+            self._args = (*head, ctypes.byref(self._opt), *tail, _ptr(o.num_emitted), _stream(stream))
+        elif lenience is not None:
+            self._fn, self._name = lib.spec_verify_sample_lenient, "spec_verify_sample_lenient"
+            self._args = (*head, float(lenience), *tail, _stream(stream))
+        else:
+            self._fn, self._name = lib.spec_verify_sample, "spec_verify_sample"
+            self._args = (*head, *tail, _stream(stream))
 
     def __call__(self) -> VerifyOutput:
         st = self._fn(*self._args)
         if st:
-            _lib.check("spec_verify_sample", st)
+            _lib.check(self._name, st)
         return self.out

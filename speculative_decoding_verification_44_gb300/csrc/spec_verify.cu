@@ -27,6 +27,10 @@ namespace sv {
 __host__ __device__ inline bool rule_ok(const spec_sampling_params_t& p) {
   return isfinite(p.temperature) && p.temperature > 0.0f && p.top_k >= 0 && p.top_p > 0.0f && p.top_p <= 1.0f;
 }
+// ... and, when the caller promised kept-list rules, 1 <= top_k <= kSmallK (and < V).
+__host__ __device__ inline bool rule_ok(const spec_sampling_params_t& p, bool kept_only, int V) {
+  return rule_ok(p) && (!kept_only || (p.top_k >= 1 && p.top_k <= kSmallK && p.top_k < V));
+}
 
 // A rule prepared for the row kernels (the same arithmetic on host and device).
 __host__ __device__ inline RowParams row_params_of(const spec_sampling_params_t& p, int V) {
@@ -59,6 +63,7 @@ struct SampleArgs {
   const spec_sampling_params_t* dps;   // [B] per-sequence draft rules (device), or null
   float beta;           // lenience: beta q stands in for q (1 = the lossless rule)
   int eos;              // end-of-sequence token (-1: none): nothing is committed after it
+  int kept_only;        // per-sequence rules promised on the kept-list path
   int B, G, V;
   int aligned;
   size_t row_bytes;
@@ -489,8 +494,8 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   if (tid == kThreads - 1) sm.b_f32[0] = a.u_samp[b];
   if (EX && tid == kThreads - 2) {              // per-sequence rules the sequence uses
     bool ok = true;
-    if (a.tps) ok = rule_ok(a.tps[b]);
-    if (a.dps && !onehot) ok = ok && rule_ok(a.dps[b]);
+    if (a.tps) ok = rule_ok(a.tps[b], a.kept_only != 0, a.V);
+    if (a.dps && !onehot) ok = ok && rule_ok(a.dps[b], a.kept_only != 0, a.V);
     sm.b_i32[8] = ok ? 1 : 0;
   }
   __syncthreads();
@@ -673,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   if (EX && rules) {                             // this sequence's own rule [wrblog §15]
     if (threadIdx.x == 0) {
       const spec_sampling_params_t sp = rules[b];
-      const bool ok = rule_ok(sp);
+      const bool ok = rule_ok(sp, a.kept_only != 0, a.V);
       sm.b_i32[6] = ok ? 1 : 0;
       if (ok) sm.rowp = row_params_of(sp, a.V);
     }
@@ -1349,8 +1354,9 @@ spec_status_t spec_verify_workspace_size_ex(int32_t batch, int32_t gamma_max, in
     return SPEC_ERR_INVALID_ARG;
   if (gamma_max > kMaxGamma) return SPEC_ERR_UNSUPPORTED;
   const bool tps = options && options->target_params_seq, dps = options && options->draft_params_seq;
+  const bool any_path = !(options && options->kept_list_only);
   *bytes = sample_layout(batch, gamma_max, vocab, make_row_params(target_params, vocab, SPEC_BF16),
-                         make_row_params(draft_params, vocab, SPEC_BF16), tps, dps).total;
+                         make_row_params(draft_params, vocab, SPEC_BF16), any_path && tps, any_path && dps).total;
   return SPEC_OK;
 }
 
@@ -1378,6 +1384,7 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   const int32_t eos = options ? options->eos_token : -1;
   const spec_sampling_params_t* tps = options ? options->target_params_seq : nullptr;
   const spec_sampling_params_t* dps = options ? options->draft_params_seq : nullptr;
+  const bool kept_only = options && options->kept_list_only && (tps || dps);
   if (!(lenience > 0.0f && lenience <= 1.0f)) return SPEC_ERR_INVALID_ARG;
   if (eos < -1 || eos >= vocab) return SPEC_ERR_INVALID_ARG;
   if (!aligned_to(tps, 4) || !aligned_to(dps, 4) || !aligned_to(out_num_emitted, 4)) return SPEC_ERR_MISALIGNED;
@@ -1396,12 +1403,16 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   SampleArgs a;
   a.tp = make_row_params(target_params, vocab, dtype);
   a.dp = make_row_params(draft_params, vocab, dtype);
-  const SampleLayout L = sample_layout(batch, gamma_max, vocab, a.tp, a.dp, tps != nullptr, dps != nullptr);
+  // promised kept-list rules: the scalar rules must keep the promise too
+  if (kept_only && (a.tp.path != PATH_STREAM || a.dp.path != PATH_STREAM)) return SPEC_ERR_INVALID_ARG;
+  const bool any_path = !kept_only && (tps || dps);     // per-sequence rows may take either path
+  const SampleLayout L = sample_layout(batch, gamma_max, vocab, a.tp, a.dp, any_path && tps, any_path && dps);
   if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   a.tps = tps;
   a.dps = dps;
   a.eos = eos;
+  a.kept_only = kept_only ? 1 : 0;
   a.out_nemit = out_num_emitted;
   a.tgt = static_cast<const char*>(target_logits);
   a.dft = static_cast<const char*>(draft_logits);
@@ -1425,9 +1436,9 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   a.out_aprob = out_accept_prob;
   a.out_Z = out_residual_z;
   a.out_status = out_status;
-  a.defer = (tps != nullptr || a.tp.path == PATH_FULL) ? 1 : 0;
+  a.defer = ((any_path && tps) || a.tp.path == PATH_FULL) ? 1 : 0;
   // per-sequence rules: any row may take the full-row path with a top-p cut
-  const size_t smem = (tps || dps) ? sizeof(Smem) + sizeof(FullExtra) : smem_for(a.tp, a.dp);
+  const size_t smem = any_path ? sizeof(Smem) + sizeof(FullExtra) : smem_for(a.tp, a.dp);
   a.chunk_vecs = kChunkVecs;
   a.nchunk = draw_chunks(vocab, dtype);
   a.dcount = reinterpret_cast<uint32_t*>(ws + L.dcount);
@@ -1496,6 +1507,7 @@ spec_status_t spec_verify_sample_lenient(const void* target_logits, const void* 
   opt.eos_token = -1;
   opt.target_params_seq = nullptr;
   opt.draft_params_seq = nullptr;
+  opt.kept_list_only = 0;
   return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
                             draft_is_onehot, u_accept, u_sample, target_params, draft_params, &opt,
                             batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,

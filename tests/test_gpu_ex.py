@@ -123,3 +123,30 @@ def test_bad_rules_fail_only_their_sequence():
     assert [st[i] for i in (0, 2, 4, 7)] == [0, 0, 0, 0]
     assert (out.num_accepted.cpu()[[1, 3, 5, 6]] == -1).all()
     assert (out.num_emitted.cpu()[[1, 3, 5, 6]] == -1).all()
+
+
+def test_kept_list_promise():
+    """kept_list_only: the same results as without the promise when every rule keeps
+    it; a per-sequence rule that breaks it fails only its sequence; scalar rules
+    that break it are refused before launch."""
+    import speculative_decoding_verification_44_gb300 as sv
+    from speculative_decoding_verification_44_gb300 import _lib
+    w = workload(3, B=10, V=9000)
+    kept = [(0.7, 50, 0.9), (1.0, 1, 1.0), (0.9, 128, 0.8), (1.2, 7, 1.0)]
+    tr = [sv.SamplingParams(*kept[b % 4]) for b in range(w.B)]
+    dr = [sv.SamplingParams(*kept[(b + 1) % 4]) for b in range(w.B)]
+    a = gpu_sample(w, target_rules=tr, draft_rules=dr)
+    b = gpu_sample(w, target_rules=tr, draft_rules=dr, kept_list_only=True)
+    torch.cuda.synchronize()
+    same(a, b)
+    tr[3] = sv.SamplingParams(1.0, 0, 0.9)            # top-k off: the full-row path
+    dr[6] = sv.SamplingParams(1.0, 300, 1.0)          # top-k above the kept-list limit
+    c = gpu_sample(w, target_rules=tr, draft_rules=dr, kept_list_only=True)
+    torch.cuda.synchronize()
+    st = [s & 0xFF for s in c.status.tolist()]
+    assert st[3] == 6 and st[6] == 6 and all(st[i] == 0 for i in range(w.B) if i not in (3, 6))
+    w.target_params = sv.SamplingParams(1.0, 0, 0.9)
+    with pytest.raises(_lib.SpecError) as e:
+        gpu_sample(w, target_rules=tr, draft_rules=dr, kept_list_only=True,
+                   workspace=sv.new_workspace(1 << 24, "cuda"))
+    assert e.value.status == 1
