@@ -197,7 +197,7 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
     } else {
       const Row drow = seq_row<DT>(a, b, r, true);
       q = full_prob(load_elem<DT>(drow.base, te.token), static_cast<uint32_t>(te.token), cut_test(ds.cut), ds.m,
-                    ds.cT, static_cast<float>(1.0 / ds.W));
+                    ds.cT, ds.invW);
     }
     const float bq = a.beta * q;                      // beta q exactly, as hi + lo
     const df d = df_add(pw, {-bq, -fmaf(a.beta, q, -bq)});
@@ -447,8 +447,8 @@ __device__ ScanCtx make_scan(const SampleArgs& a, int b, int r, int mode, bool o
   c.md = ds.m;
   c.cTt = ts.cT;
   c.cTd = ds.cT;
-  c.invWt = static_cast<float>(1.0 / ts.W);
-  c.invWd = static_cast<float>(1.0 / ds.W);
+  c.invWt = ts.invW;
+  c.invWd = ds.invW;
   c.dj = dj;
   c.beta = a.beta;
   c.nq = 0;
@@ -606,7 +606,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   const int r = j;   // == gb when every draft was accepted
   const RowStat ts = E.rs[r];
   RowStat ds;
-  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f;
+  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f; ds.invW = 1.0f;
   if (residual && !onehot) ds = E.rs[a.G + 1 + r];
   const int dj = residual ? E.dtok[j] : -1;
   const float uf = sm.b_f32[0];
@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
     if (threadIdx.x == 0) {
       RowStat st;
       st.W = 1.0; st.cut = 0; st.m = 0.0f; st.p_tok = 0.0f; st.status = SEQ_OK; st.n_list = 0;
-      st.path = PATH_FULL; st.argmax = -1; st.cT = 0.0f; st.pad = 0;
+      st.path = PATH_FULL; st.argmax = -1; st.cT = 0.0f; st.invW = 0.0f;
       sm.st = st;
     }
     __syncthreads();
@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
   const RowStat* S = a.stats + static_cast<size_t>(b) * slots;
   const RowStat ts = load_stat(S + rec.j);
   RowStat ds;
-  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f;
+  ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f; ds.invW = 1.0f;
   if (residual && !onehot) ds = load_stat(S + a.G + 1 + rec.j);
   ScanCtx c = make_scan<DT>(a, b, rec.j, rec.mode, onehot, ts, ds, rec.dj, sm);
   const int nv = c.trow.nvec;
@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
       float w[P];
       if (n[i]) ls += scan_weights<DT>(c, v0 + i * kThreads + tid, n[i], rt[i], rd[i], sm, w);
     }
-    const double cs = block_sum_d(static_cast<double>(ls), sm);
+    const double cs = block_sum_fd(ls, sm);
     if (tid == 0) {
       a.dsum[static_cast<size_t>(b) * a.nchunk + ch] = cs;
       __threadfence();
@@ -1217,7 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 5) transform_kernel(const char* logi
     if (st.status == SEQ_OK)
       for (int e = threadIdx.x; e < st.n_list; e += kThreads) o[sm.list_tok[e]] = sm.list_ph[e];
   } else {
-    const float invW = static_cast<float>(1.0 / st.W);
+    const float invW = st.invW;
     const CutTest ct = cut_test(st.cut);
     for (int x = threadIdx.x; x < V; x += kThreads)
       o[x] = full_prob(load_elem<DT>(row.base, x), static_cast<uint32_t>(x), ct, st.m, P.cT, invW);

@@ -55,7 +55,7 @@ struct __align__(16) RowStat {
   int32_t path;
   int32_t argmax;  // greedy rows: argmax token
   float cT;        // the row's log2(e) / T (its sampling rule, for the draw)
-  int32_t pad;
+  float invW;      // PATH_FULL: (float)(1 / W), formed once per row (float64 is slow here)
 };
 static_assert(sizeof(RowStat) == 48, "RowStat layout");
 
@@ -100,6 +100,7 @@ struct __align__(16) Smem {
   int nfull;                         // PATH_STREAM: threads whose vectors need a full re-read
   int16_t full[kMaxFull];
   float red_f[kWarps];
+  float red_lo[kWarps];
   double red_d[kWarps];
   uint64_t red_u[kWarps];
   int red_i[kWarps];
@@ -205,12 +206,37 @@ __device__ __forceinline__ float block_max_f(float v, Smem& sm) {
   return r;
 }
 __device__ __forceinline__ double block_sum_d(double v, Smem& sm) {
+  // float64 adds are slow on this part: one thread adds the warps' partials
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_sum_f64(v);
   if (lane == 0) sm.red_d[warp] = v;
   __syncthreads();
-  double r = 0.0;
-  for (int w = 0; w < kWarps; ++w) r += sm.red_d[w];
+  if (threadIdx.x == 0) {
+    double r = 0.0;
+    for (int w = 0; w < kWarps; ++w) r += sm.red_d[w];
+    sm.b_f64[3] = r;
+  }
+  __syncthreads();
+  const double r = sm.b_f64[3];
+  __syncthreads();
+  return r;
+}
+// A block sum of float terms in double-float (float pipe only), returned as a double.
+__device__ __forceinline__ double block_sum_fd(float v, Smem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const df w = warp_sum_df(df_from(v));
+  if (lane == 0) {
+    sm.red_f[warp] = w.hi;
+    sm.red_lo[warp] = w.lo;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    df r = df_from(0.0f);
+    for (int k = 0; k < kWarps; ++k) r = df_add(r, {sm.red_f[k], sm.red_lo[k]});
+    sm.b_f64[3] = df_to_double(r);
+  }
+  __syncthreads();
+  const double r = sm.b_f64[3];
   __syncthreads();
   return r;
 }
@@ -364,7 +390,7 @@ __device__ __noinline__ double full_sum_kept(const Row row, float m, float cT, u
       s = t;
     }
   }
-  return block_sum_d(static_cast<double>(s), sm);
+  return block_sum_fd(s, sm);
 }
 
 // Warp segments: warp w owns the contiguous vectors [w L, (w + 1) L) of a row,
@@ -1317,13 +1343,16 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm) 
       st.cut = ck;
       st.W = full_sum_kept<DT>(row, m, P.cT, ck, sm);
     }
-    if (dtok >= 0) {
+  }
+  if (tid == 0) {                    // one thread forms the float64 quotients
+    st.invW = st.status == SEQ_OK ? static_cast<float>(1.0 / st.W) : 0.0f;
+    if (st.status == SEQ_OK && dtok >= 0) {
       const float z = load_elem<DT>(row.base, dtok);
       if (composite(fkey(z), static_cast<uint32_t>(dtok)) >= st.cut)
         st.p_tok = static_cast<float>(static_cast<double>(fast_exp2((z - m) * P.cT)) / st.W);
     }
+    sm.st = st;
   }
-  if (tid == 0) sm.st = st;
   __syncthreads();
 }
 
@@ -1459,6 +1488,7 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
     st.p_tok = 0.0f;
     st.n_list = 0;
     st.cT = P.cT;
+    st.invW = 0.0f;
     if (st.status == SEQ_OK) {
       float w[4];
       df s = df_from(0.0f);
