@@ -750,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
 // C(x) > u Z [wrblog §5, §6].  Z == 0 after a rejection falls back to the
 // draw from p, over the whole row, as the sequence epilogue did.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) draw_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) draw_kernel(const SampleArgs a) {  // 5 CTAs/SM: more loads in flight
   constexpr int P = Elem<DT>::kPer;
   constexpr int kVPT = 4;   // vectors per thread in a chunk (chunk_vecs == kVPT * kThreads)
   extern __shared__ __align__(16) unsigned char smem_raw[];
