@@ -18,6 +18,10 @@
  * and, in greedy mode, emits the longest argmax-matching prefix plus the
  * target's argmax at the first mismatch (or the bonus position)
  *                                           [wrblog §7.1; baisen §2, §6].
+ * Beyond that: lenient acceptance [magicnet §8], an end-of-sequence commit
+ * and per-sequence sampling rules [wrblog §14.3, §15], early-exit greedy
+ * verification, and greedy verification of draft trees [baisen §8;
+ * magicnet §7].
  *
  * Readings of points the sources leave open (the library and its tests use
  * exactly these):

@@ -127,6 +127,40 @@ def test_host_validation_before_any_launch(lib):
     for beta in (0.0, -1.0, 1.0000001, float("nan"), float("inf")):
         assert lcall(beta) == _lib.SPEC_ERR_INVALID_ARG, beta
     assert lcall(0.5, wsb=16) == _lib.SPEC_ERR_WORKSPACE     # a valid lenience reaches the later checks
+
+    exf = _lib.spec_verify_sample_ex
+    Pk = SamplingParams(1.0, 50, 1.0).c()
+
+    def xcall(lenience=1.0, eos=-1, tps=None, dps=None, kept=0, tp=P, V=64, nemit=None, wsb=1 << 30):
+        opt = _lib.spec_verify_options_t(lenience, eos, tps, dps, kept)
+        return exf(fake, fake, 0, fake, None, None, fake, fake, tp, tp, ctypes.byref(opt), 2, 3, V, fake, wsb,
+                   fake, fake, None, None, None, nemit, None)
+
+    assert xcall(eos=64) == _lib.SPEC_ERR_INVALID_ARG                   # eos outside [-1, vocab)
+    assert xcall(eos=-2) == _lib.SPEC_ERR_INVALID_ARG
+    assert xcall(lenience=0.0) == _lib.SPEC_ERR_INVALID_ARG
+    assert xcall(tps=fake + 2) == _lib.SPEC_ERR_MISALIGNED             # rule arrays: 4-byte aligned
+    assert xcall(nemit=fake + 1) == _lib.SPEC_ERR_MISALIGNED
+    assert xcall(tps=fake, kept=1) == _lib.SPEC_ERR_INVALID_ARG        # scalar rule breaks the promise
+    assert xcall(tps=fake, kept=1, tp=Pk, wsb=16) == _lib.SPEC_ERR_WORKSPACE
+    assert xcall(eos=5, wsb=16) == _lib.SPEC_ERR_WORKSPACE
+    need = _lib.spec_verify_workspace_size_ex(2, 3, 64, Pk, Pk, _lib.spec_verify_options_t(1.0, -1, fake, fake, 0))
+    kept_need = _lib.spec_verify_workspace_size_ex(2, 3, 64, Pk, Pk, _lib.spec_verify_options_t(1.0, -1, fake, fake, 1))
+    plain_need = _lib.spec_verify_workspace_size(2, 3, 64, Pk, Pk)
+    assert need > kept_need == plain_need                              # the promise drops the draw records
+
+    tree = _lib.spec_verify_greedy_tree
+
+    def tcall(tgt=fake, tok=fake, par=fake, nodes=None, N=4, ws=fake, wsb=1 << 30, path=None):
+        return tree(tgt, 0, tok, par, nodes, 2, N, 64, ws, wsb, fake, fake, path, None, None)
+
+    assert tcall(tok=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert tcall(par=None) == _lib.SPEC_ERR_INVALID_ARG
+    assert tcall(N=0) == _lib.SPEC_ERR_INVALID_ARG
+    assert tcall(par=fake + 2) == _lib.SPEC_ERR_MISALIGNED
+    assert tcall(path=fake + 1) == _lib.SPEC_ERR_MISALIGNED
+    assert tcall(wsb=8) == _lib.SPEC_ERR_WORKSPACE
+    assert _lib.spec_tree_workspace_size(2, 4) >= 2 * 4 + 2 * 4 * 8
     assert _lib.spec_transform_probs(fake, 0, 0, 64, P, fake, None, None) == _lib.SPEC_ERR_INVALID_ARG
     assert _lib.spec_transform_probs(fake + 2, 1, 1, 64, P, fake, None, None) == _lib.SPEC_ERR_MISALIGNED
 
