@@ -61,3 +61,57 @@ def test_ragged_mixed_full_batch_sampled():
     c = compare_sample(out, run_oracle_sample(w, seqs), w, seqs)
     assert c["n"] == len(seqs) and c["flagged"] + c["boundary"] <= 3, c
     assert (out.status.cpu() & 0xFF == 0).all()
+
+
+def test_serving_full_batch_lenient_and_per_sequence_rules():
+    """The serving workload through spec_verify_sample_lenient (beta 0.5) and through
+    spec_verify_sample_ex with the workload's rule given per sequence (kept-list
+    promise, as the benchmark runs it) and an end-of-sequence token: all 64 sequences."""
+    import oracle
+    w = make(3)
+    len_out = gpu_sample(w, lenience=0.5)
+    torch.cuda.synchronize()
+    c = compare_sample(len_out, run_oracle_sample(w, lenience=float(np.float32(0.5))), w)
+    assert c["n"] == 64 and c["flagged"] + c["boundary"] <= 3, c
+    eos = int(w.draft_tokens[0, 0])
+    ex = gpu_sample(w, eos_token=eos, target_rules=[w.target_params] * 64, draft_rules=[w.draft_params] * 64,
+                    kept_list_only=True)
+    torch.cuda.synchronize()
+    ref = run_oracle_sample(w, rules=[(w.target_params, w.draft_params)] * 64, eos_token=eos)
+    c = compare_sample(ex, ref, w)
+    assert c["n"] == 64 and c["flagged"] + c["boundary"] <= 3, c
+    nem = ex.num_emitted.cpu().numpy()
+    for b, r in enumerate(ref.seqs):
+        if r.accept_margin >= 1e-6 and not r.draft_ambiguous:
+            assert nem[b] == r.num_emitted, (b, nem[b], r.num_emitted)
+    st = ex.status.cpu().numpy()
+    for b, r in enumerate(ref.seqs):                 # the EOS flag where the oracle's block ends in it
+        if r.accept_margin >= 1e-6 and not r.draft_ambiguous and not r.status & oracle.SEQ_ERROR_MASK:
+            assert bool(st[b] & oracle.SEQ_FLAG_EOS) == bool(r.status & oracle.SEQ_FLAG_EOS), b
+
+
+def test_greedy_trees_full_batch_sampled():
+    """Draft trees over the greedy-at-scale rows (B=256, 9 nodes, V=152064 bf16), the
+    benchmark's tree recipe: 64 sequences recomputed by the oracle, bit-exact."""
+    import oracle
+    import speculative_decoding_verification_44_gb300 as sv
+    w = make(4)
+    B, N, V = w.B, w.G + 1, w.V
+    rng = np.random.default_rng(5000)
+    arg = w.target_logits.float().argmax(dim=-1).cpu().numpy()
+    tok = np.zeros((B, N), dtype=np.int32)
+    par = np.full((B, N), -1, dtype=np.int32)
+    for b in range(B):
+        for i in range(1, N):
+            par[b, i] = rng.integers(0, i)
+            tok[b, i] = arg[b, par[b, i]] if rng.random() < 0.8 else rng.integers(0, V)
+    out, path = sv.verify_greedy_tree(w.target_logits, torch.from_numpy(tok).cuda(), torch.from_numpy(par).cuda())
+    torch.cuda.synchronize()
+    seqs = list(range(0, 256, 4))
+    tl = w.target_logits[seqs].float().double().cpu().numpy()
+    ref = oracle.verify_greedy_tree(tl, tok[seqs], par[seqs])
+    np.testing.assert_array_equal(out.tokens.cpu().numpy()[seqs], ref.tokens)
+    np.testing.assert_array_equal(out.num_accepted.cpu().numpy()[seqs], ref.num_accepted)
+    P = path.cpu().numpy()[seqs]
+    for k, r in enumerate(ref.seqs):
+        assert list(P[k, : r.num_accepted + 1]) == r.path
