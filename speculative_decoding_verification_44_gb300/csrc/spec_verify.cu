@@ -474,8 +474,9 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   const RowStat* S = a.stats + static_cast<size_t>(b) * slots;
   const size_t tokb = static_cast<size_t>(b) * a.G;
 
-  // 1. gather, in parallel, every row's status and draft-token probability,
-  //    the draft tokens and the uniforms (one round trip for the whole CTA)
+  // 1. gather, in parallel, every row's status and draft-token probability
+  //    (one round trip for the whole CTA; the draft tokens and uniforms were
+  //    copied into shared memory while the row streamed)
   SmemEpi& E = sm.u.e;
   for (int t = tid; t < slots; t += kThreads) {
     const bool used = t <= gb || (t > a.G && !onehot && t - a.G - 1 < gb);
@@ -487,11 +488,6 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     if (used) rs = load_stat(S + t);
     E.rs[t] = rs;
   }
-  for (int t = tid; t < gb; t += kThreads) {
-    E.dtok[t] = a.tokens[tokb + t];
-    E.uacc[t] = a.u_acc[tokb + t];
-  }
-  if (tid == kThreads - 1) sm.b_f32[0] = a.u_samp[b];
   if (EX && tid == kThreads - 2) {              // per-sequence rules the sequence uses
     bool ok = true;
     if (a.tps) ok = rule_ok(a.tps[b], a.kept_only != 0, a.V);
@@ -503,11 +499,11 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   if (warp == 0) {
     bool bad_tok = false, bad_u = false;
     for (int i = lane; i < gb; i += 32) {
-      bad_tok |= E.dtok[i] < 0 || E.dtok[i] >= a.V;
-      bad_u |= !(E.uacc[i] >= 0.0f && E.uacc[i] < 1.0f);
+      bad_tok |= sm.seq_tok[i] < 0 || sm.seq_tok[i] >= a.V;
+      bad_u |= !(sm.seq_u[i] >= 0.0f && sm.seq_u[i] < 1.0f);
     }
     if (lane == 0) {
-      const float us = sm.b_f32[0];
+      const float us = sm.seq_us;
       bad_u |= !(us >= 0.0f && us < 1.0f);
     }
     int status = SEQ_OK;
@@ -543,7 +539,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
           float ai;
           if (q > 0.0f) ai = fminf(1.0f, p / (a.beta * q));   // [magicnet §8]; beta = 1: p / q
           else { ai = p > 0.0f ? 1.0f : 0.0f; zq = true; }
-          rej = !(E.uacc[i] < ai);
+          rej = !(sm.seq_u[i] < ai);
           if (a.out_aprob) a.out_aprob[tokb + i] = ai;
         } else if (i < a.G && a.out_aprob) {
           a.out_aprob[tokb + i] = -1.0f;
@@ -566,7 +562,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     int cut = -1;
     if (EX && status == SEQ_OK && a.eos >= 0) {
       for (int base = 0; base < j && cut < 0; base += 32) {
-        const unsigned m = __ballot_sync(kFull, base + lane < j && E.dtok[base + lane] == a.eos);
+        const unsigned m = __ballot_sync(kFull, base + lane < j && sm.seq_tok[base + lane] == a.eos);
         if (m) cut = base + __ffs(m) - 1;
       }
     }
@@ -590,7 +586,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   if (EX && cut >= 0) {
     // an accepted draft is the end-of-sequence token: the committed block ends
     // there, with no replacement or bonus token (so no draw)
-    for (int t = tid; t <= a.G; t += kThreads) a.out_tokens[ob + t] = t <= cut ? E.dtok[t] : -1;
+    for (int t = tid; t <= a.G; t += kThreads) a.out_tokens[ob + t] = t <= cut ? sm.seq_tok[t] : -1;
     if (tid == 0) {
       a.out_nacc[b] = cut + 1;
       if (a.out_nemit) a.out_nemit[b] = cut + 1;
@@ -608,8 +604,8 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   RowStat ds;
   ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f; ds.invW = 1.0f;
   if (residual && !onehot) ds = E.rs[a.G + 1 + r];
-  const int dj = residual ? E.dtok[j] : -1;
-  const float uf = sm.b_f32[0];
+  const int dj = residual ? sm.seq_tok[j] : -1;
+  const float uf = sm.seq_us;
   double Z_resid = -1.0;
   int tok = -1;
   bool deferred = false;
@@ -637,7 +633,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   // 4. outputs: accepted drafts, the drawn token, then -1
   for (int t = tid; t <= a.G; t += kThreads) {
     int v = -1;
-    if (t < j) v = E.dtok[t];
+    if (t < j) v = sm.seq_tok[t];
     else if (t == j) v = tok;
     if (t != j || !deferred) a.out_tokens[ob + t] = v;
   }
@@ -686,6 +682,17 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
     rule_valid = sm.b_i32[6] != 0;
     if (rule_valid) P = sm.rowp;
   }
+  {
+    // the sequence's draft tokens and uniforms, for the epilogue: copied while
+    // the row streams, waited for only before this CTA counts its row in
+    const size_t tb = static_cast<size_t>(b) * a.G;
+    if (static_cast<int>(threadIdx.x) < gb) {
+      cp_async4(&sm.seq_tok[threadIdx.x], a.tokens + tb + threadIdx.x);
+      cp_async4(&sm.seq_u[threadIdx.x], a.u_acc + tb + threadIdx.x);
+    }
+    if (threadIdx.x == kThreads - 1) cp_async4(&sm.seq_us, a.u_samp + b);
+    cp_async_commit();
+  }
   const Row row = seq_row<DT>(a, b, i, is_draft);
   int dtok = -1;
   if (i < gb) {
@@ -719,21 +726,28 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
       le.p_lo = sm.list_pl[threadIdx.x];
       le.token = sm.list_tok[threadIdx.x];
       le.pad = 0;
+      const int4* lt = reinterpret_cast<const int4*>(sm.list_tok);   // padded with INT_MAX
       int rank = 0;
-      for (int f = 0; f < n; ++f) rank += sm.list_tok[f] < le.token ? 1 : 0;
+#pragma unroll 4
+      for (int f = 0; f < ((n + 3) >> 2); ++f) {
+        const int4 t = lt[f];
+        rank += (t.x < le.token ? 1 : 0) + (t.y < le.token ? 1 : 0) + (t.z < le.token ? 1 : 0) +
+                (t.w < le.token ? 1 : 0);
+      }
       dst[rank] = le;
     }
   }
-  __threadfence();
+  cp_async_wait<0>();
   __syncthreads();
   if (threadIdx.x == 0) {
+    // release (this CTA's summary and list, ordered before by the barrier) and
+    // acquire (the last arriver then sees every other row's) in one atomic
     const unsigned rows_b = static_cast<unsigned>((gb + 1) + (onehot ? 0 : gb));
-    const unsigned prev = atomicAdd(&a.counters[b], 1u);
+    const unsigned prev = atom_add_acq_rel_gpu(&a.counters[b], 1u);
     sm.b_i32[7] = (prev + 1u == rows_b) ? 1 : 0;
   }
   __syncthreads();
   if (!sm.b_i32[7]) return;
-  __threadfence();
   sample_epilogue<DT, EX>(a, b, gb, onehot, sm);
   __syncthreads();
   if (threadIdx.x == 0) a.counters[b] = 0u;   // leave the workspace reusable

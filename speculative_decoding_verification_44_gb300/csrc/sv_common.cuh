@@ -131,6 +131,21 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// Asynchronous 4-byte global -> shared copy (both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(s), "l"(gmem) : "memory");
+}
+
+// Arrival on a counter in global memory with release-acquire semantics at GPU
+// scope (one thread of the CTA, after a barrier): writes the CTA made before
+// the barrier are visible to whoever later reads the count, and the thread
+// that reads the final count sees every earlier arriver's writes.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 // Re-read load (second pass over a row that should still sit in L2).
 __device__ __forceinline__ uint4 ld_reread(const void* p) {

@@ -80,8 +80,6 @@ struct __align__(16) SmemEpi {
   double wtot[kWarps];               // per-warp segment totals of the block scan
   double csum[kWarps][kScanChunks];  // per-chunk totals of the block scan
   RowStat rs[2 * kMaxGamma + 1];     // the sequence's row summaries
-  int32_t dtok[kMaxGamma];
-  float uacc[kMaxGamma];
 };
 struct __align__(16) Smem {
   union {
@@ -90,10 +88,10 @@ struct __align__(16) Smem {
     uint4 ring[kRing][kThreads];     // PATH_STREAM pass 1: each thread's cp.async ring of vectors
   } u;
   uint32_t khist[2][256];            // PATH_STREAM: digit histograms of the per-thread maxima
-  uint64_t cand[kCandCap];           // PATH_STREAM: candidates (composites >= the lower bound)
-  uint64_t topk[kSmallK];
+  alignas(16) uint64_t cand[kCandCap];   // PATH_STREAM: candidates (composites >= the lower bound)
+  alignas(16) uint64_t topk[kSmallK];
   uint64_t sorted[kSmallK];          // PATH_STREAM: top-k in descending order
-  int32_t list_tok[kListCap];
+  alignas(16) int32_t list_tok[kListCap];   // padded with INT_MAX to a multiple of 4 entries
   float list_ph[kListCap], list_pl[kListCap];   // kept probabilities, double-float
   int nw[kWarps];
   int ncand;
@@ -112,6 +110,11 @@ struct __align__(16) Smem {
   int b_i32[10];
   RowParams rowp;                    // a row's sampling rule when it is given per sequence
   RowStat st;
+  // the sequence's draft tokens and uniforms, copied in while the row streams
+  // (read by the sequence epilogue)
+  int32_t seq_tok[kMaxGamma];
+  float seq_u[kMaxGamma];
+  float seq_us;
 };
 
 // ------------------------------------------------------------------ digit walks
@@ -1460,8 +1463,14 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
   static_assert(kListCap <= kThreads, "one thread per candidate");
   if (tid < nsrc) {
     const uint64_t c = src[tid];
+    const ulonglong2* src2 = reinterpret_cast<const ulonglong2*>(src);   // two composites per load
     int rank = 0;
-    for (int j = 0; j < nsrc; ++j) rank += src[j] > c ? 1 : 0;
+#pragma unroll 2
+    for (int j = 0; j < (nsrc >> 1); ++j) {
+      const ulonglong2 e = src2[j];
+      rank += (e.x > c ? 1 : 0) + (e.y > c ? 1 : 0);
+    }
+    if (nsrc & 1) rank += src[nsrc - 1] > c ? 1 : 0;
     if (rank < k) sm.sorted[rank] = c;
   }
   __syncthreads();
@@ -1540,6 +1549,8 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
           sm.list_ph[pos] = hi;
           sm.list_pl[pos] = pl - (hi - ph);
           if (tok == dtok) { hit = lane; ptok = hi; }
+        } else if (pos < ((n_keep + 3) & ~3)) {
+          sm.list_tok[pos] = 0x7fffffff;                        // pad for the 4-wide rank loop
         }
       }
       const unsigned hb = __ballot_sync(kFull, hit >= 0);
