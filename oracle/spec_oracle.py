@@ -99,6 +99,13 @@ Sources:
   [baisen]   "投机采样 / 投机解码（Speculative Decoding）" (baisen.site)
   [magicnet] "投机解码到底能加速多少：把接受率、草稿成本与墙钟收益算清楚"
              (magicnetworld.com)
+* R16 early-exit sampling (the sampling counterpart of R11): positions are
+      read in order -- target row i, then draft row i -- and the scan stops at
+      the first position whose rows fail or whose draft is rejected, the
+      sequential verifier of [wrblog §6].  Rows after that position are never
+      read, so they cannot fail the sequence, and their acceptance
+      probabilities are reported as -1.  On inputs whose every row is valid
+      the emitted tokens, counts, flags and residual mass equal R1-R10's.
 """
 from __future__ import annotations
 
@@ -313,12 +320,15 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
                            target_params: tuple[float, int, float],
                            draft_params: tuple[float, int, float],
                            gamma_b: int, gamma_max: int, one_hot: bool,
-                           keep_cdf: bool = False, lenience: float = 1.0) -> SeqResult:
+                           keep_cdf: bool = False, lenience: float = 1.0,
+                           early_exit: bool = False) -> SeqResult:
     """Verify one sequence in sampling mode  [wrblog §6; rainlin §1].
 
     target: (gamma_max+1, V) float64 logits; rows 0..gamma_b are used.
     draft:  (gamma_max, V) float64 logits, rows 0..gamma_b-1 used; ignored when one_hot.
     tokens: (gamma_max,) draft tokens d_1..d_gamma (0-based positions).
+    early_exit: read the rows position by position and stop at the first
+    failed row or rejected draft (R16).
     """
     V = target.shape[1]
     if not 0.0 < lenience <= 1.0:                                   # [magicnet §8]: 0 < beta <= 1
@@ -334,33 +344,66 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
         return _error_result(SEQ_BAD_PARAMS, gamma_max)
 
     # Step 1: p_1..p_{gamma+1} and q_1..q_gamma, each with its own transform [wrblog §7.2].
-    p_rows, q_rows = [], []
-    for i in range(gamma_b + 1):
-        p_i = transform_row(target[i], *target_params)
-        if p_i.status != SEQ_OK:
-            return _error_result(p_i.status, gamma_max)
-        p_rows.append(p_i)
-        if i < gamma_b:
-            q_i = one_hot_row(V, d[i]) if one_hot else transform_row(draft[i], *draft_params)
-            if q_i.status != SEQ_OK:
-                return _error_result(q_i.status, gamma_max)
-            q_rows.append(q_i)
-
     # Step 2: a_i for every draft position; the scan stops at the first rejection [wrblog §6].
+    p_rows, q_rows = [], []
     a = np.full(gamma_max, -1.0)
     zero_q = np.zeros(gamma_max, dtype=bool)
-    for i in range(gamma_b):
-        a[i], zero_q[i] = acceptance_probability(p_rows[i].probs[d[i]], q_rows[i].probs[d[i]], lenience)
     status = SEQ_OK
     rejected_at = None
     accept_margin = np.inf
-    for i in range(gamma_b):
+
+    def draft_row(i):
+        return one_hot_row(V, d[i]) if one_hot else transform_row(draft[i], *draft_params)
+
+    def judge(i) -> bool:
+        """a_i, the flags and the margin for position i; True if d_i is rejected."""
+        nonlocal status, accept_margin
+        a[i], zero_q[i] = acceptance_probability(p_rows[i].probs[d[i]], q_rows[i].probs[d[i]], lenience)
         if zero_q[i]:
             status |= SEQ_FLAG_ZERO_Q
         accept_margin = min(accept_margin, abs(float(u_accept[i]) - a[i]))
-        if not float(u_accept[i]) < a[i]:          # R4: strict comparison
-            rejected_at = i
-            break
+        return not float(u_accept[i]) < a[i]       # R4: strict comparison
+
+    if early_exit:
+        # R16: target row i, then draft row i, then the decision at i
+        for i in range(gamma_b + 1):
+            p_i = transform_row(target[i], *target_params)
+            if p_i.status != SEQ_OK:
+                res = _error_result(p_i.status, gamma_max)
+                res.rows_read = i + 1
+                return res
+            p_rows.append(p_i)
+            if i == gamma_b:
+                break
+            q_i = draft_row(i)
+            if q_i.status != SEQ_OK:
+                res = _error_result(q_i.status, gamma_max)
+                res.rows_read = i + 1
+                return res
+            q_rows.append(q_i)
+            if judge(i):
+                rejected_at = i
+                break
+    else:
+        for i in range(gamma_b + 1):
+            p_i = transform_row(target[i], *target_params)
+            if p_i.status != SEQ_OK:
+                return _error_result(p_i.status, gamma_max)
+            p_rows.append(p_i)
+            if i < gamma_b:
+                q_i = draft_row(i)
+                if q_i.status != SEQ_OK:
+                    return _error_result(q_i.status, gamma_max)
+                q_rows.append(q_i)
+        for i in range(gamma_b):                    # a_i for every position, then the scan
+            a[i], zero_q[i] = acceptance_probability(p_rows[i].probs[d[i]], q_rows[i].probs[d[i]], lenience)
+        for i in range(gamma_b):
+            if zero_q[i]:
+                status |= SEQ_FLAG_ZERO_Q
+            accept_margin = min(accept_margin, abs(float(u_accept[i]) - a[i]))
+            if not float(u_accept[i]) < a[i]:      # R4: strict comparison
+                rejected_at = i
+                break
 
     # Step 3: residual at the rejected position, else the bonus from p_{gamma+1}.
     residual_Z = -1.0
@@ -389,7 +432,8 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
     sample_amb = np.unique(np.concatenate([r.ambiguous for r in sample_rows]))
     res = SeqResult(out, n_acc, status, a, residual_Z, accept_margin, top_p_margin,
                     draft_ambiguous=draft_amb, sample_ambiguous=sample_amb,
-                    sample_u=float(u_sample), sample_lo=lo, sample_hi=hi, num_emitted=n_acc + 1)
+                    sample_u=float(u_sample), sample_lo=lo, sample_hi=hi, num_emitted=n_acc + 1,
+                    rows_read=n_acc + 1 if early_exit else -1)
     if keep_cdf:
         C = np.cumsum(w)
         res.sample_cdf = C / C[-1]
@@ -559,7 +603,7 @@ def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarr
                   gamma_per_seq: np.ndarray | None = None, one_hot: np.ndarray | None = None,
                   seqs: list[int] | None = None, keep_cdf: bool = False,
                   lenience: float = 1.0, params_per_seq: list | None = None,
-                  eos_token: int = -1) -> BatchResult:
+                  eos_token: int = -1, early_exit: bool = False) -> BatchResult:
     """Batched sampling verification, one sequence at a time.
 
     target (B, gamma_max+1, V), draft (B, gamma_max, V) or None (all one-hot),
@@ -568,6 +612,8 @@ def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarr
     ``params_per_seq``: per sequence b, the pair (target rule, draft rule)
     replacing target_params / draft_params (R13).  ``eos_token`` >= 0 cuts
     each committed block after its first end-of-sequence token (R14).
+    ``early_exit`` reads each sequence's rows in position order and stops at
+    the first failed row or rejected draft (R16).
     """
     B, G1, _ = target.shape
     gamma_max = G1 - 1
@@ -579,7 +625,7 @@ def verify_sample(target: np.ndarray, draft: np.ndarray | None, tokens: np.ndarr
         tp, dp = (target_params, draft_params) if params_per_seq is None else params_per_seq[b]
         res = verify_sample_sequence(target[b], None if oh else draft[b], tokens[b],
                                      u_accept[b], float(u_sample[b]), tp, dp, g, gamma_max, oh,
-                                     keep_cdf, lenience)
+                                     keep_cdf, lenience, early_exit)
         out.append(commit_at_eos(res, eos_token))
     return _collect(out)
 
