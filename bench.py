@@ -67,7 +67,8 @@ def parse():
                     help="workload to time (default: the serving workload); the others exist for "
                          "profiling the full-row, small-vocabulary and greedy paths")
     ap.add_argument("--early-exit", action="store_true",
-                    help="greedy workload only: spec_verify_greedy_early instead of spec_verify_greedy")
+                    help="greedy: spec_verify_greedy_early; sampling: spec_verify_sample_ex with early_exit "
+                         "(positions in order, rows after each sequence's stop skipped)")
     return ap.parse_args()
 
 
@@ -247,6 +248,8 @@ def variant_of(args) -> str:
         parts.append(f"eos {args.eos}")
     if args.per_seq_rules:
         parts.append("per-sequence rules")
+    if getattr(args, "early_exit", False):
+        parts.append("early exit")
     return f" ({', '.join(parts)})" if parts else ""
 
 
@@ -421,6 +424,8 @@ def main():
     # rule for every sequence; promised kept-list when that rule is on the kept-list path)
     kept = not full_target and 1 <= w0.draft_params.top_k <= 128
     opts = dict(lenience=args.lenience, eos_token=args.eos)
+    if args.early_exit:
+        opts["early_exit"] = True
     if args.per_seq_rules:
         opts.update(target_rules=[w0.target_params] * B, draft_rules=[w0.draft_params] * B, kept_list_only=kept)
         if not kept:
@@ -502,6 +507,18 @@ def main():
     # average launch duration over the timed region: the graph replay's K back-to-back
     # launches (events around one eager launch also hold its launch latency)
     avg_launch_s = (total_ms / K if graph is not None else statistics.mean(launch_ms)) / 1e3
+    if args.early_exit:
+        # early exit: the bytes a sequential verifier needs -- target rows 0..j and draft
+        # rows 0..min(j, gamma_b - 1) of each sequence -- averaged over the rotation sets
+        needed = []
+        for r, w in enumerate(sets):
+            j = outs[r].num_accepted.long().clamp(min=0)
+            gb = w.gamma_per_seq.long() if w.gamma_per_seq is not None else torch.full_like(j, G)
+            model = (torch.ones_like(j, dtype=torch.bool) if w.draft_is_onehot is None
+                     else w.draft_is_onehot == 0) if w.draft_logits is not None else torch.zeros_like(j, dtype=torch.bool)
+            rows = (j + 1) + torch.where(model, torch.minimum(j + 1, gb), torch.zeros_like(j))
+            needed.append(int(rows.sum().item()) * V * esize + io_bytes)
+        alg_bytes = statistics.mean(needed)
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = profile_traffic() if wid == WID else None
     dname = "bf16" if esize == 2 else "f32"
@@ -534,7 +551,7 @@ def main():
             sv.verify_sample(dbuf["target_logits"], dbuf["draft_logits"], dbuf["draft_tokens"],
                              dbuf["u_accept"], dbuf["u_sample"], w.target_params, w.draft_params,
                              gamma_per_seq=dbuf.get("gamma_per_seq"), draft_is_onehot=dbuf.get("draft_is_onehot"),
-                             workspace=ws, out=dout)
+                             workspace=ws, out=dout, **({"early_exit": True} if args.early_exit else {}))
             hout["tokens"].copy_(dout.tokens, non_blocking=True)
             hout["num_accepted"].copy_(dout.num_accepted, non_blocking=True)
             hout["status"].copy_(dout.status, non_blocking=True)
@@ -568,7 +585,7 @@ def main():
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dname, "data": "synthetic",
             "config": {"workload": workloads.NAMES[wid], "B": B, "gamma": G, "V": V,
-                       **params_of(w0), "batches_per_gpu": 1,
+                       **params_of(w0), "batches_per_gpu": 1, "early_exit": bool(args.early_exit),
                        "l2": f"inputs rotate over {ROTATE} independent sets of {logits_bytes / 1e6:.1f} MB "
                              f"(each larger than the {L2_BYTES / 2**20:.0f} MiB L2)",
                        "parallelism": f"replicas x{world} (one batch per GPU, no data-path collective)",

@@ -242,13 +242,25 @@ SPEC_API spec_status_t spec_verify_sample_lenient(const void* target_logits, con
  *                    path; the launch then keeps the plain call's occupancy and
  *                    workspace.  A per-sequence rule outside the promise fails
  *                    its sequence with SPEC_SEQ_BAD_PARAMS.  The scalar rules
- *                    must keep it too.  Ignored without per-sequence rules. */
+ *                    must keep it too.  Ignored without per-sequence rules.
+ * early_exit         non-zero: the sequential verifier of [wrblog §6] -- positions
+ *                    are taken in order (target row i, draft row i, the decision
+ *                    at i) and a sequence stops at its first failed row or
+ *                    rejected draft.  The grid runs position-major, and a row
+ *                    CTA that starts after an earlier position of its sequence
+ *                    has stopped skips its row, so a launch of several waves
+ *                    reads fewer rows.  Results: the same as without it on
+ *                    valid rows; a NaN / +inf / all -inf row after the stop
+ *                    does not fail the sequence, and out_accept_prob holds a_i
+ *                    up to the stop and -1 after it.  Which rows are skipped
+ *                    depends on timing, the results do not. */
 typedef struct {
     float lenience;
     int32_t eos_token;
     const spec_sampling_params_t* target_params_seq;
     const spec_sampling_params_t* draft_params_seq;
     int32_t kept_list_only;
+    int32_t early_exit;
 } spec_verify_options_t;
 
 /* Bytes of workspace spec_verify_sample_ex needs with these options (per-

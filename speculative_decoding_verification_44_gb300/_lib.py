@@ -49,7 +49,7 @@ class spec_sampling_params_t(ctypes.Structure):
 class spec_verify_options_t(ctypes.Structure):
     _fields_ = [("lenience", ctypes.c_float), ("eos_token", ctypes.c_int32),
                 ("target_params_seq", ctypes.c_void_p), ("draft_params_seq", ctypes.c_void_p),
-                ("kept_list_only", ctypes.c_int32)]
+                ("kept_list_only", ctypes.c_int32), ("early_exit", ctypes.c_int32)]
 
 
 class SpecError(RuntimeError):

@@ -103,24 +103,27 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
                   workspace: torch.Tensor | None = None, out: VerifyOutput | None = None,
                   stream: torch.cuda.Stream | None = None,
                   lenience: float | None = None, eos_token: int | None = None,
-                  target_rules=None, draft_rules=None, kept_list_only: bool = False) -> VerifyOutput:
+                  target_rules=None, draft_rules=None, kept_list_only: bool = False,
+                  early_exit: bool = False) -> VerifyOutput:
     """spec_verify_sample on torch tensors; spec_verify_sample_lenient when only
-    ``lenience`` is given; spec_verify_sample_ex when ``eos_token`` or per-sequence
-    rules are given.
+    ``lenience`` is given; spec_verify_sample_ex when ``eos_token``, per-sequence
+    rules or ``early_exit`` are given.
 
     target_logits [B, G+1, V] and draft_logits [B, G, V] (or None: all one-hot) of
     bfloat16 / float32; draft_tokens [B, G] int32; u_accept [B, G] and u_sample [B]
     float32; gamma_per_seq [B] int32; draft_is_onehot [B] uint8; lenience in (0, 1];
     target_rules / draft_rules: per-sequence rules, a list of SamplingParams or a
     tensor from rules_tensor() (the scalar ``target`` / ``draft`` then only size the call);
-    kept_list_only: the promise that every per-sequence rule has 1 <= top_k <= 128.
+    kept_list_only: the promise that every per-sequence rule has 1 <= top_k <= 128;
+    early_exit: positions in order, each sequence stopping at its first failed row
+    or rejected draft (rows after it may be skipped).
     """
     B, G1, V = target_logits.shape
     G = G1 - 1
     if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
         raise TypeError("target and draft logits must share a dtype")
     dev = target_logits.device
-    ex = eos_token is not None or target_rules is not None or draft_rules is not None
+    ex = eos_token is not None or target_rules is not None or draft_rules is not None or early_exit
     if isinstance(target_rules, (list, tuple)):
         target_rules = rules_tensor(target_rules, dev)
     if isinstance(draft_rules, (list, tuple)):
@@ -142,7 +145,8 @@ def verify_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor | None
     if ex:
         opt = _lib.spec_verify_options_t(1.0 if lenience is None else float(lenience),
                                          -1 if eos_token is None else int(eos_token),
-                                         _ptr(target_rules), _ptr(draft_rules), int(kept_list_only))
+                                         _ptr(target_rules), _ptr(draft_rules), int(kept_list_only),
+                                         int(bool(early_exit)))
         _lib.check("spec_verify_sample_ex",
                    _lib.spec_verify_sample_ex(*head, ctypes.byref(opt), *tail[:-1], _ptr(out.num_emitted), tail[-1]))
     elif lenience is None:
@@ -249,7 +253,8 @@ class BoundSample:
     def __init__(self, target_logits, draft_logits, draft_tokens, u_accept, u_sample,
                  target: SamplingParams, draft: SamplingParams, gamma_per_seq=None,
                  draft_is_onehot=None, workspace=None, out=None, stream=None, lenience=None,
-                 eos_token=None, target_rules=None, draft_rules=None, kept_list_only=False):
+                 eos_token=None, target_rules=None, draft_rules=None, kept_list_only=False,
+                 early_exit=False):
         B, G1, V = target_logits.shape
         G = G1 - 1
         dev = target_logits.device
@@ -260,7 +265,7 @@ class BoundSample:
         if isinstance(draft_rules, (list, tuple)):
             draft_rules = rules_tensor(draft_rules, dev)
         per = target_rules is not None or draft_rules is not None
-        ex = per or eos_token is not None
+        ex = per or eos_token is not None or bool(early_exit)
         self.workspace = workspace if workspace is not None else new_workspace(
             workspace_size(B, G, V, target, draft, per_sequence=per, kept_list_only=kept_list_only), dev)
         self.out = out if out is not None else alloc_outputs(B, G, dev)
@@ -278,7 +283,8 @@ class BoundSample:
         if ex:
             self._opt = _lib.spec_verify_options_t(1.0 if lenience is None else float(lenience),
                                                    -1 if eos_token is None else int(eos_token),
-                                                   _ptr(target_rules), _ptr(draft_rules), int(kept_list_only))
+                                                   _ptr(target_rules), _ptr(draft_rules), int(kept_list_only),
+                                                   int(bool(early_exit)))
             self._fn, self._name = lib.spec_verify_sample_ex, "spec_verify_sample_ex"
             self._args = (*head, ctypes.byref(self._opt), *tail, _ptr(o.num_emitted), _stream(stream))
         elif lenience is not None:

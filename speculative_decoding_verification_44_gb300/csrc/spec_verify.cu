@@ -82,6 +82,10 @@ struct SampleArgs {
   int nchunk;           // chunks per row
   uint32_t* dcount;     // [B] chunk CTAs finished (self-cleaning)
   struct DrawRec* drec; // [B]
+  // early exit (spec_verify_sample_ex): position-major grid, stop marks
+  int early;
+  uint32_t* stop_enc;          // [B] G + 1 - (earliest position known to stop), 0 = none (self-cleaning)
+  unsigned long long* pairx;   // [B][G] exchange of a position's two draft-token probabilities (self-cleaning)
   double* dsum;         // [B][nchunk] weight sum per chunk
 };
 
@@ -510,7 +514,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     if (__any_sync(kFull, bad_tok)) status = SEQ_BAD_TOKEN;
     else if (__any_sync(kFull, bad_u)) status = SEQ_BAD_UNIFORM;
     else if (EX && !sm.b_i32[8]) status = SEQ_BAD_PARAMS;
-    else {
+    else if (!(EX && a.early)) {
       // rows in order: target 0, draft 0, target 1, draft 1, ..., target gb
       const int norder = 2 * gb + 1;
       for (int base = 0; base < norder && status == SEQ_OK; base += 32) {
@@ -529,7 +533,45 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     // 2. a_i = min(1, p_i(d_i) / q_i(d_i)); accept iff u_i < a_i; stop at the
     //    first rejection -- in the same warp pass, once the status is clean
     int j = gb, flags = 0;
-    if (status == SEQ_OK) {
+    if (EX && a.early && status == SEQ_OK) {
+      // early exit: position by position -- target row i, draft row i, the
+      // decision at i -- up to the first failed row or rejected draft; rows
+      // after it may not have been read and are ignored
+      const auto a_of = [&](int i, bool& zq) {
+        const float p = E.rs[i].p_tok;
+        const float q = onehot ? 1.0f : E.rs[a.G + 1 + i].p_tok;
+        zq = !(q > 0.0f);
+        return q > 0.0f ? fminf(1.0f, p / (a.beta * q)) : (p > 0.0f ? 1.0f : 0.0f);
+      };
+      bool done = false;
+      for (int base = 0; base <= gb && !done; base += 32) {
+        const int i = base + lane;
+        int st = SEQ_OK;
+        bool rej = false, zq = false;
+        if (i <= gb) {
+          st = E.rs[i].status;
+          if (st == SEQ_OK && i < gb && !onehot) st = E.rs[a.G + 1 + i].status;
+          if (st == SEQ_OK && i < gb) rej = !(sm.seq_u[i] < a_of(i, zq));
+        }
+        const unsigned ev = __ballot_sync(kFull, i <= gb && (st != SEQ_OK || rej));
+        const unsigned zm = __ballot_sync(kFull, zq);
+        const int f = ev ? __ffs(ev) - 1 : 31;
+        const unsigned upto = (f == 31) ? kFull : ((2u << f) - 1u);
+        if (zm & upto) flags |= SEQ_FLAG_ZERO_Q;
+        if (ev) {
+          const int fst = __shfl_sync(kFull, st, f);
+          if (fst != SEQ_OK) status = fst;
+          else j = base + f;
+          done = true;
+        }
+      }
+      if (status == SEQ_OK && a.out_aprob) {
+        for (int i = lane; i < a.G; i += 32) {           // a_i up to the stop, -1 after it
+          bool zq;
+          a.out_aprob[tokb + i] = (i < gb && i <= j) ? a_of(i, zq) : -1.0f;
+        }
+      }
+    } else if (status == SEQ_OK) {
       for (int base = 0; base < a.G; base += 32) {
         const int i = base + lane;
         bool rej = false, zq = false;
@@ -648,15 +690,57 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
   }
 }
 
+// Early exit: the second of position i's two rows to finish (the target row
+// alone for a one-hot draft) decides position i exactly as the epilogue will
+// -- a_i = min(1, p / (beta q)), rejected iff !(u_i < a_i) -- and marks the
+// sequence stopped at i when d_i is rejected or a row of position i failed or
+// was not read.  Rows of later positions that start after the mark skip
+// their row.  The two rows meet in one 64-bit exchange word per position:
+// bit 63 present, bit 62 failed or not read, low 32 bits the row's
+// probability of d_i.  Thread 0, after the row summary is final.
+__device__ void early_mark(const SampleArgs& a, int b, int i, bool is_draft, bool onehot, bool skipped,
+                           const Smem& sm) {
+  const RowStat& st = sm.st;
+  const bool bad = skipped || st.status != SEQ_OK;
+  const unsigned long long mine = (1ull << 63) | (bad ? (1ull << 62) : 0ull) | __float_as_uint(st.p_tok);
+  unsigned long long other = (1ull << 63) | __float_as_uint(1.0f);   // one-hot draft: q(d_i) = 1
+  if (!onehot) {
+    unsigned long long* w = a.pairx + static_cast<size_t>(b) * a.G + i;
+    other = atomicExch(w, mine);
+    if (other == 0ull) return;        // the other row of position i decides
+    *w = 0ull;                        // both rows are in: leave the workspace zero
+  }
+  bool stop = bad || ((other >> 62) & 1ull);
+  if (!stop) {
+    const float p = is_draft ? __uint_as_float(static_cast<unsigned>(other)) : st.p_tok;
+    const float q = is_draft ? st.p_tok : __uint_as_float(static_cast<unsigned>(other));
+    float ai;
+    if (q > 0.0f) ai = fminf(1.0f, p / (a.beta * q));
+    else ai = p > 0.0f ? 1.0f : 0.0f;
+    stop = !(sm.seq_u[i] < ai);
+  }
+  if (stop) atomicMax(a.stop_enc + b, static_cast<unsigned>(a.G + 1 - i));
+}
+
 // EX: the spec_verify_sample_ex features (per-sequence rules, end-of-sequence
-// commit, emitted counts) are compiled in; the plain instantiation omits them.
+// commit, emitted counts, early exit) are compiled in; the plain instantiation
+// omits them.
 template <int DT, bool EX>
 __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int slots = 2 * a.G + 1;
-  const int b = blockIdx.x / slots;
-  const int slot = blockIdx.x - b * slots;
+  int b, slot;
+  if (EX && a.early) {
+    // position-major: the target and draft rows of position i for every
+    // sequence, then position i + 1 (the draft "row" of position G is empty)
+    const int i2 = blockIdx.x / (2 * a.B), r2 = blockIdx.x - i2 * 2 * a.B;
+    b = r2 >> 1;
+    slot = (r2 & 1) ? a.G + 1 + i2 : i2;
+  } else {
+    b = blockIdx.x / slots;
+    slot = blockIdx.x - b * slots;
+  }
   const int gb = a.gammas ? a.gammas[b] : a.G;
   const bool onehot = a.dft == nullptr || (a.onehot != nullptr && a.onehot[b] != 0);
   if (gb < 0 || gb > a.G) {
@@ -693,13 +777,23 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
     if (threadIdx.x == kThreads - 1) cp_async4(&sm.seq_us, a.u_samp + b);
     cp_async_commit();
   }
+  bool skip = false;
+  if (EX && a.early && i > 0) {
+    // an earlier position of this sequence already stopped it: this row is not read
+    if (threadIdx.x == 0) {
+      const unsigned se = *reinterpret_cast<volatile const unsigned*>(a.stop_enc + b);
+      sm.early_skip = (se != 0u && a.G + 1 - static_cast<int>(se) < i) ? 1 : 0;
+    }
+    __syncthreads();
+    skip = sm.early_skip != 0;
+  }
   const Row row = seq_row<DT>(a, b, i, is_draft);
   int dtok = -1;
   if (i < gb) {
     const int t = a.tokens[static_cast<size_t>(b) * a.G + i];
     dtok = (t >= 0 && t < a.V) ? t : -1;
   }
-  if (EX && !rule_valid) {                       // the epilogue reports the sequence's bad rule
+  if (EX && (!rule_valid || skip)) {            // the epilogue reports a bad rule, ignores a skipped row
     if (threadIdx.x == 0) {
       RowStat st;
       st.W = 1.0; st.cut = 0; st.m = 0.0f; st.p_tok = 0.0f; st.status = SEQ_OK; st.n_list = 0;
@@ -743,6 +837,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
     // release (this CTA's summary and list, ordered before by the barrier) and
     // acquire (the last arriver then sees every other row's) in one atomic
     const unsigned rows_b = static_cast<unsigned>((gb + 1) + (onehot ? 0 : gb));
+    if (EX && a.early && i < gb) early_mark(a, b, i, is_draft, onehot, skip, sm);
     const unsigned prev = atom_add_acq_rel_gpu(&a.counters[b], 1u);
     sm.b_i32[7] = (prev + 1u == rows_b) ? 1 : 0;
   }
@@ -750,7 +845,10 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   if (!sm.b_i32[7]) return;
   sample_epilogue<DT, EX>(a, b, gb, onehot, sm);
   __syncthreads();
-  if (threadIdx.x == 0) a.counters[b] = 0u;   // leave the workspace reusable
+  if (threadIdx.x == 0) {                       // leave the workspace reusable
+    a.counters[b] = 0u;
+    if (EX && a.early) a.stop_enc[b] = 0u;
+  }
 }
 
 // ------------------------------------------------------------------ chunk-parallel full-row draw
@@ -1269,9 +1367,13 @@ int draw_chunks(int V, spec_dtype_t dt) {
 // Workspace: the two per-sequence counter arrays come first -- the only part
 // that must be zero when a call starts (kernels leave them zero again).
 struct SampleLayout {
-  size_t counters, dcount, stats, lists, drec, dsum, total;
+  size_t counters, dcount, stop, pairx, stats, lists, drec, dsum, total;
 };
-size_t zero_region_bytes(int B) { return 2 * round_up(static_cast<size_t>(B) * sizeof(uint32_t)); }
+// counters, draw counters, early-exit stop marks, early-exit exchange words
+size_t zero_region_bytes(int B, int G) {
+  return 3 * round_up(static_cast<size_t>(B) * sizeof(uint32_t)) +
+         round_up(static_cast<size_t>(B) * G * sizeof(unsigned long long));
+}
 // tps / dps: that side's rules come per sequence, so its rows may take either path.
 SampleLayout sample_layout(int B, int G, int V, const RowParams& tp, const RowParams& dp, bool tps = false,
                            bool dps = false) {
@@ -1279,7 +1381,9 @@ SampleLayout sample_layout(int B, int G, int V, const RowParams& tp, const RowPa
   const size_t slots = static_cast<size_t>(2 * G + 1);
   L.counters = 0;
   L.dcount = round_up(static_cast<size_t>(B) * sizeof(uint32_t));
-  L.stats = zero_region_bytes(B);
+  L.stop = 2 * L.dcount;
+  L.pairx = 3 * L.dcount;
+  L.stats = zero_region_bytes(B, G);
   L.lists = L.stats + round_up(static_cast<size_t>(B) * slots * sizeof(RowStat));
   const bool need_lists = tps || dps || tp.path == PATH_STREAM || dp.path == PATH_STREAM;
   L.drec = L.lists + (need_lists ? round_up(static_cast<size_t>(B) * slots * kListCap * sizeof(ListEntry)) : 0);
@@ -1399,6 +1503,7 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   const spec_sampling_params_t* tps = options ? options->target_params_seq : nullptr;
   const spec_sampling_params_t* dps = options ? options->draft_params_seq : nullptr;
   const bool kept_only = options && options->kept_list_only && (tps || dps);
+  const bool early = options && options->early_exit;
   if (!(lenience > 0.0f && lenience <= 1.0f)) return SPEC_ERR_INVALID_ARG;
   if (eos < -1 || eos >= vocab) return SPEC_ERR_INVALID_ARG;
   if (!aligned_to(tps, 4) || !aligned_to(dps, 4) || !aligned_to(out_num_emitted, 4)) return SPEC_ERR_MISALIGNED;
@@ -1458,11 +1563,16 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   a.dcount = reinterpret_cast<uint32_t*>(ws + L.dcount);
   a.drec = reinterpret_cast<DrawRec*>(ws + L.drec);
   a.dsum = reinterpret_cast<double*>(ws + L.dsum);
-  const unsigned grid = static_cast<unsigned>(batch) * static_cast<unsigned>(2 * gamma_max + 1);
+  a.early = early ? 1 : 0;
+  a.stop_enc = reinterpret_cast<uint32_t*>(ws + L.stop);
+  a.pairx = reinterpret_cast<unsigned long long*>(ws + L.pairx);
+  // early exit: position-major, two CTA slots (target, draft) per sequence and position
+  const unsigned grid = early ? static_cast<unsigned>(batch) * 2u * static_cast<unsigned>(gamma_max + 1)
+                              : static_cast<unsigned>(batch) * static_cast<unsigned>(2 * gamma_max + 1);
   const dim3 dgrid(static_cast<unsigned>(batch), static_cast<unsigned>(a.nchunk));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  const bool ex = tps || dps || eos >= 0 || out_num_emitted;
+  const bool ex = tps || dps || eos >= 0 || out_num_emitted || early;
   if (dtype == SPEC_BF16 && ex) {
     err = prepare(sample_kernel<DT_BF16, true>, g_ready[10]);
     if (err == cudaSuccess) sample_kernel<DT_BF16, true><<<grid, kThreads, smem, s>>>(a);
@@ -1522,6 +1632,7 @@ spec_status_t spec_verify_sample_lenient(const void* target_logits, const void* 
   opt.target_params_seq = nullptr;
   opt.draft_params_seq = nullptr;
   opt.kept_list_only = 0;
+  opt.early_exit = 0;
   return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
                             draft_is_onehot, u_accept, u_sample, target_params, draft_params, &opt,
                             batch, gamma_max, vocab, workspace, workspace_bytes, out_tokens,
@@ -1779,7 +1890,7 @@ extern "C" SPEC_API spec_status_t spec_verify_sample_noalloc(
   if (static_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
   // The per-sequence counters at the start of the scratch must be zero when the
   // kernels start; clear them on the caller's stream.
-  if (cudaMemsetAsync(scratch, 0, zero_region_bytes(batch), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, zero_region_bytes(batch, gamma_max), static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return spec_verify_sample(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
                             draft_is_onehot, u_accept, u_sample, target_params, draft_params, batch,

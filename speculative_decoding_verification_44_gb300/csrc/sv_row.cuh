@@ -115,6 +115,7 @@ struct __align__(16) Smem {
   int32_t seq_tok[kMaxGamma];
   float seq_u[kMaxGamma];
   float seq_us;
+  int early_skip;                    // early exit: this CTA's row is not read
 };
 
 // ------------------------------------------------------------------ digit walks

@@ -37,7 +37,7 @@ def oracle_probs(rows: torch.Tensor, params) -> torch.Tensor:
     return torch.from_numpy(p)
 
 
-def run_oracle_sample(w, seqs=None, keep_cdf=True, lenience=1.0, rules=None, eos_token=-1):
+def run_oracle_sample(w, seqs=None, keep_cdf=True, lenience=1.0, rules=None, eos_token=-1, early_exit=False):
     """The oracle on workload ``w``; ``rules``: per sequence (target SamplingParams, draft SamplingParams)."""
     tl = to_f64(w.target_logits) if seqs is None else to_f64(w.target_logits[seqs])
     dl = None
@@ -56,7 +56,8 @@ def run_oracle_sample(w, seqs=None, keep_cdf=True, lenience=1.0, rules=None, eos
             per = [per[b] for b in seqs]
     return oracle.verify_sample(tl, dl, toks, ua, us, params_tuple(w.target_params),
                                 params_tuple(w.draft_params), gam, oh, keep_cdf=keep_cdf,
-                                lenience=lenience, params_per_seq=per, eos_token=eos_token)
+                                lenience=lenience, params_per_seq=per, eos_token=eos_token,
+                                early_exit=early_exit)
 
 
 def run_oracle_greedy(w, seqs=None):
@@ -77,8 +78,9 @@ def gpu_greedy(w, **kw):
     return sv.verify_greedy(w.target_logits, w.draft_tokens, w.gamma_per_seq, **kw)
 
 
-def compare_sample(out, ref, w, seqs=None):
-    """Element-by-element comparison under the boundary rules; returns counters."""
+def compare_sample(out, ref, w, seqs=None, early=False):
+    """Element-by-element comparison under the boundary rules; returns counters.
+    ``early``: early-exit results, whose a_i stop at each side's own stop."""
     seqs = list(range(w.B)) if seqs is None else list(seqs)
     toks = out.tokens.cpu().numpy()
     nacc = out.num_accepted.cpu().numpy()
@@ -112,7 +114,12 @@ def compare_sample(out, ref, w, seqs=None):
             continue
         assert 0 <= toks[b, n] < w.V, (b, toks[b])
         assert (toks[b, n + 1:] == -1).all(), (b, toks[b])
-        if aprob is not None:
+        if aprob is not None and early:
+            k = min(n, r.num_accepted, gb - 1) + 1           # positions both sides decided
+            np.testing.assert_allclose(aprob[b, :k], r.accept_prob[:k], atol=TOL_PROB, rtol=0,
+                                       err_msg=f"accept_prob seq {b}")
+            assert (aprob[b, n + 1:] == -1).all(), (b, aprob[b])
+        elif aprob is not None:
             np.testing.assert_allclose(aprob[b, :gb], r.accept_prob[:gb], atol=TOL_PROB, rtol=0,
                                        err_msg=f"accept_prob seq {b}")
             assert (aprob[b, gb:] == -1).all()
@@ -159,9 +166,9 @@ def compare_greedy(out, ref, w, seqs=None):
     return len(seqs)
 
 
-def check_sample_counts(out, ref, w, seqs=None, min_exact=0.9):
+def check_sample_counts(out, ref, w, seqs=None, min_exact=0.9, early=False):
     """compare_sample plus the parity bar: few flagged / boundary sequences, the rest exact."""
-    c = compare_sample(out, ref, w, seqs)
+    c = compare_sample(out, ref, w, seqs, early)
     assert c["flagged"] + c["boundary"] <= max(2, 0.02 * c["n"]), c
     assert c["exact"] >= min_exact * (c["n"] - c["flagged"] - c["errors"]), c
     return c
