@@ -19,8 +19,8 @@
  * target's argmax at the first mismatch (or the bonus position)
  *                                           [wrblog §7.1; baisen §2, §6].
  * Beyond that: lenient acceptance [magicnet §8], an end-of-sequence commit
- * and per-sequence sampling rules [wrblog §14.3, §15], early-exit greedy
- * verification, and greedy verification of draft trees [baisen §8;
+ * and per-sequence sampling rules [wrblog §14.3, §15], early-exit greedy and
+ * sampling verification [wrblog §6], and greedy verification of draft trees [baisen §8;
  * magicnet §7].
  *
  * Readings of points the sources leave open (the library and its tests use
@@ -121,7 +121,8 @@ enum {
 };
 /* Checks run in this order and the first failure is reported: length, draft
  * tokens, uniforms, per-sequence rules (spec_verify_sample_ex), then rows
- * i = 0..gamma_b (target row i, then draft row i). */
+ * i = 0..gamma_b (target row i, then draft row i) -- with early exit only up
+ * to the sequence's first rejected draft. */
 
 typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype_t;
 
@@ -213,7 +214,7 @@ SPEC_API spec_status_t spec_verify_sample_lenient(const void* target_logits, con
                                          float* out_accept_prob, float* out_residual_z,
                                          int32_t* out_status, void* stream);
 
-/* Options of spec_verify_sample_ex.  {1.0f, -1, NULL, NULL, 0} is
+/* Options of spec_verify_sample_ex.  {1.0f, -1, NULL, NULL, 0, 0} is
  * spec_verify_sample exactly.
  *
  * lenience           (0, 1]: as for spec_verify_sample_lenient [magicnet §8].
