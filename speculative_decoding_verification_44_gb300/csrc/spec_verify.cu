@@ -801,10 +801,16 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
       sm.st = st;
     }
     __syncthreads();
-  } else if (P.path == PATH_STREAM) {
-    stream_row<DT>(row, P, dtok, sm);
   } else {
-    full_row<DT>(row, P, dtok, sm);
+    // early exit: a row of a later position keeps watching its sequence's stop
+    // mark and is abandoned if an earlier position stops the sequence meanwhile
+    StopCheck sc;
+    if (EX && a.early && i > 0) {
+      sc.p = a.stop_enc + b;
+      sc.thr = static_cast<unsigned>(a.G + 1 - i);
+    }
+    if (P.path == PATH_STREAM) stream_row<DT>(row, P, dtok, sm, sc);
+    else full_row<DT>(row, P, dtok, sm, sc);
   }
 
   // publish the row summary, then count this row in

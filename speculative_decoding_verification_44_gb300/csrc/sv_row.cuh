@@ -118,6 +118,38 @@ struct __align__(16) Smem {
   int early_skip;                    // early exit: this CTA's row is not read
 };
 
+// ------------------------------------------------------------------ early-exit stop marks
+// A row CTA under early exit watches its sequence's stop mark: once *p > thr
+// an earlier position has stopped the sequence, the row's result is never
+// used, and the row may be abandoned.  p == nullptr: nothing to watch.
+struct StopCheck {
+  const unsigned* p = nullptr;
+  unsigned thr = 0;
+};
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Block-wide (every thread calls it): true when the mark says stop.
+__device__ __forceinline__ bool stop_now(const StopCheck& sc, Smem& sm) {
+  if (!sc.p) return false;
+  __syncthreads();                                 // earlier readers of sm.early_skip are done
+  if (threadIdx.x == 0) sm.early_skip = ld_relaxed_u32(sc.p) > sc.thr ? 1 : 0;
+  __syncthreads();
+  return sm.early_skip != 0;
+}
+// The summary of an abandoned row (never read by the epilogue).
+__device__ __forceinline__ void abandon_row(Smem& sm, float cT) {
+  if (threadIdx.x == 0) {
+    RowStat st;
+    st.W = 1.0; st.cut = 0; st.m = 0.0f; st.p_tok = 0.0f; st.status = SEQ_OK; st.n_list = 0;
+    st.path = PATH_FULL; st.argmax = -1; st.cT = cT; st.invW = 0.0f;
+    sm.st = st;
+  }
+  __syncthreads();
+}
+
 // ------------------------------------------------------------------ digit walks
 // Warp-wide: positions 0..255 visit digits in the order given by `desc`
 // (descending digits 255..0, or ascending 0..255).  Finds the position whose
@@ -1099,11 +1131,21 @@ __device__ __forceinline__ bool kc_count_table(uint32_t keys, uint32_t cnt, uint
 // The counting loop of kc_pass, for aligned or element-wise rows.
 template <bool kAligned>
 __device__ __forceinline__ void kc_loop(const Row row, int v0, int v1, uint32_t keys, uint32_t cnt,
-                                        volatile int* ovf, volatile int* bad) {
+                                        volatile int* ovf, volatile int* bad, const StopCheck& sc,
+                                        volatile int* abandoned) {
   constexpr int P = Elem<DT_BF16>::kPer;
   const int lane = threadIdx.x & 31;
   bool counting = true;   // this thread's; an overflow anywhere discards the counts
-  for (int s = v0; s < v1 && counting; s += 32 * kUnroll) {
+  unsigned seen = 0u;     // the stop mark as read two iterations earlier (one load per warp)
+  int it = 0;
+  for (int s = v0; s < v1 && counting; s += 32 * kUnroll, ++it) {
+    if (sc.p && (it & 1)) {
+      if (seen > sc.thr) {                             // the sequence stopped: abandon the row
+        *abandoned = 1;
+        break;
+      }
+      seen = ld_relaxed_u32(sc.p);                     // consumed two iterations later
+    }
     uint4 r[kUnroll];
     int c[kUnroll];
 #pragma unroll
@@ -1137,21 +1179,25 @@ __device__ __forceinline__ void kc_loop(const Row row, int v0, int v1, uint32_t 
 // quarter of the row; then the maximum (the largest value counted) and the
 // NaN / +inf flag.  Returns 1 if the small table overflowed -- the maximum is
 // then incomplete and the caller takes it with full_max.
-__device__ __noinline__ int kc_pass(const Row row, Smem& sm, FullExtra& fx, float& m_out, int& bad_out) {
+__device__ __noinline__ int kc_pass(const Row row, Smem& sm, FullExtra& fx, float& m_out, int& bad_out,
+                                    const StopCheck sc, int& abandoned) {
   const int tid = threadIdx.x, warp = tid >> 5;
   for (int s = tid; s < kKH; s += kThreads) fx.u.kc.keys[s] = kNoKey;
   for (int s = tid; s < kPairs * kKCSlots; s += kThreads) (&fx.u.kc.cnt[0][0])[s] = 0u;
   if (tid == 0) {
     fx.bi[0] = 0;
     fx.bi[1] = 0;
+    fx.bi[4] = 0;
   }
   __syncthreads();
   const uint32_t keys = smem_u32(fx.u.kc.keys), cnt = smem_u32(fx.u.kc.cnt[warp >> 1]);
   const int Ls = seg_len(row);
   const int v0 = warp * Ls, v1 = min(row.nvec, v0 + Ls);
-  if (row.aligned) kc_loop<true>(row, v0, v1, keys, cnt, &fx.bi[0], &fx.bi[1]);
-  else kc_loop<false>(row, v0, v1, keys, cnt, &fx.bi[0], &fx.bi[1]);
+  if (row.aligned) kc_loop<true>(row, v0, v1, keys, cnt, &fx.bi[0], &fx.bi[1], sc, &fx.bi[4]);
+  else kc_loop<false>(row, v0, v1, keys, cnt, &fx.bi[0], &fx.bi[1], sc, &fx.bi[4]);
   __syncthreads();
+  abandoned = fx.bi[4];
+  if (abandoned) return 1;                             // same in every thread
   // the maximum is the largest value with a count
   const KeyCount& T = fx.u.kc;
   float m = -__int_as_float(0x7f800000);
@@ -1302,7 +1348,7 @@ __device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float 
 }
 
 template <int DT>
-__device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
+__device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm, const StopCheck sc = StopCheck()) {
   const int tid = threadIdx.x;
   float m;
   double S = 0.0;
@@ -1313,12 +1359,21 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm) 
   const bool keycount = DT == DT_BF16 && extra && P.k == 0 && P.top_p < 1.0f;
   int kc_overflow = 1;
   if (keycount) {
-    kc_overflow = kc_pass(row, sm, fx, m, bad);
+    int abandoned = 0;
+    kc_overflow = kc_pass(row, sm, fx, m, bad, sc, abandoned);
+    if (abandoned) {
+      abandon_row(sm, P.cT);
+      return;
+    }
     if (kc_overflow) full_max<DT>(row, sm, m, bad);
   }
   // the softmax denominator of the whole row is W only with neither cut
   else if (P.k > 0 || P.top_p < 1.0f) full_max<DT>(row, sm, m, bad);
   else full_pass1<DT>(row, P.cT, sm, m, S, bad);
+  if (stop_now(sc, sm)) {                              // stopped during the first pass
+    abandon_row(sm, P.cT);
+    return;
+  }
   RowStat st;
   st.path = PATH_FULL;
   st.m = m;
@@ -1589,7 +1644,7 @@ __device__ __forceinline__ void append_from_vector(const uint4& r, int c, int v,
 // its groups when all four tracked vectors qualify (there may be more).  The
 // collected elements >= K are a small superset of the top-k.
 template <int DT>
-__device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
+__device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm, const StopCheck sc = StopCheck()) {
   const int tid = threadIdx.x;
   constexpr int step = kThreads * kStreamUnroll;
   const int iters = (row.nvec + step - 1) / step;
@@ -1644,6 +1699,10 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
       if (cnt[u]) take(r[u], cnt[u], it * step + u * kThreads + tid);
   }
   const int any_bad = __syncthreads_or(bad ? 1 : 0);
+  if (stop_now(sc, sm)) {                              // stopped while the row streamed
+    abandon_row(sm, P.cT);
+    return;
+  }
   // K = the k-th largest of the kThreads maxima: MSB-first radix select, one
   // 8-bit digit per round (bf16 keys: the top 16 bits, two rounds)
   constexpr int kRounds = DT == DT_BF16 ? 2 : 4;
