@@ -355,7 +355,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
     def draft_row(i):
         return one_hot_row(V, d[i]) if one_hot else transform_row(draft[i], *draft_params)
 
-    def judge(i) -> bool:
+    def decide(i) -> bool:
         """a_i, the flags and the margin for position i; True if d_i is rejected."""
         nonlocal status, accept_margin
         a[i], zero_q[i] = acceptance_probability(p_rows[i].probs[d[i]], q_rows[i].probs[d[i]], lenience)
@@ -381,7 +381,7 @@ def verify_sample_sequence(target: np.ndarray, draft: np.ndarray | None, tokens:
                 res.rows_read = i + 1
                 return res
             q_rows.append(q_i)
-            if judge(i):
+            if decide(i):
                 rejected_at = i
                 break
     else:

@@ -134,3 +134,31 @@ def test_workspace_reuse_across_modes():
     torch.cuda.synchronize()
     same_up_to_stop(first, full)
     same_up_to_stop(second, full)
+
+
+@pytest.mark.parametrize("V", [9000, 30000])
+def test_early_exit_with_rules_and_eos(V):
+    """Early exit together with the other options: per-sequence rules (both row
+    paths in one launch) and an end-of-sequence commit, against the oracle's
+    early-exit reading with the same rules and the same EOS cut."""
+    import speculative_decoding_verification_44_gb300 as sv
+    from speculative_decoding_verification_44_gb300.workloads import sample_from_probs
+    rules = [(0.7, 50, 0.9), (1.0, 0, 0.95), (1.3, 0, 1.0), (0.8, 128, 0.8), (0.6, 7, 1.0)]
+    w = workload(5, B=40, V=V)
+    tr = [sv.SamplingParams(*rules[b % len(rules)]) for b in range(w.B)]
+    dr = [sv.SamplingParams(*rules[(b + 2) % len(rules)]) for b in range(w.B)]
+    toks = []
+    for b in range(w.B):
+        q = oracle_probs(w.draft_logits[b].cpu(), dr[b])
+        toks.append(sample_from_probs(q, torch.Generator().manual_seed(300 + b)))
+    w.draft_tokens = torch.stack(toks).to(torch.int32).cuda()
+    eos = int(w.draft_tokens[0, 0])
+    out = gpu_sample(w, target_rules=tr, draft_rules=dr, eos_token=eos, early_exit=True)
+    torch.cuda.synchronize()
+    ref = run_oracle_sample(w, rules=list(zip(tr, dr)), eos_token=eos, early_exit=True)
+    c = check_sample_counts(out, ref, w, early=True)
+    assert c["errors"] == 0 and c["n"] == w.B
+    nem = out.num_emitted.cpu().numpy()
+    for b, r in enumerate(ref.seqs):
+        if r.accept_margin >= 1e-6 and not r.draft_ambiguous:
+            assert nem[b] == r.num_emitted, (b, nem[b], r.num_emitted)
