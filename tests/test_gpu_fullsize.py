@@ -115,3 +115,23 @@ def test_greedy_trees_full_batch_sampled():
     P = path.cpu().numpy()[seqs]
     for k, r in enumerate(ref.seqs):
         assert list(P[k, : r.num_accepted + 1]) == r.path
+
+
+def test_ragged_full_batch_early_exit():
+    """The ragged workload at full size (B=512, V=256000) with early exit, as the
+    benchmark's --early-exit runs it: the same outputs as the all-rows call (a_i up
+    to each stop), and the oracle's early-exit reading on sampled sequences."""
+    w = make(5)
+    full = gpu_sample(w)
+    early = gpu_sample(w, early_exit=True)
+    torch.cuda.synchronize()
+    for n in ("tokens", "num_accepted", "status", "residual_z"):
+        assert torch.equal(getattr(early, n), getattr(full, n)), n
+    j = full.num_accepted.cpu().numpy()
+    ae, af = early.accept_prob.cpu().numpy(), full.accept_prob.cpu().numpy()
+    for b in range(w.B):
+        np.testing.assert_array_equal(ae[b, : j[b] + 1], af[b, : j[b] + 1])
+        assert (ae[b, j[b] + 1:] == -1).all(), b
+    seqs = list(range(3, 512, 16))
+    c = compare_sample(early, run_oracle_sample(w, seqs, early_exit=True), w, seqs, early=True)
+    assert c["n"] == len(seqs) and c["flagged"] + c["boundary"] <= 3, c
