@@ -173,3 +173,49 @@ def test_product_path_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_struct_layouts_match_the_binding(tmp_path):
+    """The ctypes mirrors of the header's structs have the C layout: a plain C
+    program compiled against the header prints each struct's size and field
+    offsets (gcc on the host; no GPU, no CUDA headers)."""
+    import shutil
+    from speculative_decoding_verification_44_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"spec_sampling_params_t": _lib.spec_sampling_params_t,
+               "spec_verify_options_t": _lib.spec_verify_options_t}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "spec_verify.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["  return 0;", "}"]
+    src, exe = tmp_path / "layout.c", tmp_path / "layout"
+    src.write_text("\n".join(lines) + "\n")
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        name, field, value = line.split()
+        got[(name, field)] = int(value)
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert got[(name, field)] == getattr(cls, field).offset, (name, field)
+
+
+def test_early_exit_needs_no_other_workspace(lib):
+    """The early-exit stop marks and exchange words live in the leading zero region
+    every sampling workspace has: the size does not depend on the option."""
+    from speculative_decoding_verification_44_gb300 import _lib
+    P = _lib.spec_sampling_params_t(0.7, 50, 0.9)
+    sizes = []
+    for early in (0, 1):
+        opt = _lib.spec_verify_options_t(1.0, -1, None, None, 0, early)
+        n = ctypes.c_size_t()
+        assert lib.spec_verify_workspace_size_ex(64, 5, 128256, P, P, ctypes.byref(opt), ctypes.byref(n)) == 0
+        sizes.append(n.value)
+    plain = ctypes.c_size_t()
+    assert lib.spec_verify_workspace_size(64, 5, 128256, P, P, ctypes.byref(plain)) == 0
+    assert sizes[0] == sizes[1] == plain.value
