@@ -88,10 +88,15 @@ def test_rows_after_the_stop_are_never_read(seed):
     rng = np.random.default_rng(100 + seed)
     V, gmax = int(rng.integers(3, 9)), int(rng.integers(2, 6))
     target, draft, tokens, u_acc, u_s = random_case(rng, V, gmax)
+    # a sure rejection no later than position k: a draft token with q > p there
+    # (so a_k < 1) and u_k just below 1
+    k = int(rng.integers(0, gmax))
+    sm = lambda z: np.exp(z - z.max()) / np.exp(z - z.max()).sum()
+    tokens[k] = int(np.argmax(sm(draft[k]) - sm(target[k])))
+    u_acc[k] = np.nextafter(1.0, 0.0)
     full = one(target, draft, tokens, u_acc, u_s, gmax, gmax, False)
     j = full.num_accepted
-    if j == gmax:
-        pytest.skip("every draft accepted: no row after the stop")
+    assert j <= k
     bad_t, bad_d = target.copy(), draft.copy()
     bad_t[j + 1:] = np.nan
     bad_d[j + 1:] = np.nan
@@ -147,3 +152,16 @@ def test_batch_wrapper_passes_the_flag():
             assert early.status[b] == full.status[b] and early.num_accepted[b] == full.num_accepted[b]
         else:
             assert early.status[b] == oracle.SEQ_NONFINITE
+
+
+def test_target_row_is_checked_before_its_draft_row():
+    """R16's order within a position: target row i, then draft row i.  Target row
+    1 all -inf (empty support) and draft row 1 NaN: the target's failure is the
+    one reported."""
+    rng = np.random.default_rng(21)
+    target, draft, tokens, u_acc, u_s = random_case(rng, 6, 3)
+    u_acc[0] = 0.0                                   # position 0 accepted: position 1 is read
+    target[1] = -np.inf
+    draft[1, 0] = np.nan
+    r = one(target, draft, tokens, u_acc, u_s, 3, 3, True)
+    assert r.status == oracle.SEQ_EMPTY_SUPPORT and r.rows_read == 2
