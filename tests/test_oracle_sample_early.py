@@ -165,3 +165,25 @@ def test_target_row_is_checked_before_its_draft_row():
     draft[1, 0] = np.nan
     r = one(target, draft, tokens, u_acc, u_s, 3, 3, True)
     assert r.status == oracle.SEQ_EMPTY_SUPPORT and r.rows_read == 2
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_eos_commit_and_per_sequence_rules_under_early_exit(seed):
+    """The end-of-sequence cut (R14) and per-sequence rules (R13) apply to the
+    early-exit result exactly as to the all-rows one: on valid rows the
+    committed blocks agree."""
+    rng = np.random.default_rng(500 + seed)
+    B, gmax, V = 6, 4, 7
+    target = rng.normal(0, 2, (B, gmax + 1, V))
+    draft = target[:, :gmax] + rng.normal(0, 1, (B, gmax, V))
+    tokens = rng.integers(0, V, (B, gmax))
+    u_acc, u_s = rng.random((B, gmax)), rng.random(B)
+    per = [RULES[(b + seed) % len(RULES)] for b in range(B)]
+    eos = int(tokens[0, 0])
+    kw = dict(params_per_seq=per, eos_token=eos, lenience=(1.0, 0.7)[seed % 2])
+    full = oracle.verify_sample(target, draft, tokens, u_acc, u_s, OFF, OFF, **kw)
+    early = oracle.verify_sample(target, draft, tokens, u_acc, u_s, OFF, OFF, early_exit=True, **kw)
+    np.testing.assert_array_equal(full.tokens, early.tokens)
+    np.testing.assert_array_equal(full.num_accepted, early.num_accepted)
+    np.testing.assert_array_equal(full.status, early.status)
+    assert [r.num_emitted for r in full.seqs] == [r.num_emitted for r in early.seqs]
