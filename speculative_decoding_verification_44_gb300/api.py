@@ -30,7 +30,7 @@ class VerifyOutput:
     tokens: torch.Tensor          # [B, gamma_max+1] int32; accepted drafts, new token, then -1
     num_accepted: torch.Tensor    # [B] int32; -1 = error, commit nothing
     status: torch.Tensor          # [B] int32 SPEC_SEQ_* codes
-    accept_prob: torch.Tensor | None = None   # [B, gamma_max] float32
+    accept_prob: torch.Tensor | None = None   # [B, gamma_max] float32 a_i; -1 past gamma_b (early exit: past the stop)
     residual_z: torch.Tensor | None = None    # [B] float32
     num_emitted: torch.Tensor | None = None   # [B] int32 tokens committed (spec_verify_sample_ex)
 
