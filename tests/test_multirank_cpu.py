@@ -47,3 +47,13 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.replica_ids(0) == [0, 1, 2, 3]
+
+
+def test_metric_names_the_call_variant():
+    """Each non-default call is named in the metric; the plain call adds nothing."""
+    import argparse
+    base = dict(lenience=None, eos=None, per_seq_rules=False, early_exit=False)
+    assert bench.variant_of(argparse.Namespace(**base)) == ""
+    assert bench.variant_of(argparse.Namespace(**{**base, "early_exit": True})) == " (early exit)"
+    both = bench.variant_of(argparse.Namespace(**{**base, "lenience": 0.5, "early_exit": True}))
+    assert "lenience 0.5" in both and "early exit" in both
