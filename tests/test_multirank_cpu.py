@@ -52,6 +52,7 @@ def test_single_rank_needs_no_process_group():
 def test_metric_names_the_call_variant():
     """Each non-default call is named in the metric; the plain call adds nothing."""
     import argparse
+    import bench
     base = dict(lenience=None, eos=None, per_seq_rules=False, early_exit=False)
     assert bench.variant_of(argparse.Namespace(**base)) == ""
     assert bench.variant_of(argparse.Namespace(**{**base, "early_exit": True})) == " (early exit)"
