@@ -57,7 +57,11 @@
  * - The caller allocates and owns every buffer, including the workspace.  The
  *   library allocates nothing, keeps no state between calls and never
  *   synchronises: all work is enqueued on `stream` (a cudaStream_t; NULL is
- *   the legacy default stream) and the call returns immediately.
+ *   the legacy default stream) and the call returns immediately.  The one
+ *   exception is spec_verify_sample_noalloc (at the end of this header): its
+ *   scratch is a fixed array of the library's own device memory that keeps
+ *   its contents between calls, shared by every call (overlapping calls race),
+ *   plus a per-device cache of that array's address.
  * - Logits are row-major.  Element (b, i, x) of target_logits is at
  *   ((b * (gamma_max + 1) + i) * vocab + x); of draft_logits at
  *   ((b * gamma_max + i) * vocab + x).  Rows with i > gamma_b (target) or
@@ -388,14 +392,19 @@ SPEC_API spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dty
  * GPU that loads the library holds it until the process exits.  Requests whose
  * workspace (spec_verify_workspace_size) exceeds 8 MiB return
  * SPEC_ERR_WORKSPACE and launch nothing.  Nothing is allocated: no cudaMalloc,
- * cudaFree or allocating library routine is called.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Each call
- * clears the scratch's counters with cudaMemsetAsync on `stream`, then runs
- * spec_verify_sample on it.  All calls share the one array, which keeps the
- * last call's contents: calls that overlap on the GPU (other streams, other
- * host threads) race and must not be issued.  Other arguments, outputs and
- * errors are as for spec_verify_sample. */
+ * cudaFree or allocating library routine is called.  Each call made outside
+ * stream capture looks up the array's device address (cudaGetSymbolAddress)
+ * with the current device and remembers it for that device; a call made while
+ * `stream` is being captured uses the remembered address, so make a first call
+ * on each device before any stream capture (under capture with none
+ * remembered the call returns SPEC_ERR_CUDA).  After the host checks of
+ * spec_verify_sample have passed, each call clears the scratch's counters with
+ * cudaMemsetAsync on `stream` and then launches as spec_verify_sample does; a
+ * call refused by those checks launches nothing and leaves the scratch alone.
+ * All calls share the one array, which keeps the last call's contents: calls
+ * that overlap on the GPU (other streams, other host threads) race and must
+ * not be issued.  Other arguments, outputs and errors are as for
+ * spec_verify_sample. */
 SPEC_API spec_status_t spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
                                                   spec_dtype_t dtype, const int32_t* draft_tokens,
                                                   const int32_t* gamma_per_seq,

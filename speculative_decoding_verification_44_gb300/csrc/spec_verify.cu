@@ -1502,7 +1502,8 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
                                         void* workspace, size_t workspace_bytes,
                                         int32_t* out_tokens, int32_t* out_num_accepted,
                                         float* out_accept_prob, float* out_residual_z,
-                                        int32_t* out_status, int32_t* out_num_emitted, void* stream) {
+                                        int32_t* out_status, int32_t* out_num_emitted, void* stream,
+                                        bool clear_zero_region = false) {
   if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
   const float lenience = options ? options->lenience : 1.0f;
   const int32_t eos = options ? options->eos_token : -1;
@@ -1578,6 +1579,10 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   const dim3 dgrid(static_cast<unsigned>(batch), static_cast<unsigned>(a.nchunk));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
+  // every host check has passed: a caller-less scratch gets its counters cleared
+  // on the stream, right before the launches
+  if (clear_zero_region && cudaMemsetAsync(workspace, 0, zero_region_bytes(batch, gamma_max), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   const bool ex = tps || dps || eos >= 0 || out_num_emitted || early;
   if (dtype == SPEC_BF16 && ex) {
     err = prepare(sample_kernel<DT_BF16, true>, g_ready[10]);
@@ -1860,20 +1865,30 @@ namespace {
 constexpr size_t kStaticScratchBytes = 8u << 20;   // 8 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device (host code only sees a stand-in symbol, never a usable pointer).
+// Device address of g_static_scratch on the current device.  Host code only
+// sees a stand-in symbol, never a usable pointer, so the address is asked of
+// the runtime: on every call made outside stream capture (a cudaDeviceReset
+// reloads the module, and the array may move), and from the per-device cache
+// while the stream is being captured (the runtime is not asked then; a first
+// call under capture finds no cache and fails with SPEC_ERR_CUDA).
 std::atomic<void*> g_scratch_addr[64];
 
-cudaError_t static_scratch(void** out) {
+cudaError_t static_scratch(cudaStream_t stream, void** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  err = cudaStreamIsCapturing(stream, &cap);
+  if (err != cudaSuccess) return err;
+  void* p = nullptr;
+  if (cap == cudaStreamCaptureStatusNone) {
     err = cudaGetSymbolAddress(&p, g_static_scratch);
     if (err != cudaSuccess) return err;
     g_scratch_addr[dev].store(p, std::memory_order_release);
+  } else {
+    p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) return cudaErrorStreamCaptureUnsupported;
   }
   *out = p;
   return cudaSuccess;
@@ -1893,13 +1908,14 @@ extern "C" SPEC_API spec_status_t spec_verify_sample_noalloc(
   if (st != SPEC_OK) return st;
   if (need > kStaticScratchBytes) return SPEC_ERR_WORKSPACE;   // beyond the 8 MiB static scratch
   void* scratch = nullptr;
-  if (static_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (static_scratch(static_cast<cudaStream_t>(stream), &scratch) != cudaSuccess) return SPEC_ERR_CUDA;
   // The per-sequence counters at the start of the scratch must be zero when the
-  // kernels start; clear them on the caller's stream.
-  if (cudaMemsetAsync(scratch, 0, zero_region_bytes(batch, gamma_max), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  return spec_verify_sample(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
-                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, batch,
-                            gamma_max, vocab, scratch, kStaticScratchBytes, out_tokens,
-                            out_num_accepted, out_accept_prob, out_residual_z, out_status, stream);
+  // kernels start: verify_sample_impl clears them on the caller's stream once
+  // every host check has passed (an invalid call launches nothing and leaves
+  // the scratch as it was).
+  return verify_sample_impl(target_logits, draft_logits, dtype, draft_tokens, gamma_per_seq,
+                            draft_is_onehot, u_accept, u_sample, target_params, draft_params, nullptr,
+                            batch, gamma_max, vocab, scratch, kStaticScratchBytes, out_tokens,
+                            out_num_accepted, out_accept_prob, out_residual_z, out_status, nullptr, stream,
+                            true);
 }

@@ -6,22 +6,20 @@ latency-critical path that must not pay cudaMalloc's device-wide
 synchronisation.  For them the library keeps its scratch in a fixed 8 MiB
 array of its own device memory.  This test calls that entry point through the
 C ABI twice in a row and checks both results against spec_verify_sample on the
-same inputs (tokens and accept counts exactly, probabilities within 1e-5), and
-that a request needing more than 8 MiB of scratch is refused before launching.
+same inputs (every output bit for bit: the same kernels run on the same
+inputs), that a request needing more than 8 MiB of scratch is refused before
+launching, and that a call refused by the host checks writes nothing and does
+not disturb the calls around it.
 
 It sits in its own file, collected last, so a stop-at-first-failure run has
 already run every other test; it also passes alone in a fresh process.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 pytestmark = pytest.mark.gpu
-
-TOL_PROB = 1e-5
-
 
 @pytest.fixture(scope="module")
 def lib():
@@ -92,8 +90,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, B):
         assert torch.equal(got["tokens"], ref["tokens"])
         assert torch.equal(got["nacc"], ref["nacc"])
         assert torch.equal(got["status"], ref["status"])
-        np.testing.assert_allclose(got["aprob"].cpu().numpy(), ref["aprob"].cpu().numpy(), atol=TOL_PROB, rtol=0)
-        np.testing.assert_allclose(got["z"].cpu().numpy(), ref["z"].cpu().numpy(), atol=TOL_PROB, rtol=0)
+        # the same kernels on the same inputs: the probabilities agree bit for bit
+        assert torch.equal(got["aprob"], ref["aprob"])
+        assert torch.equal(got["z"], ref["z"])
     assert (ref["nacc"].cpu() >= 0).all()
 
 
@@ -110,3 +109,32 @@ def test_noalloc_refuses_requests_beyond_its_scratch(lib):
     assert st == lib.SPEC_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert (o["tokens"].cpu() == -7).all()   # nothing was launched
+
+
+def test_noalloc_invalid_call_launches_nothing(lib):
+    """A call refused by the host checks (here a misaligned output pointer)
+    returns its status with nothing written, and the valid calls before and
+    after it still match the workspace entry point."""
+    x = serving_inputs(8, 128256, seed=11)
+    ref = outputs(8, x["G"])
+    st, ws = call_with_workspace(lib, x, ref)
+    assert st == lib.SPEC_OK
+    got = outputs(8, x["G"])
+    assert call_noalloc(lib, x, got) == lib.SPEC_OK
+    bad = outputs(8, x["G"])
+    s = torch.cuda.current_stream().cuda_stream
+    st = lib.spec_verify_sample_noalloc(
+        x["tgt"].data_ptr(), x["dft"].data_ptr(), lib.SPEC_BF16, x["toks"].data_ptr(), None, None,
+        x["ua"].data_ptr(), x["us"].data_ptr(), x["p"].c(), x["p"].c(), x["B"], x["G"], x["V"],
+        bad["tokens"].data_ptr() + 2, bad["nacc"].data_ptr(), bad["aprob"].data_ptr(), bad["z"].data_ptr(),
+        bad["status"].data_ptr(), s)
+    assert st == lib.SPEC_ERR_MISALIGNED
+    torch.cuda.synchronize()
+    assert (bad["tokens"].cpu() == -7).all()
+    for k in ref:
+        assert torch.equal(got[k], ref[k]), k
+    again = outputs(8, x["G"])
+    assert call_noalloc(lib, x, again) == lib.SPEC_OK
+    torch.cuda.synchronize()
+    for k in ref:
+        assert torch.equal(again[k], ref[k]), k
