@@ -87,7 +87,20 @@ struct SampleArgs {
   uint32_t* stop_enc;          // [B] G + 1 - (earliest position known to stop), 0 = none (self-cleaning)
   unsigned long long* pairx;   // [B][G] exchange of a position's two draft-token probabilities (self-cleaning)
   double* dsum;         // [B][nchunk] weight sum per chunk
+  // kept-list kernel: per (sequence, row slot) a block of wpr 16-byte words,
+  // a ListRec then the row's kept list in token order
+  uint4* fast;
+  int wpr;
 };
+
+// Row record of the kept-list kernel (the first word of a row's block).
+struct __align__(16) ListRec {
+  float p_tok;      // probability of the draft token this row scores
+  int32_t status;   // SEQ_OK, SEQ_NONFINITE or SEQ_EMPTY_SUPPORT
+  int32_t n_list;   // kept-list entries that follow
+  int32_t pad;
+};
+static_assert(sizeof(ListRec) == 16 && sizeof(ListEntry) == 16, "kept-list words");
 
 // What draw_kernel needs from the sequence epilogue; j < 0: nothing to draw.
 struct DrawRec {
@@ -145,92 +158,52 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const float* p,
   return 0.0f;
 }
 
-// Inverse-CDF draw over a PATH_STREAM target row's kept list, block-wide.
-// Residual weights max(0, p - beta q) [wrblog §5; magicnet §8], or p itself for
-// the bonus draw; the token is the smallest x (vocabulary order) with
-// C(x) > u Z.  Kept lists are stored in token order, so thread e takes target
-// entry e (one round trip for both lists), looks q up by binary search in the
-// draft list, and a block scan in double-float gives every C(x) and Z at once.
-// The draw is the first entry whose C(x) exceeds u Z (the last entry with
-// weight if rounding leaves none).
-template <int DT>
-__device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
-                                      const RowStat& ds, float uf, double& Z_resid, int& flags, Smem& sm) {
-  static_assert(kThreads >= 2 * kListCap, "one thread per entry of both lists");
-  constexpr int kScanWarps = kListCap / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slots = 2 * a.G + 1;
-  SmemEpi& E = sm.u.e;
-  const int nt = E.rs[r].n_list;
-  const bool draft_list = residual && !onehot && ds.path == PATH_STREAM;
-  const int nq = draft_list ? ds.n_list : 0;
-  const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
-  const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
-  ListEntry te;
-  te.p = 0.0f;
-  te.p_lo = 0.0f;
-  te.token = 0x7fffffff;
-  if (tid < nt) {
-    te = load_entry(tl + tid);
-    E.tok[tid] = te.token;
-  } else if (tid >= kListCap && tid - kListCap < nq) {
-    const ListEntry q = load_entry(ql + tid - kListCap);
-    E.qtok[tid - kListCap] = q.token;
-    E.qp[tid - kListCap] = q.p + q.p_lo;
-  }
-  if (tid == 0) {
-    sm.b_i32[3] = 0x7fffffff;
-    sm.b_i32[6] = -1;
-  }
-  __syncthreads();
-  // weights as double-float (no float64 arithmetic: that pipe is slow here)
-  const df pw = {te.p, te.p_lo};
-  df w = pw;
-  if (residual && tid < nt) {
-    float q = 0.0f;
-    if (onehot) {
-      q = (te.token == dj) ? 1.0f : 0.0f;
-    } else if (draft_list) {
-      int lo = 0, hi = nq - 1;
-      while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        const int t = E.qtok[mid];
-        if (t == te.token) { q = E.qp[mid]; break; }
-        if (t < te.token) lo = mid + 1; else hi = mid - 1;
-      }
-    } else {
-      const Row drow = seq_row<DT>(a, b, r, true);
-      q = full_prob(load_elem<DT>(drow.base, te.token), static_cast<uint32_t>(te.token), cut_test(ds.cut), ds.m,
-                    ds.cT, ds.invW);
+// Warp-wide inverse-CDF draw over a kept list stored in token order (n <=
+// kListCap entries; lane l takes entries 4l .. 4l+3, so lane order is
+// vocabulary order).  Weights max(0, p - beta q(x)) for a residual [wrblog §5;
+// magicnet §8], p itself for the bonus draw; C(x) and Z come from a
+// double-float warp scan (no float64 arithmetic: that pipe is slow here).  The
+// token is the smallest x with C(x) > u Z, or the last entry with weight if
+// rounding leaves none.  Z == 0 after a rejection falls back to the draw from
+// p and sets SEQ_FLAG_Z_ZERO.  Returns -1 when no entry has weight.
+// entry_at(e) gives entry e; q_of(x) gives q(x) (residual draws only).
+template <class EntryAt, class QOf>
+__device__ __forceinline__ int warp_list_draw(EntryAt entry_at, int n, bool residual, QOf q_of, float beta,
+                                              float uf, float& Z_resid, int& flags) {
+  const int lane = threadIdx.x & 31;
+  int tok[4];
+  df pw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * lane + j;
+    tok[j] = 0x7fffffff;
+    pw[j] = df_from(0.0f);
+    if (e < n) {
+      const ListEntry le = entry_at(e);
+      tok[j] = le.token;
+      pw[j] = {le.p, le.p_lo};
     }
-    const float bq = a.beta * q;                      // beta q exactly, as hi + lo
-    const df d = df_add(pw, {-bq, -fmaf(a.beta, q, -bq)});
-    w = d.hi > 0.0f ? d : df_from(0.0f);
   }
   for (int pass = 0; pass < 2; ++pass) {
-    const df xd = pass == 0 ? w : pw;
-    const float xh = xd.hi;
-    df incl = df_from(0.0f);
-    if (warp < kScanWarps) {
-      incl = warp_incl_scan_df(xd, lane);
-      if (lane == 31) {
-        E.wh[warp] = incl.hi;
-        E.wl[warp] = incl.lo;
-      }
-    }
-    __syncthreads();
-    df Z = df_from(0.0f), base = df_from(0.0f);
+    const bool resid = residual && pass == 0;
+    df w[4];
+    df s = df_from(0.0f);
 #pragma unroll
-    for (int k = 0; k < kScanWarps; ++k) {       // every thread: the same Z, in the same order
-      const df s = {E.wh[k], E.wl[k]};
-      if (k < warp) base = df_add(base, s);
-      Z = df_add(Z, s);
+    for (int j = 0; j < 4; ++j) {
+      w[j] = pw[j];
+      if (resid && 4 * lane + j < n) {
+        const float q = q_of(tok[j]);
+        const float bq = beta * q;                      // beta q exactly, as hi + lo
+        const df d = df_add(pw[j], {-bq, -fmaf(beta, q, -bq)});
+        w[j] = d.hi > 0.0f ? d : df_from(0.0f);
+      }
+      s = df_add(s, w[j]);
     }
-    incl = df_add(base, incl);
-    if (pass == 0 && residual && tid == 0) Z_resid = Z.hi;   // only thread 0 reports it
+    const df incl = warp_incl_scan_df(s, lane);
+    const df Z = df_shfl(incl, 31);
+    if (resid) Z_resid = Z.hi;
     if (!(Z.hi > 0.0f)) {
-      __syncthreads();                           // E.wh / E.wl are rewritten by the next pass
-      if (pass == 0 && residual) {               // Z == 0 after a rejection: draw from p instead
+      if (resid) {                                      // Z == 0 after a rejection: draw from p instead
         flags |= SEQ_FLAG_Z_ZERO;
         continue;
       }
@@ -238,17 +211,85 @@ __device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool re
     }
     const float th = uf * Z.hi;
     const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
-    if (tid < nt && xh > 0.0f) {
-      if (!df_ge(t, incl)) atomicMin(&sm.b_i32[3], tid);     // C(x) > u Z
-      atomicMax(&sm.b_i32[6], tid);
+    df c = df_shfl_up(incl, 1);                         // exclusive prefix of this lane
+    if (lane == 0) c = df_from(0.0f);
+    int first = 0x7fffffff, lastp = -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (w[j].hi > 0.0f) {
+        c = df_add(c, w[j]);
+        lastp = 4 * lane + j;
+        if (first == 0x7fffffff && !df_ge(t, c)) first = 4 * lane + j;   // C(x) > u Z
+      }
     }
-    __syncthreads();
-    const int e = sm.b_i32[3] != 0x7fffffff ? sm.b_i32[3] : sm.b_i32[6];
-    const int sel = e >= 0 ? E.tok[e] : -1;
-    __syncthreads();
-    return sel;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      first = min(first, __shfl_xor_sync(kFull, first, o));
+      lastp = max(lastp, __shfl_xor_sync(kFull, lastp, o));
+    }
+    const int sel = first != 0x7fffffff ? first : lastp;
+    if (sel < 0) return -1;
+    const int js = sel & 3;
+    const int mine = js == 0 ? tok[0] : (js == 1 ? tok[1] : (js == 2 ? tok[2] : tok[3]));
+    return __shfl_sync(kFull, mine, sel >> 2);
   }
   return -1;
+}
+
+// q(x) of a kept list in token order: binary search (0 if x is not kept).
+__device__ __forceinline__ float kept_q(const ListEntry* ql, int nq, int x) {
+  int lo = 0, hi = nq - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    const ListEntry e = ql[mid];
+    if (e.token == x) return e.p + e.p_lo;
+    if (e.token < x) lo = mid + 1; else hi = mid - 1;
+  }
+  return 0.0f;
+}
+
+// The residual or bonus draw over a PATH_STREAM target row's kept list
+// (stored in token order in the workspace), by warp 0 with warp_list_draw.
+// The draft's probability comes from its kept list (staged in shared memory
+// for the lookups), from its full row, or is the delta of a one-hot draft.
+// Block-wide; returns the token to every thread.
+template <int DT>
+__device__ __noinline__ int list_draw(const SampleArgs& a, int b, int r, bool residual, bool onehot, int dj,
+                                      const RowStat& ds, float uf, double& Z_resid, int& flags, Smem& sm) {
+  const int tid = threadIdx.x;
+  const int slots = 2 * a.G + 1;
+  SmemEpi& E = sm.u.e;
+  const int nt = E.rs[r].n_list;
+  const bool draft_list = residual && !onehot && ds.path == PATH_STREAM;
+  const int nq = draft_list ? ds.n_list : 0;
+  const ListEntry* tl = a.lists + (static_cast<size_t>(b) * slots + r) * kListCap;
+  const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + r) * kListCap;
+  if (tid < nq) {
+    const ListEntry q = load_entry(ql + tid);
+    E.qtok[tid] = q.token;
+    E.qp[tid] = q.p + q.p_lo;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const Row drow = seq_row<DT>(a, b, r, true);
+    const auto q_of = [&](int x) -> float {
+      if (onehot) return x == dj ? 1.0f : 0.0f;
+      if (draft_list) return list_lookup(E.qtok, E.qp, nq, x);
+      return full_prob(load_elem<DT>(drow.base, x), static_cast<uint32_t>(x), cut_test(ds.cut), ds.m, ds.cT,
+                       ds.invW);
+    };
+    float Zr = -1.0f;
+    const int sel = warp_list_draw([&](int e) { return load_entry(tl + e); }, nt, residual, q_of, a.beta, uf,
+                                   Zr, flags);
+    if (tid == 0) {
+      sm.b_i32[3] = sel;
+      if (residual) Z_resid = static_cast<double>(Zr);
+    }
+  }
+  __syncthreads();
+  const int sel = sm.b_i32[3];
+  __syncthreads();
+  return sel;
 }
 
 // Per-element weight for the block scan over a PATH_FULL target row.
@@ -857,6 +898,237 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
   }
 }
 
+// ------------------------------------------------------------------ kept-list kernel
+// The verifier for the common serving case: every used row takes the
+// streaming top-k path (1 <= top_k <= kSmallK on both sides, or one-hot
+// drafts), rows are 16-byte aligned and gamma_max <= 31.  Each row CTA streams
+// its row keeping its best vectors in registers (stash_stream_row: the
+// candidates above the bound need no second read of the row), and publishes
+// one contiguous block: a ListRec and the kept list in token order.  The CTA that
+// finishes last for a sequence reads all of the sequence's blocks in one
+// round trip, draws at every position in parallel and lets warp 0 decide:
+// status, the left-to-right acceptance scan, the outputs [wrblog §5, §6;
+// rainlin §1].  Results are those of sample_kernel: the same row analysis,
+// the same acceptance arithmetic and the same draw (warp_list_draw).
+constexpr int kGatherWords = static_cast<int>(sizeof(Smem::u)) / 16;   // the epilogue gathers into sm.u
+
+// One position's draw, computed by the epilogue's drawing warps for every
+// position while warp 0 decides which one the sequence uses.
+struct PosDraw {
+  int32_t tok;
+  float Z;
+  int32_t flags;
+  int32_t pad;
+};
+static_assert(sizeof(PosDraw) * 64 <= sizeof(Smem::sorted), "per-position draws in sm.sorted");
+
+// Sequence epilogue of the kept-list kernel.  `words` (sm.u, dead by now) receives the sequence's row blocks by cp.async, one round
+// trip.  Then, at once: warp 0 checks the status and runs the acceptance scan
+// (position j of the first rejection, or gamma_b), and warps 1..7 each draw
+// for their positions -- the residual draw at i < gamma_b, the bonus draw at
+// gamma_b -- since none of the draws depends on j.  Warp 0 then writes the
+// outputs with the draw at j.
+__device__ __noinline__ void list_epilogue(const SampleArgs& a, int b, int gb, bool onehot, Smem& sm,
+                                           uint4* words) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slots = 2 * a.G + 1, wpr = a.wpr;
+  const uint4* src = a.fast + static_cast<size_t>(b) * slots * wpr;
+  const int total = slots * wpr;
+  for (int t = tid; t < total; t += kThreads) {
+    const int s = t / wpr;
+    const bool used = s <= gb || (s > a.G && !onehot && s - a.G - 1 < gb);
+    if (used) cp_async16(&words[t], src + t);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  const auto rec = [&](int s) { return *reinterpret_cast<const ListRec*>(&words[s * wpr]); };
+  PosDraw* pd = reinterpret_cast<PosDraw*>(sm.sorted);
+  const size_t tokb = static_cast<size_t>(b) * a.G;
+  const size_t ob = static_cast<size_t>(b) * (a.G + 1);
+  if (warp > 0) {
+    // the draw at each position i (i < gb: residual weights (p_i - beta q_i)+;
+    // i == gb: the bonus draw from p_gb) [wrblog §5, §6; magicnet §8]
+    for (int i = warp - 1; i <= gb; i += kWarps - 1) {
+      const bool residual = i < gb;
+      const int dj = residual ? sm.seq_tok[i] : -1;
+      const ListEntry* tl = reinterpret_cast<const ListEntry*>(&words[i * wpr + 1]);
+      const ListEntry* ql = reinterpret_cast<const ListEntry*>(&words[(a.G + 1 + i) * wpr + 1]);
+      const int nt = min(rec(i).n_list, wpr - 1);
+      const int nq = (residual && !onehot) ? min(rec(a.G + 1 + i).n_list, wpr - 1) : 0;
+      float Z = -1.0f;
+      int flags = 0;
+      const int tok = warp_list_draw([&](int e) { return tl[e]; }, nt, residual,
+                                     [&](int x) { return onehot ? (x == dj ? 1.0f : 0.0f) : kept_q(ql, nq, x); },
+                                     a.beta, sm.seq_us, Z, flags);
+      if (lane == 0) {
+        PosDraw d;
+        d.tok = tok;
+        d.Z = Z;
+        d.flags = flags;
+        d.pad = 0;
+        pd[i] = d;
+      }
+    }
+  } else {
+    const int i = lane;                         // lane i: position i (gamma_max <= 31)
+    // status, in the documented order: tokens, uniforms, rows (target 0, draft 0, target 1, ...)
+    bool bad_tok = false, bad_u = false;
+    if (i < gb) {
+      const int t = sm.seq_tok[i];
+      const float u = sm.seq_u[i];
+      bad_tok = t < 0 || t >= a.V;
+      bad_u = !(u >= 0.0f && u < 1.0f);
+    }
+    if (lane == 0) bad_u |= !(sm.seq_us >= 0.0f && sm.seq_us < 1.0f);
+    int status = SEQ_OK;
+    if (__any_sync(kFull, bad_tok)) {
+      status = SEQ_BAD_TOKEN;
+    } else if (__any_sync(kFull, bad_u)) {
+      status = SEQ_BAD_UNIFORM;
+    } else {
+      int st = SEQ_OK;
+      if (i <= gb) {
+        st = rec(i).status;
+        if (st == SEQ_OK && i < gb && !onehot) st = rec(a.G + 1 + i).status;
+      }
+      const unsigned bm = __ballot_sync(kFull, st != SEQ_OK);
+      if (bm) status = __shfl_sync(kFull, st, __ffs(bm) - 1);
+    }
+    // a_i = min(1, p_i(d_i) / (beta q_i(d_i))); accept iff u_i < a_i; stop at the first rejection
+    int j = gb, flags = 0;
+    if (status == SEQ_OK) {
+      bool rej = false, zq = false;
+      float ai = -1.0f;
+      if (i < gb) {
+        const float p = rec(i).p_tok;
+        const float q = onehot ? 1.0f : rec(a.G + 1 + i).p_tok;
+        if (q > 0.0f) ai = fminf(1.0f, p / (a.beta * q));   // [magicnet §8]; beta = 1: p / q
+        else { ai = p > 0.0f ? 1.0f : 0.0f; zq = true; }
+        rej = !(sm.seq_u[i] < ai);
+      }
+      if (a.out_aprob && i < a.G) a.out_aprob[tokb + i] = ai;
+      const unsigned rm = __ballot_sync(kFull, rej);
+      const unsigned zm = __ballot_sync(kFull, zq);
+      if (rm) {
+        const int f = __ffs(rm) - 1;
+        j = f;
+        const unsigned upto = (f == 31) ? kFull : ((2u << f) - 1u);
+        if (zm & upto) flags |= SEQ_FLAG_ZERO_Q;
+      } else if (zm) {
+        flags |= SEQ_FLAG_ZERO_Q;
+      }
+    }
+    if (lane == 0) {
+      sm.b_i32[0] = status;
+      sm.b_i32[1] = j;
+      sm.b_i32[2] = flags;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const int status = sm.b_i32[0], j = sm.b_i32[1];
+  const int i = lane;
+  if (status != SEQ_OK) {                       // commit nothing [wrblog §15]
+    if (i <= a.G) a.out_tokens[ob + i] = -1;
+    if (a.out_aprob && i < a.G) a.out_aprob[tokb + i] = -1.0f;
+    if (lane == 0) {
+      a.out_nacc[b] = -1;
+      if (a.out_Z) a.out_Z[b] = -1.0f;
+      if (a.out_status) a.out_status[b] = status;
+      a.counters[b] = 0u;                       // leave the workspace reusable
+    }
+    return;
+  }
+  // outputs: accepted drafts, the drawn token at j, then -1
+  const PosDraw d = pd[j];
+  if (i <= a.G) a.out_tokens[ob + i] = i < j ? sm.seq_tok[i] : (i == j ? d.tok : -1);
+  if (lane == 0) {
+    a.out_nacc[b] = j;
+    if (a.out_Z) a.out_Z[b] = j < gb ? d.Z : -1.0f;
+    if (a.out_status) a.out_status[b] = sm.b_i32[2] | d.flags;
+    a.counters[b] = 0u;                         // leave the workspace reusable
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int slots = 2 * a.G + 1;
+  const int b = blockIdx.x / slots;
+  const int slot = blockIdx.x - b * slots;
+  const int gb = a.gammas ? a.gammas[b] : a.G;
+  const bool onehot = a.dft == nullptr || (a.onehot != nullptr && a.onehot[b] != 0);
+  if (gb < 0 || gb > a.G) {
+    if (slot == 0) write_error(a, b, SEQ_BAD_LENGTH);
+    return;
+  }
+  const bool is_draft = slot > a.G;
+  const int i = is_draft ? slot - a.G - 1 : slot;
+  if (!is_draft && i > gb) return;
+  if (is_draft && (onehot || i >= gb)) return;
+  {
+    // the sequence's draft tokens and uniforms, for the epilogue: copied while
+    // the row streams, waited for only before this CTA counts its row in
+    const size_t tb = static_cast<size_t>(b) * a.G;
+    if (tid < gb) {
+      cp_async4(&sm.seq_tok[tid], a.tokens + tb + tid);
+      cp_async4(&sm.seq_u[tid], a.u_acc + tb + tid);
+    }
+    if (tid == kThreads - 1) cp_async4(&sm.seq_us, a.u_samp + b);
+    cp_async_commit();
+  }
+  const Row row = seq_row<DT>(a, b, i, is_draft);
+  int dtok = -1;
+  if (i < gb) {
+    const int t = a.tokens[static_cast<size_t>(b) * a.G + i];
+    dtok = (t >= 0 && t < a.V) ? t : -1;
+  }
+  stash_stream_row<DT>(row, is_draft ? a.dp : a.tp, dtok, sm);
+
+  // publish the row's block: its record, then its kept list in token order
+  uint4* dst = a.fast + (static_cast<size_t>(b) * slots + slot) * a.wpr;
+  const int n = sm.st.n_list;
+  if (tid == 0) {
+    ListRec rec;
+    rec.p_tok = sm.st.p_tok;
+    rec.status = sm.st.status;
+    rec.n_list = n;
+    rec.pad = 0;
+    dst[0] = *reinterpret_cast<const uint4*>(&rec);
+  }
+  if (tid < n) {
+    ListEntry le;
+    le.p = sm.list_ph[tid];
+    le.p_lo = sm.list_pl[tid];
+    le.token = sm.list_tok[tid];
+    le.pad = 0;
+    const int4* lt = reinterpret_cast<const int4*>(sm.list_tok);   // padded with INT_MAX
+    int rank = 0;
+#pragma unroll 4
+    for (int f = 0; f < ((n + 3) >> 2); ++f) {
+      const int4 t = lt[f];
+      rank += (t.x < le.token ? 1 : 0) + (t.y < le.token ? 1 : 0) + (t.z < le.token ? 1 : 0) +
+              (t.w < le.token ? 1 : 0);
+    }
+    reinterpret_cast<ListEntry*>(dst + 1)[rank] = le;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid == 0) {
+    // release (this CTA's block, ordered before by the barrier) and acquire
+    // (the last arriver then sees every other row's) in one atomic
+    const unsigned rows_b = static_cast<unsigned>((gb + 1) + (onehot ? 0 : gb));
+    const unsigned prev = atom_add_acq_rel_gpu(&a.counters[b], 1u);
+    sm.b_i32[7] = (prev + 1u == rows_b) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sm.b_i32[7]) return;
+  list_epilogue(a, b, gb, onehot, sm, &sm.u.ring[0][0]);
+}
+
 // ------------------------------------------------------------------ chunk-parallel full-row draw
 // The residual or bonus draw over a PATH_FULL target row reads up to two whole
 // rows; one CTA doing it alone is latency-bound.  Here every sequence with a
@@ -1434,7 +1706,7 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
-std::atomic<uint64_t> g_ready[14];  // sample, greedy, transform, draw, greedy-early, sample-ex, tree x {bf16, f32}
+std::atomic<uint64_t> g_ready[16];  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list x {bf16, f32}
 
 // Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
 // needs FullExtra after Smem; launches without such rows keep their occupancy.
@@ -1527,6 +1799,8 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
       !aligned_to(workspace, kAlign))
     return SPEC_ERR_MISALIGNED;
   SampleArgs a;
+  a.fast = nullptr;
+  a.wpr = 0;
   a.tp = make_row_params(target_params, vocab, dtype);
   a.dp = make_row_params(draft_params, vocab, dtype);
   // promised kept-list rules: the scalar rules must keep the promise too
@@ -1584,7 +1858,24 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   if (clear_zero_region && cudaMemsetAsync(workspace, 0, zero_region_bytes(batch, gamma_max), s) != cudaSuccess)
     return SPEC_ERR_CUDA;
   const bool ex = tps || dps || eos >= 0 || out_num_emitted || early;
-  if (dtype == SPEC_BF16 && ex) {
+  // the kept-list kernel: every used row on the streaming top-k path, aligned
+  // rows, and each sequence's row blocks within the epilogue's gather buffer
+  const int kcap = std::max(a.tp.k, draft_logits ? a.dp.k : 0);
+  const bool list_path = !ex && a.aligned && a.tp.path == PATH_STREAM &&
+                         (draft_logits == nullptr || a.dp.path == PATH_STREAM) && gamma_max <= 31 &&
+                         (2 * gamma_max + 1) * (1 + kcap) <= kGatherWords;
+  if (list_path) {
+    a.fast = reinterpret_cast<uint4*>(ws + L.stats);
+    a.wpr = 1 + kcap;
+    const size_t smem_l = sizeof(Smem);
+    if (dtype == SPEC_BF16) {
+      err = prepare(sample_list_kernel<DT_BF16>, g_ready[14]);
+      if (err == cudaSuccess) sample_list_kernel<DT_BF16><<<grid, kThreads, smem_l, s>>>(a);
+    } else {
+      err = prepare(sample_list_kernel<DT_F32>, g_ready[15]);
+      if (err == cudaSuccess) sample_list_kernel<DT_F32><<<grid, kThreads, smem_l, s>>>(a);
+    }
+  } else if (dtype == SPEC_BF16 && ex) {
     err = prepare(sample_kernel<DT_BF16, true>, g_ready[10]);
     if (err == cudaSuccess) sample_kernel<DT_BF16, true><<<grid, kThreads, smem, s>>>(a);
     if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6]);

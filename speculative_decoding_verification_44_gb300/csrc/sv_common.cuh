@@ -31,7 +31,7 @@ enum { PATH_STREAM = 0, PATH_FULL = 1 };
 
 enum {
   SEQ_OK = 0, SEQ_BAD_LENGTH = 1, SEQ_BAD_TOKEN = 2, SEQ_BAD_UNIFORM = 3,
-  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6, SEQ_BAD_TREE = 7,
+  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6, SEQ_BAD_TREE = 7, SEQ_TIMEOUT = 8,
   SEQ_FLAG_ZERO_Q = 0x100, SEQ_FLAG_Z_ZERO = 0x200, SEQ_FLAG_EOS = 0x400
 };
 
@@ -145,6 +145,49 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
   unsigned old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+
+// ---------------------------------------------------------------- bulk copies (TMA) and mbarriers
+// One-dimensional bulk copies global -> shared by the copy engine, completion
+// counted in bytes on an mbarrier in shared memory.  Addresses 16-byte
+// aligned, sizes multiples of 16.
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Makes mbarrier initialisation visible to the copy engine (before first use).
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// Orders this thread's earlier shared-memory accesses (and those ordered
+// before them by a barrier) before later bulk copies into shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  unsigned ok;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for phase `parity` of *bar to complete, for at most about kWaitNs of
+// wall time; false if it ran out (the caller reports SEQ_TIMEOUT).
+constexpr uint64_t kWaitNs = 50ull * 1000 * 1000;   // 50 ms
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
 }
 
 // Re-read load (second pass over a row that should still sit in L2).
@@ -270,6 +313,53 @@ __device__ __forceinline__ float vec_max(const uint4& r, int n, bool& bad) {
   }
   bad = b;
   return m;
+}
+
+// ---------------------------------------------------------------- vector maxima for the stream
+// Offset-binary order key of a float's bit pattern: 2^31 plus the value's
+// sign-magnitude as a signed integer, so -0 and +0 share the key 2^31.  It is
+// monotone in the value, +inf maps to kOkeyPosInf and every positive-sign NaN
+// above it; a bf16 value in the high half of a word keeps the key's low 16
+// bits zero.  Cheaper than fkey in the streaming loop (no -0 test).
+__device__ __forceinline__ uint32_t okey_bits(uint32_t bits) {
+  const uint32_t s = static_cast<uint32_t>(static_cast<int32_t>(bits) >> 31);   // 0 or all ones
+  return 0x80000000u + (((bits & 0x7fffffffu) ^ s) - s);
+}
+constexpr uint32_t kOkeyPosInf = 0xff800000u;
+// The fkey of the value whose order key is k (okey_bits inverted).
+__device__ __forceinline__ uint32_t fkey_of_okey(uint32_t k) {
+  const uint32_t bits = k >= 0x80000000u ? (k - 0x80000000u) : (0x80000000u | (0x80000000u - k));
+  return fkey(__uint_as_float(bits));
+}
+// Order key of the largest element of a full vector.  NaN-propagating maxima
+// (max.NaN returns the canonical, positive NaN), so a vector holding a NaN or
+// +inf has a key >= kOkeyPosInf.  bf16: three packed maxima, then the two
+// halves against each other.
+template <int DT>
+__device__ __forceinline__ uint32_t vec_max_okey(const uint4& r) {
+  if (DT == DT_BF16) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
+    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    const __nv_bfloat162 mm = __hmax2_nan(m, __lowhigh2highlow(m));
+    return okey_bits(*reinterpret_cast<const uint32_t*>(&mm) & 0xffff0000u);
+  }
+  float m;
+  asm("{\n\t.reg .f32 t0, t1;\n\tmax.NaN.f32 t0, %1, %2;\n\tmax.NaN.f32 t1, %3, %4;\n\tmax.NaN.f32 %0, t0, t1;\n\t}"
+      : "=f"(m) : "f"(__uint_as_float(r.x)), "f"(__uint_as_float(r.y)), "f"(__uint_as_float(r.z)),
+        "f"(__uint_as_float(r.w)));
+  return okey_bits(__float_as_uint(m));
+}
+// cp.async of 16 bytes to a shared-window address; 16-byte shared load.
+__device__ __forceinline__ void cp_async16_to(uint32_t saddr, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(saddr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr) : "memory");
+  return v;
 }
 
 // ---------------------------------------------------------------- warp helpers

@@ -116,6 +116,7 @@ struct __align__(16) Smem {
   float seq_u[kMaxGamma];
   float seq_us;
   int early_skip;                    // early exit: this CTA's row is not read
+  uint64_t mbar[kRing];              // stash_stream_row: one mbarrier per stage of sm.u.ring
 };
 
 // ------------------------------------------------------------------ early-exit stop marks
@@ -1635,6 +1636,40 @@ __device__ __forceinline__ void append_from_vector(const uint4& r, int c, int v,
   }
 }
 
+// Lower bound K for the k-th largest element of a row: the k-th largest of the
+// per-thread maxima mk (k distinct elements reach it), found by an MSB-first
+// radix select over 8-bit digits with block-wide counts (bf16 keys: the top
+// 16 bits, two rounds).  sm.khist must be zero and visible (a barrier after
+// the clear).  Block-wide.
+template <int DT>
+__device__ __forceinline__ uint32_t select_bound(uint32_t mk0, int k, Smem& sm) {
+  const int tid = threadIdx.x;
+  constexpr int kRounds = DT == DT_BF16 ? 2 : 4;
+  uint32_t prefix = 0u;
+  uint32_t need = static_cast<uint32_t>(k);
+#pragma unroll
+  for (int rd = 0; rd < kRounds; ++rd) {
+    const int sh = 24 - 8 * rd;
+    uint32_t* hist = sm.khist[rd & 1];
+    if (rd == 0 || (mk0 >> (sh + 8)) == prefix) atomicAdd(&hist[(mk0 >> sh) & 0xffu], 1u);
+    __syncthreads();
+    if ((tid >> 5) == 0) {
+      int digit;
+      uint32_t before;
+      pick_digit_count(hist, need, true, tid & 31, digit, before);
+      if (tid == 0) {
+        sm.b_i32[4] = static_cast<int>((prefix << 8) | static_cast<uint32_t>(digit));
+        sm.b_i32[5] = static_cast<int>(need - before);
+      }
+    }
+    __syncthreads();
+    prefix = static_cast<uint32_t>(sm.b_i32[4]);
+    need = static_cast<uint32_t>(sm.b_i32[5]);
+    if (rd + 2 < kRounds) hist[tid] = 0u;           // reused two rounds later, after a barrier
+  }
+  return prefix << (32 - 8 * kRounds);
+}
+
 // PATH_STREAM row (1 <= k <= kSmallK).  Pass 1 streams the row from HBM once.
 // Each thread keeps the keys and positions of its four largest vector maxima
 // .  The k-th largest of the per-thread maxima is a lower bound K for
@@ -1703,32 +1738,7 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
     abandon_row(sm, P.cT);
     return;
   }
-  // K = the k-th largest of the kThreads maxima: MSB-first radix select, one
-  // 8-bit digit per round (bf16 keys: the top 16 bits, two rounds)
-  constexpr int kRounds = DT == DT_BF16 ? 2 : 4;
-  uint32_t prefix = 0u;
-  uint32_t need = static_cast<uint32_t>(P.k);
-#pragma unroll
-  for (int rd = 0; rd < kRounds; ++rd) {
-    const int sh = 24 - 8 * rd;
-    uint32_t* hist = sm.khist[rd & 1];
-    if (rd == 0 || (mk0 >> (sh + 8)) == prefix) atomicAdd(&hist[(mk0 >> sh) & 0xffu], 1u);
-    __syncthreads();
-    if ((tid >> 5) == 0) {
-      int digit;
-      uint32_t before;
-      pick_digit_count(hist, need, true, tid & 31, digit, before);
-      if (tid == 0) {
-        sm.b_i32[4] = static_cast<int>((prefix << 8) | static_cast<uint32_t>(digit));
-        sm.b_i32[5] = static_cast<int>(need - before);
-      }
-    }
-    __syncthreads();
-    prefix = static_cast<uint32_t>(sm.b_i32[4]);
-    need = static_cast<uint32_t>(sm.b_i32[5]);
-    if (rd + 2 < kRounds) hist[tid] = 0u;           // reused two rounds later, after a barrier
-  }
-  const uint32_t K = prefix << (32 - 8 * kRounds);
+  const uint32_t K = select_bound<DT>(mk0, P.k, sm);
   if (tid == 0) {
     sm.ncand = 0;
     sm.nfull = 0;
@@ -1763,6 +1773,119 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
       uint4 r;
       const int c = load_vec<DT, false>(row, v, r);
       if (c) append_from_vector<DT>(r, c, v, K, sm);
+    }
+    __syncthreads();
+  }
+  stream_finish<DT>(row, P, dtok, any_bad, 0.0f, sm);
+}
+
+// PATH_STREAM row for 16-byte aligned rows without stream_row's second read.
+// Thread t takes vectors t, t + kThreads, ... through its cp.async ring of
+// kRing slots, as stream_row does, and tracks its four largest vector maxima
+// (order keys and positions) -- and also keeps the vectors behind its three
+// largest in registers, so that after the stream the candidates above the
+// bound K come straight from registers.  The loop is lean on purpose: at five
+// row CTAs per SM the stream is close to bound by instruction issue, and the
+// warp schedulers then favour the oldest warps, so every instruction per
+// vector slows the last rows most.  The ring is unrolled by its depth
+// (constant slots), addresses advance by one add, the vector maximum's key is
+// vec_max_okey's, and the NaN / +inf test is made once, on the largest key.
+// Nothing is written to shared memory while the thread's copies are in flight
+// (a shared store or atomic then waits for them).  If the fourth tracked
+// maximum reaches K the thread may hold more qualifying vectors than it
+// tracked, and its vectors are re-read as in stream_row.
+template <int DT>
+__device__ void stash_stream_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
+  static_assert(kRing == 4, "the loop below is unrolled for four slots");
+  constexpr uint32_t kSlot = kThreads * 16;                 // bytes per ring slot
+  constexpr size_t kStride = static_cast<size_t>(kThreads) * 16;
+  const int tid = threadIdx.x;
+  uint32_t mk0 = 0u, mk1 = 0u, mk2 = 0u, mk3 = 0u;      // four largest vector-max keys, descending
+  int mv0 = 0, mv1 = 0, mv2 = 0, mv3 = 0;               // their vector indices
+  uint4 t0 = make_uint4(0u, 0u, 0u, 0u), t1 = t0, t2 = t0;   // the vectors of places 0, 1, 2
+#pragma unroll
+  for (int h = 0; h < 2; ++h) sm.khist[h][tid] = 0u;   // visible after the barrier below
+  const int nk = (row.nvec - tid + kThreads - 1) / kThreads;
+  const uint32_t rs = smem_u32(&sm.u.ring[0][tid]);      // slot s of this thread: rs + s kSlot
+  const char* gp = row.base + static_cast<size_t>(tid) * 16;
+#pragma unroll
+  for (int s = 0; s < kRing - 1; ++s) {
+    if (s < nk) cp_async16_to(rs + s * kSlot, gp + s * kStride);
+    cp_async_commit();
+  }
+  gp += (kRing - 1) * kStride;                           // the next vector to copy: k + 3
+  // one vector: its maximum's key, and an insertion among the tracked four
+  // (earlier vectors stay first on ties)
+  const auto take = [&](const uint4& r, int v) {
+    const uint32_t vk = vec_max_okey<DT>(r);
+    if (vk > mk3) {
+      const bool g0 = vk > mk0, g1 = vk > mk1, g2 = vk > mk2;
+      if (g2) {
+        t2 = g1 ? t1 : r;
+        t1 = g1 ? (g0 ? t0 : r) : t1;
+        t0 = g0 ? r : t0;
+      }
+      mk3 = g2 ? mk2 : vk;                 mv3 = g2 ? mv2 : v;
+      mk2 = g2 ? (g1 ? mk1 : vk) : mk2;   mv2 = g2 ? (g1 ? mv1 : v) : mv2;
+      mk1 = g1 ? (g0 ? mk0 : vk) : mk1;   mv1 = g1 ? (g0 ? mv0 : v) : mv1;
+      mk0 = g0 ? vk : mk0;                 mv0 = g0 ? v : mv0;
+    }
+  };
+  int k = 0;
+  for (; k + 2 * kRing - 1 <= nk; k += kRing) {          // every copy issued below is in range
+#pragma unroll
+    for (int j = 0; j < kRing; ++j) {
+      cp_async16_to(rs + ((j + kRing - 1) & (kRing - 1)) * kSlot, gp);
+      gp += kStride;
+      cp_async_commit();
+      cp_async_wait<kRing - 1>();                        // the copy of vector k + j has landed
+      take(lds128(rs + j * kSlot), tid + (k + j) * kThreads);
+    }
+  }
+  for (; k < nk; ++k) {
+    if (k + kRing - 1 < nk) {
+      cp_async16_to(rs + ((k + kRing - 1) & (kRing - 1)) * kSlot, gp);
+      gp += kStride;
+    }
+    cp_async_commit();
+    cp_async_wait<kRing - 1>();
+    take(lds128(rs + (k & (kRing - 1)) * kSlot), tid + k * kThreads);
+  }
+  cp_async_wait<0>();
+  // a NaN or +inf anywhere in the thread's vectors puts its largest key at or above +inf's
+  const int any_bad = __syncthreads_or(mk0 >= kOkeyPosInf ? 1 : 0);
+  const uint32_t K = select_bound<DT>(mk0, P.k, sm);     // order-key bound
+  const uint32_t Kf = fkey_of_okey(K);                   // the same bound on fkey's scale
+  if (tid == 0) {
+    sm.ncand = 0;
+    sm.nfull = 0;
+  }
+  __syncthreads();
+  if (!any_bad && mk3 != 0u && mk3 >= K) {
+    // every tracked vector qualifies and more may: the CTA re-reads all of them below
+    const int pos = atomicAdd(&sm.nfull, 1);
+    if (pos < kMaxFull) sm.full[pos] = tid;
+  } else if (!any_bad && mk0 != 0u && mk0 >= K) {
+    append_from_vector<DT>(t0, Elem<DT>::kPer, mv0, Kf, sm);
+    if (mk1 != 0u && mk1 >= K) append_from_vector<DT>(t1, Elem<DT>::kPer, mv1, Kf, sm);
+    if (mk2 != 0u && mk2 >= K) append_from_vector<DT>(t2, Elem<DT>::kPer, mv2, Kf, sm);
+  }
+  __syncthreads();
+  const int nfull = sm.nfull;
+  if (nfull > 0) {
+    // cooperative re-read: one vector per job, jobs spread over the whole CTA
+    const int per = (row.nvec + kThreads - 1) / kThreads;       // vectors per thread
+    const bool all = nfull > kMaxFull;                           // too many: re-read the whole row
+    if (all) {                       // the whole row is re-read: drop what the registers added
+      if (tid == 0) sm.ncand = 0;
+      __syncthreads();
+    }
+    const int jobs = all ? row.nvec : nfull * per;
+    for (int job = tid; job < jobs; job += kThreads) {
+      const int v = all ? job : sm.full[job / per] + (job % per) * kThreads;
+      uint4 r;
+      const int c = load_vec<DT, false>(row, v, r);
+      if (c) append_from_vector<DT>(r, c, v, Kf, sm);
     }
     __syncthreads();
   }
