@@ -117,10 +117,6 @@ enum {
                                      rule the sequence uses is outside its domain     */
     SPEC_SEQ_BAD_TREE = 7,        /* spec_verify_greedy_tree: a node whose parent is
                                      not an earlier node                              */
-    SPEC_SEQ_TIMEOUT = 8,         /* a bounded wait inside the kernel for a bulk copy
-                                     into shared memory ran out (never expected: the
-                                     copies read valid device memory); the row is
-                                     treated as failed and nothing is committed      */
     SPEC_SEQ_ERROR_MASK = 0xFF,
     SPEC_SEQ_FLAG_ZERO_Q = 0x100, /* an evaluated draft token had q(d) == 0           */
     SPEC_SEQ_FLAG_Z_ZERO = 0x200, /* residual mass was 0 after a rejection            */

@@ -31,7 +31,7 @@ enum { PATH_STREAM = 0, PATH_FULL = 1 };
 
 enum {
   SEQ_OK = 0, SEQ_BAD_LENGTH = 1, SEQ_BAD_TOKEN = 2, SEQ_BAD_UNIFORM = 3,
-  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6, SEQ_BAD_TREE = 7, SEQ_TIMEOUT = 8,
+  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6, SEQ_BAD_TREE = 7,
   SEQ_FLAG_ZERO_Q = 0x100, SEQ_FLAG_Z_ZERO = 0x200, SEQ_FLAG_EOS = 0x400
 };
 
@@ -145,49 +145,6 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
   unsigned old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
-}
-
-// ---------------------------------------------------------------- bulk copies (TMA) and mbarriers
-// One-dimensional bulk copies global -> shared by the copy engine, completion
-// counted in bytes on an mbarrier in shared memory.  Addresses 16-byte
-// aligned, sizes multiples of 16.
-__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-// Makes mbarrier initialisation visible to the copy engine (before first use).
-__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-// Orders this thread's earlier shared-memory accesses (and those ordered
-// before them by a barrier) before later bulk copies into shared memory.
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
-  unsigned ok;
-  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Waits for phase `parity` of *bar to complete, for at most about kWaitNs of
-// wall time; false if it ran out (the caller reports SEQ_TIMEOUT).
-constexpr uint64_t kWaitNs = 50ull * 1000 * 1000;   // 50 ms
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
-  }
 }
 
 // Re-read load (second pass over a row that should still sit in L2).

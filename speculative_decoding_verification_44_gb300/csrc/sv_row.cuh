@@ -116,7 +116,6 @@ struct __align__(16) Smem {
   float seq_u[kMaxGamma];
   float seq_us;
   int early_skip;                    // early exit: this CTA's row is not read
-  uint64_t mbar[kRing];              // stash_stream_row: one mbarrier per stage of sm.u.ring
 };
 
 // ------------------------------------------------------------------ early-exit stop marks
