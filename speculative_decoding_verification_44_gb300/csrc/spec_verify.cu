@@ -159,48 +159,45 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const float* p,
 }
 
 // Warp-wide inverse-CDF draw over a kept list stored in token order (n <=
-// kListCap entries; lane l takes entries 4l .. 4l+3, so lane order is
-// vocabulary order).  Weights max(0, p - beta q(x)) for a residual [wrblog §5;
-// magicnet §8], p itself for the bonus draw; C(x) and Z come from a
-// double-float warp scan (no float64 arithmetic: that pipe is slow here).  The
-// token is the smallest x with C(x) > u Z, or the last entry with weight if
-// rounding leaves none.  Z == 0 after a rejection falls back to the draw from
-// p and sets SEQ_FLAG_Z_ZERO.  Returns -1 when no entry has weight.
+// kListCap entries, taken in chunks of 32: entry 32c + l is lane l's entry of
+// chunk c, so lane order within a chunk and chunk order are vocabulary order).
+// Weights max(0, p - beta q(x)) for a residual [wrblog §5; magicnet §8], p
+// itself for the bonus draw; C(x) and Z come from double-float warp scans
+// (no float64 arithmetic: that pipe is slow here).  The token is the
+// smallest x with C(x) > u Z, or the last entry with weight if rounding
+// leaves none.  Z == 0 after a rejection falls back to the draw from p and
+// sets SEQ_FLAG_Z_ZERO.  Returns -1 when no entry has weight.
 // entry_at(e) gives entry e; q_of(x) gives q(x) (residual draws only).
 template <class EntryAt, class QOf>
 __device__ __forceinline__ int warp_list_draw(EntryAt entry_at, int n, bool residual, QOf q_of, float beta,
                                               float uf, float& Z_resid, int& flags) {
   const int lane = threadIdx.x & 31;
-  int tok[4];
-  df pw[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int e = 4 * lane + j;
-    tok[j] = 0x7fffffff;
-    pw[j] = df_from(0.0f);
-    if (e < n) {
-      const ListEntry le = entry_at(e);
-      tok[j] = le.token;
-      pw[j] = {le.p, le.p_lo};
-    }
-  }
+  const int nch = (n + 31) >> 5;
+  // lane's entry of chunk c: its token and weight (weights (p - beta q)+ when resid)
+  const auto weight_of = [&](int c, bool resid, int& tok) -> df {
+    const int e = 32 * c + lane;
+    tok = 0x7fffffff;
+    if (e >= n) return df_from(0.0f);
+    const ListEntry le = entry_at(e);
+    tok = le.token;
+    const df p = {le.p, le.p_lo};
+    if (!resid) return p;
+    const float q = q_of(le.token);
+    const float bq = beta * q;                          // beta q exactly, as hi + lo
+    const df d = df_add(p, {-bq, -fmaf(beta, q, -bq)});
+    return d.hi > 0.0f ? d : df_from(0.0f);
+  };
   for (int pass = 0; pass < 2; ++pass) {
     const bool resid = residual && pass == 0;
-    df w[4];
-    df s = df_from(0.0f);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      w[j] = pw[j];
-      if (resid && 4 * lane + j < n) {
-        const float q = q_of(tok[j]);
-        const float bq = beta * q;                      // beta q exactly, as hi + lo
-        const df d = df_add(pw[j], {-bq, -fmaf(beta, q, -bq)});
-        w[j] = d.hi > 0.0f ? d : df_from(0.0f);
-      }
-      s = df_add(s, w[j]);
+    // Z over all chunks; chunk 0 (the whole list when n <= 32) stays in registers
+    int tok0;
+    const df w0 = weight_of(0, resid, tok0);
+    const df incl0 = warp_incl_scan_df(w0, lane);
+    df Z = df_shfl(incl0, 31);
+    for (int c = 1; c < nch; ++c) {
+      int tk;
+      Z = df_add(Z, df_shfl(warp_incl_scan_df(weight_of(c, resid, tk), lane), 31));
     }
-    const df incl = warp_incl_scan_df(s, lane);
-    const df Z = df_shfl(incl, 31);
     if (resid) Z_resid = Z.hi;
     if (!(Z.hi > 0.0f)) {
       if (resid) {                                      // Z == 0 after a rejection: draw from p instead
@@ -211,27 +208,23 @@ __device__ __forceinline__ int warp_list_draw(EntryAt entry_at, int n, bool resi
     }
     const float th = uf * Z.hi;
     const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
-    df c = df_shfl_up(incl, 1);                         // exclusive prefix of this lane
-    if (lane == 0) c = df_from(0.0f);
-    int first = 0x7fffffff, lastp = -1;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (w[j].hi > 0.0f) {
-        c = df_add(c, w[j]);
-        lastp = 4 * lane + j;
-        if (first == 0x7fffffff && !df_ge(t, c)) first = 4 * lane + j;   // C(x) > u Z
+    df base = df_from(0.0f);
+    int last_tok = -1;
+    for (int c = 0; c < nch; ++c) {
+      int tk = tok0;
+      df w = w0, incl = incl0;
+      if (c > 0) {
+        w = weight_of(c, resid, tk);
+        incl = warp_incl_scan_df(w, lane);
       }
+      const bool pos = w.hi > 0.0f;
+      const unsigned hit = __ballot_sync(kFull, pos && !df_ge(t, df_add(base, incl)));   // C(x) > u Z
+      if (hit) return __shfl_sync(kFull, tk, __ffs(hit) - 1);
+      const unsigned any = __ballot_sync(kFull, pos);
+      if (any) last_tok = __shfl_sync(kFull, tk, 31 - __clz(any));
+      base = df_add(base, df_shfl(incl, 31));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      first = min(first, __shfl_xor_sync(kFull, first, o));
-      lastp = max(lastp, __shfl_xor_sync(kFull, lastp, o));
-    }
-    const int sel = first != 0x7fffffff ? first : lastp;
-    if (sel < 0) return -1;
-    const int js = sel & 3;
-    const int mine = js == 0 ? tok[0] : (js == 1 ? tok[1] : (js == 2 ? tok[2] : tok[3]));
-    return __shfl_sync(kFull, mine, sel >> 2);
+    return last_tok;                                    // rounding left u Z at or above the total
   }
   return -1;
 }
@@ -1055,6 +1048,12 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  // launched as a programmatic dependent: the previous grid in the stream must
+  // be complete, its writes visible, before this one touches any memory; the
+  // next call's CTAs may then be placed as this grid's CTAs retire, so its
+  // launch overlaps this call's tail
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int tid = threadIdx.x;
   const int slots = 2 * a.G + 1;
   const int b = blockIdx.x / slots;
@@ -1867,13 +1866,22 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   if (list_path) {
     a.fast = reinterpret_cast<uint4*>(ws + L.stats);
     a.wpr = 1 + kcap;
-    const size_t smem_l = sizeof(Smem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(Smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (dtype == SPEC_BF16) {
       err = prepare(sample_list_kernel<DT_BF16>, g_ready[14]);
-      if (err == cudaSuccess) sample_list_kernel<DT_BF16><<<grid, kThreads, smem_l, s>>>(a);
+      if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, sample_list_kernel<DT_BF16>, a);
     } else {
       err = prepare(sample_list_kernel<DT_F32>, g_ready[15]);
-      if (err == cudaSuccess) sample_list_kernel<DT_F32><<<grid, kThreads, smem_l, s>>>(a);
+      if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, sample_list_kernel<DT_F32>, a);
     }
   } else if (dtype == SPEC_BF16 && ex) {
     err = prepare(sample_kernel<DT_BF16, true>, g_ready[10]);

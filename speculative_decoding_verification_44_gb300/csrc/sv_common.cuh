@@ -309,6 +309,11 @@ __device__ __forceinline__ uint32_t vec_max_okey(const uint4& r) {
         "f"(__uint_as_float(r.w)));
   return okey_bits(__float_as_uint(m));
 }
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible (returns at once without such a
+// dependency); allow the grids that depend on this one to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // cp.async of 16 bytes to a shared-window address; 16-byte shared load.
 __device__ __forceinline__ void cp_async16_to(uint32_t saddr, const void* gmem) {
   asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(saddr), "l"(gmem) : "memory");

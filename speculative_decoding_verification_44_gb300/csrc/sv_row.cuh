@@ -1563,32 +1563,38 @@ __device__ __noinline__ void stream_finish(const Row row, const RowParams P, con
         s = df_add(s, df_from(w[j]));
       }
       const df incl = warp_incl_scan_df(s, lane);
+      // W = the kept weights' sum: the cumulative sum through the last kept
+      // position (all of them without a top-p cut)
+      df W = df_shfl(incl, 31);
       int n_keep = ntop;
       if (P.top_p < 1.0f) {
-        const df S = df_shfl(incl, 31);
+        const df S = W;
         const float th = P.top_p * S.hi;                       // target = top_p * S, double-float
         const df target = {th, fmaf(P.top_p, S.hi, -th) + P.top_p * S.lo};
-        df acc = df_add(incl, {-s.hi, -s.lo});                 // exclusive prefix
+        df acc = df_shfl_up(incl, 1);                          // exclusive prefix of this lane
+        if (lane == 0) acc = df_from(0.0f);
         int first = 0x7fffffff;
+        df at_first = S;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int pos = 4 * lane + j;
           if (pos < ntop) {
             acc = df_add(acc, df_from(w[j]));
-            if (first == 0x7fffffff && df_ge(acc, target)) first = pos;
+            if (first == 0x7fffffff && df_ge(acc, target)) {
+              first = pos;
+              at_first = acc;
+            }
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(kFull, first, o));
-        n_keep = first == 0x7fffffff ? ntop : first + 1;
+        const unsigned fb = __ballot_sync(kFull, first != 0x7fffffff);   // positions are lane-blocked
+        if (fb) {
+          const int L = __ffs(fb) - 1;
+          n_keep = __shfl_sync(kFull, first, L) + 1;
+          W = df_shfl(at_first, L);
+        }
       }
-      df part = df_from(0.0f);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (4 * lane + j < n_keep) part = df_add(part, df_from(w[j]));
       // 1 / W as a double-float: a float reciprocal refined by one Newton step
       // (the float64 pipe is far slower than the float pipe on this part)
-      const df W = warp_sum_df(part);
       const float r = __frcp_rn(W.hi);
       const float r_lo = r * (fmaf(-W.hi, r, 1.0f) - W.lo * r);
       int hit = -1;
