@@ -195,6 +195,9 @@ def oracle_sample_time(w, seqs, budget_s=None):
     gam = w.gamma_per_seq.cpu().numpy() if w.gamma_per_seq is not None else None
     oh = w.draft_is_onehot.cpu().numpy() if w.draft_is_onehot is not None else None
     positions, elapsed, n = 0, 0.0, 0
+    seqs = list(seqs)
+    if budget_s is not None:                  # cycle over the sequences until the budget is spent
+        seqs = seqs * 1000
     for b in seqs:
         tl = f64(w.target_logits[b:b + 1])
         dl = f64(w.draft_logits[b:b + 1])
@@ -211,6 +214,89 @@ def oracle_sample_time(w, seqs, budget_s=None):
         if budget_s is not None and elapsed >= budget_s:
             break
     return positions, elapsed, n
+
+
+def _oracle_one(args):
+    """One sequence through the oracle (a worker of the all-cores baseline)."""
+    import oracle
+    tl, dl, toks, ua, us, tp, dp, g, o = args
+    oracle.verify_sample(tl, dl, toks, ua, us, tp, dp, gamma_per_seq=g, one_hot=o)
+    return (int(g[0]) if g is not None else toks.shape[1]) + 1
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                k = ln.split(":", 1)[0].strip().lower()
+                if k in ("model name", "cpu model"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_sample_time_pool(w, seqs, budget_s=12.0):
+    """The oracle on all host cores: a spawn-started process pool, one sequence per task.
+    Returns (positions, seconds, sequences, workers)."""
+    import multiprocessing as mp
+    import numpy as np
+
+    def f64(t):
+        return t.detach().to("cpu").float().double().numpy()
+
+    tp = (float(np.float32(w.target_params.temperature)), int(w.target_params.top_k),
+          float(np.float32(w.target_params.top_p)))
+    dp = (float(np.float32(w.draft_params.temperature)), int(w.draft_params.top_k),
+          float(np.float32(w.draft_params.top_p)))
+    gam = w.gamma_per_seq.cpu().numpy() if w.gamma_per_seq is not None else None
+    oh = w.draft_is_onehot.cpu().numpy() if w.draft_is_onehot is not None else None
+    workers = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    ctx = mp.get_context("spawn")
+    tasks = [(f64(w.target_logits[b:b + 1]), f64(w.draft_logits[b:b + 1]), w.draft_tokens[b:b + 1].cpu().numpy(),
+              w.u_accept[b:b + 1].cpu().double().numpy(), w.u_sample[b:b + 1].cpu().double().numpy(), tp, dp,
+              gam[b:b + 1] if gam is not None else None, oh[b:b + 1] if oh is not None else None) for b in seqs]
+    with ctx.Pool(workers) as pool:
+        pool.map(_oracle_one, tasks[:workers])            # warm the workers (imports)
+        positions, n = 0, 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:   # cycle over the sequences until the budget is spent
+            chunk = [tasks[(n + i) % len(tasks)] for i in range(workers)]
+            positions += sum(pool.map(_oracle_one, chunk))
+            n += len(chunk)
+        elapsed = time.perf_counter() - t0
+    return positions, elapsed, n, workers
+
+
+def outcome_stats(outs, sets, G):
+    """Per-position empirical acceptance and the emitted-count histogram of the given outputs:
+    acceptance at position i = P(draft i accepted | drafts before i accepted), over the
+    sequences with gamma_b > i."""
+    import torch
+    acc_n = [0] * G
+    acc_d = [0] * G
+    hist = [0] * (G + 2)
+    for o, w in zip(outs, sets):
+        nacc = o.num_accepted.cpu().long()
+        gb = (w.gamma_per_seq.cpu().long() if w.gamma_per_seq is not None
+              else torch.full_like(nacc, G))
+        for i in range(G):
+            reach = (nacc >= i) & (gb > i)
+            acc_d[i] += int(reach.sum())
+            acc_n[i] += int((reach & (nacc > i)).sum())
+        for e in (nacc[nacc >= 0] + 1).tolist():
+            hist[e] += 1
+    return {"acceptance_per_position": [round(n / d, 4) if d else None for n, d in zip(acc_n, acc_d)],
+            "emitted_count_histogram": {str(k): v for k, v in enumerate(hist) if k >= 1},
+            "sequences": sum(int(o.num_accepted.numel()) for o in outs)}
 
 
 def replica_ids(rank: int, rotate: int = ROTATE) -> list[int]:
@@ -449,6 +535,7 @@ def main():
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     graph = None
+    g_ev = None
     if not args.no_graph:
         # the same K calls captured once as a CUDA graph (serving loops replay graphs:
         # no host launch gap between steps); each call is still one C-ABI launch
@@ -464,9 +551,20 @@ def main():
                 gcalls[i]()
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
+        # timing events recorded inside the graph (event-record nodes): the region is
+        # the K steps' device work, without the host's graph launch latency
+        try:
+            g_ev = (torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True))
+        except TypeError:
+            g_ev = None
         with torch.cuda.graph(graph, stream=gstream):
+            if g_ev is not None:
+                g_ev[0].record(gstream)
             for i in range(K):
                 gcalls[i % ROTATE]()
+            if g_ev is not None:
+                g_ev[1].record(gstream)
         graph.replay()
         torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
@@ -493,7 +591,32 @@ def main():
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    total_ms = t_all0.elapsed_time(t_all1)
+        in_graph_ms = g_ev[0].elapsed_time(g_ev[1]) if g_ev is not None else None
+        # spread: the same K-step region repeated until >= 200 calls and >= 0.5 s, each
+        # repetition timed on the device (per-step times: median, p10, p90)
+        rep_ms = []
+        r_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        t_spread = time.perf_counter()
+        while len(rep_ms) < 4096 and (len(rep_ms) * K < 200 or time.perf_counter() - t_spread < 0.5):
+            r_ev[0].record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(K):
+                    step(i)
+            r_ev[1].record(stream)
+            torch.cuda.synchronize()
+            ev_pair = g_ev if g_ev is not None else r_ev
+            rep_ms.append(ev_pair[0].elapsed_time(ev_pair[1]) / K)
+    rep_ms.sort()
+
+    def pct(v, q):
+        return v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]
+
+    spread = {"repetitions": len(rep_ms), "calls": len(rep_ms) * K, "ms_per_step_median": pct(rep_ms, 0.5),
+              "ms_per_step_p10": pct(rep_ms, 0.1), "ms_per_step_p90": pct(rep_ms, 0.9)}
+    outer_ms = t_all0.elapsed_time(t_all1)
+    total_ms = in_graph_ms if in_graph_ms is not None else outer_ms
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / K
@@ -522,7 +645,16 @@ def main():
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = profile_traffic() if wid == WID else None
     dname = "bf16" if esize == 2 else "f32"
-    kname = f"sv::sample_kernel<{dname}>" + (f" + sv::draw_kernel<{dname}>" if full_target else "")
+    # the kept-list kernel serves the plain and lenient calls when every row is on the
+    # streaming top-k path, rows are 16-byte aligned and each sequence's row blocks
+    # fit its gather buffer (the library's own dispatch rule)
+    tk, dk = int(w0.target_params.top_k), int(w0.draft_params.top_k)
+    kcap = max(tk, dk if w0.draft_logits is not None else 0)
+    list_path = (not args.early_exit and args.eos is None and not args.per_seq_rules and not full_target
+                 and (w0.draft_logits is None or 1 <= dk <= 128 and dk < V) and (V * esize) % 16 == 0
+                 and G <= 31 and (2 * G + 1) * (1 + kcap) <= 1024)
+    kname = (f"sv::sample_list_kernel<{dname}>" if list_path else f"sv::sample_kernel<{dname}>"
+             + (f" + sv::draw_kernel<{dname}>" if full_target else ""))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_kind": f"of {peak_kind}",
                 "kernel": kname, "algorithmic_bytes_per_launch": alg_bytes,
@@ -573,10 +705,16 @@ def main():
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        pos, secs, n = oracle_sample_time(w0, list(range(B)), budget_s=12.0)
-        cpu_baseline = {"value": pos / secs, "unit": "positions/s", "cores": 1, "kind": "oracle",
-                        "sample": f"first {n} of {B} sequences of the same workload (rotation set 0), "
-                                  f"{pos} verified positions in {secs:.1f} s"}
+        pos, secs, n = oracle_sample_time(w0, list(range(B)), budget_s=10.0)
+        single = {"value": pos / secs, "unit": "positions/s", "cores": 1,
+                  "sample": f"{n} sequence verifications cycling over the {B} sequences of the same workload "
+                            f"(rotation set 0), {pos} verified positions in {secs:.1f} s"}
+        ppos, psecs, pn, workers = oracle_sample_time_pool(w0, list(range(B)), budget_s=10.0)
+        cpu_baseline = {"value": ppos / psecs, "unit": "positions/s", "cores": workers, "kind": "oracle",
+                        "sample": f"{pn} sequence verifications cycling over the {B} sequences of the same "
+                                  f"workload (rotation set 0), one per task on a {workers}-process pool, "
+                                  f"{ppos} verified positions in {psecs:.1f} s",
+                        "cpu": cpu_model(), "single_core": single}
 
     if rank == 0:
         line = {
@@ -589,11 +727,16 @@ def main():
                        "l2": f"inputs rotate over {ROTATE} independent sets of {logits_bytes / 1e6:.1f} MB "
                              f"(each larger than the {L2_BYTES / 2**20:.0f} MiB L2)",
                        "parallelism": f"replicas x{world} (one batch per GPU, no data-path collective)",
-                       "launch": ("K steps as one CUDA graph replay" if graph is not None else "K eager launches")
-                                 + "; roofline from per-launch events on eager launches"},
+                       "launch": ("K steps as one CUDA graph replay, timed by event-record nodes inside the graph"
+                                  if g_ev is not None else
+                                  "K steps as one CUDA graph replay" if graph is not None else "K eager launches")
+                                 + "; roofline from the timed region's average time per launch"},
+            "ms_per_step_with_graph_launch": outer_ms / K,
+            "spread": spread,
             "sequences_per_s": B * world / (ms_per_step / 1e3),
             "drafts_judged_per_s": B * G * world / (ms_per_step / 1e3),
             "emitted_tokens_per_s_last_step": emitted * world / (ms_per_step / 1e3),
+            "outcomes": outcome_stats(outs, sets, G),
             "logits_bytes_per_verified_position": logits_bytes / rt,
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
             "gpu_launches": K * (2 if full_target else 1),
