@@ -322,11 +322,12 @@ SPEC_API spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_
  * One launch over (position, sequence) pairs, positions first, so a row's
  * predecessors have usually finished when it starts; no CTA waits for
  * another.  A row whose predecessors are still running is read
- * speculatively: out_rows_read can exceed (the stop + 1).
+ * speculatively (and abandoned part-way if an earlier row stops the sequence
+ * meanwhile): out_rows_read can exceed (the stop + 1).
  * workspace     spec_greedy_workspace_size() bytes, same zero-fill rule
  *               (the kernel leaves it reusable).
- * out_rows_read [batch] int32: target rows read (0 for a length or token
- *               error), or NULL.  Other arguments as for spec_verify_greedy. */
+ * out_rows_read [batch] int32: target rows read to the end (0 for a length or
+ *               token error), or NULL.  Other arguments as for spec_verify_greedy. */
 SPEC_API spec_status_t spec_verify_greedy_early(const void* target_logits, spec_dtype_t dtype,
                                        const int32_t* draft_tokens, const int32_t* gamma_per_seq,
                                        int32_t batch, int32_t gamma_max, int32_t vocab,

@@ -1505,7 +1505,9 @@ __global__ void __launch_bounds__(kThreads, 5) greedy_tree_kernel(const TreeArgs
 // it.  Stop records encode row s as G + 1 - s (0 = none) so that atomicMax
 // keeps the earliest stop and a zero-filled workspace means "no stop".
 //
-// Rows whose predecessors are still running are read speculatively.  Making
+// Rows whose predecessors are still running are read speculatively; each
+// warp of such a row keeps watching the stop record and the row is abandoned
+// (reported as not read) once an earlier row stops the sequence.  Making
 // such a CTA wait (bounded) for the row a wave earlier cut the rows read from
 // about 7.1 to 5.3 per sequence at greedy-at-scale sizes but made the launch
 // slower (waiting CTAs hold slots, and the waves serialise), so nothing waits.
@@ -1532,17 +1534,27 @@ __global__ void __launch_bounds__(kThreads, 5) greedy_early_kernel(const GreedyA
     return;
   }
   if (i > gb) return;
-  if (threadIdx.x == 0) sm.b_i32[0] = static_cast<int>(__ldcg(&stop_enc[b]));
+  if (threadIdx.x == 0) {
+    sm.b_i32[0] = static_cast<int>(__ldcg(&stop_enc[b]));
+    sm.early_skip = 0;
+  }
   __syncthreads();
   const bool skip = static_cast<uint32_t>(sm.b_i32[0]) > static_cast<uint32_t>(slots - i);   // a stop before row i
-  int2 res = make_int2(-1, -1);   // (argmax, status); status -1 = row not read
+  int2 res = make_int2(-1, -1);   // (argmax, status); status -1 = row not read (or abandoned)
   if (!skip) {
     const Row row = make_row<DT>(a.tgt + (ob + i) * a.row_bytes, a.V, a.aligned != 0);
+    StopCheck sc;                  // a stop before row i arriving meanwhile abandons the row
+    if (i > 0) {
+      sc.p = stop_enc + b;
+      sc.thr = static_cast<unsigned>(slots - i);
+    }
     int g, st;
-    greedy_row<DT>(row, sm, g, st);
-    res = make_int2(g, st);
-    if (threadIdx.x == 0 && (st != SEQ_OK || (i < gb && a.tokens[tb + i] != g)))
-      atomicMax(&stop_enc[b], static_cast<uint32_t>(slots - i));
+    greedy_row<DT>(row, sm, g, st, sc);
+    if (!sm.early_skip) {
+      res = make_int2(g, st);
+      if (threadIdx.x == 0 && (st != SEQ_OK || (i < gb && a.tokens[tb + i] != g)))
+        atomicMax(&stop_enc[b], static_cast<uint32_t>(slots - i));
+    }
   }
   if (threadIdx.x == 0) a.rows[ob + i] = res;
   __threadfence();

@@ -299,14 +299,26 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, Smem& sm) {
 
 // ------------------------------------------------------------------ greedy row
 // argmax_x z(x), lowest index on ties [wrblog §7.1]; status for NaN / +inf / all -inf.
+// sc: the early-exit stop mark to watch (none by default); a warp that sees
+// it set stops reading and raises sm.early_skip, which the caller has cleared
+// behind a barrier and reads after this function returns.
 template <int DT>
-__device__ void greedy_row(const Row row, Smem& sm, int& argmax, int& status) {
+__device__ void greedy_row(const Row row, Smem& sm, int& argmax, int& status, const StopCheck sc = StopCheck()) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x;
   float best = -__int_as_float(0x7f800000);
   int best_i = -1;
   bool bad = false;
-  for (int base = 0; base < row.nvec; base += kThreads * kUnroll) {
+  unsigned seen = 0u;     // the stop mark as read two iterations earlier (one load per warp)
+  int it = 0;
+  for (int base = 0; base < row.nvec; base += kThreads * kUnroll, ++it) {
+    if (sc.p && (it & 1)) {
+      if (seen > sc.thr) {                             // the sequence stopped: abandon the row
+        if ((tid & 31) == 0) sm.early_skip = 1;
+        break;
+      }
+      seen = ld_relaxed_u32(sc.p);                     // consumed two iterations later
+    }
     uint4 r[kUnroll];
     int cnt[kUnroll];
 #pragma unroll
