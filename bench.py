@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--workload", default="serving-zipf-topk-topp",
                     help="workload to time (default: the serving workload); the others exist for "
                          "profiling the full-row, small-vocabulary and greedy paths")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (smaller cases for profiling; not a bench line)")
     ap.add_argument("--early-exit", action="store_true",
                     help="greedy: spec_verify_greedy_early; sampling: spec_verify_sample_ex with early_exit "
                          "(positions in order, rows after each sequence's stop skipped)")
@@ -377,7 +379,8 @@ def run_reference(args, rank):
 def run_greedy(args, rank, world, dev, sv, workloads):
     """Greedy workload (all rows, or early exit): device-timed steps over rotating inputs."""
     import torch
-    sets = [workloads.make(GREEDY_WID, dev, replica=rep) for rep in replica_ids(rank)]
+    sets = [workloads.make(GREEDY_WID, dev, replica=rep, **({"B": args.batch} if args.batch else {}))
+            for rep in replica_ids(rank)]
     w0 = sets[0]
     B, G, V = w0.B, w0.G, w0.V
     rt, _ = w0.rows_used()
@@ -496,7 +499,8 @@ def main():
     if wid == GREEDY_WID:
         run_greedy(args, rank, world, dev, sv, workloads)
         return
-    sets = [workloads.make(wid, dev, draft_probs=gpu_draft_probs, replica=rep) for rep in replica_ids(rank)]
+    sets = [workloads.make(wid, dev, draft_probs=gpu_draft_probs, replica=rep,
+                           **({"B": args.batch} if args.batch else {})) for rep in replica_ids(rank)]
     w0 = sets[0]
     B, G, V = w0.B, w0.G, w0.V
     rt, rd = w0.rows_used()

@@ -895,9 +895,8 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
 // The verifier for the common serving case: every used row takes the
 // streaming top-k path (1 <= top_k <= kSmallK on both sides, or one-hot
 // drafts), rows are 16-byte aligned and gamma_max <= 31.  Each row CTA streams
-// its row keeping its best vectors in registers (stash_stream_row: the
-// candidates above the bound need no second read of the row), and publishes
-// one contiguous block: a ListRec and the kept list in token order.  The CTA that
+// its row with the lean loop of lean_stream_row and publishes one contiguous
+// block: a ListRec and the kept list in token order.  The CTA that
 // finishes last for a sequence reads all of the sequence's blocks in one
 // round trip, draws at every position in parallel and lets warp 0 decide:
 // status, the left-to-right acceptance scan, the outputs [wrblog §5, §6;
@@ -1085,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleAr
     const int t = a.tokens[static_cast<size_t>(b) * a.G + i];
     dtok = (t >= 0 && t < a.V) ? t : -1;
   }
-  stash_stream_row<DT>(row, is_draft ? a.dp : a.tp, dtok, sm);
+  lean_stream_row<DT>(row, is_draft ? a.dp : a.tp, dtok, sm);
 
   // publish the row's block: its record, then its kept list in token order
   uint4* dst = a.fast + (static_cast<size_t>(b) * slots + slot) * a.wpr;

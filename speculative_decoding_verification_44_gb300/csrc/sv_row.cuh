@@ -1796,30 +1796,30 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
   stream_finish<DT>(row, P, dtok, any_bad, 0.0f, sm);
 }
 
-// PATH_STREAM row for 16-byte aligned rows without stream_row's second read.
-// Thread t takes vectors t, t + kThreads, ... through its cp.async ring of
-// kRing slots, as stream_row does, and tracks its four largest vector maxima
-// (order keys and positions) -- and also keeps the vectors behind its three
-// largest in registers, so that after the stream the candidates above the
-// bound K come straight from registers.  The loop is lean on purpose: at five
-// row CTAs per SM the stream is close to bound by instruction issue, and the
-// warp schedulers then favour the oldest warps, so every instruction per
-// vector slows the last rows most.  The ring is unrolled by its depth
-// (constant slots), addresses advance by one add, the vector maximum's key is
-// vec_max_okey's, and the NaN / +inf test is made once, on the largest key.
-// Nothing is written to shared memory while the thread's copies are in flight
-// (a shared store or atomic then waits for them).  If the fourth tracked
-// maximum reaches K the thread may hold more qualifying vectors than it
-// tracked, and its vectors are re-read as in stream_row.
+// PATH_STREAM row for 16-byte aligned rows: stream_row's analysis with a
+// leaner streaming loop.  Thread t takes vectors t, t + kThreads, ... through
+// its cp.async ring of kRing slots and tracks its four largest vector maxima
+// (order keys and positions).  At five row CTAs per SM the stream is close to
+// bound by instruction issue, and the warp schedulers then favour the oldest
+// warps, so every instruction per vector slows the last rows most: the ring is
+// unrolled by its depth (constant slots), addresses advance by one add, the
+// vector maximum's key is vec_max_okey's, and the NaN / +inf test is made
+// once, on the largest key.  Nothing is written to shared memory while the
+// thread's copies are in flight (a shared store or atomic then waits for
+// them).  After the bound K is known each thread re-reads its qualifying
+// tracked vectors in one round trip; if the fourth tracked maximum reaches K
+// the thread may hold more qualifying vectors than it tracked, and the block
+// re-reads all of them.  (Keeping the three best vectors in registers instead
+// of re-reading them measured slower: the register moves ride on the
+// insertion that nearly every warp-iteration takes.)
 template <int DT>
-__device__ void stash_stream_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
+__device__ void lean_stream_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
   static_assert(kRing == 4, "the loop below is unrolled for four slots");
   constexpr uint32_t kSlot = kThreads * 16;                 // bytes per ring slot
   constexpr size_t kStride = static_cast<size_t>(kThreads) * 16;
   const int tid = threadIdx.x;
   uint32_t mk0 = 0u, mk1 = 0u, mk2 = 0u, mk3 = 0u;      // four largest vector-max keys, descending
   int mv0 = 0, mv1 = 0, mv2 = 0, mv3 = 0;               // their vector indices
-  uint4 t0 = make_uint4(0u, 0u, 0u, 0u), t1 = t0, t2 = t0;   // the vectors of places 0, 1, 2
 #pragma unroll
   for (int h = 0; h < 2; ++h) sm.khist[h][tid] = 0u;   // visible after the barrier below
   const int nk = (row.nvec - tid + kThreads - 1) / kThreads;
@@ -1837,11 +1837,6 @@ __device__ void stash_stream_row(const Row row, const RowParams& P, int dtok, Sm
     const uint32_t vk = vec_max_okey<DT>(r);
     if (vk > mk3) {
       const bool g0 = vk > mk0, g1 = vk > mk1, g2 = vk > mk2;
-      if (g2) {
-        t2 = g1 ? t1 : r;
-        t1 = g1 ? (g0 ? t0 : r) : t1;
-        t0 = g0 ? r : t0;
-      }
       mk3 = g2 ? mk2 : vk;                 mv3 = g2 ? mv2 : v;
       mk2 = g2 ? (g1 ? mk1 : vk) : mk2;   mv2 = g2 ? (g1 ? mv1 : v) : mv2;
       mk1 = g1 ? (g0 ? mk0 : vk) : mk1;   mv1 = g1 ? (g0 ? mv0 : v) : mv1;
@@ -1883,9 +1878,13 @@ __device__ void stash_stream_row(const Row row, const RowParams& P, int dtok, Sm
     const int pos = atomicAdd(&sm.nfull, 1);
     if (pos < kMaxFull) sm.full[pos] = tid;
   } else if (!any_bad && mk0 != 0u && mk0 >= K) {
-    append_from_vector<DT>(t0, Elem<DT>::kPer, mv0, Kf, sm);
-    if (mk1 != 0u && mk1 >= K) append_from_vector<DT>(t1, Elem<DT>::kPer, mv1, Kf, sm);
-    if (mk2 != 0u && mk2 >= K) append_from_vector<DT>(t2, Elem<DT>::kPer, mv2, Kf, sm);
+    uint4 r0, r1, r2;
+    const int c0 = load_vec<DT, false>(row, mv0, r0);
+    const int c1 = (mk1 != 0u && mk1 >= K) ? load_vec<DT, false>(row, mv1, r1) : 0;
+    const int c2 = (mk2 != 0u && mk2 >= K) ? load_vec<DT, false>(row, mv2, r2) : 0;
+    append_from_vector<DT>(r0, c0, mv0, Kf, sm);
+    if (c1) append_from_vector<DT>(r1, c1, mv1, Kf, sm);
+    if (c2) append_from_vector<DT>(r2, c2, mv2, Kf, sm);
   }
   __syncthreads();
   const int nfull = sm.nfull;
