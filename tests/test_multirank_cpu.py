@@ -58,3 +58,63 @@ def test_metric_names_the_call_variant():
     assert bench.variant_of(argparse.Namespace(**{**base, "early_exit": True})) == " (early exit)"
     both = bench.variant_of(argparse.Namespace(**{**base, "lenience": 0.5, "early_exit": True}))
     assert "lenience 0.5" in both and "early exit" in both
+
+
+def _shard_worker(rank, world, port, out):
+    """One rank: a contiguous slice of the batch through the oracle, then gather."""
+    import numpy as np
+    import torch.distributed as dist
+    import oracle
+    from speculative_decoding_verification_44_gb300 import workloads
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = _small_serving_workload(workloads, oracle, np)
+        lo, hi = rank * w.B // world, (rank + 1) * w.B // world
+        mine = _oracle_rows(w, lo, hi, oracle, np)
+        parts = [None] * world
+        dist.all_gather_object(parts, mine)
+        if rank == 0:
+            out["gathered"] = [s for p in parts for s in p]
+    finally:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _small_serving_workload(workloads, oracle, np):
+    import torch
+
+    def oracle_probs(rows, params):
+        p, _ = oracle.transform_rows(rows.float().double().numpy(), float(np.float32(params.temperature)),
+                                     int(params.top_k), float(np.float32(params.top_p)))
+        return torch.from_numpy(p)
+    return workloads.make(3, "cpu", draft_probs=oracle_probs, B=6, V=2048)
+
+
+def _oracle_rows(w, lo, hi, oracle, np):
+    """Per-sequence oracle results of sequences lo..hi-1 (tokens, count, a_i, Z)."""
+    tp = (float(np.float32(w.target_params.temperature)), int(w.target_params.top_k),
+          float(np.float32(w.target_params.top_p)))
+    res = oracle.verify_sample(w.target_logits[lo:hi].float().double().numpy(),
+                               w.draft_logits[lo:hi].float().double().numpy(), w.draft_tokens[lo:hi].numpy(),
+                               w.u_accept[lo:hi].double().numpy(), w.u_sample[lo:hi].double().numpy(), tp, tp)
+    return [(list(map(int, s.tokens)), int(s.num_accepted), [float(x) for x in s.accept_prob],
+             float(s.residual_Z)) for s in res.seqs]
+
+
+def test_batch_shards_reassemble_to_the_single_rank_result():
+    """Replicas only: sequences are independent, so two gloo ranks that each verify a
+    contiguous half of the batch and gather the results reproduce the one-rank result
+    exactly (no data-path exchange is needed).  Runs the oracle on CPU; the GPU path
+    shards the same way but is unmeasured on more than one GPU here."""
+    import numpy as np
+    import oracle
+    from speculative_decoding_verification_44_gb300 import workloads
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_shard_worker, args=(world, port, out), nprocs=world, join=True)
+        gathered = out["gathered"]
+    w = _small_serving_workload(workloads, oracle, np)
+    assert gathered == _oracle_rows(w, 0, w.B, oracle, np)
