@@ -72,8 +72,7 @@ Readings where the pages are silent (each is named where it is used):
       at a leaf).  With distinct sibling tokens this is the deepest node whose
       whole path matches the argmaxes, and a chain (p_i = i - 1) is the linear
       greedy verifier.  Every node row is read, so any failed row fails the
-      sequence (R10).  No multi-path acceptance rule for sampling mode is given
-      on the pages; none is built.
+      sequence (R10).  The sampling-mode counterpart is R17.
 * R12 lenience beta in (0, 1] [magicnet §8]: the page shrinks the draft
       distribution to beta q and then compares it with the target; here beta q
       stands in for q throughout -- acceptance min(1, p / (beta q)) and, on a
@@ -106,6 +105,22 @@ Sources:
       read, so they cannot fail the sequence, and their acceptance
       probabilities are reported as -1.  On inputs whose every row is valid
       the emitted tokens, counts, flags and residual mass equal R1-R10's.
+* R17 sampling-mode tree verification [baisen §8; magicnet §7]: the pages verify a
+      draft tree in one target forward and accept the best path, but give no
+      acceptance rule for sampling mode.  Reading, the plainest one under which
+      the output keeps the target's law: the children of a node are proposals
+      drawn independently from the draft distribution q_v at that node (so
+      siblings may repeat a token).  Walk from the root with the residual
+      r = p_v: try the children in node order; child c with token x is accepted
+      with probability min(1, r(x) / q_v(x)) (R4, R6 against its own uniform);
+      after a rejection r becomes (r - q_v)+ / Z (R7 when Z == 0: r is kept and
+      the sequence flagged).  An accepted child is entered with r = p_child.
+      When every child of the current node is rejected, the token is drawn from
+      r; at a node without children, from p_v (the bonus).  One uniform per
+      non-root node (used only if the node is tried) and one u_sample for the
+      final draw (R8).  A chain (each node one child) is the linear verifier
+      R1-R10.  Every node's target row and the draft row of every node with
+      children are read, so any failed row fails the sequence (R10).
 """
 from __future__ import annotations
 
@@ -297,7 +312,8 @@ class SeqResult:
     sample_cdf: np.ndarray | None = field(default=None, repr=False)  # normalised CDF drawn from
     rows_read: int = -1             # early-exit greedy: target rows read (R11)
     num_emitted: int = -1           # tokens committed: num_accepted + 1, or fewer after an EOS cut (R14)
-    path: list | None = None        # greedy tree verification: the accepted path's nodes, root first (R15)
+    path: list | None = None        # tree verification: the accepted path's nodes, root first (R15, R17)
+    tree_trace: list | None = None  # sampling tree (R17): (node, a) of every tried node, in order
 
 
 def _error_result(status: int, gamma_max: int) -> SeqResult:
@@ -543,6 +559,119 @@ def verify_greedy_tree(target: np.ndarray, tokens: np.ndarray, parents: np.ndarr
     for b in range(B):
         n = N if nodes_per_seq is None else int(nodes_per_seq[b])
         out.append(verify_greedy_tree_sequence(target[b], tokens[b], parents[b], n, N))
+    return _collect(out)
+
+
+def verify_sample_tree_sequence(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
+                                parents: np.ndarray, u_node: np.ndarray, u_sample: float,
+                                n_nodes: int, max_nodes: int,
+                                target_params: tuple[float, int, float],
+                                draft_params: tuple[float, int, float]) -> SeqResult:
+    """Sampling-mode verification of a draft tree (R17)  [baisen §8; magicnet §7; wrblog §4-§6].
+
+    target, draft: (max_nodes, V) float64 logits; row v is the target's / the draft's
+    distribution after the path root..v (draft rows of nodes without children are unused).
+    tokens / parents: (max_nodes,) node tokens and parent indices (entry 0, the root, unused).
+    u_node: (max_nodes,) the acceptance uniform of each node (entry 0 unused); u_sample: the
+    final draw's uniform.  Returns tokens = the accepted path's tokens then the drawn token,
+    num_accepted = the path length, accept_prob[v - 1] = a of node v if it was tried (-1
+    otherwise), residual_Z = Z of the residual the final token was drawn from (-1 for a
+    bonus draw), path = the accepted nodes (root first), tree_trace = the tried (node, a).
+    """
+    V = target.shape[1]
+    G = max_nodes - 1
+    if not 1 <= n_nodes <= max_nodes:
+        return _error_result(SEQ_BAD_LENGTH, G)
+    if any(not 0 <= int(tokens[i]) < V for i in range(1, n_nodes)):
+        return _error_result(SEQ_BAD_TOKEN, G)
+    if any(not 0 <= int(parents[i]) < i for i in range(1, n_nodes)):
+        return _error_result(SEQ_BAD_TREE, G)
+    if not all(_valid_uniform(float(u_node[i])) for i in range(1, n_nodes)) or not _valid_uniform(float(u_sample)):
+        return _error_result(SEQ_BAD_UNIFORM, G)
+    if not valid_params(target_params) or not valid_params(draft_params):
+        return _error_result(SEQ_BAD_PARAMS, G)
+    children = [[c for c in range(1, n_nodes) if int(parents[c]) == v] for v in range(n_nodes)]
+    # every node's target row; the draft row of every node with children (R10)
+    p_rows, q_rows = [], []
+    for v in range(n_nodes):
+        p_v = transform_row(target[v], *target_params)
+        if p_v.status != SEQ_OK:
+            return _error_result(p_v.status, G)
+        p_rows.append(p_v)
+        q_v = transform_row(draft[v], *draft_params) if children[v] else None
+        if q_v is not None and q_v.status != SEQ_OK:
+            return _error_result(q_v.status, G)
+        q_rows.append(q_v)
+
+    status = SEQ_OK
+    a = np.full(G, -1.0)
+    trace = []
+    accept_margin = np.inf
+    draft_amb = False
+    path = [0]
+    v = 0
+    r = p_rows[0].probs                    # the residual target distribution at v
+    w, residual_Z = r, -1.0                # what the final token is drawn from, and its mass
+    while True:
+        q_v = q_rows[v]
+        entered = None
+        for c in children[v]:
+            x = int(tokens[c])
+            a_c, zq = acceptance_probability(r[x], q_v.probs[x])
+            a[c - 1] = a_c
+            trace.append((c, a_c))
+            if zq:
+                status |= SEQ_FLAG_ZERO_Q
+            accept_margin = min(accept_margin, abs(float(u_node[c]) - a_c))
+            draft_amb = draft_amb or x in p_rows[v].ambiguous or x in q_v.ambiguous
+            if float(u_node[c]) < a_c:                     # R4
+                entered = c
+                break
+            res_w = residual_weights(r, q_v.probs)         # [wrblog §5]
+            Z = float(res_w.sum())
+            if Z > 0:
+                w, residual_Z = res_w, Z
+                r = res_w / Z
+            else:                                          # R7: keep r
+                status |= SEQ_FLAG_Z_ZERO
+                w, residual_Z = r, Z
+        if entered is None:
+            if not children[v]:                            # a leaf: the bonus from p_v [wrblog §6]
+                w, residual_Z = p_rows[v].probs, -1.0
+            break
+        path.append(entered)
+        v = entered
+        r = p_rows[v].probs
+    tok, lo, hi = inverse_cdf(w, float(u_sample))
+    L = len(path) - 1
+    out = np.full(max_nodes, -1, dtype=np.int64)
+    out[:L] = [int(tokens[c]) for c in path[1:]]
+    out[L] = tok
+    used = [p_rows[u] for u in range(n_nodes)] + [q for q in q_rows if q is not None]
+    sample_rows = [p_rows[v]] + ([q_rows[v]] if children[v] else [])
+    res = SeqResult(out, L, status, a, residual_Z, accept_margin,
+                    min([row.top_p_margin for row in used] + [np.inf]),
+                    draft_ambiguous=draft_amb,
+                    sample_ambiguous=np.unique(np.concatenate([row.ambiguous for row in sample_rows])),
+                    sample_u=float(u_sample), sample_lo=lo, sample_hi=hi, num_emitted=L + 1)
+    res.path = path
+    res.tree_trace = trace
+    C = np.cumsum(w)
+    res.sample_cdf = C / C[-1]
+    return res
+
+
+def verify_sample_tree(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray, parents: np.ndarray,
+                       u_node: np.ndarray, u_sample: np.ndarray,
+                       target_params: tuple[float, int, float], draft_params: tuple[float, int, float],
+                       nodes_per_seq: np.ndarray | None = None) -> BatchResult:
+    """Batched sampling-mode tree verification (R17), one sequence at a time."""
+    B, N, _ = target.shape
+    out = []
+    for b in range(B):
+        n = N if nodes_per_seq is None else int(nodes_per_seq[b])
+        out.append(verify_sample_tree_sequence(target[b], draft[b], tokens[b], parents[b], u_node[b],
+                                               float(u_sample[b]), n, N, target_params, draft_params))
     return _collect(out)
 
 
