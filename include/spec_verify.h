@@ -372,6 +372,65 @@ SPEC_API spec_status_t spec_verify_greedy_tree(const void* target_logits, spec_d
                                       int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_path,
                                       int32_t* out_status, void* stream);
 
+/* Sampling-mode verification of a draft tree [baisen §8; magicnet §7]; the
+ * acceptance rule is the plainest one that keeps the target's distribution,
+ * since the pages give none for sampling mode.  Node 0 of each sequence's tree
+ * is the root (the position after the committed prefix); node c > 0 carries
+ * a draft token and a parent p_c < c.  The children of a node must be
+ * independent draws from the draft distribution at that node (siblings may
+ * repeat a token): that is what makes the result follow the target's law.
+ * Walking from the root with the residual r = p_v (the target's distribution
+ * at node v), the children are tried in node order: child c with token x is
+ * accepted iff u_node[c] < min(1, r(x) / q_v(x)) [wrblog §4.1]; a rejection
+ * replaces r by (r - q_v)+ / Z [wrblog §5] (Z == 0: r is kept and
+ * SPEC_SEQ_FLAG_Z_ZERO set); an accepted child is entered with r = p_child.
+ * When every child of the current node is rejected the token is drawn from r
+ * with u_sample (inverse CDF in vocabulary order); at a node without children
+ * it is drawn from p_v (the bonus) [wrblog §6].  With one child per node this
+ * is spec_verify_sample.
+ *
+ * target_logits, draft_logits [batch][max_nodes][vocab] of dtype: row c is
+ *               the target's / the draft's logits after the path root..c (the
+ *               draft row of a node without children is not read).
+ * tree_tokens, tree_parents [batch][max_nodes] int32 (entry 0 unused).
+ * nodes_per_seq [batch] int32 in [1, max_nodes] (other values fail the
+ *               sequence with SPEC_SEQ_BAD_LENGTH), or NULL (max_nodes).
+ * u_node        [batch][max_nodes] float in [0, 1): node c's acceptance
+ *               uniform (entry 0 unused; used only if c is tried).
+ * u_sample      [batch] float in [0, 1).
+ * target_params, draft_params: both with 1 <= top_k <= 128 and top_k < vocab
+ *               (the kept-list path); other rules return SPEC_ERR_UNSUPPORTED.
+ * max_nodes     1..32 (SPEC_ERR_UNSUPPORTED beyond).
+ * workspace     spec_tree_sample_workspace_size() bytes, zero-filled before
+ *               first use (left reusable).
+ * out_tokens    [batch][max_nodes]: the accepted path's tokens, the drawn
+ *               token, then -1.  out_num_accepted [batch]: the path length
+ *               (-1 on error).  out_path [batch][max_nodes]: the path's nodes,
+ *               root first, then -1, or NULL.  out_accept_prob
+ *               [batch][max_nodes - 1]: entry c - 1 the acceptance probability
+ *               of node c if it was tried, -1 otherwise, or NULL.
+ *               out_residual_z [batch]: Z of the residual the token was drawn
+ *               from (-1 for a bonus draw), or NULL.  out_status [batch]
+ *               SPEC_SEQ_* (checks in order: length, node tokens, parents ->
+ *               SPEC_SEQ_BAD_TREE, uniforms, rows in node order: target row c,
+ *               then draft row c), or NULL.
+ * One launch; every node's target row and the draft row of every node with
+ * children are read; other conventions as above. */
+SPEC_API spec_status_t spec_tree_sample_workspace_size(int32_t batch, int32_t max_nodes, int32_t vocab,
+                                              spec_sampling_params_t target_params,
+                                              spec_sampling_params_t draft_params, size_t* bytes);
+SPEC_API spec_status_t spec_verify_sample_tree(const void* target_logits, const void* draft_logits,
+                                      spec_dtype_t dtype, const int32_t* tree_tokens,
+                                      const int32_t* tree_parents, const int32_t* nodes_per_seq,
+                                      const float* u_node, const float* u_sample,
+                                      spec_sampling_params_t target_params,
+                                      spec_sampling_params_t draft_params, int32_t batch,
+                                      int32_t max_nodes, int32_t vocab, void* workspace,
+                                      size_t workspace_bytes, int32_t* out_tokens,
+                                      int32_t* out_num_accepted, int32_t* out_path,
+                                      float* out_accept_prob, float* out_residual_z,
+                                      int32_t* out_status, void* stream);
+
 /* The transform step alone [wrblog §7.2, §7.3]: writes the full probability
  * rows p = top_p(top_k(softmax(z / T))) the verifier samples from.
  * logits [rows][vocab] of dtype; out_probs [rows][vocab] float;

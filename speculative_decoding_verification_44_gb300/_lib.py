@@ -39,7 +39,7 @@ EXPORTED = ("spec_verify_workspace_size", "spec_verify_sample", "spec_greedy_wor
             "spec_verify_greedy", "spec_transform_probs", "spec_status_string",
             "spec_verify_sample_noalloc", "spec_verify_greedy_early", "spec_verify_sample_lenient",
             "spec_verify_workspace_size_ex", "spec_verify_sample_ex", "spec_tree_workspace_size",
-            "spec_verify_greedy_tree")
+            "spec_verify_greedy_tree", "spec_tree_sample_workspace_size", "spec_verify_sample_tree")
 
 
 class spec_sampling_params_t(ctypes.Structure):
@@ -94,6 +94,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_greedy_tree.restype = ctypes.c_int
     lib.spec_verify_greedy_tree.argtypes = [vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, vp, sz,
                                             vp, vp, vp, vp, vp]
+    lib.spec_tree_sample_workspace_size.restype = ctypes.c_int
+    lib.spec_tree_sample_workspace_size.argtypes = [i32, i32, i32, P, P, ctypes.POINTER(sz)]
+    lib.spec_verify_sample_tree.restype = ctypes.c_int
+    lib.spec_verify_sample_tree.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, i32, i32, i32, vp, sz,
+                                            vp, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_sample_lenient.restype = ctypes.c_int
     lib.spec_verify_sample_lenient.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, P, P, ctypes.c_float,
                                                i32, i32, i32, vp, sz, vp, vp, vp, vp, vp, vp]
@@ -147,6 +152,18 @@ def spec_tree_workspace_size(batch: int, max_nodes: int) -> int:
 
 def spec_verify_greedy_tree(*args) -> int:
     return load().spec_verify_greedy_tree(*args)
+
+
+def spec_tree_sample_workspace_size(batch: int, max_nodes: int, vocab: int, target_params, draft_params) -> int:
+    out = sz(0)
+    check("spec_tree_sample_workspace_size",
+          load().spec_tree_sample_workspace_size(batch, max_nodes, vocab, target_params, draft_params,
+                                                 ctypes.byref(out)))
+    return out.value
+
+
+def spec_verify_sample_tree(*args) -> int:
+    return load().spec_verify_sample_tree(*args)
 
 
 def spec_greedy_workspace_size(batch: int, gamma_max: int) -> int:

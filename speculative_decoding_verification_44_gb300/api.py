@@ -228,6 +228,42 @@ def verify_greedy_tree(target_logits: torch.Tensor, tree_tokens: torch.Tensor, t
     return out, path
 
 
+def tree_sample_workspace_size(batch: int, max_nodes: int, vocab: int, target: SamplingParams,
+                                draft: SamplingParams) -> int:
+    return _lib.spec_tree_sample_workspace_size(batch, max_nodes, vocab, target.c(), draft.c())
+
+
+def verify_sample_tree(target_logits: torch.Tensor, draft_logits: torch.Tensor, tree_tokens: torch.Tensor,
+                       tree_parents: torch.Tensor, u_node: torch.Tensor, u_sample: torch.Tensor,
+                       target_params: SamplingParams, draft_params: SamplingParams,
+                       nodes_per_seq: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       out: VerifyOutput | None = None, path: torch.Tensor | None = None,
+                       stream: torch.cuda.Stream | None = None) -> tuple[VerifyOutput, torch.Tensor]:
+    """spec_verify_sample_tree on torch tensors: target_logits and draft_logits [B, N, V],
+    tree_tokens and tree_parents [B, N] int32, u_node [B, N] and u_sample [B] float32,
+    nodes_per_seq [B] int32.  Returns the outputs (tokens [B, N], accept_prob [B, N - 1])
+    and the accepted path's nodes [B, N]."""
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    if workspace is None:
+        workspace = new_workspace(tree_sample_workspace_size(B, N, V, target_params, draft_params), dev)
+    if out is None:
+        out = VerifyOutput(tokens=torch.empty(B, N, dtype=torch.int32, device=dev),
+                           num_accepted=torch.empty(B, dtype=torch.int32, device=dev),
+                           status=torch.empty(B, dtype=torch.int32, device=dev),
+                           accept_prob=torch.empty(B, max(N - 1, 1), dtype=torch.float32, device=dev),
+                           residual_z=torch.empty(B, dtype=torch.float32, device=dev))
+    if path is None:
+        path = torch.empty(B, N, dtype=torch.int32, device=dev)
+    st = _lib.spec_verify_sample_tree(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(tree_tokens),
+        _ptr(tree_parents), _ptr(nodes_per_seq), _ptr(u_node), _ptr(u_sample), target_params.c(),
+        draft_params.c(), B, N, V, _ptr(workspace), workspace.numel(), _ptr(out.tokens), _ptr(out.num_accepted),
+        _ptr(path), _ptr(out.accept_prob), _ptr(out.residual_z), _ptr(out.status), _stream(stream))
+    _lib.check("spec_verify_sample_tree", st)
+    return out, path
+
+
 def transform_probs(logits: torch.Tensor, params: SamplingParams,
                     stream: torch.cuda.Stream | None = None) -> tuple[torch.Tensor, torch.Tensor]:
     """spec_transform_probs: full probability rows of a [rows, V] logits tensor."""

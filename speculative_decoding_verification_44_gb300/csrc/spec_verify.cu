@@ -158,6 +158,56 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const float* p,
   return 0.0f;
 }
 
+// Z and the inverse-CDF pick over weights held in chunks of 32 entries (entry
+// 32c + l is lane l's entry of chunk c, chunk and lane order vocabulary
+// order).  wt(c, tok) returns this lane's weight of chunk c and sets its token
+// (0 weight past the list's end).  Z is the sum of the chunks' double-float
+// scan totals in chunk order; the token is the smallest x with C(x) > u Z, or
+// the last entry with weight if rounding leaves none.  Returns -1 (Z_out <= 0)
+// when no entry has weight.  Chunk 0 stays in registers, later chunks are
+// recomputed (so nothing spills).
+template <class WT>
+__device__ __forceinline__ int warp_weight_draw(WT wt, int nch, float uf, df& Z_out) {
+  const int lane = threadIdx.x & 31;
+  int tok0;
+  const df w0 = wt(0, tok0);
+  const df incl0 = warp_incl_scan_df(w0, lane);
+  df Z = df_shfl(incl0, 31);
+  for (int c = 1; c < nch; ++c) {
+    int tk;
+    Z = df_add(Z, df_shfl(warp_incl_scan_df(wt(c, tk), lane), 31));
+  }
+  Z_out = Z;
+  if (!(Z.hi > 0.0f)) return -1;
+  const float th = uf * Z.hi;
+  const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
+  df base = df_from(0.0f);
+  int last_tok = -1;
+  for (int c = 0; c < nch; ++c) {
+    int tk = tok0;
+    df w = w0, incl = incl0;
+    if (c > 0) {
+      w = wt(c, tk);
+      incl = warp_incl_scan_df(w, lane);
+    }
+    const bool pos = w.hi > 0.0f;
+    const unsigned hit = __ballot_sync(kFull, pos && !df_ge(t, df_add(base, incl)));   // C(x) > u Z
+    if (hit) return __shfl_sync(kFull, tk, __ffs(hit) - 1);
+    const unsigned any = __ballot_sync(kFull, pos);
+    if (any) last_tok = __shfl_sync(kFull, tk, 31 - __clz(any));
+    base = df_add(base, df_shfl(incl, 31));
+  }
+  return last_tok;                                      // rounding left u Z at or above the total
+}
+
+// The weight (p - beta q)+ of a kept entry as a double-float [wrblog §5; magicnet
+// §8] (beta q is formed exactly, as hi + lo).
+__device__ __forceinline__ df residual_weight(const df p, float q, float beta) {
+  const float bq = beta * q;
+  const df d = df_add(p, {-bq, -fmaf(beta, q, -bq)});
+  return d.hi > 0.0f ? d : df_from(0.0f);
+}
+
 // Warp-wide inverse-CDF draw over a kept list stored in token order (n <=
 // kListCap entries, taken in chunks of 32: entry 32c + l is lane l's entry of
 // chunk c, so lane order within a chunk and chunk order are vocabulary order).
@@ -167,37 +217,27 @@ __device__ __forceinline__ float list_lookup(const int32_t* tok, const float* p,
 // smallest x with C(x) > u Z, or the last entry with weight if rounding
 // leaves none.  Z == 0 after a rejection falls back to the draw from p and
 // sets SEQ_FLAG_Z_ZERO.  Returns -1 when no entry has weight.
-// entry_at(e) gives entry e; q_of(x) gives q(x) (residual draws only).
+// entry_at(e) gives entry e; q_of(x) gives q(x) (residual draws only).  The
+// scan and the pick are warp_weight_draw's.
 template <class EntryAt, class QOf>
 __device__ __forceinline__ int warp_list_draw(EntryAt entry_at, int n, bool residual, QOf q_of, float beta,
                                               float uf, float& Z_resid, int& flags) {
   const int lane = threadIdx.x & 31;
   const int nch = (n + 31) >> 5;
-  // lane's entry of chunk c: its token and weight (weights (p - beta q)+ when resid)
-  const auto weight_of = [&](int c, bool resid, int& tok) -> df {
-    const int e = 32 * c + lane;
-    tok = 0x7fffffff;
-    if (e >= n) return df_from(0.0f);
-    const ListEntry le = entry_at(e);
-    tok = le.token;
-    const df p = {le.p, le.p_lo};
-    if (!resid) return p;
-    const float q = q_of(le.token);
-    const float bq = beta * q;                          // beta q exactly, as hi + lo
-    const df d = df_add(p, {-bq, -fmaf(beta, q, -bq)});
-    return d.hi > 0.0f ? d : df_from(0.0f);
-  };
   for (int pass = 0; pass < 2; ++pass) {
     const bool resid = residual && pass == 0;
-    // Z over all chunks; chunk 0 (the whole list when n <= 32) stays in registers
-    int tok0;
-    const df w0 = weight_of(0, resid, tok0);
-    const df incl0 = warp_incl_scan_df(w0, lane);
-    df Z = df_shfl(incl0, 31);
-    for (int c = 1; c < nch; ++c) {
-      int tk;
-      Z = df_add(Z, df_shfl(warp_incl_scan_df(weight_of(c, resid, tk), lane), 31));
-    }
+    // lane's entry of chunk c: its token and weight (weights (p - beta q)+ when resid)
+    const auto weight_of = [&](int c, int& tok) -> df {
+      const int e = 32 * c + lane;
+      tok = 0x7fffffff;
+      if (e >= n) return df_from(0.0f);
+      const ListEntry le = entry_at(e);
+      tok = le.token;
+      const df p = {le.p, le.p_lo};
+      return resid ? residual_weight(p, q_of(le.token), beta) : p;
+    };
+    df Z;
+    const int sel = warp_weight_draw(weight_of, nch, uf, Z);
     if (resid) Z_resid = Z.hi;
     if (!(Z.hi > 0.0f)) {
       if (resid) {                                      // Z == 0 after a rejection: draw from p instead
@@ -206,25 +246,7 @@ __device__ __forceinline__ int warp_list_draw(EntryAt entry_at, int n, bool resi
       }
       return -1;
     }
-    const float th = uf * Z.hi;
-    const df t = {th, fmaf(uf, Z.hi, -th) + uf * Z.lo};
-    df base = df_from(0.0f);
-    int last_tok = -1;
-    for (int c = 0; c < nch; ++c) {
-      int tk = tok0;
-      df w = w0, incl = incl0;
-      if (c > 0) {
-        w = weight_of(c, resid, tk);
-        incl = warp_incl_scan_df(w, lane);
-      }
-      const bool pos = w.hi > 0.0f;
-      const unsigned hit = __ballot_sync(kFull, pos && !df_ge(t, df_add(base, incl)));   // C(x) > u Z
-      if (hit) return __shfl_sync(kFull, tk, __ffs(hit) - 1);
-      const unsigned any = __ballot_sync(kFull, pos);
-      if (any) last_tok = __shfl_sync(kFull, tk, 31 - __clz(any));
-      base = df_add(base, df_shfl(incl, 31));
-    }
-    return last_tok;                                    // rounding left u Z at or above the total
+    return sel;
   }
   return -1;
 }
@@ -1043,6 +1065,37 @@ __device__ __noinline__ void list_epilogue(const SampleArgs& a, int b, int gb, b
   }
 }
 
+// A kept-list row's block: its record, then its kept list in token order
+// (entry e goes to its token's rank).  Block-wide, after the row analysis.
+__device__ __forceinline__ void publish_block(uint4* dst, const Smem& sm) {
+  const int tid = threadIdx.x;
+  const int n = sm.st.n_list;
+  if (tid == 0) {
+    ListRec rec;
+    rec.p_tok = sm.st.p_tok;
+    rec.status = sm.st.status;
+    rec.n_list = n;
+    rec.pad = 0;
+    dst[0] = *reinterpret_cast<const uint4*>(&rec);
+  }
+  if (tid < n) {
+    ListEntry le;
+    le.p = sm.list_ph[tid];
+    le.p_lo = sm.list_pl[tid];
+    le.token = sm.list_tok[tid];
+    le.pad = 0;
+    const int4* lt = reinterpret_cast<const int4*>(sm.list_tok);   // padded with INT_MAX
+    int rank = 0;
+#pragma unroll 4
+    for (int f = 0; f < ((n + 3) >> 2); ++f) {
+      const int4 t = lt[f];
+      rank += (t.x < le.token ? 1 : 0) + (t.y < le.token ? 1 : 0) + (t.z < le.token ? 1 : 0) +
+              (t.w < le.token ? 1 : 0);
+    }
+    reinterpret_cast<ListEntry*>(dst + 1)[rank] = le;
+  }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -1086,33 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleAr
   }
   lean_stream_row<DT>(row, is_draft ? a.dp : a.tp, dtok, sm);
 
-  // publish the row's block: its record, then its kept list in token order
-  uint4* dst = a.fast + (static_cast<size_t>(b) * slots + slot) * a.wpr;
-  const int n = sm.st.n_list;
-  if (tid == 0) {
-    ListRec rec;
-    rec.p_tok = sm.st.p_tok;
-    rec.status = sm.st.status;
-    rec.n_list = n;
-    rec.pad = 0;
-    dst[0] = *reinterpret_cast<const uint4*>(&rec);
-  }
-  if (tid < n) {
-    ListEntry le;
-    le.p = sm.list_ph[tid];
-    le.p_lo = sm.list_pl[tid];
-    le.token = sm.list_tok[tid];
-    le.pad = 0;
-    const int4* lt = reinterpret_cast<const int4*>(sm.list_tok);   // padded with INT_MAX
-    int rank = 0;
-#pragma unroll 4
-    for (int f = 0; f < ((n + 3) >> 2); ++f) {
-      const int4 t = lt[f];
-      rank += (t.x < le.token ? 1 : 0) + (t.y < le.token ? 1 : 0) + (t.z < le.token ? 1 : 0) +
-              (t.w < le.token ? 1 : 0);
-    }
-    reinterpret_cast<ListEntry*>(dst + 1)[rank] = le;
-  }
+  publish_block(a.fast + (static_cast<size_t>(b) * slots + slot) * a.wpr, sm);
   cp_async_wait<0>();
   __syncthreads();
   if (tid == 0) {
@@ -1125,6 +1152,316 @@ __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleAr
   __syncthreads();
   if (!sm.b_i32[7]) return;
   list_epilogue(a, b, gb, onehot, sm, &sm.u.ring[0][0]);
+}
+
+// ------------------------------------------------------------------ sampling-mode tree verification
+// A draft tree per sequence [baisen §8; magicnet §7]: node 0 is the root, node
+// c > 0 carries a token and a parent p_c < c; target row c is the target's
+// distribution after the path root..c, draft row c the draft's (the
+// distribution the children of c were drawn from).  The children of a node
+// are independent proposals from its draft distribution.  Walk from the root
+// with the residual r = p_v; try the children in node order with
+// min(1, r(x) / q_v(x)); after a rejection r becomes (r - q_v)+ / Z; enter an
+// accepted child (r = p_child); when every child is rejected draw from r, at
+// a node without children from p_v (the bonus).  With one child per node this
+// is the linear verifier (and the arithmetic below is sample_list_kernel's).
+//
+// Rows take the kept-list path, one CTA per node target row and per node
+// draft row (a childless node's draft CTA arrives without reading its row);
+// each publishes a block as in sample_list_kernel.  The CTA that finishes last
+// for a sequence gathers the row records and the tree, validates, and warp 0
+// walks: per visited node one round trip brings the node's target list into
+// the lanes (chunks of 32 entries) and its draft list into shared memory.  The
+// residual is kept unnormalised, as weights w over the target list's entries
+// with S = sum w, so a rejection is w <- (w - S q)+ and S <- sum w without a
+// division (S = 1 exactly at a freshly entered node, where w = p).
+struct SampleTreeArgs {
+  const char* tgt;          // [B][N][V]
+  const char* dft;          // [B][N][V]
+  const int32_t* tokens;    // [B][N]
+  const int32_t* parents;   // [B][N]
+  const int32_t* nodes;     // [B] or null (N everywhere)
+  const float* u_node;      // [B][N]
+  const float* u_samp;      // [B]
+  RowParams tp, dp;
+  int B, N, V;
+  int aligned;
+  size_t row_bytes;
+  uint32_t* counters;       // [B]
+  uint4* blocks;            // [B][2N][wpr]: target rows, then draft rows
+  int wpr;
+  int32_t* out_tokens;      // [B][N]
+  int32_t* out_nacc;        // [B]
+  int32_t* out_path;        // [B][N] or null
+  float* out_aprob;         // [B][N - 1] or null
+  float* out_Z;             // [B] or null
+  int32_t* out_status;      // [B] or null
+};
+
+// Commit nothing [wrblog §15]: the lanes of one warp.
+__device__ void tree_sample_fail(const SampleTreeArgs& a, int b, int status, int lane) {
+  const size_t ob = static_cast<size_t>(b) * a.N;
+  for (int t = lane; t < a.N; t += 32) {
+    a.out_tokens[ob + t] = -1;
+    if (a.out_path) a.out_path[ob + t] = -1;
+  }
+  if (a.out_aprob)
+    for (int t = lane; t < a.N - 1; t += 32) a.out_aprob[static_cast<size_t>(b) * (a.N - 1) + t] = -1.0f;
+  if (lane == 0) {
+    a.out_nacc[b] = -1;
+    if (a.out_Z) a.out_Z[b] = -1.0f;
+    if (a.out_status) a.out_status[b] = status;
+  }
+}
+
+// q(x) (hi part) of a kept list in token order: binary search (0 if x is not kept).
+__device__ __forceinline__ float kept_q_hi(const ListEntry* ql, int nq, int x) {
+  int lo = 0, hi = nq - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    const int t = ql[mid].token;
+    if (t == x) return ql[mid].p;
+    if (t < x) lo = mid + 1; else hi = mid - 1;
+  }
+  return 0.0f;
+}
+
+// Sequence epilogue of the tree verifier (max_nodes <= 32: one lane per node).
+__device__ __noinline__ void tree_sample_epilogue(const SampleTreeArgs& a, int b, int n, Smem& sm) {
+  constexpr int kChunks = kListCap / 32;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int slots = 2 * a.N, wpr = a.wpr;
+  const uint4* blk = a.blocks + static_cast<size_t>(b) * slots * wpr;
+  uint4* recs = &sm.u.ring[0][0];                      // [2N] row records
+  ListEntry* ql = reinterpret_cast<ListEntry*>(&sm.u.ring[0][0] + 64);   // a node's draft list
+  int32_t* tok = sm.seq_tok;
+  int32_t* par = sm.list_tok;
+  float* un = sm.seq_u;
+  const size_t nb = static_cast<size_t>(b) * a.N;
+  if (tid < slots && (tid % a.N) < n) cp_async16(&recs[tid], blk + static_cast<size_t>(tid) * wpr);
+  if (tid < n) {
+    cp_async4(&tok[tid], a.tokens + nb + tid);
+    cp_async4(&par[tid], a.parents + nb + tid);
+    cp_async4(&un[tid], a.u_node + nb + tid);
+  }
+  if (tid == kThreads - 1) cp_async4(&sm.seq_us, a.u_samp + b);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid >= 32) return;
+  const auto rec = [&](int s) { return *reinterpret_cast<const ListRec*>(&recs[s]); };
+  // status, in the documented order: node tokens, parents, uniforms, rows in node order
+  const int v0 = lane;
+  const bool node = v0 >= 1 && v0 < n;
+  int status = SEQ_OK;
+  if (__any_sync(kFull, node && !(tok[v0] >= 0 && tok[v0] < a.V))) {
+    status = SEQ_BAD_TOKEN;
+  } else if (__any_sync(kFull, node && !(par[v0] >= 0 && par[v0] < v0))) {
+    status = SEQ_BAD_TREE;
+  } else if (__any_sync(kFull, (node && !(un[v0] >= 0.0f && un[v0] < 1.0f)) ||
+                               (lane == 0 && !(sm.seq_us >= 0.0f && sm.seq_us < 1.0f)))) {
+    status = SEQ_BAD_UNIFORM;
+  } else {
+    int st = SEQ_OK;
+    if (v0 < n) {
+      st = rec(v0).status;
+      if (st == SEQ_OK) st = rec(a.N + v0).status;     // SEQ_OK for a childless node's draft row
+    }
+    const unsigned bm = __ballot_sync(kFull, st != SEQ_OK);
+    if (bm) status = __shfl_sync(kFull, st, __ffs(bm) - 1);
+  }
+  if (status != SEQ_OK) {
+    tree_sample_fail(a, b, status, lane);
+    if (lane == 0) a.counters[b] = 0u;
+    return;
+  }
+  const size_t ob = static_cast<size_t>(b) * a.N;
+  const size_t ab = static_cast<size_t>(b) * (a.N - 1);
+  float a_node = -1.0f;                                 // lane l: a of node l + 1 if it was tried
+  int flags = 0;
+  int v = 0, L = 0;
+  int path_node = lane == 0 ? 0 : -1;                  // lane l: the path's l-th node
+  float Z_out = -1.0f;
+  int drawn = -1;
+  for (;;) {
+    const unsigned kids = __ballot_sync(kFull, lane >= 1 && lane < n && par[lane] == v);
+    // node v's target list into the lanes, its draft list (if it has children) into shared memory
+    const int nt = min(rec(v).n_list, wpr - 1);
+    const int nq = kids ? min(rec(a.N + v).n_list, wpr - 1) : 0;
+    const int nch = (nt + 31) >> 5;
+    const ListEntry* tl = reinterpret_cast<const ListEntry*>(blk + static_cast<size_t>(v) * wpr + 1);
+    const ListEntry* gq = reinterpret_cast<const ListEntry*>(blk + static_cast<size_t>(a.N + v) * wpr + 1);
+    df w[kChunks];
+    int tk[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const int e = 32 * c + lane;
+      w[c] = df_from(0.0f);
+      tk[c] = 0x7fffffff;
+      if (e < nt) {
+        const ListEntry le = load_entry(tl + e);
+        w[c] = {le.p, le.p_lo};
+        tk[c] = le.token;
+      }
+      if (e < nq) ql[e] = load_entry(gq + e);
+    }
+    __syncwarp();
+    bool unit = true;                                  // w = p and S = 1 exactly
+    df S = df_from(1.0f);
+    int entered = -1;
+    for (unsigned m = kids; m; m &= m - 1) {           // children in node order
+      const int c = __ffs(m) - 1;
+      const int x = tok[c];
+      df px = df_from(0.0f);                           // w(x)
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch) {
+        const unsigned hit = __ballot_sync(kFull, ch < nch && tk[ch] == x);
+        if (hit) px = df_shfl(w[ch], __ffs(hit) - 1);
+      }
+      const float qx = kept_q_hi(ql, nq, x);
+      float ac;
+      if (qx > 0.0f) {
+        ac = unit ? fminf(1.0f, px.hi / (1.0f * qx))   // min(1, p / q), the linear verifier's arithmetic
+                  : fminf(1.0f, (px.hi + px.lo) / ((S.hi + S.lo) * qx));
+      } else {
+        ac = (px.hi > 0.0f) ? 1.0f : 0.0f;
+        flags |= SEQ_FLAG_ZERO_Q;
+      }
+      if (lane == c - 1) a_node = ac;
+      if (un[c] < ac) {                                // accept: enter the child
+        entered = c;
+        break;
+      }
+      // reject: w <- (w - S q)+ and S <- sum w [wrblog §5]; S == 0 keeps w (R7 of the oracle)
+      df nw[kChunks];
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch) {
+        nw[ch] = df_from(0.0f);
+        if (ch < nch && 32 * ch + lane < nt) {
+          const float q = kept_q(ql, nq, tk[ch]);
+          if (unit) {
+            nw[ch] = residual_weight(w[ch], q, 1.0f);
+          } else {
+            const float sq = S.hi * q;                 // S q exactly, as hi + lo
+            const df d = df_add(w[ch], {-sq, -(fmaf(S.hi, q, -sq) + S.lo * q)});
+            nw[ch] = d.hi > 0.0f ? d : df_from(0.0f);
+          }
+        }
+      }
+      df Zn;
+      const auto nwt = [&](int ch, int& t) -> df {
+        df r = nw[0];
+        t = tk[0];
+#pragma unroll
+        for (int k = 1; k < kChunks; ++k) {
+          r = ch == k ? nw[k] : r;
+          t = ch == k ? tk[k] : t;
+        }
+        return r;
+      };
+      warp_weight_draw(nwt, nch, 0.0f, Zn);            // the total only (the pick is discarded)
+      // the residual's mass relative to r = w / S: sum (r - q)+ = Zn / S
+      Z_out = unit ? Zn.hi : (Zn.hi + Zn.lo) / (S.hi + S.lo);
+      if (Zn.hi > 0.0f) {
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch) w[ch] = nw[ch];
+        S = Zn;
+        unit = false;
+      } else {
+        flags |= SEQ_FLAG_Z_ZERO;
+      }
+    }
+    if (entered >= 0) {
+      ++L;
+      if (lane == L) path_node = entered;
+      v = entered;
+      __syncwarp();
+      continue;
+    }
+    // every child rejected: draw from the residual; no children: the bonus from p_v [wrblog §5, §6]
+    if (!kids) Z_out = -1.0f;
+    const auto wt = [&](int ch, int& t) -> df {
+      df r = w[0];
+      t = tk[0];
+#pragma unroll
+      for (int k = 1; k < kChunks; ++k) {
+        r = ch == k ? w[k] : r;
+        t = ch == k ? tk[k] : t;
+      }
+      return r;
+    };
+    df Zd;
+    drawn = warp_weight_draw(wt, nch, sm.seq_us, Zd);
+    break;
+  }
+  // outputs: the path's tokens, the drawn token, then -1
+  const int pn = __shfl_sync(kFull, path_node, min(lane + 1, 31));   // the path's (lane+1)-th node
+  if (lane < a.N) {
+    a.out_tokens[ob + lane] = lane < L ? tok[pn] : (lane == L ? drawn : -1);
+    if (a.out_path) a.out_path[ob + lane] = lane <= L ? path_node : -1;
+  }
+  if (a.out_aprob && lane < a.N - 1) a.out_aprob[ab + lane] = a_node;
+  if (lane == 0) {
+    a.out_nacc[b] = L;
+    if (a.out_Z) a.out_Z[b] = Z_out;
+    if (a.out_status) a.out_status[b] = flags;
+    a.counters[b] = 0u;                                // leave the workspace reusable
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTreeArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int slots = 2 * a.N;
+  const int b = blockIdx.x / slots;
+  const int slot = blockIdx.x - b * slots;
+  const int n = a.nodes ? a.nodes[b] : a.N;
+  if (n < 1 || n > a.N) {
+    if (slot == 0 && tid < 32) tree_sample_fail(a, b, SEQ_BAD_LENGTH, lane);
+    return;
+  }
+  const bool is_draft = slot >= a.N;
+  const int v = is_draft ? slot - a.N : slot;
+  if (v >= n) return;
+  bool read = true;
+  if (is_draft) {                                      // only a node with children has its draft row read
+    if (tid < 32) {
+      bool has = false;
+      for (int c = v + 1 + lane; c < n; c += 32) has |= a.parents[static_cast<size_t>(b) * a.N + c] == v;
+      has = __any_sync(kFull, has);
+      if (lane == 0) sm.b_i32[6] = has ? 1 : 0;
+    }
+    __syncthreads();
+    read = sm.b_i32[6] != 0;
+  }
+  uint4* dst = a.blocks + (static_cast<size_t>(b) * slots + slot) * a.wpr;
+  if (read) {
+    const Row row = make_row<DT>((is_draft ? a.dft : a.tgt) + (static_cast<size_t>(b) * a.N + v) * a.row_bytes,
+                                 a.V, a.aligned != 0);
+    const RowParams P = is_draft ? a.dp : a.tp;
+    if (row.aligned) lean_stream_row<DT>(row, P, -1, sm);
+    else stream_row<DT>(row, P, -1, sm);
+    publish_block(dst, sm);
+  } else if (tid == 0) {
+    ListRec rec;
+    rec.p_tok = 0.0f;
+    rec.status = SEQ_OK;
+    rec.n_list = 0;
+    rec.pad = 0;
+    dst[0] = *reinterpret_cast<const uint4*>(&rec);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atom_add_acq_rel_gpu(&a.counters[b], 1u);
+    sm.b_i32[7] = (prev + 1u == static_cast<unsigned>(2 * n)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sm.b_i32[7]) return;
+  tree_sample_epilogue(a, b, n, sm);
 }
 
 // ------------------------------------------------------------------ chunk-parallel full-row draw
@@ -1716,7 +2053,7 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
-std::atomic<uint64_t> g_ready[16];  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list x {bf16, f32}
+std::atomic<uint64_t> g_ready[18];  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list, sample-tree x {bf16, f32}
 
 // Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
 // needs FullExtra after Smem; launches without such rows keep their occupancy.
@@ -2030,6 +2367,110 @@ spec_status_t spec_verify_greedy_tree(const void* target_logits, spec_dtype_t dt
   } else {
     err = prepare(greedy_tree_kernel<DT_F32>, g_ready[13]);
     if (err == cudaSuccess) greedy_tree_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
+  }
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// Sampling tree workspace: per-sequence counters, then [B][2N] row blocks of
+// wpr 16-byte words (a ListRec and the kept list).
+constexpr int kMaxTreeNodes = 32;
+struct TreeSampleLayout {
+  size_t counters, blocks, total;
+  int wpr;
+};
+bool tree_sample_layout(int B, int N, int V, const spec_sampling_params_t& tp, const spec_sampling_params_t& dp,
+                        TreeSampleLayout& L, spec_status_t& why) {
+  why = SPEC_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || V < 1 || !params_ok(tp) || !params_ok(dp)) return false;
+  if (static_cast<long long>(B) * 2 * N > 0x7fffffffLL) return false;
+  why = SPEC_ERR_UNSUPPORTED;
+  if (N > kMaxTreeNodes) return false;
+  const RowParams t = row_params_of(tp, V), d = row_params_of(dp, V);
+  if (t.path != PATH_STREAM || d.path != PATH_STREAM) return false;   // kept-list rules only
+  L.wpr = 1 + std::max(t.k, d.k);
+  L.counters = 0;
+  L.blocks = round_up(static_cast<size_t>(B) * sizeof(uint32_t));
+  L.total = L.blocks + round_up(static_cast<size_t>(B) * 2 * N * L.wpr * sizeof(uint4));
+  return true;
+}
+
+spec_status_t spec_tree_sample_workspace_size(int32_t batch, int32_t max_nodes, int32_t vocab,
+                                              spec_sampling_params_t target_params,
+                                              spec_sampling_params_t draft_params, size_t* bytes) {
+  if (!bytes) return SPEC_ERR_INVALID_ARG;
+  TreeSampleLayout L;
+  spec_status_t why;
+  if (!tree_sample_layout(batch, max_nodes, vocab, target_params, draft_params, L, why)) return why;
+  *bytes = L.total;
+  return SPEC_OK;
+}
+
+spec_status_t spec_verify_sample_tree(const void* target_logits, const void* draft_logits, spec_dtype_t dtype,
+                                      const int32_t* tree_tokens, const int32_t* tree_parents,
+                                      const int32_t* nodes_per_seq, const float* u_node, const float* u_sample,
+                                      spec_sampling_params_t target_params, spec_sampling_params_t draft_params,
+                                      int32_t batch, int32_t max_nodes, int32_t vocab, void* workspace,
+                                      size_t workspace_bytes, int32_t* out_tokens, int32_t* out_num_accepted,
+                                      int32_t* out_path, float* out_accept_prob, float* out_residual_z,
+                                      int32_t* out_status, void* stream) {
+  if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+  TreeSampleLayout L;
+  spec_status_t why;
+  if (!tree_sample_layout(batch, max_nodes, vocab, target_params, draft_params, L, why)) return why;
+  if (!target_logits || !draft_logits || !tree_tokens || !tree_parents || !u_node || !u_sample || !out_tokens ||
+      !out_num_accepted || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype);
+  if (!aligned_to(target_logits, es) || !aligned_to(draft_logits, es) || !aligned_to(tree_tokens, 4) ||
+      !aligned_to(tree_parents, 4) || !aligned_to(nodes_per_seq, 4) || !aligned_to(u_node, 4) ||
+      !aligned_to(u_sample, 4) || !aligned_to(out_tokens, 4) || !aligned_to(out_num_accepted, 4) ||
+      !aligned_to(out_path, 4) || !aligned_to(out_accept_prob, 4) || !aligned_to(out_residual_z, 4) ||
+      !aligned_to(out_status, 4) || !aligned_to(workspace, kAlign))
+    return SPEC_ERR_MISALIGNED;
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  SampleTreeArgs a;
+  a.tgt = static_cast<const char*>(target_logits);
+  a.dft = static_cast<const char*>(draft_logits);
+  a.tokens = tree_tokens;
+  a.parents = tree_parents;
+  a.nodes = nodes_per_seq;
+  a.u_node = u_node;
+  a.u_samp = u_sample;
+  a.tp = make_row_params(target_params, vocab, dtype);
+  a.dp = make_row_params(draft_params, vocab, dtype);
+  a.B = batch;
+  a.N = max_nodes;
+  a.V = vocab;
+  a.aligned = (vocab % elems_per_vec(dtype) == 0) && aligned_to(target_logits, 16) && aligned_to(draft_logits, 16);
+  a.row_bytes = static_cast<size_t>(vocab) * es;
+  a.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  a.blocks = reinterpret_cast<uint4*>(ws + L.blocks);
+  a.wpr = L.wpr;
+  a.out_tokens = out_tokens;
+  a.out_nacc = out_num_accepted;
+  a.out_path = out_path;
+  a.out_aprob = out_accept_prob;
+  a.out_Z = out_residual_z;
+  a.out_status = out_status;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(batch) * 2u * static_cast<unsigned>(max_nodes));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err;
+  if (dtype == SPEC_BF16) {
+    err = prepare(sample_tree_kernel<DT_BF16>, g_ready[16]);
+    if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, sample_tree_kernel<DT_BF16>, a);
+  } else {
+    err = prepare(sample_tree_kernel<DT_F32>, g_ready[17]);
+    if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, sample_tree_kernel<DT_F32>, a);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
