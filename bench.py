@@ -60,7 +60,8 @@ def parse():
     ap.add_argument("--per-seq-rules", action="store_true",
                     help="sampling workloads: spec_verify_sample_ex with the workload's rules given per sequence")
     ap.add_argument("--tree", action="store_true",
-                    help="greedy workload: spec_verify_greedy_tree over draft trees of the same rows")
+                    help="spec_verify_greedy_tree (greedy workload) or spec_verify_sample_tree (sampling "
+                         "workloads) over draft trees of the same rows")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the steps as eager launches instead of one CUDA-graph replay")
     ap.add_argument("--workload", default="serving-zipf-topk-topp",
@@ -470,6 +471,94 @@ def run_greedy(args, rank, world, dev, sv, workloads):
         dist.destroy_process_group()
 
 
+def run_sample_tree(args, rank, world, dev, sv, workloads, wid):
+    """Sampling workloads as draft trees over the same rows (spec_verify_sample_tree): node c of
+    sequence b (c = 1..G) gets a random earlier parent and a token drawn from the draft distribution
+    at that parent; node c's target row is the workload's target row c, its draft row draft row c
+    (the last node's draft row is never read: it has no children)."""
+    import torch
+    sets = [workloads.make(wid, dev, draft_probs=gpu_draft_probs, replica=rep,
+                           **({"B": args.batch} if args.batch else {})) for rep in replica_ids(rank)]
+    w0 = sets[0]
+    B, G, V = w0.B, w0.G, w0.V
+    N = G + 1
+    esize = w0.target_logits.element_size()
+    trees = []
+    alg = []
+    for r, w in enumerate(sets):
+        gen = torch.Generator(device=dev).manual_seed(6000 + 100 * rank + r)
+        q, _ = sv.transform_probs(w.draft_logits.reshape(B * G, V).contiguous(), w.draft_params)
+        q = q.view(B, G, V)
+        par = torch.full((B, N), -1, dtype=torch.int32, device=dev)
+        tok = torch.zeros(B, N, dtype=torch.int32, device=dev)
+        for c in range(1, N):
+            pc = torch.floor(torch.rand(B, generator=gen, device=dev) * c).long().clamp(max=c - 1)
+            par[:, c] = pc.int()
+            tok[:, c] = torch.multinomial(q[torch.arange(B, device=dev), pc], 1, generator=gen).squeeze(1).int()
+        dft = torch.cat([w.draft_logits, torch.zeros_like(w.draft_logits[:, :1])], dim=1).contiguous()
+        u_node = torch.cat([torch.zeros(B, 1, device=dev), w.u_accept], dim=1).contiguous()
+        has_child = torch.zeros(B, N, dtype=torch.bool, device=dev)
+        has_child.scatter_(1, par[:, 1:].long(), True)
+        alg.append(int((N + has_child.sum(dim=1)).sum().item()) * V * esize)
+        trees.append((w.target_logits, dft, tok, par, u_node, w.u_sample))
+    ws = sv.new_workspace(sv.tree_sample_workspace_size(B, N, V, w0.target_params, w0.draft_params), dev)
+    outs = []
+    for _ in range(ROTATE):
+        outs.append(sv.VerifyOutput(tokens=torch.empty(B, N, dtype=torch.int32, device=dev),
+                                    num_accepted=torch.empty(B, dtype=torch.int32, device=dev),
+                                    status=torch.empty(B, dtype=torch.int32, device=dev),
+                                    accept_prob=torch.empty(B, N - 1, dtype=torch.float32, device=dev),
+                                    residual_z=torch.empty(B, dtype=torch.float32, device=dev)))
+    paths = [torch.empty(B, N, dtype=torch.int32, device=dev) for _ in range(ROTATE)]
+
+    def step(i):
+        r = i % ROTATE
+        t = trees[r]
+        sv.verify_sample_tree(*t, w0.target_params, w0.draft_params, workspace=ws, out=outs[r], path=paths[r])
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(K):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms_per_step = max_over_ranks(t0.elapsed_time(t1), world, dev) / K
+    peak, peak_kind = measured_peaks()
+    alg_bytes = statistics.mean(alg)
+    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+    depth = statistics.mean(float(o.num_accepted.float().mean().item()) for o in outs)
+    if rank == 0:
+        dname = "bf16" if esize == 2 else "f32"
+        line = {
+            "metric": metric_of(wid, w0) + " (draft trees of the same rows)",
+            "value": whole_job_rate(B * N, world, ms_per_step), "unit": "tree nodes/s", "n_gpus": world,
+            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dname, "data": "synthetic",
+            "config": {"workload": w0.name, "B": B, "nodes": N, "V": V, **params_of(w0), "tree": True,
+                       "l2": f"inputs rotate over {ROTATE} independent sets", "launch": "K eager launches"},
+            "accepted_path_length_mean": depth,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "peak_kind": f"of {peak_kind}", "kernel": f"sv::sample_tree_kernel<{dname}>",
+                         "algorithmic_bytes_per_launch": alg_bytes},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": K, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -498,6 +587,9 @@ def main():
     wid = workload_id(args.workload)
     if wid == GREEDY_WID:
         run_greedy(args, rank, world, dev, sv, workloads)
+        return
+    if args.tree:
+        run_sample_tree(args, rank, world, dev, sv, workloads, wid)
         return
     sets = [workloads.make(wid, dev, draft_probs=gpu_draft_probs, replica=rep,
                            **({"B": args.batch} if args.batch else {})) for rep in replica_ids(rank)]
