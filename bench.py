@@ -42,7 +42,7 @@ ROTATE = 4
 KERNEL_SOURCES = ["speculative_decoding_verification_44_gb300/csrc/spec_verify.cu",
                   "speculative_decoding_verification_44_gb300/csrc/sv_row.cuh",
                   "speculative_decoding_verification_44_gb300/csrc/sv_common.cuh"]
-PROFILE = os.path.join(ROOT, "profiles", "sample_kernel_serving_B64_g5_V128256.txt")
+PROFILE = os.path.join(ROOT, "profiles", "sample_list_kernel_serving_B64_g5_V128256.txt")
 
 
 def parse():
