@@ -511,16 +511,41 @@ def run_sample_tree(args, rank, world, dev, sv, workloads, wid):
                                     residual_z=torch.empty(B, dtype=torch.float32, device=dev)))
     paths = [torch.empty(B, N, dtype=torch.int32, device=dev) for _ in range(ROTATE)]
 
-    def step(i):
+    def step(i, stream=None):
         r = i % ROTATE
         t = trees[r]
-        sv.verify_sample_tree(*t, w0.target_params, w0.draft_params, workspace=ws, out=outs[r], path=paths[r])
+        sv.verify_sample_tree(*t, w0.target_params, w0.draft_params, workspace=ws, out=outs[r], path=paths[r],
+                              stream=stream)
 
     for i in range(max(3, args.warmup)):
         step(i)
     torch.cuda.synchronize()
     K = args.steps
     stream = torch.cuda.current_stream()
+    graph = g_ev = None
+    if not args.no_graph:
+        # K calls captured as one CUDA graph, timed by event-record nodes inside it
+        gstream = torch.cuda.Stream()
+        gstream.wait_stream(stream)
+        with torch.cuda.stream(gstream):
+            for i in range(ROTATE):
+                step(i, gstream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        try:
+            g_ev = (torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True))
+        except TypeError:
+            g_ev = None
+        with torch.cuda.graph(graph, stream=gstream):
+            if g_ev is not None:
+                g_ev[0].record(gstream)
+            for i in range(K):
+                step(i, gstream)
+            if g_ev is not None:
+                g_ev[1].record(gstream)
+        graph.replay()
+        torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         if world > 1:
             import torch.distributed as dist
@@ -528,11 +553,15 @@ def run_sample_tree(args, rank, world, dev, sv, workloads, wid):
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for i in range(K):
-            step(i)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(K):
+                step(i)
         t1.record(stream)
         torch.cuda.synchronize()
-    ms_per_step = max_over_ranks(t0.elapsed_time(t1), world, dev) / K
+    total_ms = g_ev[0].elapsed_time(g_ev[1]) if g_ev is not None else t0.elapsed_time(t1)
+    ms_per_step = max_over_ranks(total_ms, world, dev) / K
     peak, peak_kind = measured_peaks()
     alg_bytes = statistics.mean(alg)
     achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
@@ -545,7 +574,10 @@ def run_sample_tree(args, rank, world, dev, sv, workloads, wid):
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dname, "data": "synthetic",
             "config": {"workload": w0.name, "B": B, "nodes": N, "V": V, **params_of(w0), "tree": True,
-                       "l2": f"inputs rotate over {ROTATE} independent sets", "launch": "K eager launches"},
+                       "l2": f"inputs rotate over {ROTATE} independent sets",
+                       "launch": ("K eager launches" if graph is None else
+                                  "K steps as one CUDA graph replay" + (", timed by event-record nodes inside the graph"
+                                                                        if g_ev is not None else ""))},
             "accepted_path_length_mean": depth,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": None, "peak_kind": f"of {peak_kind}", "kernel": f"sv::sample_tree_kernel<{dname}>",

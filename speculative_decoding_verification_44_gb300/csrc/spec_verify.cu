@@ -1226,19 +1226,30 @@ __device__ __forceinline__ float kept_q_hi(const ListEntry* ql, int nq, int x) {
   return 0.0f;
 }
 
-// Sequence epilogue of the tree verifier (max_nodes <= 32: one lane per node).
+// Sequence epilogue of the tree verifier (max_nodes <= 32: one lane per node);
+// kChunks 32-entry chunks cover the longest kept list the rules allow.
+template <int kChunks>
 __device__ __noinline__ void tree_sample_epilogue(const SampleTreeArgs& a, int b, int n, Smem& sm) {
-  constexpr int kChunks = kListCap / 32;
   const int tid = threadIdx.x, lane = tid & 31;
   const int slots = 2 * a.N, wpr = a.wpr;
   const uint4* blk = a.blocks + static_cast<size_t>(b) * slots * wpr;
-  uint4* recs = &sm.u.ring[0][0];                      // [2N] row records
-  ListEntry* ql = reinterpret_cast<ListEntry*>(&sm.u.ring[0][0] + 64);   // a node's draft list
+  // every row block in one round trip when they fit the gather buffer (the walk
+  // then reads shared memory only); otherwise the row records now and each
+  // visited node's lists when the walk reaches it
+  const bool all = slots * wpr <= kGatherWords;
+  uint4* words = &sm.u.ring[0][0];
+  const int rstride = all ? wpr : 1;                   // records at words[s * rstride]
+  ListEntry* ql = reinterpret_cast<ListEntry*>(&sm.u.ring[0][0] + 64);   // a node's draft list (not all)
   int32_t* tok = sm.seq_tok;
   int32_t* par = sm.list_tok;
   float* un = sm.seq_u;
   const size_t nb = static_cast<size_t>(b) * a.N;
-  if (tid < slots && (tid % a.N) < n) cp_async16(&recs[tid], blk + static_cast<size_t>(tid) * wpr);
+  if (all) {
+    for (int t = tid; t < slots * wpr; t += kThreads)
+      if ((t / wpr) % a.N < n) cp_async16(&words[t], blk + t);
+  } else if (tid < slots && (tid % a.N) < n) {
+    cp_async16(&words[tid], blk + static_cast<size_t>(tid) * wpr);
+  }
   if (tid < n) {
     cp_async4(&tok[tid], a.tokens + nb + tid);
     cp_async4(&par[tid], a.parents + nb + tid);
@@ -1249,7 +1260,7 @@ __device__ __noinline__ void tree_sample_epilogue(const SampleTreeArgs& a, int b
   cp_async_wait<0>();
   __syncthreads();
   if (tid >= 32) return;
-  const auto rec = [&](int s) { return *reinterpret_cast<const ListRec*>(&recs[s]); };
+  const auto rec = [&](int s) { return *reinterpret_cast<const ListRec*>(&words[s * rstride]); };
   // status, in the documented order: node tokens, parents, uniforms, rows in node order
   const int v0 = lane;
   const bool node = v0 >= 1 && v0 < n;
@@ -1289,8 +1300,10 @@ __device__ __noinline__ void tree_sample_epilogue(const SampleTreeArgs& a, int b
     const int nt = min(rec(v).n_list, wpr - 1);
     const int nq = kids ? min(rec(a.N + v).n_list, wpr - 1) : 0;
     const int nch = (nt + 31) >> 5;
-    const ListEntry* tl = reinterpret_cast<const ListEntry*>(blk + static_cast<size_t>(v) * wpr + 1);
-    const ListEntry* gq = reinterpret_cast<const ListEntry*>(blk + static_cast<size_t>(a.N + v) * wpr + 1);
+    const ListEntry* tl = reinterpret_cast<const ListEntry*>((all ? words : blk) + static_cast<size_t>(v) * wpr + 1);
+    const ListEntry* gq = reinterpret_cast<const ListEntry*>((all ? words : blk) +
+                                                             static_cast<size_t>(a.N + v) * wpr + 1);
+    const ListEntry* qv = all ? gq : ql;               // node v's draft list in shared memory
     df w[kChunks];
     int tk[kChunks];
 #pragma unroll
@@ -1299,11 +1312,11 @@ __device__ __noinline__ void tree_sample_epilogue(const SampleTreeArgs& a, int b
       w[c] = df_from(0.0f);
       tk[c] = 0x7fffffff;
       if (e < nt) {
-        const ListEntry le = load_entry(tl + e);
+        const ListEntry le = all ? tl[e] : load_entry(tl + e);
         w[c] = {le.p, le.p_lo};
         tk[c] = le.token;
       }
-      if (e < nq) ql[e] = load_entry(gq + e);
+      if (!all && e < nq) ql[e] = load_entry(gq + e);
     }
     __syncwarp();
     bool unit = true;                                  // w = p and S = 1 exactly
@@ -1318,7 +1331,7 @@ __device__ __noinline__ void tree_sample_epilogue(const SampleTreeArgs& a, int b
         const unsigned hit = __ballot_sync(kFull, ch < nch && tk[ch] == x);
         if (hit) px = df_shfl(w[ch], __ffs(hit) - 1);
       }
-      const float qx = kept_q_hi(ql, nq, x);
+      const float qx = kept_q_hi(qv, nq, x);
       float ac;
       if (qx > 0.0f) {
         ac = unit ? fminf(1.0f, px.hi / (1.0f * qx))   // min(1, p / q), the linear verifier's arithmetic
@@ -1338,7 +1351,7 @@ __device__ __noinline__ void tree_sample_epilogue(const SampleTreeArgs& a, int b
       for (int ch = 0; ch < kChunks; ++ch) {
         nw[ch] = df_from(0.0f);
         if (ch < nch && 32 * ch + lane < nt) {
-          const float q = kept_q(ql, nq, tk[ch]);
+          const float q = kept_q(qv, nq, tk[ch]);
           if (unit) {
             nw[ch] = residual_weight(w[ch], q, 1.0f);
           } else {
@@ -1461,7 +1474,9 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
   }
   __syncthreads();
   if (!sm.b_i32[7]) return;
-  tree_sample_epilogue(a, b, n, sm);
+  if (a.wpr - 1 <= 32) tree_sample_epilogue<1>(a, b, n, sm);
+  else if (a.wpr - 1 <= 64) tree_sample_epilogue<2>(a, b, n, sm);
+  else tree_sample_epilogue<kListCap / 32>(a, b, n, sm);
 }
 
 // ------------------------------------------------------------------ chunk-parallel full-row draw

@@ -122,6 +122,8 @@ def compare_tree(out, path, ref, u_sample):
 RULES = [
     (dict(temperature=0.7, top_k=50, top_p=0.9), dict(temperature=0.7, top_k=50, top_p=0.9)),
     (dict(temperature=1.0, top_k=20, top_p=1.0), dict(temperature=1.3, top_k=40, top_p=0.95)),
+    (dict(temperature=1.0, top_k=100, top_p=0.95), dict(temperature=0.9, top_k=120, top_p=1.0)),   # 4 chunks
+    (dict(temperature=0.8, top_k=16, top_p=0.9), dict(temperature=0.8, top_k=32, top_p=0.9)),     # 1 chunk
 ]
 
 
