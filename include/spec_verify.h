@@ -117,6 +117,9 @@ enum {
                                      rule the sequence uses is outside its domain     */
     SPEC_SEQ_BAD_TREE = 7,        /* spec_verify_greedy_tree: a node whose parent is
                                      not an earlier node                              */
+    SPEC_SEQ_STALLED = 8,         /* a full-row draw's copies into shared memory did
+                                     not arrive within its bounded wait (about a
+                                     second): a device fault, not a data error       */
     SPEC_SEQ_ERROR_MASK = 0xFF,
     SPEC_SEQ_FLAG_ZERO_Q = 0x100, /* an evaluated draft token had q(d) == 0           */
     SPEC_SEQ_FLAG_Z_ZERO = 0x200, /* residual mass was 0 after a rejection            */

@@ -26,6 +26,7 @@ SPEC_SEQ_NONFINITE = 4
 SPEC_SEQ_EMPTY_SUPPORT = 5
 SPEC_SEQ_BAD_PARAMS = 6
 SPEC_SEQ_BAD_TREE = 7
+SPEC_SEQ_STALLED = 8
 SPEC_SEQ_ERROR_MASK = 0xFF
 SPEC_SEQ_FLAG_ZERO_Q = 0x100
 SPEC_SEQ_FLAG_Z_ZERO = 0x200

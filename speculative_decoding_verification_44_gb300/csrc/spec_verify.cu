@@ -47,8 +47,11 @@ __host__ __device__ inline RowParams row_params_of(const spec_sampling_params_t&
   for (uint32_t v = static_cast<uint32_t>(V); v; v >>= 1) ++bits;
   const int sh = 62 - bits;
   r.fixed_shift = sh < 24 ? 24 : (sh > 40 ? 40 : sh);
+  r.lazy = 0;
   return r;
 }
+
+struct ChunkSum;
 
 struct SampleArgs {
   const char* tgt;
@@ -80,18 +83,21 @@ struct SampleArgs {
   int defer;
   int chunk_vecs;       // vectors per draw chunk
   int nchunk;           // chunks per row
+  int draw_run;         // chunks per draw CTA (gridDim.y CTAs per sequence)
   uint32_t* dcount;     // [B] chunk CTAs finished (self-cleaning)
   struct DrawRec* drec; // [B]
   // early exit (spec_verify_sample_ex): position-major grid, stop marks
   int early;
   uint32_t* stop_enc;          // [B] G + 1 - (earliest position known to stop), 0 = none (self-cleaning)
   unsigned long long* pairx;   // [B][G] exchange of a position's two draft-token probabilities (self-cleaning)
-  double* dsum;         // [B][nchunk] weight sum per chunk
+  ChunkSum* dsum;       // [B][nchunk] weight sums per chunk
   // kept-list kernel: per (sequence, row slot) a block of wpr 16-byte words,
   // a ListRec then the row's kept list in token order
   uint4* fast;
   int wpr;
 };
+
+constexpr int kChunkVecs = 4 * kThreads;   // full-row draw: vectors per chunk (four per thread)
 
 // Row record of the kept-list kernel (the first word of a row's block).
 struct __align__(16) ListRec {
@@ -785,6 +791,9 @@ template <int DT, bool EX>
 __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  // the full-row draw may be scheduled once every row CTA has started (it
+  // waits for this grid to complete before reading anything it wrote)
+  grid_launch_dependents();
   const int slots = 2 * a.G + 1;
   int b, slot;
   if (EX && a.early) {
@@ -821,6 +830,24 @@ __global__ void __launch_bounds__(kThreads, 5) sample_kernel(const SampleArgs a)
     __syncthreads();
     rule_valid = sm.b_i32[6] != 0;
     if (rule_valid) P = sm.rowp;
+  }
+  // A full-row cut that only the full-row draw (which ranks ties itself) and
+  // the row's own draft token read may leave open which of its ties of the cut
+  // value come first: every target row on that path when draws are deferred,
+  // and draft rows whose sequence's target rows take it too (a draft row under
+  // a kept-list target is read by the list draw, which needs the exact cut).
+  if (a.defer && P.path == PATH_FULL) {
+    bool lazy = !is_draft;
+    if (is_draft) {
+      if (EX && a.tps) {
+        if (threadIdx.x == 0) sm.b_i32[5] = row_params_of(a.tps[b], a.V).path;
+        __syncthreads();
+        lazy = sm.b_i32[5] == PATH_FULL;
+      } else {
+        lazy = a.tp.path == PATH_FULL;
+      }
+    }
+    P.lazy = lazy ? 1 : 0;
   }
   {
     // the sequence's draft tokens and uniforms, for the epilogue: copied while
@@ -1489,161 +1516,596 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
 // block-wide with identical per-element arithmetic for the first x with
 // C(x) > u Z [wrblog §5, §6].  Z == 0 after a rejection falls back to the
 // draw from p, over the whole row, as the sequence epilogue did.
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 5) draw_kernel(const SampleArgs a) {  // 5 CTAs/SM: more loads in flight
+// ------------------------------------------------------------------ full-row draw
+// The draw at the position the epilogue chose, over whole rows: the inverse
+// CDF, in vocabulary order, of w(x) = p(x) (the bonus draw) or
+// (p(x) - beta q(x))+ (after a rejection) [wrblog §5, §6].  The rows are cut
+// into chunks of kChunkVecs vectors; CTA (b, s) sums the weights of a run of
+// draw_run chunks with per-warp partials (no barrier per chunk), and the
+// sequence's last CTA finds the chunk holding u Z and the token inside it.
+//
+// Ties of a cut value.  The streaming sums keep every element whose value is
+// at least the row's cut value, ties included, and each chunk also records
+// its ties of the target's and of the draft's cut value and how its sum
+// changes when the target's, the draft's or both rows' ties are dropped.  A
+// row decides its ties either by index (an exact cut: ties up to the index of
+// its last kept one) or by rank (a lazy cut, RowStat::n_list = n > 0: the
+// first n ties in index order); so a chunk keeps all its ties, none, or --
+// the one chunk per row where the last kept tie falls -- some, and that chunk
+// is summed again exactly.  No row pass has to locate a lazy cut's last tie,
+// and the streaming loop makes no index test.
+struct __align__(16) ChunkSum {
+  double s;         // weight sum, every tie of either cut value kept
+  double d[3];      // change when the target's, the draft's, or both rows' ties are dropped
+  int32_t nt, nd;   // ties of the target / draft cut value in the chunk
+  int32_t pad[2];
+};
+static_assert(sizeof(ChunkSum) == 48, "ChunkSum layout");
+
+constexpr int kDrawMaxRun = 32;   // chunks one draw CTA sums (its per-warp partials live in shared memory)
+constexpr int kDrawStages = 2;    // chunks of each row in flight per draw CTA (bulk copies)
+constexpr int kStageRowBytes = kChunkVecs * 16;
+
+struct DrawCtx {
+  Row trow, drow;
+  float kt, kd;            // cut values: kept iff value >= them, ties decided per chunk
+  float tt, td;            // tie values (NaN: the row has no cut, nothing ties)
+  uint32_t it, id;         // exact cuts: index of the last kept tie
+  int nt, nd;              // lazy cuts: ties kept (0: an exact cut)
+  float cTt, bt, cTd, bd;  // kept weight 2^(z cT + b), b = -m cT - log2 W: the probability
+  float beta;
+  int dj, nq;
+};
+
+struct DrawPart {
+  df s[kDrawMaxRun][kWarps];     // per chunk and warp: weight sum (ties kept)
+  df at[kDrawMaxRun][kWarps];    // weight on target ties
+  df ad[kDrawMaxRun][kWarps];    // p - w on draft ties
+  df ab[kDrawMaxRun][kWarps];    // p - w on elements that tie both cuts
+  int nt[kDrawMaxRun][kWarps], nd[kDrawMaxRun][kWarps];
+  double xs[2];        // exact sums of the (at most two) chunks where a row's last kept tie falls
+  int xk[2];           // their chunk indices (-1: none)
+  int xbt[2], xbd[2];  // ties before them (target, draft)
+  double tl, Z;        // the draw's offset inside the chosen chunk; the total weight
+  int K, Kbt, Kbd;     // the chosen chunk and the ties before it
+  DrawCtx ctx;         // the draw's context, for the last CTA's block-wide steps
+  RowStat ts;          // the target row's summary (Z = 0 fallback)
+  unsigned long long bar[kDrawStages];   // bulk-copy barriers, one per stage
+};
+// Dynamic shared memory of a draw CTA: Smem, DrawPart, then the stages
+// (stage s, row r at kStageRowBytes (2 s + r)).
+constexpr size_t kDrawStageOff = (sizeof(Smem) + sizeof(DrawPart) + 127) / 128 * 128;
+constexpr size_t kDrawSmem = kDrawStageOff + static_cast<size_t>(kDrawStages) * 2 * kStageRowBytes;
+
+__device__ __forceinline__ float kept_w(float z, float k, float cT, float b) {
+  return z >= k ? fast_exp2(fmaf(z, cT, b)) : 0.0f;
+}
+template <int MODE>
+__device__ __forceinline__ float draw_w(float p, float q, float beta) {
+  return MODE == 0 ? p : fmaxf(p - beta * q, 0.0f);
+}
+// q(x) of the draw, ties kept: 0 (bonus), the draft's full row, its kept list, or one-hot at dj.
+template <int MODE>
+__device__ __forceinline__ float draw_qk(const DrawCtx& c, float zd, uint32_t x, const Smem& sm) {
+  if (MODE == 1) return kept_w(zd, c.kd, c.cTd, c.bd);
+  if (MODE == 2) return list_lookup(sm.u.e.qtok, sm.u.e.qp, c.nq, static_cast<int>(x));
+  if (MODE == 3) return static_cast<int>(x) == c.dj ? 1.0f : 0.0f;
+  return 0.0f;
+}
+
+template <int DT, int MODE>
+__device__ __forceinline__ int draw_load(const DrawCtx& c, int v, uint4& rt, uint4& rd) {
+  const int n = load_vec<DT, false>(c.trow, v, rt);
+  rd = make_uint4(0u, 0u, 0u, 0u);
+  if (MODE == 1 && n) load_vec<DT, false>(c.drow, v, rd);
+  return n;
+}
+
+// How a chunk treats one row's ties: 0 keeps them all, 1 none, 2 some.
+__device__ __forceinline__ int tie_status(int n, uint32_t idx, uint32_t before, uint32_t cnt, uint32_t x0,
+                                          uint32_t x1) {
+  if (cnt == 0u) return 0;
+  if (n > 0) return before + cnt <= static_cast<uint32_t>(n) ? 0 : (before >= static_cast<uint32_t>(n) ? 1 : 2);
+  return x1 - 1u <= idx ? 0 : (x0 > idx ? 1 : 2);
+}
+
+// Weights of chunk k with every tie decided: by rank for a lazy cut (bt / bd
+// ties before the chunk, then in index order), by index for an exact one.
+// The chunk is taken in two halves; in each, thread t takes two consecutive
+// vectors, so thread order is index order.  Returns the chunk's sum (every
+// thread); with find, also the first token where the running sum exceeds tl
+// (else the last token with weight) in *tok.  Block-wide; c lives in shared
+// memory.
+template <int DT, int MODE>
+__device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int k, int bt, int bd, bool find,
+                                           double tl, int* tok, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
-  constexpr int kVPT = 4;   // vectors per thread in a chunk (chunk_vecs == kVPT * kThreads)
+  constexpr int kVPT = 2;
+  static_assert(2 * kVPT * kThreads == kChunkVecs, "two halves of two vectors per thread make a chunk");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nv = c.trow.nvec;
+  if (tid == 0) { sm.b_i32[5] = -1; sm.b_i32[6] = -1; sm.b_i32[7] = -1; }
+  double run = 0.0;            // weight of the halves before
+  uint32_t rbt = static_cast<uint32_t>(bt), rbd = static_cast<uint32_t>(bd);
+  for (int half = 0; half < 2; ++half) {
+    const int v0 = k * chunk_vecs + half * kVPT * kThreads + tid * kVPT;
+    uint4 rt[kVPT], rd[kVPT];
+    int n[kVPT];
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) n[i] = (v0 + i < nv) ? draw_load<DT, MODE>(c, v0 + i, rt[i], rd[i]) : 0;
+    uint32_t ct = 0, cd = 0;
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+      float zt[P], zd[P];
+      unpack<DT>(rt[i], zt);
+      unpack<DT>(rd[i], zd);
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        ct += (e < n[i] && zt[e] == c.tt) ? 1u : 0u;
+        cd += (MODE == 1 && e < n[i] && zd[e] == c.td) ? 1u : 0u;
+      }
+    }
+    const uint32_t it_ = warp_incl_scan_u32(ct, lane), id_ = warp_incl_scan_u32(cd, lane);
+    if (lane == 31) { sm.nw[warp] = static_cast<int>(it_); sm.red_i[warp] = static_cast<int>(id_); }
+    __syncthreads();
+    uint32_t rt0 = rbt + it_ - ct, rd0 = rbd + id_ - cd;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) { rt0 += static_cast<uint32_t>(sm.nw[w]); rd0 += static_cast<uint32_t>(sm.red_i[w]); }
+      rbt += static_cast<uint32_t>(sm.nw[w]);
+      rbd += static_cast<uint32_t>(sm.red_i[w]);
+    }
+    auto walk = [&](auto&& visit) {
+      uint32_t rt_ = rt0, rd_ = rd0;
+#pragma unroll
+      for (int i = 0; i < kVPT; ++i) {
+        float zt[P], zd[P];
+        unpack<DT>(rt[i], zt);
+        unpack<DT>(rd[i], zd);
+#pragma unroll
+        for (int e = 0; e < P; ++e) {
+          if (e >= n[i]) continue;
+          const uint32_t x = static_cast<uint32_t>((v0 + i) * P + e);
+          float p = kept_w(zt[e], c.kt, c.cTt, c.bt);
+          if (zt[e] == c.tt && !(c.nt > 0 ? rt_++ < static_cast<uint32_t>(c.nt) : x <= c.it)) p = 0.0f;
+          float q = draw_qk<MODE>(c, zd[e], x, sm);
+          if (MODE == 1 && zd[e] == c.td && !(c.nd > 0 ? rd_++ < static_cast<uint32_t>(c.nd) : x <= c.id)) q = 0.0f;
+          visit(static_cast<int>(x), draw_w<MODE>(p, q, c.beta));
+        }
+      }
+    };
+    float ts = 0.0f;
+    int last = -1;
+    walk([&](int x, float w) { ts += w; if (w > 0.0f) last = x; });
+    const df incl = warp_incl_scan_df(df_from(ts), lane);
+    if (lane == 31) { sm.red_f[warp] = incl.hi; sm.red_lo[warp] = incl.lo; }
+    __syncthreads();
+    df base = df_add(incl, df_from(-ts)), tot = df_from(0.0f);
+    for (int w = 0; w < kWarps; ++w) {
+      const df x = {sm.red_f[w], sm.red_lo[w]};
+      if (w < warp) base = df_add(base, x);
+      tot = df_add(tot, x);
+    }
+    const double b0 = run + df_to_double(base);
+    if (find && sm.b_i32[5] == -1) {         // not found in an earlier half (same in every thread)
+      __syncthreads();
+      if (ts > 0.0f && b0 + static_cast<double>(ts) > tl)
+        atomicMin(reinterpret_cast<unsigned*>(&sm.b_i32[5]), static_cast<unsigned>(tid));
+      if (last >= 0) atomicMax(&sm.b_i32[6], last);
+      __syncthreads();
+      if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
+        float c32 = 0.0f;
+        int found = -1;
+        walk([&](int x, float w) {
+          if (w > 0.0f) {
+            c32 += w;
+            if (found < 0 && b0 + static_cast<double>(c32) > tl) found = x;
+          }
+        });
+        sm.b_i32[7] = found >= 0 ? found : last;
+      }
+    }
+    run += df_to_double(tot);
+    __syncthreads();
+  }
+  if (find) *tok = sm.b_i32[5] == -1 ? sm.b_i32[6] : sm.b_i32[7];   // rounding: the last weighted token
+  __syncthreads();
+  return run;
+}
+
+template <int DT, int MODE>
+__device__ __noinline__ void draw_pick(const SampleArgs& a, int b, int j, int mode, int flags, bool onehot, Smem& sm,
+                                       DrawPart& dp);
+
+// One draw CTA: its run of chunk sums, then (the sequence's last CTA) the draw.
+template <int DT, int MODE>
+__device__ __noinline__ void draw_body(const SampleArgs& a, int b, const DrawRec rec, const RowStat ts,
+                                       const RowStat ds, bool onehot, Smem& sm, DrawPart& dp, uint32_t stage0) {
+  constexpr int P = Elem<DT>::kPer;
+  constexpr int kVPT = 4;
+  constexpr int kStep = MODE == 1 ? 2 : 4;   // 64 bytes of each thread in flight per step
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float qnan = __int_as_float(0x7fc00000);
+  DrawCtx c;
+  c.trow = seq_row<DT>(a, b, rec.j, false);
+  c.drow = MODE == 1 ? seq_row<DT>(a, b, rec.j, true) : c.trow;
+  const CutTest ctt = cut_test(ts.cut), ctd = cut_test(ds.cut);
+  c.kt = ctt.v; c.it = ctt.i;
+  c.kd = ctd.v; c.id = ctd.i;
+  c.tt = ts.cut != 0ull ? ctt.v : qnan;
+  c.td = (MODE == 1 && ds.cut != 0ull) ? ctd.v : qnan;
+  c.nt = ts.path == PATH_FULL ? ts.n_list : 0;
+  c.nd = (MODE == 1 && ds.path == PATH_FULL) ? ds.n_list : 0;
+  c.cTt = ts.cT;
+  c.bt = static_cast<float>(-static_cast<double>(ts.m) * static_cast<double>(ts.cT) - log2(ts.W));
+  c.cTd = ds.cT;
+  c.bd = static_cast<float>(-static_cast<double>(ds.m) * static_cast<double>(ds.cT) - log2(ds.W));
+  c.beta = a.beta;
+  c.dj = rec.dj;
+  c.nq = 0;
+  if (MODE == 2) {                 // the draft's kept list, in token order
+    const int slots = 2 * a.G + 1;
+    const ListEntry* ql = a.lists + (static_cast<size_t>(b) * slots + a.G + 1 + rec.j) * kListCap;
+    c.nq = ds.n_list;
+    if (tid < c.nq) {
+      const ListEntry q = load_entry(ql + tid);
+      sm.u.e.qtok[tid] = q.token;
+      sm.u.e.qp[tid] = q.p + q.p_lo;
+    }
+    __syncthreads();
+  }
+  const int nv = c.trow.nvec;
+  const int k0 = blockIdx.y * a.draw_run, k1 = min(a.nchunk, k0 + a.draw_run);
+
+  // 1. this CTA's run of chunks: per-warp partial sums, no barrier per chunk
+  float s = 0.0f, at = 0.0f, ad = 0.0f, ab = 0.0f, ct = 0.0f, cd = 0.0f;
+  // one element: its weight with ties kept, and the tie bookkeeping
+  auto elem = [&](float zt, float zd, uint32_t x) {
+    const float pk = kept_w(zt, c.kt, c.cTt, c.bt);
+    const float qk = draw_qk<MODE>(c, zd, x, sm);
+    const float w = draw_w<MODE>(pk, qk, c.beta);
+    s += w;
+    const bool tie_t = zt == c.tt;
+    at += tie_t ? w : 0.0f;
+    ct += tie_t ? 1.0f : 0.0f;
+    if (MODE == 1) {
+      const bool tie_d = zd == c.td;
+      ad += tie_d ? pk - w : 0.0f;
+      cd += tie_d ? 1.0f : 0.0f;
+      if (tie_t && tie_d) ab += pk - w;
+    }
+  };
+  // a chunk done: this warp's partials
+  auto chunk_done = [&](int k) {
+    const df ws = warp_sum_df(df_from(s));
+    const bool ties = __any_sync(kFull, ct + cd > 0.0f);
+    df wt = df_from(0.0f), wd = df_from(0.0f), wb = df_from(0.0f);
+    int nt = 0, nd = 0;
+    if (ties) {
+      wt = warp_sum_df(df_from(at));
+      wd = warp_sum_df(df_from(ad));
+      wb = warp_sum_df(df_from(ab));
+      nt = __reduce_add_sync(kFull, static_cast<unsigned>(ct));
+      nd = __reduce_add_sync(kFull, static_cast<unsigned>(cd));
+    }
+    if (lane == 0) {
+      const int r = k - k0;
+      dp.s[r][warp] = ws;
+      dp.at[r][warp] = wt;
+      dp.ad[r][warp] = wd;
+      dp.ab[r][warp] = wb;
+      dp.nt[r][warp] = nt;
+      dp.nd[r][warp] = nd;
+    }
+    s = at = ad = ab = ct = cd = 0.0f;
+  };
+  bool stalled = false;
+  if (c.trow.aligned && (MODE != 1 || c.drow.aligned)) {
+    // bulk copies: one thread streams whole chunks of both rows into the
+    // stages, kDrawStages ahead; every thread reads its vectors from there
+    const uint32_t bar = smem_u32(&dp.bar[0]);
+    if (tid == 0) {
+      for (int st = 0; st < kDrawStages; ++st) mbar_init(bar + 8u * st, 1u);
+      mbar_init_fence();
+    }
+    __syncthreads();
+    auto issue = [&](int k, int st) {
+      const int v0 = k * a.chunk_vecs;
+      const uint32_t bytes = static_cast<uint32_t>(min(a.chunk_vecs, nv - v0)) * 16u;
+      mbar_expect_tx(bar + 8u * st, (MODE == 1 ? 2u : 1u) * bytes);
+      bulk_g2s(stage0 + 2u * st * kStageRowBytes, c.trow.base + static_cast<size_t>(v0) * 16, bytes, bar + 8u * st);
+      if (MODE == 1)
+        bulk_g2s(stage0 + (2u * st + 1u) * kStageRowBytes, c.drow.base + static_cast<size_t>(v0) * 16, bytes,
+                 bar + 8u * st);
+    };
+    if (tid == 0)
+      for (int st = 0; st < kDrawStages && k0 + st < k1; ++st) issue(k0 + st, st);
+    int k = k0;
+    for (; k < k1; ++k) {
+      const int r = k - k0, st = r % kDrawStages;
+      const bool ok = mbar_wait(bar + 8u * st, static_cast<uint32_t>(r / kDrawStages) & 1u);
+      if (__syncthreads_or(!ok)) { stalled = true; break; }
+      const int v0 = k * a.chunk_vecs, nvk = min(a.chunk_vecs, nv - v0);
+      const uint32_t srow = stage0 + 2u * st * kStageRowBytes;
+#pragma unroll
+      for (int i = 0; i < kVPT; ++i) {
+        const int vl = i * kThreads + tid;
+        if (vl >= nvk) continue;
+        const uint4 rt = lds128(srow + 16u * vl);
+        const uint4 rd = MODE == 1 ? lds128(srow + kStageRowBytes + 16u * vl) : make_uint4(0u, 0u, 0u, 0u);
+        float zt[P], zd[P];
+        unpack<DT>(rt, zt);
+        unpack<DT>(rd, zd);
+#pragma unroll
+        for (int e = 0; e < P; ++e) elem(zt[e], zd[e], static_cast<uint32_t>((v0 + vl) * P + e));
+      }
+      chunk_done(k);
+      __syncthreads();                            // every thread is done with stage st
+      if (tid == 0 && k + kDrawStages < k1) {
+        fence_proxy_async_smem();
+        issue(k + kDrawStages, st);
+      }
+    }
+    if (stalled && tid == 0) {
+      // let the copies still in flight land (bounded) before the CTA leaves
+      for (int q = k; q < min(k1, k + kDrawStages); ++q)
+        mbar_wait(bar + 8u * ((q - k0) % kDrawStages), static_cast<uint32_t>((q - k0) / kDrawStages) & 1u);
+    }
+  } else {
+    for (int k = k0; k < k1; ++k) {
+      const int v0 = k * a.chunk_vecs;
+#pragma unroll 1
+      for (int h = 0; h < kVPT; h += kStep) {   // kStep vectors of each row in flight per step
+        uint4 rt[kStep], rd[kStep];
+        int n[kStep];
+#pragma unroll
+        for (int i = 0; i < kStep; ++i) {
+          const int v = v0 + (h + i) * kThreads + tid;
+          n[i] = v < nv ? draw_load<DT, MODE>(c, v, rt[i], rd[i]) : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < kStep; ++i) {
+          const int v = v0 + (h + i) * kThreads + tid;
+          float zt[P], zd[P];
+          unpack<DT>(rt[i], zt);
+          unpack<DT>(rd[i], zd);
+          if (n[i] == P) {
+#pragma unroll
+            for (int e = 0; e < P; ++e) elem(zt[e], zd[e], static_cast<uint32_t>(v * P + e));
+          } else {
+            for (int e = 0; e < n[i]; ++e) elem(zt[e], zd[e], static_cast<uint32_t>(v * P + e));
+          }
+        }
+      }
+      chunk_done(k);
+    }
+  }
+  __syncthreads();
+  ChunkSum* D = a.dsum + static_cast<size_t>(b) * a.nchunk;
+  for (int r = tid; r < k1 - k0; r += kThreads) {
+    double sw = 0.0, st = 0.0, sd = 0.0, sb = 0.0;
+    int nt = 0, nd = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      sw += df_to_double(dp.s[r][w]);
+      st += df_to_double(dp.at[r][w]);
+      sd += df_to_double(dp.ad[r][w]);
+      sb += df_to_double(dp.ab[r][w]);
+      nt += dp.nt[r][w];
+      nd += dp.nd[r][w];
+    }
+    ChunkSum cs;
+    cs.s = sw;
+    cs.d[0] = -st;             // target ties dropped: their weight goes
+    cs.d[1] = sd;              // draft ties dropped: their weight becomes p
+    cs.d[2] = sd - st - sb;    // both: target ties lose their weight, draft-only ties become p
+    cs.nt = stalled ? 0 : nt;
+    cs.nd = stalled ? 0 : nd;
+    cs.pad[0] = stalled ? 1 : 0;   // this CTA's copies stalled: the sequence reports SEQ_STALLED
+    cs.pad[1] = 0;
+    D[k0 + r] = cs;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // release this CTA's chunk sums, acquire the others' (the last arriver reads them all)
+    const unsigned prev = atom_add_acq_rel_gpu(&a.dcount[b], 1u);
+    sm.b_i32[7] = (prev + 1u == gridDim.y) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sm.b_i32[7]) return;
+  if (tid == 0) {
+    dp.ctx = c;
+    dp.ts = ts;
+  }
+  __syncthreads();
+  draw_pick<DT, MODE>(a, b, rec.j, rec.mode, rec.flags, onehot, sm, dp);
+}
+
+// The sequence's last draw CTA: each chunk's tie statuses, exact sums where a
+// row's last kept tie falls, Z, the chunk holding u Z and the token inside
+// it; then the outputs.
+template <int DT, int MODE>
+__device__ __noinline__ void draw_pick(const SampleArgs& a, int b, int j, int mode, int flags, bool onehot, Smem& sm,
+                                       DrawPart& dp) {
+  constexpr int P = Elem<DT>::kPer;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const DrawCtx& c = dp.ctx;
+  const ChunkSum* D = a.dsum + static_cast<size_t>(b) * a.nchunk;
+  const double u = static_cast<double>(a.u_samp[b]);
+  const uint32_t cx = static_cast<uint32_t>(a.chunk_vecs) * P;   // elements per chunk
+  // chunk k's weight under the ties it keeps; -1: some of a row's ties (summed exactly)
+  auto chunk_w = [&](int k, const ChunkSum& cs, uint32_t bt, uint32_t bd) -> double {
+    const uint32_t x0 = static_cast<uint32_t>(k) * cx, x1 = min(static_cast<uint32_t>(a.V), x0 + cx);
+    const int st = tie_status(c.nt, c.it, bt, static_cast<uint32_t>(cs.nt), x0, x1);
+    const int sd = tie_status(c.nd, c.id, bd, static_cast<uint32_t>(cs.nd), x0, x1);
+    if (st == 2 || sd == 2) return -1.0;
+    return fmax(cs.s + (st ? (sd ? cs.d[2] : cs.d[0]) : (sd ? cs.d[1] : 0.0)), 0.0);
+  };
+  auto load_cs = [&](int k) {
+    ChunkSum cs;
+    cs.s = 0.0; cs.d[0] = cs.d[1] = cs.d[2] = 0.0; cs.nt = cs.nd = 0; cs.pad[0] = cs.pad[1] = 0;
+    if (k < a.nchunk) {
+      cs.s = __ldcg(&D[k].s);
+      cs.d[0] = __ldcg(&D[k].d[0]);
+      cs.d[1] = __ldcg(&D[k].d[1]);
+      cs.d[2] = __ldcg(&D[k].d[2]);
+      cs.nt = __ldcg(&D[k].nt);
+      cs.nd = __ldcg(&D[k].nd);
+      cs.pad[0] = __ldcg(&D[k].pad[0]);
+    }
+    return cs;
+  };
+  if (warp == 0) {
+    if (lane == 0) { dp.xk[0] = dp.xk[1] = -1; dp.K = 0; }
+    __syncwarp();
+    uint32_t bt = 0, bd = 0;
+    int nx = 0;
+    bool stalled = false;
+    for (int base = 0; base < a.nchunk; base += 32) {
+      const int k = base + lane;
+      const ChunkSum cs = load_cs(k);
+      stalled = __any_sync(kFull, cs.pad[0] != 0) || stalled;
+      const uint32_t it_ = warp_incl_scan_u32(static_cast<uint32_t>(cs.nt), lane);
+      const uint32_t id_ = warp_incl_scan_u32(static_cast<uint32_t>(cs.nd), lane);
+      const uint32_t kbt = bt + it_ - cs.nt, kbd = bd + id_ - cs.nd;
+      const bool exact = k < a.nchunk && chunk_w(k, cs, kbt, kbd) < 0.0;
+      const unsigned m = __ballot_sync(kFull, exact);
+      if (exact) {
+        const int slot = nx + __popc(m & ((1u << lane) - 1u));
+        if (slot < 2) { dp.xk[slot] = k; dp.xbt[slot] = static_cast<int>(kbt); dp.xbd[slot] = static_cast<int>(kbd); }
+      }
+      nx += __popc(m);
+      bt += __shfl_sync(kFull, it_, 31);
+      bd += __shfl_sync(kFull, id_, 31);
+    }
+    if (lane == 0 && stalled) dp.K = -2;
+  }
+  __syncthreads();
+  if (dp.K == -2) {                     // a CTA of this draw stalled: commit nothing
+    const size_t ob = static_cast<size_t>(b) * (a.G + 1);
+    for (int t = tid; t <= a.G; t += kThreads) a.out_tokens[ob + t] = -1;
+    if (tid == 0) {
+      a.out_nacc[b] = -1;
+      if (a.out_nemit) a.out_nemit[b] = -1;
+      if (a.out_Z) a.out_Z[b] = -1.0f;
+      if (a.out_status) a.out_status[b] = SEQ_STALLED;
+      a.dcount[b] = 0u;
+    }
+    return;
+  }
+  for (int x = 0; x < 2; ++x) {
+    if (dp.xk[x] < 0) continue;
+    const double v = chunk_exact<DT, MODE>(c, a.chunk_vecs, dp.xk[x], dp.xbt[x], dp.xbd[x], false, 0.0, nullptr, sm);
+    if (tid == 0) dp.xs[x] = fmax(v, 0.0);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // Z, then the first chunk (with weight) whose range holds t = u Z; the
+    // last chunk with weight if rounding leaves t at or above the total
+    double Z = 0.0;
+    for (int pass = 0; pass < 2; ++pass) {
+      const double t = u * Z;
+      uint32_t bt = 0, bd = 0;
+      double run = 0.0, tl = 0.0, last_start = 0.0, tot = 0.0;
+      int K = -1, lastK = -1, Kbt = 0, Kbd = 0, lbt = 0, lbd = 0;
+      for (int base = 0; base < a.nchunk; base += 32) {
+        const int k = base + lane;
+        const ChunkSum cs = load_cs(k);
+        const uint32_t it_ = warp_incl_scan_u32(static_cast<uint32_t>(cs.nt), lane);
+        const uint32_t id_ = warp_incl_scan_u32(static_cast<uint32_t>(cs.nd), lane);
+        const uint32_t kbt = bt + it_ - cs.nt, kbd = bd + id_ - cs.nd;
+        double w = 0.0;
+        if (k < a.nchunk) {
+          w = chunk_w(k, cs, kbt, kbd);
+          if (w < 0.0) w = (k == dp.xk[0]) ? dp.xs[0] : dp.xs[1];
+        }
+        bt += __shfl_sync(kFull, it_, 31);
+        bd += __shfl_sync(kFull, id_, 31);
+        if (pass == 0) {
+          tot += warp_sum_f64(w);
+          continue;
+        }
+        if (K >= 0) continue;
+        const double incl = warp_incl_scan_f64(w, lane);
+        const unsigned hit = __ballot_sync(kFull, w > 0.0 && run + incl > t);
+        const unsigned pos = __ballot_sync(kFull, w > 0.0);
+        if (hit) {
+          const int L = __ffs(hit) - 1;
+          K = base + L;
+          tl = t - (run + __shfl_sync(kFull, incl - w, L));
+          Kbt = static_cast<int>(__shfl_sync(kFull, kbt, L));
+          Kbd = static_cast<int>(__shfl_sync(kFull, kbd, L));
+        } else if (pos) {
+          const int L = 31 - __clz(pos);
+          lastK = base + L;
+          last_start = run + __shfl_sync(kFull, incl - w, L);
+          lbt = static_cast<int>(__shfl_sync(kFull, kbt, L));
+          lbd = static_cast<int>(__shfl_sync(kFull, kbd, L));
+        }
+        run += __shfl_sync(kFull, incl, 31);
+      }
+      if (pass == 0) {
+        Z = tot;
+        continue;
+      }
+      if (K < 0) { K = lastK; tl = t - last_start; Kbt = lbt; Kbd = lbd; }
+      if (lane == 0) { dp.Z = Z; dp.tl = tl; dp.K = K; dp.Kbt = Kbt; dp.Kbd = Kbd; }
+    }
+  }
+  __syncthreads();
+  const double Z = dp.Z;
+  int tok = -1;
+  if (!(Z > 0.0) || dp.K < 0) {
+    // no weight at all: after a rejection, draw from p over the whole row
+    if (mode != 0) {
+      flags |= SEQ_FLAG_Z_ZERO;
+      RowStat t2 = dp.ts;
+      if (c.nt > 0) {                  // a lazy cut: locate its last kept tie first
+        const uint32_t K = static_cast<uint32_t>(t2.cut >> 32);
+        const int idx = find_nth_with_key<DT>(c.trow, K, static_cast<uint32_t>(c.nt), sm);
+        t2.cut = composite(K, static_cast<uint32_t>(idx));
+      }
+      RowStat d0;
+      d0.path = PATH_FULL; d0.W = 1.0; d0.cut = 0; d0.m = 0.0f; d0.n_list = 0; d0.cT = 0.0f; d0.invW = 1.0f;
+      ScanCtx sc = make_scan<DT>(a, b, j, 0, onehot, t2, d0, -1, sm);
+      double Zp;
+      tok = block_scan_draw<DT>(sc, u, false, Zp, flags, sm);
+    }
+  } else {
+    chunk_exact<DT, MODE>(c, a.chunk_vecs, dp.K, dp.Kbt, dp.Kbd, true, dp.tl, &tok, sm);
+  }
+  if (tid == 0) {
+    a.out_tokens[static_cast<size_t>(b) * (a.G + 1) + j] = tok;
+    if (a.out_Z) a.out_Z[b] = mode != 0 ? static_cast<float>(Z) : -1.0f;
+    if (a.eos >= 0 && tok == a.eos) flags |= SEQ_FLAG_EOS;
+    if (a.out_status) a.out_status[b] = flags;
+    a.dcount[b] = 0u;   // leave the workspace reusable
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) draw_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  const int b = blockIdx.x, ch = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  DrawPart& dp = *reinterpret_cast<DrawPart*>(smem_raw + sizeof(Smem));
+  // launched as a programmatic dependent of the row kernel: its records are
+  // read only once that grid has completed
+  grid_dependency_wait();
+  const int b = blockIdx.x;
   const DrawRec rec = a.drec[b];
   if (rec.j < 0) return;
   const int slots = 2 * a.G + 1;
   const bool onehot = a.dft == nullptr || (a.onehot != nullptr && a.onehot[b] != 0);
-  const bool residual = rec.mode != 0;
   const RowStat* S = a.stats + static_cast<size_t>(b) * slots;
   const RowStat ts = load_stat(S + rec.j);
   RowStat ds;
   ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f; ds.invW = 1.0f;
-  if (residual && !onehot) ds = load_stat(S + a.G + 1 + rec.j);
-  ScanCtx c = make_scan<DT>(a, b, rec.j, rec.mode, onehot, ts, ds, rec.dj, sm);
-  const int nv = c.trow.nvec;
-
-  // 1. this chunk's weight sum
-  {
-    const int v0 = ch * a.chunk_vecs;
-    uint4 rt[kVPT], rd[kVPT];
-    int n[kVPT];
-#pragma unroll
-    for (int i = 0; i < kVPT; ++i) {
-      const int v = v0 + i * kThreads + tid;
-      n[i] = v < nv ? scan_load<DT>(c, v, rt[i], rd[i]) : 0;
-    }
-    float ls = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kVPT; ++i) {
-      float w[P];
-      if (n[i]) ls += scan_weights<DT>(c, v0 + i * kThreads + tid, n[i], rt[i], rd[i], sm, w);
-    }
-    const double cs = block_sum_fd(ls, sm);
-    if (tid == 0) {
-      a.dsum[static_cast<size_t>(b) * a.nchunk + ch] = cs;
-      __threadfence();
-      const unsigned prev = atomicAdd(&a.dcount[b], 1u);
-      sm.b_i32[7] = (prev + 1u == static_cast<unsigned>(a.nchunk)) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!sm.b_i32[7]) return;
-    __threadfence();
-  }
-
-  // 2. the last chunk CTA: Z, the chunk holding u Z, the element inside it
-  const double* D = a.dsum + static_cast<size_t>(b) * a.nchunk;
-  const double u = static_cast<double>(a.u_samp[b]);
-  int flags = rec.flags;
-  if (warp == 0) {
-    double Z = 0.0;
-    for (int base = 0; base < a.nchunk; base += 32) {
-      const int k = base + lane;
-      Z += warp_sum_f64(k < a.nchunk ? __ldcg(D + k) : 0.0);
-    }
-    const double t = u * Z;
-    double run = 0.0, tl = 0.0, last_start = 0.0;
-    int K = -1, lastK = -1;
-    for (int base = 0; base < a.nchunk && K < 0; base += 32) {
-      const int k = base + lane;
-      const double cs = k < a.nchunk ? __ldcg(D + k) : 0.0;
-      const double incl = warp_incl_scan_f64(cs, lane);
-      const unsigned hit = __ballot_sync(kFull, cs > 0.0 && run + incl > t);
-      const unsigned pos = __ballot_sync(kFull, cs > 0.0);
-      if (hit) {
-        const int L = __ffs(hit) - 1;
-        K = base + L;
-        tl = t - (run + __shfl_sync(kFull, incl - cs, L));
-      } else if (pos) {
-        const int L = 31 - __clz(pos);
-        lastK = base + L;
-        last_start = run + __shfl_sync(kFull, incl - cs, L);
-      }
-      run += __shfl_sync(kFull, incl, 31);
-    }
-    if (K < 0) { K = lastK; tl = t - last_start; }     // rounding: the last chunk with weight
-    if (lane == 0) {
-      sm.b_f64[0] = Z;
-      sm.b_f64[1] = tl;
-      sm.b_i32[4] = K;
-    }
-  }
-  __syncthreads();
-  const double Z = sm.b_f64[0];
-  int tok = -1;
-  if (!(Z > 0.0) || sm.b_i32[4] < 0) {
-    // no weight at all: after a rejection draw from p over the whole row
-    if (residual) {
-      flags |= SEQ_FLAG_Z_ZERO;
-      c.mode = 0;
-      double Zp;
-      tok = block_scan_draw<DT>(c, u, false, Zp, flags, sm);
-    }
-  } else {
-    // block-wide re-scan of chunk K: thread t takes kVPT consecutive vectors
-    const double tl = sm.b_f64[1];
-    const int v0 = sm.b_i32[4] * a.chunk_vecs + tid * kVPT;
-    float w[kVPT][P];
-    float ts_sum = 0.0f;
-    int last_pos = -1;
-#pragma unroll
-    for (int i = 0; i < kVPT; ++i) {
-      const int v = v0 + i;
-      uint4 rt, rd;
-      const int n = v < nv ? scan_load<DT>(c, v, rt, rd) : 0;
-      if (n) ts_sum += scan_weights<DT>(c, v, n, rt, rd, sm, w[i]);
-      else {
-#pragma unroll
-        for (int e = 0; e < P; ++e) w[i][e] = 0.0f;
-      }
-#pragma unroll
-      for (int e = 0; e < P; ++e) if (w[i][e] > 0.0f) last_pos = v * P + e;
-    }
-    // exclusive prefix of the per-thread sums, in thread (= vocabulary) order
-    const double incl = warp_incl_scan_f64(static_cast<double>(ts_sum), lane);
-    if (lane == 31) sm.u.e.wtot[warp] = incl;
-    if (tid == 0) { sm.b_i32[5] = -1; sm.b_i32[6] = -1; }
-    __syncthreads();
-    double wbase = 0.0;
-    for (int k = 0; k < warp; ++k) wbase += sm.u.e.wtot[k];
-    const double base = wbase + incl - static_cast<double>(ts_sum);
-    const bool mine = ts_sum > 0.0f && base + static_cast<double>(ts_sum) > tl;
-    if (mine) atomicMin(reinterpret_cast<unsigned*>(&sm.b_i32[5]), static_cast<unsigned>(tid));
-    if (last_pos >= 0) atomicMax(&sm.b_i32[6], last_pos);
-    __syncthreads();
-    if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
-      float c32 = 0.0f;
-      int found = -1, lastp = -1;
-#pragma unroll
-      for (int i = 0; i < kVPT; ++i) {
-#pragma unroll
-        for (int e = 0; e < P; ++e) {
-          if (w[i][e] > 0.0f) {
-            c32 += w[i][e];
-            lastp = (v0 + i) * P + e;
-            if (found < 0 && base + static_cast<double>(c32) > tl) found = lastp;
-          }
-        }
-      }
-      sm.b_i32[7] = found >= 0 ? found : lastp;
-    }
-    if (tid == 0 && sm.b_i32[5] == -1) sm.b_i32[7] = sm.b_i32[6];   // rounding: last weighted element
-    __syncthreads();
-    tok = sm.b_i32[7];
-  }
-  if (tid == 0) {
-    a.out_tokens[static_cast<size_t>(b) * (a.G + 1) + rec.j] = tok;
-    if (a.out_Z) a.out_Z[b] = residual ? static_cast<float>(Z) : -1.0f;
-    if (a.eos >= 0 && tok == a.eos) flags |= SEQ_FLAG_EOS;
-    if (a.out_status) a.out_status[b] = flags;
-    a.dcount[b] = 0u;   // leave the workspace reusable
+  if (rec.mode != 0 && !onehot) ds = load_stat(S + a.G + 1 + rec.j);
+  const uint32_t stage0 = smem_u32(smem_raw + kDrawStageOff);
+  switch (rec.mode) {
+    case 0: draw_body<DT, 0>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
+    case 1: draw_body<DT, 1>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
+    case 2: draw_body<DT, 2>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
+    default: draw_body<DT, 3>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
   }
 }
 
@@ -1996,7 +2458,6 @@ bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t elem_bytes(spec_dtype_t dt) { return dt == SPEC_BF16 ? 2 : 4; }
 int elems_per_vec(spec_dtype_t dt) { return dt == SPEC_BF16 ? 8 : 4; }
 
-constexpr int kChunkVecs = 4 * kThreads;   // draw_kernel: vectors per chunk (four per thread)
 
 // Chunks per row of the full-row draw (float32 rows have the most vectors).
 int draw_chunks(int V, spec_dtype_t dt) {
@@ -2029,7 +2490,7 @@ SampleLayout sample_layout(int B, int G, int V, const RowParams& tp, const RowPa
   L.drec = L.lists + (need_lists ? round_up(static_cast<size_t>(B) * slots * kListCap * sizeof(ListEntry)) : 0);
   const bool defer = tps || tp.path == PATH_FULL;
   L.dsum = L.drec + (defer ? round_up(static_cast<size_t>(B) * sizeof(DrawRec)) : 0);
-  L.total = L.dsum + (defer ? round_up(static_cast<size_t>(B) * draw_chunks(V, SPEC_F32) * sizeof(double)) : 0);
+  L.total = L.dsum + (defer ? round_up(static_cast<size_t>(B) * draw_chunks(V, SPEC_F32) * sizeof(ChunkSum)) : 0);
   return L;
 }
 
@@ -2057,18 +2518,57 @@ bool shape_ok(int B, int G, int V) {
 // Raises a kernel's dynamic shared memory limit once per device (the attribute
 // is per device; later calls only read an atomic bit mask).
 template <typename K>
-cudaError_t prepare(K kernel, std::atomic<uint64_t>& done) {
+cudaError_t prepare(K kernel, std::atomic<uint64_t>& done, size_t smem = sizeof(Smem) + sizeof(FullExtra)) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   const uint64_t bit = 1ull << (dev & 63);
   if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(Smem) + sizeof(FullExtra)));
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
 std::atomic<uint64_t> g_ready[18];  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list, sample-tree x {bf16, f32}
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  const int d = dev & 63;
+  int n = cache[d].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+  cache[d].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Chunks per draw CTA: about two waves of two draw CTAs per SM over the
+// batch, each CTA summing at least one and at most kDrawMaxRun chunks.
+int draw_run(int B, int nchunk) {
+  const int target = 2 * 2 * sm_count();
+  int splits = std::max(1, std::min(nchunk, (target + B - 1) / B));
+  splits = std::max(splits, (nchunk + kDrawMaxRun - 1) / kDrawMaxRun);
+  return (nchunk + splits - 1) / splits;
+}
+
+// The full-row draw, as a programmatic dependent of the row kernel (it waits
+// for that grid before reading its records; launching early hides the gap).
+template <typename K>
+cudaError_t launch_draw(K kernel, const SampleArgs& a, dim3 grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDrawSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 
 // Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
 // needs FullExtra after Smem; launches without such rows keep their occupancy.
@@ -2205,14 +2705,15 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   a.nchunk = draw_chunks(vocab, dtype);
   a.dcount = reinterpret_cast<uint32_t*>(ws + L.dcount);
   a.drec = reinterpret_cast<DrawRec*>(ws + L.drec);
-  a.dsum = reinterpret_cast<double*>(ws + L.dsum);
+  a.dsum = reinterpret_cast<ChunkSum*>(ws + L.dsum);
   a.early = early ? 1 : 0;
   a.stop_enc = reinterpret_cast<uint32_t*>(ws + L.stop);
   a.pairx = reinterpret_cast<unsigned long long*>(ws + L.pairx);
   // early exit: position-major, two CTA slots (target, draft) per sequence and position
   const unsigned grid = early ? static_cast<unsigned>(batch) * 2u * static_cast<unsigned>(gamma_max + 1)
                               : static_cast<unsigned>(batch) * static_cast<unsigned>(2 * gamma_max + 1);
-  const dim3 dgrid(static_cast<unsigned>(batch), static_cast<unsigned>(a.nchunk));
+  a.draw_run = draw_run(batch, a.nchunk);
+  const dim3 dgrid(static_cast<unsigned>(batch), static_cast<unsigned>((a.nchunk + a.draw_run - 1) / a.draw_run));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   // every host check has passed: a caller-less scratch gets its counters cleared
@@ -2249,23 +2750,23 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   } else if (dtype == SPEC_BF16 && ex) {
     err = prepare(sample_kernel<DT_BF16, true>, g_ready[10]);
     if (err == cudaSuccess) sample_kernel<DT_BF16, true><<<grid, kThreads, smem, s>>>(a);
-    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6]);
-    if (err == cudaSuccess && a.defer) draw_kernel<DT_BF16><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6], kDrawSmem);
+    if (err == cudaSuccess && a.defer) err = launch_draw(draw_kernel<DT_BF16>, a, dgrid, s);
   } else if (ex) {
     err = prepare(sample_kernel<DT_F32, true>, g_ready[11]);
     if (err == cudaSuccess) sample_kernel<DT_F32, true><<<grid, kThreads, smem, s>>>(a);
-    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_F32>, g_ready[7]);
-    if (err == cudaSuccess && a.defer) draw_kernel<DT_F32><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_F32>, g_ready[7], kDrawSmem);
+    if (err == cudaSuccess && a.defer) err = launch_draw(draw_kernel<DT_F32>, a, dgrid, s);
   } else if (dtype == SPEC_BF16) {
     err = prepare(sample_kernel<DT_BF16, false>, g_ready[0]);
     if (err == cudaSuccess) sample_kernel<DT_BF16, false><<<grid, kThreads, smem, s>>>(a);
-    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6]);
-    if (err == cudaSuccess && a.defer) draw_kernel<DT_BF16><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_BF16>, g_ready[6], kDrawSmem);
+    if (err == cudaSuccess && a.defer) err = launch_draw(draw_kernel<DT_BF16>, a, dgrid, s);
   } else {
     err = prepare(sample_kernel<DT_F32, false>, g_ready[1]);
     if (err == cudaSuccess) sample_kernel<DT_F32, false><<<grid, kThreads, smem, s>>>(a);
-    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_F32>, g_ready[7]);
-    if (err == cudaSuccess && a.defer) draw_kernel<DT_F32><<<dgrid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess && a.defer) err = prepare(draw_kernel<DT_F32>, g_ready[7], kDrawSmem);
+    if (err == cudaSuccess && a.defer) err = launch_draw(draw_kernel<DT_F32>, a, dgrid, s);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

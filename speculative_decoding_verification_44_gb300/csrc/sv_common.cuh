@@ -31,7 +31,7 @@ enum { PATH_STREAM = 0, PATH_FULL = 1 };
 
 enum {
   SEQ_OK = 0, SEQ_BAD_LENGTH = 1, SEQ_BAD_TOKEN = 2, SEQ_BAD_UNIFORM = 3,
-  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6, SEQ_BAD_TREE = 7,
+  SEQ_NONFINITE = 4, SEQ_EMPTY_SUPPORT = 5, SEQ_BAD_PARAMS = 6, SEQ_BAD_TREE = 7, SEQ_STALLED = 8,
   SEQ_FLAG_ZERO_Q = 0x100, SEQ_FLAG_Z_ZERO = 0x200, SEQ_FLAG_EOS = 0x400
 };
 
@@ -313,6 +313,44 @@ __device__ __forceinline__ uint32_t vec_max_okey(const uint4& r) {
 // have completed and their memory is visible (returns at once without such a
 // dependency); allow the grids that depend on this one to be scheduled.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------- bulk copies
+// One-dimensional global -> shared bulk copies (the copy engine, no tensor
+// map) that complete on an mbarrier: one thread arms the barrier with the
+// bytes to expect and issues the copies; every consumer waits on the phase.
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// bytes: a multiple of 16; both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// Orders this thread's earlier generic accesses to shared memory before later
+// bulk copies into it (reuse of a buffer that threads have read).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the barrier phase of the given parity; false if it has not
+// completed within about a second (the caller reports SEQ_STALLED).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+    if (global_ns() - t0 > 1000000000ull) return false;
+  }
+}
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // cp.async of 16 bytes to a shared-window address; 16-byte shared load.
 __device__ __forceinline__ void cp_async16_to(uint32_t saddr, const void* gmem) {

@@ -42,6 +42,7 @@ struct RowParams {
   float top_p;      // 1 = off
   int path;         // PATH_STREAM or PATH_FULL
   int fixed_shift;  // fixed-point scale 2^fixed_shift for probability masses
+  int lazy;         // PATH_FULL top-p: leave open which ties of the cut value come first (RowStat::n_list)
 };
 
 // Per-row result, mirrored into the workspace for the sequence epilogue.
@@ -51,7 +52,10 @@ struct __align__(16) RowStat {
   float m;         // row maximum
   float p_tok;     // probability of the draft token this row scores (0 if none)
   int32_t status;  // SEQ_OK, SEQ_NONFINITE or SEQ_EMPTY_SUPPORT
-  int32_t n_list;  // PATH_STREAM: kept-list length
+  int32_t n_list;  // PATH_STREAM: kept-list length.  PATH_FULL: 0, or n > 0 when the row left
+                   // open which of its elements equal to the cut value come first: cut then
+                   // counts every such tie as kept, and only the first n of them in index
+                   // order are (the full-row draw resolves them by rank)
   int32_t path;
   int32_t argmax;  // greedy rows: argmax token
   float cT;        // the row's log2(e) / T (its sampling rule, for the draw)
@@ -548,6 +552,40 @@ __device__ __noinline__ int range_find_nth(const Row row, uint32_t K, int v0, in
 template <int DT>
 __device__ __forceinline__ int find_nth_with_key(const Row row, uint32_t K, uint32_t n, Smem& sm) {
   return range_find_nth<DT>(row, K, 0, row.nvec, n, sm);
+}
+
+// Elements with key K among indices [0, x), block-wide (the same in every thread).
+template <int DT>
+__device__ __noinline__ uint32_t count_key_before(const Row row, uint32_t K, int x, Smem& sm) {
+  constexpr int P = Elem<DT>::kPer;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const KeyBits<DT> kb(K);
+  const int vfull = x / P;                    // vectors wholly before x
+  uint32_t my = 0;
+  for (int s = 0; s < vfull; s += kThreads * kUnroll) {
+    uint4 q[kUnroll];
+    int c[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = s + u * kThreads + tid;
+      c[u] = v < vfull ? load_vec<DT, false>(row, v, q[u]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) my += __popc(kb.mask(q[u], c[u]));
+  }
+  if (tid == 0 && x % P) {
+    uint4 q;
+    const int c = load_vec<DT, false>(row, vfull, q);
+    my += __popc(kb.mask(q, min(c, x % P)));
+  }
+  my = __reduce_add_sync(kFull, my);
+  if (lane == 0) sm.u.f.wcnt[warp] = my;
+  __syncthreads();
+  uint32_t tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) tot += sm.u.f.wcnt[w];
+  __syncthreads();
+  return tot;
 }
 
 // One radix round over a re-read of the row.  Elements taking part: composite
@@ -1227,7 +1265,7 @@ __device__ __noinline__ int kc_pass(const Row row, Smem& sm, FullExtra& fx, floa
 // The cut from the value counts; false when the crossing bin holds more
 // values than the list (the caller then brackets).
 __device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float scale, float top_p, Smem& sm,
-                                        FullExtra& fx, uint64_t& cut, double& W) {
+                                        FullExtra& fx, bool lazy, uint64_t& cut, double& W, int& ties) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const KeyCount& T = fx.u.kc;
   auto count_of = [&](int s) {
@@ -1343,6 +1381,8 @@ __device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float 
       sm.b_i32[1] = static_cast<int>(fkey(bf16_key_value(static_cast<uint32_t>(e >> 48))));
       sm.b_i32[2] = Q;
       sm.b_i32[3] = static_cast<int>(r);
+      sm.b_i32[8] = static_cast<int>(need);
+      sm.b_i32[9] = static_cast<int>(c);
     }
   }
   __syncthreads();
@@ -1350,12 +1390,21 @@ __device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float 
   const unsigned long long Wf = sm.b_u64[2];
   const int Ls = seg_len(row), Q = sm.b_i32[2];
   const uint32_t r = static_cast<uint32_t>(sm.b_i32[3]);
+  const int need = sm.b_i32[8], nK = sm.b_i32[9];
   __syncthreads();
+  W = static_cast<double>(Wf) / static_cast<double>(scale);
+  if (lazy || need == nK) {
+    // every tie of the cut value counted as kept; a lazy row keeps only the
+    // first `need` of them in index order and leaves finding them to the draw
+    cut = composite(K32, 0xffffffffu);
+    ties = need == nK ? 0 : need;
+    return true;
+  }
+  ties = 0;
   const int v0 = min(row.nvec, 2 * Q * Ls), v1 = min(row.nvec, v0 + 2 * Ls);
   const int idx = range_find_nth<DT_BF16>(row, K32, v0, v1, r, sm);
   if (idx < 0) return false;
   cut = composite(K32, static_cast<uint32_t>(idx));
-  W = static_cast<double>(Wf) / static_cast<double>(scale);
   return true;
 }
 
@@ -1403,7 +1452,8 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm, 
     if (P.top_p < 1.0f) {
       // key counts, else bracketing, else the radix rounds (which need no extra memory)
       bool done = false;
-      if (keycount && !kc_overflow) done = kc_resolve(row, m, P.cT, scale, P.top_p, sm, fx, st.cut, st.W);
+      if (keycount && !kc_overflow)
+        done = kc_resolve(row, m, P.cT, scale, P.top_p, sm, fx, P.lazy != 0, st.cut, st.W, st.n_list);
       if (!done && extra) done = topp_bracketed<DT>(row, m, P.cT, ck, P.top_p, sm, fx, st.cut, st.W);
       if (!done) {
         unsigned long long Wf = 0;
@@ -1415,11 +1465,19 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm, 
       st.W = full_sum_kept<DT>(row, m, P.cT, ck, sm);
     }
   }
+  // a lazy cut: the draft token, if it equals the cut value, is kept iff fewer
+  // than n_list ties come before it (same decision in every thread)
+  bool tie_kept = true;
+  if (st.status == SEQ_OK && dtok >= 0 && st.n_list > 0) {
+    const uint32_t K = static_cast<uint32_t>(st.cut >> 32);
+    if (fkey(load_elem<DT>(row.base, dtok)) == K)
+      tie_kept = count_key_before<DT>(row, K, dtok, sm) < static_cast<uint32_t>(st.n_list);
+  }
   if (tid == 0) {                    // one thread forms the float64 quotients
     st.invW = st.status == SEQ_OK ? static_cast<float>(1.0 / st.W) : 0.0f;
     if (st.status == SEQ_OK && dtok >= 0) {
       const float z = load_elem<DT>(row.base, dtok);
-      if (composite(fkey(z), static_cast<uint32_t>(dtok)) >= st.cut)
+      if (tie_kept && composite(fkey(z), static_cast<uint32_t>(dtok)) >= st.cut)
         st.p_tok = static_cast<float>(static_cast<double>(fast_exp2((z - m) * P.cT)) / st.W);
     }
     sm.st = st;
