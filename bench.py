@@ -737,6 +737,31 @@ def main():
             ev_pair = g_ev if g_ev is not None else r_ev
             rep_ms.append(ev_pair[0].elapsed_time(ev_pair[1]) / K)
     rep_ms.sort()
+    # one call alone: a graph of a single call per rotation set (events inside it),
+    # replayed with a synchronize between replays -- the latency of one verify with no
+    # neighbouring call to overlap (back-to-back calls overlap: a call streams its rows
+    # before it waits for the previous call in the stream)
+    single_ms = None
+    if graph is not None and g_ev is not None:
+        g1 = []
+        for r in range(ROTATE):
+            ev1 = (torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True))
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=gstream):
+                ev1[0].record(gstream)
+                gcalls[r]()
+                ev1[1].record(gstream)
+            g1.append((gr, ev1))
+        torch.cuda.synchronize()
+        single = []
+        for t in range(4 * ROTATE + 32):
+            gr, ev1 = g1[t % ROTATE]
+            gr.replay()
+            torch.cuda.synchronize()
+            if t >= 2 * ROTATE:
+                single.append(ev1[0].elapsed_time(ev1[1]))
+        single_ms = max_over_ranks(statistics.median(single), world, dev)
 
     def pct(v, q):
         return v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]
@@ -789,6 +814,11 @@ def main():
                 "launch_ms_avg_timed_region": avg_launch_s * 1e3,
                 "launch_ms_median_eager": statistics.median(launch_ms),
                 "frac_of_nominal_8TBps": achieved / 8000.0}
+    if single_ms is not None:
+        roofline["single_call"] = {"ms_median": single_ms,
+                                   "frac": alg_bytes / (single_ms / 1e3) / 1e9 / peak,
+                                   "how": "one call alone: a one-call graph per rotation set, events inside it, "
+                                          "a synchronize between replays"}
 
     # end to end through the public API with host buffers (pinned), rank-local
     e2e = None
@@ -858,7 +888,9 @@ def main():
                        "launch": ("K steps as one CUDA graph replay, timed by event-record nodes inside the graph"
                                   if g_ev is not None else
                                   "K steps as one CUDA graph replay" if graph is not None else "K eager launches")
-                                 + "; roofline from the timed region's average time per launch"},
+                                 + "; consecutive calls overlap where the library allows it (a kept-list call "
+                                   "streams its rows before it waits for the previous call); roofline from the "
+                                   "timed region's average time per call, single_call from one call alone"},
             "ms_per_step_with_graph_launch": outer_ms / K,
             "spread": spread,
             "sequences_per_s": B * world / (ms_per_step / 1e3),

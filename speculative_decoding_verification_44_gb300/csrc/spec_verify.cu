@@ -1127,11 +1127,16 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  // launched as a programmatic dependent: the previous grid in the stream must
-  // be complete, its writes visible, before this one touches any memory; the
-  // next call's CTAs may then be placed as this grid's CTAs retire, so its
-  // launch overlaps this call's tail
-  grid_dependency_wait();
+  // Launched as a programmatic dependent: the previous grid in the stream
+  // must be complete, its writes visible, before this one reads anything that
+  // grid may have written or writes anything itself.  Without per-sequence
+  // lengths or one-hot flags every row is used, so which row a CTA takes needs
+  // no memory: it streams its logits (which no kernel of this library writes)
+  // first and waits only before reading the draft tokens, so back-to-back
+  // calls overlap one call's tail with the next call's stream.  The next
+  // call's CTAs may be placed as soon as this grid's CTAs retire.
+  const bool stream_first = a.gammas == nullptr && a.onehot == nullptr;
+  if (!stream_first) grid_dependency_wait();
   grid_launch_dependents();
   const int tid = threadIdx.x;
   const int slots = 2 * a.G + 1;
@@ -1147,24 +1152,36 @@ __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleAr
   const int i = is_draft ? slot - a.G - 1 : slot;
   if (!is_draft && i > gb) return;
   if (is_draft && (onehot || i >= gb)) return;
-  {
-    // the sequence's draft tokens and uniforms, for the epilogue: copied while
-    // the row streams, waited for only before this CTA counts its row in
-    const size_t tb = static_cast<size_t>(b) * a.G;
+  // the sequence's draft tokens and uniforms, for the epilogue: copied while
+  // the row streams (or finishes), waited for only before this CTA counts its row in
+  const int32_t* tok = a.tokens + static_cast<size_t>(b) * a.G;
+  const float* uacc = a.u_acc + static_cast<size_t>(b) * a.G;
+  const float* usamp = a.u_samp + b;
+  Smem* smp = &sm;
+  auto copy_seq = [=] {
     if (tid < gb) {
-      cp_async4(&sm.seq_tok[tid], a.tokens + tb + tid);
-      cp_async4(&sm.seq_u[tid], a.u_acc + tb + tid);
+      cp_async4(&smp->seq_tok[tid], tok + tid);
+      cp_async4(&smp->seq_u[tid], uacc + tid);
     }
-    if (tid == kThreads - 1) cp_async4(&sm.seq_us, a.u_samp + b);
+    if (tid == kThreads - 1) cp_async4(&smp->seq_us, usamp);
     cp_async_commit();
-  }
+  };
+  if (!stream_first) copy_seq();
   const Row row = seq_row<DT>(a, b, i, is_draft);
-  int dtok = -1;
-  if (i < gb) {
-    const int t = a.tokens[static_cast<size_t>(b) * a.G + i];
-    dtok = (t >= 0 && t < a.V) ? t : -1;
-  }
-  lean_stream_row<DT>(row, is_draft ? a.dp : a.tp, dtok, sm);
+  const int V = a.V;
+  auto dtok_of = [=] {
+    if (stream_first) {
+      grid_dependency_wait();
+      copy_seq();
+    }
+    int dtok = -1;
+    if (i < gb) {
+      const int t = tok[i];
+      dtok = (t >= 0 && t < V) ? t : -1;
+    }
+    return dtok;
+  };
+  lean_stream_row<DT>(row, is_draft ? a.dp : a.tp, dtok_of, sm);
 
   publish_block(a.fast + (static_cast<size_t>(b) * slots + slot) * a.wpr, sm);
   cp_async_wait<0>();
@@ -1483,7 +1500,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
     const Row row = make_row<DT>((is_draft ? a.dft : a.tgt) + (static_cast<size_t>(b) * a.N + v) * a.row_bytes,
                                  a.V, a.aligned != 0);
     const RowParams P = is_draft ? a.dp : a.tp;
-    if (row.aligned) lean_stream_row<DT>(row, P, -1, sm);
+    if (row.aligned) lean_stream_row<DT>(row, P, [] { return -1; }, sm);
     else stream_row<DT>(row, P, -1, sm);
     publish_block(dst, sm);
   } else if (tid == 0) {
@@ -1611,29 +1628,45 @@ __device__ __forceinline__ int tie_status(int n, uint32_t idx, uint32_t before, 
 
 // Weights of chunk k with every tie decided: by rank for a lazy cut (bt / bd
 // ties before the chunk, then in index order), by index for an exact one.
-// The chunk is taken in two halves; in each, thread t takes two consecutive
-// vectors, so thread order is index order.  Returns the chunk's sum (every
-// thread); with find, also the first token where the running sum exceeds tl
-// (else the last token with weight) in *tok.  Block-wide; c lives in shared
-// memory.
+// Thread t takes the chunk's vectors 4t..4t+3 (one round trip), so thread
+// order is index order.  Returns the chunk's sum (every thread); with find,
+// also the first token where the running sum exceeds tl (else the last token
+// with weight) in *tok.  Block-wide; c lives in shared memory.
 template <int DT, int MODE>
 __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int k, int bt, int bd, bool find,
                                            double tl, int* tok, Smem& sm) {
   constexpr int P = Elem<DT>::kPer;
-  constexpr int kVPT = 2;
-  static_assert(2 * kVPT * kThreads == kChunkVecs, "two halves of two vectors per thread make a chunk");
+  constexpr int kVPT = 4;
+  static_assert(kVPT * kThreads == kChunkVecs, "a thread takes four consecutive vectors of a chunk");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nv = c.trow.nvec;
-  if (tid == 0) { sm.b_i32[5] = -1; sm.b_i32[6] = -1; sm.b_i32[7] = -1; }
-  double run = 0.0;            // weight of the halves before
-  uint32_t rbt = static_cast<uint32_t>(bt), rbd = static_cast<uint32_t>(bd);
-  for (int half = 0; half < 2; ++half) {
-    const int v0 = k * chunk_vecs + half * kVPT * kThreads + tid * kVPT;
-    uint4 rt[kVPT], rd[kVPT];
-    int n[kVPT];
+  const int v0 = k * chunk_vecs + tid * kVPT;
+  uint4 rt[kVPT], rd[kVPT];
+  int n[kVPT];
 #pragma unroll
-    for (int i = 0; i < kVPT; ++i) n[i] = (v0 + i < nv) ? draw_load<DT, MODE>(c, v0 + i, rt[i], rd[i]) : 0;
-    uint32_t ct = 0, cd = 0;
+  for (int i = 0; i < kVPT; ++i) n[i] = (v0 + i < nv) ? draw_load<DT, MODE>(c, v0 + i, rt[i], rd[i]) : 0;
+  // ties of each cut in this thread's elements, then their exclusive prefix over the block
+  uint32_t ct = 0, cd = 0;
+#pragma unroll
+  for (int i = 0; i < kVPT; ++i) {
+    float zt[P], zd[P];
+    unpack<DT>(rt[i], zt);
+    unpack<DT>(rd[i], zd);
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+      ct += (e < n[i] && zt[e] == c.tt) ? 1u : 0u;
+      cd += (MODE == 1 && e < n[i] && zd[e] == c.td) ? 1u : 0u;
+    }
+  }
+  const uint32_t it_ = warp_incl_scan_u32(ct, lane), id_ = warp_incl_scan_u32(cd, lane);
+  if (lane == 31) { sm.nw[warp] = static_cast<int>(it_); sm.red_i[warp] = static_cast<int>(id_); }
+  if (tid == 0) { sm.b_i32[5] = -1; sm.b_i32[6] = -1; sm.b_i32[7] = -1; }
+  __syncthreads();
+  uint32_t rt0 = static_cast<uint32_t>(bt) + it_ - ct, rd0 = static_cast<uint32_t>(bd) + id_ - cd;
+  for (int w = 0; w < warp; ++w) { rt0 += static_cast<uint32_t>(sm.nw[w]); rd0 += static_cast<uint32_t>(sm.red_i[w]); }
+  // the weights, in index order, every tie decided
+  auto walk = [&](auto&& visit) {
+    uint32_t rt_ = rt0, rd_ = rd0;
 #pragma unroll
     for (int i = 0; i < kVPT; ++i) {
       float zt[P], zd[P];
@@ -1641,75 +1674,50 @@ __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int
       unpack<DT>(rd[i], zd);
 #pragma unroll
       for (int e = 0; e < P; ++e) {
-        ct += (e < n[i] && zt[e] == c.tt) ? 1u : 0u;
-        cd += (MODE == 1 && e < n[i] && zd[e] == c.td) ? 1u : 0u;
+        if (e >= n[i]) continue;
+        const uint32_t x = static_cast<uint32_t>((v0 + i) * P + e);
+        float p = kept_w(zt[e], c.kt, c.cTt, c.bt);
+        if (zt[e] == c.tt && !(c.nt > 0 ? rt_++ < static_cast<uint32_t>(c.nt) : x <= c.it)) p = 0.0f;
+        float q = draw_qk<MODE>(c, zd[e], x, sm);
+        if (MODE == 1 && zd[e] == c.td && !(c.nd > 0 ? rd_++ < static_cast<uint32_t>(c.nd) : x <= c.id)) q = 0.0f;
+        visit(static_cast<int>(x), draw_w<MODE>(p, q, c.beta));
       }
     }
-    const uint32_t it_ = warp_incl_scan_u32(ct, lane), id_ = warp_incl_scan_u32(cd, lane);
-    if (lane == 31) { sm.nw[warp] = static_cast<int>(it_); sm.red_i[warp] = static_cast<int>(id_); }
-    __syncthreads();
-    uint32_t rt0 = rbt + it_ - ct, rd0 = rbd + id_ - cd;
-    for (int w = 0; w < kWarps; ++w) {
-      if (w < warp) { rt0 += static_cast<uint32_t>(sm.nw[w]); rd0 += static_cast<uint32_t>(sm.red_i[w]); }
-      rbt += static_cast<uint32_t>(sm.nw[w]);
-      rbd += static_cast<uint32_t>(sm.red_i[w]);
-    }
-    auto walk = [&](auto&& visit) {
-      uint32_t rt_ = rt0, rd_ = rd0;
-#pragma unroll
-      for (int i = 0; i < kVPT; ++i) {
-        float zt[P], zd[P];
-        unpack<DT>(rt[i], zt);
-        unpack<DT>(rd[i], zd);
-#pragma unroll
-        for (int e = 0; e < P; ++e) {
-          if (e >= n[i]) continue;
-          const uint32_t x = static_cast<uint32_t>((v0 + i) * P + e);
-          float p = kept_w(zt[e], c.kt, c.cTt, c.bt);
-          if (zt[e] == c.tt && !(c.nt > 0 ? rt_++ < static_cast<uint32_t>(c.nt) : x <= c.it)) p = 0.0f;
-          float q = draw_qk<MODE>(c, zd[e], x, sm);
-          if (MODE == 1 && zd[e] == c.td && !(c.nd > 0 ? rd_++ < static_cast<uint32_t>(c.nd) : x <= c.id)) q = 0.0f;
-          visit(static_cast<int>(x), draw_w<MODE>(p, q, c.beta));
-        }
-      }
-    };
-    float ts = 0.0f;
-    int last = -1;
-    walk([&](int x, float w) { ts += w; if (w > 0.0f) last = x; });
-    const df incl = warp_incl_scan_df(df_from(ts), lane);
-    if (lane == 31) { sm.red_f[warp] = incl.hi; sm.red_lo[warp] = incl.lo; }
-    __syncthreads();
-    df base = df_add(incl, df_from(-ts)), tot = df_from(0.0f);
-    for (int w = 0; w < kWarps; ++w) {
-      const df x = {sm.red_f[w], sm.red_lo[w]};
-      if (w < warp) base = df_add(base, x);
-      tot = df_add(tot, x);
-    }
-    const double b0 = run + df_to_double(base);
-    if (find && sm.b_i32[5] == -1) {         // not found in an earlier half (same in every thread)
-      __syncthreads();
-      if (ts > 0.0f && b0 + static_cast<double>(ts) > tl)
-        atomicMin(reinterpret_cast<unsigned*>(&sm.b_i32[5]), static_cast<unsigned>(tid));
-      if (last >= 0) atomicMax(&sm.b_i32[6], last);
-      __syncthreads();
-      if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
-        float c32 = 0.0f;
-        int found = -1;
-        walk([&](int x, float w) {
-          if (w > 0.0f) {
-            c32 += w;
-            if (found < 0 && b0 + static_cast<double>(c32) > tl) found = x;
-          }
-        });
-        sm.b_i32[7] = found >= 0 ? found : last;
-      }
-    }
-    run += df_to_double(tot);
-    __syncthreads();
-  }
-  if (find) *tok = sm.b_i32[5] == -1 ? sm.b_i32[6] : sm.b_i32[7];   // rounding: the last weighted token
+  };
+  float ts = 0.0f;
+  int last = -1;
+  walk([&](int x, float w) { ts += w; if (w > 0.0f) last = x; });
+  const df incl = warp_incl_scan_df(df_from(ts), lane);
+  if (lane == 31) { sm.red_f[warp] = incl.hi; sm.red_lo[warp] = incl.lo; }
   __syncthreads();
-  return run;
+  df base = df_add(incl, df_from(-ts)), tot = df_from(0.0f);
+  for (int w = 0; w < kWarps; ++w) {
+    const df x = {sm.red_f[w], sm.red_lo[w]};
+    if (w < warp) base = df_add(base, x);
+    tot = df_add(tot, x);
+  }
+  if (find) {
+    const double b0 = df_to_double(base);
+    if (ts > 0.0f && b0 + static_cast<double>(ts) > tl)
+      atomicMin(reinterpret_cast<unsigned*>(&sm.b_i32[5]), static_cast<unsigned>(tid));
+    if (last >= 0) atomicMax(&sm.b_i32[6], last);
+    __syncthreads();
+    if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
+      float c32 = 0.0f;
+      int found = -1;
+      walk([&](int x, float w) {
+        if (w > 0.0f) {
+          c32 += w;
+          if (found < 0 && b0 + static_cast<double>(c32) > tl) found = x;
+        }
+      });
+      sm.b_i32[7] = found >= 0 ? found : last;
+    }
+    __syncthreads();
+    *tok = sm.b_i32[5] == -1 ? sm.b_i32[6] : sm.b_i32[7];   // rounding: the last weighted token
+  }
+  __syncthreads();
+  return df_to_double(tot);
 }
 
 template <int DT, int MODE>

@@ -1869,9 +1869,11 @@ __device__ void stream_row(const Row row, const RowParams& P, int dtok, Smem& sm
 // the thread may hold more qualifying vectors than it tracked, and the block
 // re-reads all of them.  (Keeping the three best vectors in registers instead
 // of re-reading them measured slower: the register moves ride on the
-// insertion that nearly every warp-iteration takes.)
-template <int DT>
-__device__ void lean_stream_row(const Row row, const RowParams& P, int dtok, Smem& sm) {
+// insertion that nearly every warp-iteration takes.)  The draft token whose
+// probability the row reports comes from dtok_of(), called by every thread
+// once the stream is done (the caller may wait for a previous grid there).
+template <int DT, class DtokOf>
+__device__ void lean_stream_row(const Row row, const RowParams& P, DtokOf dtok_of, Smem& sm) {
   static_assert(kRing == 4, "the loop below is unrolled for four slots");
   constexpr uint32_t kSlot = kThreads * 16;                 // bytes per ring slot
   constexpr size_t kStride = static_cast<size_t>(kThreads) * 16;
@@ -1963,7 +1965,7 @@ __device__ void lean_stream_row(const Row row, const RowParams& P, int dtok, Sme
     }
     __syncthreads();
   }
-  stream_finish<DT>(row, P, dtok, any_bad, 0.0f, sm);
+  stream_finish<DT>(row, P, dtok_of(), any_bad, 0.0f, sm);
 }
 
 // Probability of token x under a PATH_FULL row given its logit z.
