@@ -1470,12 +1470,16 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTreeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  grid_dependency_wait();
-  grid_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31;
   const int slots = 2 * a.N;
   const int b = blockIdx.x / slots;
   const int slot = blockIdx.x - b * slots;
+  // without per-sequence node counts every target row is used and streams
+  // before this CTA waits for the previous grid (as in sample_list_kernel);
+  // a draft row needs the parents first, to know whether it is read
+  const bool stream_first = a.nodes == nullptr && slot < a.N && a.aligned != 0;
+  if (!stream_first) grid_dependency_wait();
+  grid_launch_dependents();
   const int n = a.nodes ? a.nodes[b] : a.N;
   if (n < 1 || n > a.N) {
     if (slot == 0 && tid < 32) tree_sample_fail(a, b, SEQ_BAD_LENGTH, lane);
@@ -1500,8 +1504,14 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
     const Row row = make_row<DT>((is_draft ? a.dft : a.tgt) + (static_cast<size_t>(b) * a.N + v) * a.row_bytes,
                                  a.V, a.aligned != 0);
     const RowParams P = is_draft ? a.dp : a.tp;
-    if (row.aligned) lean_stream_row<DT>(row, P, [] { return -1; }, sm);
-    else stream_row<DT>(row, P, -1, sm);
+    if (row.aligned) {
+      lean_stream_row<DT>(row, P, [stream_first] {
+        if (stream_first) grid_dependency_wait();
+        return -1;
+      }, sm);
+    } else {
+      stream_row<DT>(row, P, -1, sm);
+    }
     publish_block(dst, sm);
   } else if (tid == 0) {
     ListRec rec;
@@ -2136,6 +2146,13 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) greedy_kernel(const GreedyArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  // a programmatic dependent of the previous call: without per-sequence
+  // lengths every row is used, and a row CTA takes its argmax before it waits
+  // for the previous grid (then reads tokens and writes), so back-to-back
+  // calls overlap
+  const bool stream_first = a.gammas == nullptr;
+  if (!stream_first) grid_dependency_wait();
+  grid_launch_dependents();
   const int slots = a.G + 1;
   const int b = blockIdx.x / slots;
   const int i = blockIdx.x - b * slots;
@@ -2155,6 +2172,7 @@ __global__ void __launch_bounds__(kThreads, 5) greedy_kernel(const GreedyArgs a)
   const Row row = make_row<DT>(a.tgt + (static_cast<size_t>(b) * slots + i) * a.row_bytes, a.V, a.aligned != 0);
   int g, st;
   greedy_row<DT>(row, sm, g, st);
+  if (stream_first) grid_dependency_wait();
   if (threadIdx.x == 0) a.rows[static_cast<size_t>(b) * slots + i] = make_int2(g, st);
   __threadfence();
   __syncthreads();
@@ -2235,6 +2253,11 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) greedy_tree_kernel(const TreeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  // as greedy_kernel: without per-sequence node counts every node row is used
+  // and a CTA takes its argmax before waiting for the previous grid
+  const bool stream_first = a.nodes == nullptr;
+  if (!stream_first) grid_dependency_wait();
+  grid_launch_dependents();
   const int b = blockIdx.x / a.N;
   const int i = blockIdx.x - b * a.N;
   const int n = a.nodes ? a.nodes[b] : a.N;
@@ -2247,6 +2270,7 @@ __global__ void __launch_bounds__(kThreads, 5) greedy_tree_kernel(const TreeArgs
   const Row row = make_row<DT>(a.tgt + (static_cast<size_t>(b) * a.N + i) * a.row_bytes, a.V, a.aligned != 0);
   int g, st;
   greedy_row<DT>(row, sm, g, st);
+  if (stream_first) grid_dependency_wait();
   if (threadIdx.x == 0) a.rows[static_cast<size_t>(b) * a.N + i] = make_int2(g, st);
   __threadfence();
   __syncthreads();
@@ -2558,6 +2582,24 @@ int draw_run(int B, int nchunk) {
   int splits = std::max(1, std::min(nchunk, (target + B - 1) / B));
   splits = std::max(splits, (nchunk + kDrawMaxRun - 1) / kDrawMaxRun);
   return (nchunk + splits - 1) / splits;
+}
+
+// A launch as a programmatic dependent of the previous kernel in the stream
+// (the kernel waits for that grid itself before it reads anything the grid
+// may have written).
+template <typename K, typename Arg>
+cudaError_t launch_pdl(K kernel, dim3 grid, size_t smem, cudaStream_t s, const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
 }
 
 // The full-row draw, as a programmatic dependent of the row kernel (it waits
@@ -2887,10 +2929,10 @@ spec_status_t spec_verify_greedy_tree(const void* target_logits, spec_dtype_t dt
   cudaError_t err;
   if (dtype == SPEC_BF16) {
     err = prepare(greedy_tree_kernel<DT_BF16>, g_ready[12]);
-    if (err == cudaSuccess) greedy_tree_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess) err = launch_pdl(greedy_tree_kernel<DT_BF16>, dim3(grid), sizeof(Smem), s, a);
   } else {
     err = prepare(greedy_tree_kernel<DT_F32>, g_ready[13]);
-    if (err == cudaSuccess) greedy_tree_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess) err = launch_pdl(greedy_tree_kernel<DT_F32>, dim3(grid), sizeof(Smem), s, a);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
@@ -3039,10 +3081,10 @@ spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
   cudaError_t err;
   if (dtype == SPEC_BF16) {
     err = prepare(greedy_kernel<DT_BF16>, g_ready[2]);
-    if (err == cudaSuccess) greedy_kernel<DT_BF16><<<grid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess) err = launch_pdl(greedy_kernel<DT_BF16>, dim3(grid), sizeof(Smem), s, a);
   } else {
     err = prepare(greedy_kernel<DT_F32>, g_ready[3]);
-    if (err == cudaSuccess) greedy_kernel<DT_F32><<<grid, kThreads, sizeof(Smem), s>>>(a);
+    if (err == cudaSuccess) err = launch_pdl(greedy_kernel<DT_F32>, dim3(grid), sizeof(Smem), s, a);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
