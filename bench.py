@@ -367,7 +367,7 @@ def run_reference(args, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / max(1, n), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workloads.NAMES[wid], "B": w.B, "gamma": w.G, "V": w.V,
+        "config": {"early_logits_reads": True, "workload": workloads.NAMES[wid], "B": w.B, "gamma": w.G, "V": w.V,
                    "dtype": "bf16" if w.dtype.itemsize == 2 else "f32", **params_of(w),
                    "step": "one sequence (gamma_b + 1 verified positions) per step"},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
@@ -453,7 +453,7 @@ def run_greedy(args, rank, world, dev, sv, workloads):
             "value": whole_job_rate(rt, world, ms_per_step), "unit": "positions/s", "n_gpus": world,
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w0.name, "B": B, "gamma": G, "V": V, "early_exit": bool(args.early_exit), "tree": bool(args.tree),
+            "config": {"early_logits_reads": True, "workload": w0.name, "B": B, "gamma": G, "V": V, "early_exit": bool(args.early_exit), "tree": bool(args.tree),
                        "l2": f"inputs rotate over {ROTATE} independent sets of {rt * row_bytes / 1e6:.1f} MB"},
             "rows_read_per_step": statistics.mean(read), "rows_needed_per_step": statistics.mean(needed),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -573,7 +573,7 @@ def run_sample_tree(args, rank, world, dev, sv, workloads, wid):
             "value": whole_job_rate(B * N, world, ms_per_step), "unit": "tree nodes/s", "n_gpus": world,
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dname, "data": "synthetic",
-            "config": {"workload": w0.name, "B": B, "nodes": N, "V": V, **params_of(w0), "tree": True,
+            "config": {"early_logits_reads": True, "workload": w0.name, "B": B, "nodes": N, "V": V, **params_of(w0), "tree": True,
                        "l2": f"inputs rotate over {ROTATE} independent sets",
                        "launch": ("K eager launches" if graph is None else
                                   "K steps as one CUDA graph replay" + (", timed by event-record nodes inside the graph"
@@ -614,6 +614,11 @@ def main():
         dist.barrier()
     import speculative_decoding_verification_44_gb300 as sv
     from speculative_decoding_verification_44_gb300 import workloads
+
+    # every call here reads logits that were written before the timed region (or
+    # copied in by the e2e leg), so the verifiers may stream them before waiting
+    # for the previous call: back-to-back calls overlap
+    sv.set_early_logits_reads(True)
 
     # independent batches: replica = rank * ROTATE + r
     wid = workload_id(args.workload)
@@ -880,7 +885,7 @@ def main():
             "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dname, "data": "synthetic",
-            "config": {"workload": workloads.NAMES[wid], "B": B, "gamma": G, "V": V,
+            "config": {"early_logits_reads": True, "workload": workloads.NAMES[wid], "B": B, "gamma": G, "V": V,
                        **params_of(w0), "batches_per_gpu": 1, "early_exit": bool(args.early_exit),
                        "l2": f"inputs rotate over {ROTATE} independent sets of {logits_bytes / 1e6:.1f} MB "
                              f"(each larger than the {L2_BYTES / 2**20:.0f} MiB L2)",
@@ -888,9 +893,10 @@ def main():
                        "launch": ("K steps as one CUDA graph replay, timed by event-record nodes inside the graph"
                                   if g_ev is not None else
                                   "K steps as one CUDA graph replay" if graph is not None else "K eager launches")
-                                 + "; consecutive calls overlap where the library allows it (a kept-list call "
-                                   "streams its rows before it waits for the previous call); roofline from the "
-                                   "timed region's average time per call, single_call from one call alone"},
+                                 + "; early logits reads on (spec_set_early_logits_reads): a kept-list call "
+                                   "streams its rows before it waits for the previous call, so consecutive calls "
+                                   "overlap; roofline from the timed region's average time per call, single_call "
+                                   "from one call alone"},
             "ms_per_step_with_graph_launch": outer_ms / K,
             "spread": spread,
             "sequences_per_s": B * world / (ms_per_step / 1e3),

@@ -40,7 +40,8 @@ EXPORTED = ("spec_verify_workspace_size", "spec_verify_sample", "spec_greedy_wor
             "spec_verify_greedy", "spec_transform_probs", "spec_status_string",
             "spec_verify_sample_noalloc", "spec_verify_greedy_early", "spec_verify_sample_lenient",
             "spec_verify_workspace_size_ex", "spec_verify_sample_ex", "spec_tree_workspace_size",
-            "spec_verify_greedy_tree", "spec_tree_sample_workspace_size", "spec_verify_sample_tree")
+            "spec_verify_greedy_tree", "spec_tree_sample_workspace_size", "spec_verify_sample_tree",
+            "spec_set_early_logits_reads")
 
 
 class spec_sampling_params_t(ctypes.Structure):
@@ -77,6 +78,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [ctypes.c_int]
+    lib.spec_set_early_logits_reads.restype = ctypes.c_int
+    lib.spec_set_early_logits_reads.argtypes = [i32]
     lib.spec_verify_workspace_size.restype = ctypes.c_int
     lib.spec_verify_workspace_size.argtypes = [i32, i32, i32, P, P, ctypes.POINTER(sz)]
     lib.spec_greedy_workspace_size.restype = ctypes.c_int

@@ -58,6 +58,14 @@ def _stream(stream: torch.cuda.Stream | None) -> int:
     return s.cuda_stream
 
 
+def set_early_logits_reads(enable: bool) -> None:
+    """spec_set_early_logits_reads: let the verifiers stream their logits before they wait
+    for the previous kernel in the stream (back-to-back calls overlap).  The caller guarantees
+    that the kernel preceding a call has finished writing its logits when it lets its
+    dependents launch (any kernel without programmatic dependent launch, or this library)."""
+    _lib.check("spec_set_early_logits_reads", _lib.load().spec_set_early_logits_reads(1 if enable else 0))
+
+
 def workspace_size(batch: int, gamma_max: int, vocab: int, target: SamplingParams,
                    draft: SamplingParams, per_sequence: bool = False, kept_list_only: bool = False) -> int:
     """Workspace bytes; ``per_sequence``: sized for per-sequence rules (spec_verify_workspace_size_ex),

@@ -95,6 +95,7 @@ struct SampleArgs {
   // a ListRec then the row's kept list in token order
   uint4* fast;
   int wpr;
+  int early_logits;     // the caller allows reading logits before the previous grid completes
 };
 
 constexpr int kChunkVecs = 4 * kThreads;   // full-row draw: vectors per chunk (four per thread)
@@ -1129,13 +1130,14 @@ __global__ void __launch_bounds__(kThreads, 5) sample_list_kernel(const SampleAr
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   // Launched as a programmatic dependent: the previous grid in the stream
   // must be complete, its writes visible, before this one reads anything that
-  // grid may have written or writes anything itself.  Without per-sequence
-  // lengths or one-hot flags every row is used, so which row a CTA takes needs
-  // no memory: it streams its logits (which no kernel of this library writes)
-  // first and waits only before reading the draft tokens, so back-to-back
-  // calls overlap one call's tail with the next call's stream.  The next
-  // call's CTAs may be placed as soon as this grid's CTAs retire.
-  const bool stream_first = a.gammas == nullptr && a.onehot == nullptr;
+  // grid may have written or writes anything itself.  When the caller allows
+  // early logits reads (spec_set_early_logits_reads) and there are no
+  // per-sequence lengths or one-hot flags, every row is used, so which row a
+  // CTA takes needs no memory: it streams its logits first and waits only
+  // before reading the draft tokens, so back-to-back calls overlap one call's
+  // tail with the next call's stream.  The next call's CTAs may be placed as
+  // soon as this grid's CTAs retire.
+  const bool stream_first = a.early_logits && a.gammas == nullptr && a.onehot == nullptr;
   if (!stream_first) grid_dependency_wait();
   grid_launch_dependents();
   const int tid = threadIdx.x;
@@ -1240,6 +1242,7 @@ struct SampleTreeArgs {
   float* out_aprob;         // [B][N - 1] or null
   float* out_Z;             // [B] or null
   int32_t* out_status;      // [B] or null
+  int early_logits;         // the caller allows reading logits before the previous grid completes
 };
 
 // Commit nothing [wrblog §15]: the lanes of one warp.
@@ -1474,10 +1477,11 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
   const int slots = 2 * a.N;
   const int b = blockIdx.x / slots;
   const int slot = blockIdx.x - b * slots;
-  // without per-sequence node counts every target row is used and streams
-  // before this CTA waits for the previous grid (as in sample_list_kernel);
-  // a draft row needs the parents first, to know whether it is read
-  const bool stream_first = a.nodes == nullptr && slot < a.N && a.aligned != 0;
+  // with early logits reads allowed and no per-sequence node counts every
+  // target row is used and streams before this CTA waits for the previous grid
+  // (as in sample_list_kernel); a draft row needs the parents first, to know
+  // whether it is read
+  const bool stream_first = a.early_logits && a.nodes == nullptr && slot < a.N && a.aligned != 0;
   if (!stream_first) grid_dependency_wait();
   grid_launch_dependents();
   const int n = a.nodes ? a.nodes[b] : a.N;
@@ -2140,17 +2144,18 @@ struct GreedyArgs {
   int32_t* out_tokens;
   int32_t* out_nacc;
   int32_t* out_status;
+  int early_logits;   // the caller allows reading logits before the previous grid completes
 };
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) greedy_kernel(const GreedyArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  // a programmatic dependent of the previous call: without per-sequence
-  // lengths every row is used, and a row CTA takes its argmax before it waits
-  // for the previous grid (then reads tokens and writes), so back-to-back
-  // calls overlap
-  const bool stream_first = a.gammas == nullptr;
+  // a programmatic dependent of the previous call: with early logits reads
+  // allowed and no per-sequence lengths every row is used, and a row CTA takes
+  // its argmax before it waits for the previous grid (then reads tokens and
+  // writes), so back-to-back calls overlap
+  const bool stream_first = a.early_logits && a.gammas == nullptr;
   if (!stream_first) grid_dependency_wait();
   grid_launch_dependents();
   const int slots = a.G + 1;
@@ -2235,6 +2240,7 @@ struct TreeArgs {
   int32_t* out_nacc;        // [B]
   int32_t* out_path;        // [B][N] or null
   int32_t* out_status;      // [B] or null
+  int early_logits;         // the caller allows reading logits before the previous grid completes
 };
 
 __device__ void tree_fail(const TreeArgs& a, int b, int status, int lane) {
@@ -2253,9 +2259,10 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 5) greedy_tree_kernel(const TreeArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  // as greedy_kernel: without per-sequence node counts every node row is used
-  // and a CTA takes its argmax before waiting for the previous grid
-  const bool stream_first = a.nodes == nullptr;
+  // as greedy_kernel: with early logits reads allowed and no per-sequence node
+  // counts every node row is used and a CTA takes its argmax before waiting
+  // for the previous grid
+  const bool stream_first = a.early_logits && a.nodes == nullptr;
   if (!stream_first) grid_dependency_wait();
   grid_launch_dependents();
   const int b = blockIdx.x / a.N;
@@ -2560,7 +2567,8 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done, size_t smem = sizeof(
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
-std::atomic<uint64_t> g_ready[18];  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list, sample-tree x {bf16, f32}
+std::atomic<uint64_t> g_ready[18];
+std::atomic<int> g_early_logits{0};   // spec_set_early_logits_reads  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list, sample-tree x {bf16, f32}
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count() {
@@ -2630,6 +2638,11 @@ size_t smem_for(const RowParams& a, const RowParams& b) {
 }  // namespace
 
 extern "C" {
+
+spec_status_t spec_set_early_logits_reads(int32_t enable) {
+  g_early_logits.store(enable != 0 ? 1 : 0, std::memory_order_relaxed);
+  return SPEC_OK;
+}
 
 const char* spec_status_string(spec_status_t s) {
   switch (s) {
@@ -2711,6 +2724,7 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
       !aligned_to(workspace, kAlign))
     return SPEC_ERR_MISALIGNED;
   SampleArgs a;
+  a.early_logits = g_early_logits.load(std::memory_order_relaxed);
   a.fast = nullptr;
   a.wpr = 0;
   a.tp = make_row_params(target_params, vocab, dtype);
@@ -2909,6 +2923,7 @@ spec_status_t spec_verify_greedy_tree(const void* target_logits, spec_dtype_t dt
   char* ws = static_cast<char*>(workspace);
   const GreedyLayout L = greedy_layout(batch, max_nodes - 1);
   TreeArgs a;
+  a.early_logits = g_early_logits.load(std::memory_order_relaxed);
   a.tgt = static_cast<const char*>(target_logits);
   a.tokens = tree_tokens;
   a.parents = tree_parents;
@@ -2997,6 +3012,7 @@ spec_status_t spec_verify_sample_tree(const void* target_logits, const void* dra
   if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   SampleTreeArgs a;
+  a.early_logits = g_early_logits.load(std::memory_order_relaxed);
   a.tgt = static_cast<const char*>(target_logits);
   a.dft = static_cast<const char*>(draft_logits);
   a.tokens = tree_tokens;
@@ -3062,6 +3078,7 @@ spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t dtype,
   if (workspace_bytes < need) return SPEC_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   GreedyArgs a;
+  a.early_logits = g_early_logits.load(std::memory_order_relaxed);
   a.tgt = static_cast<const char*>(target_logits);
   a.tokens = draft_tokens;
   a.gammas = gamma_per_seq;
@@ -3111,6 +3128,7 @@ spec_status_t spec_verify_greedy_early(const void* target_logits, spec_dtype_t d
   const GreedyLayout L = greedy_layout(batch, gamma_max);
   char* ws = static_cast<char*>(workspace);
   GreedyArgs a;
+  a.early_logits = g_early_logits.load(std::memory_order_relaxed);
   a.tgt = static_cast<const char*>(target_logits);
   a.tokens = draft_tokens;
   a.gammas = gamma_per_seq;
