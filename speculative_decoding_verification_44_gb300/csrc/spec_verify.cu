@@ -1607,6 +1607,8 @@ struct DrawPart {
 // (stage s, row r at kStageRowBytes (2 s + r)).
 constexpr size_t kDrawStageOff = (sizeof(Smem) + sizeof(DrawPart) + 127) / 128 * 128;
 constexpr size_t kDrawSmem = kDrawStageOff + static_cast<size_t>(kDrawStages) * 2 * kStageRowBytes;
+static_assert(static_cast<size_t>(kDrawStages) * 2 * kStageRowBytes >= 32 * kThreads * sizeof(float),
+              "the idle stages hold 32 weights per thread for the exact chunk scans");
 
 __device__ __forceinline__ float kept_w(float z, float k, float cT, float b) {
   return z >= k ? fast_exp2(fmaf(z, cT, b)) : 0.0f;
@@ -1645,10 +1647,11 @@ __device__ __forceinline__ int tie_status(int n, uint32_t idx, uint32_t before, 
 // Thread t takes the chunk's vectors 4t..4t+3 (one round trip), so thread
 // order is index order.  Returns the chunk's sum (every thread); with find,
 // also the first token where the running sum exceeds tl (else the last token
-// with weight) in *tok.  Block-wide; c lives in shared memory.
+// with weight) in *tok.  Block-wide; c lives in shared memory, and wbuf
+// (shared memory, 32 floats per thread) keeps each element's weight for the find.
 template <int DT, int MODE>
 __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int k, int bt, int bd, bool find,
-                                           double tl, int* tok, Smem& sm) {
+                                           double tl, int* tok, Smem& sm, float* wbuf) {
   constexpr int P = Elem<DT>::kPer;
   constexpr int kVPT = 4;
   static_assert(kVPT * kThreads == kChunkVecs, "a thread takes four consecutive vectors of a chunk");
@@ -1699,8 +1702,12 @@ __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int
     }
   };
   float ts = 0.0f;
-  int last = -1;
-  walk([&](int x, float w) { ts += w; if (w > 0.0f) last = x; });
+  int last = -1, e = 0;
+  walk([&](int x, float w) {
+    ts += w;
+    if (w > 0.0f) last = x;
+    wbuf[(e++) * kThreads + tid] = w;       // element e of this thread (index order)
+  });
   const df incl = warp_incl_scan_df(df_from(ts), lane);
   if (lane == 31) { sm.red_f[warp] = incl.hi; sm.red_lo[warp] = incl.lo; }
   __syncthreads();
@@ -1717,14 +1724,18 @@ __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int
     if (last >= 0) atomicMax(&sm.b_i32[6], last);
     __syncthreads();
     if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
+      // the same weights, from the buffer, in index order
       float c32 = 0.0f;
-      int found = -1;
-      walk([&](int x, float w) {
-        if (w > 0.0f) {
-          c32 += w;
-          if (found < 0 && b0 + static_cast<double>(c32) > tl) found = x;
+      int found = -1, ei = 0;
+      for (int i = 0; i < kVPT && found < 0; ++i) {
+        for (int ee = 0; ee < n[i] && found < 0; ++ee, ++ei) {
+          const float w = wbuf[ei * kThreads + tid];
+          if (w > 0.0f) {
+            c32 += w;
+            if (b0 + static_cast<double>(c32) > tl) found = (v0 + i) * P + ee;
+          }
         }
-      });
+      }
       sm.b_i32[7] = found >= 0 ? found : last;
     }
     __syncthreads();
@@ -1736,12 +1747,13 @@ __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int
 
 template <int DT, int MODE>
 __device__ __noinline__ void draw_pick(const SampleArgs& a, int b, int j, int mode, int flags, bool onehot, Smem& sm,
-                                       DrawPart& dp);
+                                       DrawPart& dp, float* wbuf);
 
 // One draw CTA: its run of chunk sums, then (the sequence's last CTA) the draw.
 template <int DT, int MODE>
 __device__ __noinline__ void draw_body(const SampleArgs& a, int b, const DrawRec rec, const RowStat ts,
-                                       const RowStat ds, bool onehot, Smem& sm, DrawPart& dp, uint32_t stage0) {
+                                       const RowStat ds, bool onehot, Smem& sm, DrawPart& dp, uint32_t stage0,
+                                       float* wbuf) {
   constexpr int P = Elem<DT>::kPer;
   constexpr int kVPT = 4;
   constexpr int kStep = MODE == 1 ? 2 : 4;   // 64 bytes of each thread in flight per step
@@ -1939,7 +1951,9 @@ __device__ __noinline__ void draw_body(const SampleArgs& a, int b, const DrawRec
     dp.ts = ts;
   }
   __syncthreads();
-  draw_pick<DT, MODE>(a, b, rec.j, rec.mode, rec.flags, onehot, sm, dp);
+  // the stages are idle now (every copy was consumed): they hold the exact
+  // scans' per-element weights
+  draw_pick<DT, MODE>(a, b, rec.j, rec.mode, rec.flags, onehot, sm, dp, wbuf);
 }
 
 // The sequence's last draw CTA: each chunk's tie statuses, exact sums where a
@@ -1947,7 +1961,7 @@ __device__ __noinline__ void draw_body(const SampleArgs& a, int b, const DrawRec
 // it; then the outputs.
 template <int DT, int MODE>
 __device__ __noinline__ void draw_pick(const SampleArgs& a, int b, int j, int mode, int flags, bool onehot, Smem& sm,
-                                       DrawPart& dp) {
+                                       DrawPart& dp, float* wbuf) {
   constexpr int P = Elem<DT>::kPer;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const DrawCtx& c = dp.ctx;
@@ -2016,7 +2030,8 @@ __device__ __noinline__ void draw_pick(const SampleArgs& a, int b, int j, int mo
   }
   for (int x = 0; x < 2; ++x) {
     if (dp.xk[x] < 0) continue;
-    const double v = chunk_exact<DT, MODE>(c, a.chunk_vecs, dp.xk[x], dp.xbt[x], dp.xbd[x], false, 0.0, nullptr, sm);
+    const double v = chunk_exact<DT, MODE>(c, a.chunk_vecs, dp.xk[x], dp.xbt[x], dp.xbd[x], false, 0.0, nullptr, sm,
+                                           wbuf);
     if (tid == 0) dp.xs[x] = fmax(v, 0.0);
   }
   __syncthreads();
@@ -2093,7 +2108,7 @@ __device__ __noinline__ void draw_pick(const SampleArgs& a, int b, int j, int mo
       tok = block_scan_draw<DT>(sc, u, false, Zp, flags, sm);
     }
   } else {
-    chunk_exact<DT, MODE>(c, a.chunk_vecs, dp.K, dp.Kbt, dp.Kbd, true, dp.tl, &tok, sm);
+    chunk_exact<DT, MODE>(c, a.chunk_vecs, dp.K, dp.Kbt, dp.Kbd, true, dp.tl, &tok, sm, wbuf);
   }
   if (tid == 0) {
     a.out_tokens[static_cast<size_t>(b) * (a.G + 1) + j] = tok;
@@ -2123,11 +2138,12 @@ __global__ void __launch_bounds__(kThreads, 2) draw_kernel(const SampleArgs a) {
   ds.path = PATH_FULL; ds.W = 1.0; ds.cut = 0; ds.m = 0.0f; ds.n_list = 0; ds.cT = 0.0f; ds.invW = 1.0f;
   if (rec.mode != 0 && !onehot) ds = load_stat(S + a.G + 1 + rec.j);
   const uint32_t stage0 = smem_u32(smem_raw + kDrawStageOff);
+  float* wbuf = reinterpret_cast<float*>(smem_raw + kDrawStageOff);
   switch (rec.mode) {
-    case 0: draw_body<DT, 0>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
-    case 1: draw_body<DT, 1>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
-    case 2: draw_body<DT, 2>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
-    default: draw_body<DT, 3>(a, b, rec, ts, ds, onehot, sm, dp, stage0); break;
+    case 0: draw_body<DT, 0>(a, b, rec, ts, ds, onehot, sm, dp, stage0, wbuf); break;
+    case 1: draw_body<DT, 1>(a, b, rec, ts, ds, onehot, sm, dp, stage0, wbuf); break;
+    case 2: draw_body<DT, 2>(a, b, rec, ts, ds, onehot, sm, dp, stage0, wbuf); break;
+    default: draw_body<DT, 3>(a, b, rec, ts, ds, onehot, sm, dp, stage0, wbuf); break;
   }
 }
 
