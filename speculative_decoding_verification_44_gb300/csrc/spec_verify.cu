@@ -2583,6 +2583,14 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done, size_t smem = sizeof(
   if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
+// The kernels' status codes are the header's.
+static_assert(SEQ_OK == SPEC_SEQ_OK && SEQ_BAD_LENGTH == SPEC_SEQ_BAD_LENGTH && SEQ_BAD_TOKEN == SPEC_SEQ_BAD_TOKEN &&
+              SEQ_BAD_UNIFORM == SPEC_SEQ_BAD_UNIFORM && SEQ_NONFINITE == SPEC_SEQ_NONFINITE &&
+              SEQ_EMPTY_SUPPORT == SPEC_SEQ_EMPTY_SUPPORT && SEQ_BAD_PARAMS == SPEC_SEQ_BAD_PARAMS &&
+              SEQ_BAD_TREE == SPEC_SEQ_BAD_TREE && SEQ_STALLED == SPEC_SEQ_STALLED &&
+              SEQ_FLAG_ZERO_Q == SPEC_SEQ_FLAG_ZERO_Q && SEQ_FLAG_Z_ZERO == SPEC_SEQ_FLAG_Z_ZERO &&
+              SEQ_FLAG_EOS == SPEC_SEQ_FLAG_EOS, "status codes");
+
 std::atomic<uint64_t> g_ready[18];
 std::atomic<int> g_early_logits{0};   // spec_set_early_logits_reads  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list, sample-tree x {bf16, f32}
 

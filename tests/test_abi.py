@@ -219,3 +219,25 @@ def test_early_exit_needs_no_other_workspace(lib):
     plain = ctypes.c_size_t()
     assert lib.spec_verify_workspace_size(64, 5, 128256, P, P, ctypes.byref(plain)) == 0
     assert sizes[0] == sizes[1] == plain.value
+
+
+def test_status_codes_match_the_binding(tmp_path):
+    """The binding's status constants are the header's values (a plain C program
+    compiled against the header prints them; the library asserts its kernels' codes
+    against the same header at compile time)."""
+    import shutil
+    from speculative_decoding_verification_44_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [n for n in dir(_lib) if n.startswith("SPEC_SEQ_")]
+    assert "SPEC_SEQ_STALLED" in names
+    lines = ["#include <stdio.h>", '#include "spec_verify.h"', "int main(void) {"]
+    lines += [f'  printf("{n} %d\\n", (int){n});' for n in names]
+    lines += ["  return 0;", "}"]
+    src, exe = tmp_path / "codes.c", tmp_path / "codes"
+    src.write_text("\n".join(lines) + "\n")
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        name, value = line.split()
+        assert getattr(_lib, name) == int(value), name
