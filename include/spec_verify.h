@@ -492,15 +492,16 @@ SPEC_API const char* spec_status_string(spec_status_t status);
 /* Process-wide switch (default 0).  Non-zero: spec_verify_sample /
  * spec_verify_sample_lenient on the kept-list path (and the no-alloc call),
  * spec_verify_greedy and spec_verify_greedy_tree when no per-sequence lengths,
- * one-hot flags or node counts are given, and the target rows of
- * spec_verify_sample_tree without node counts, stream their logits rows
- * BEFORE they wait for the previous kernel in the stream to complete, and wait
- * only before they read any other input or write anything.  Back-to-back
+ * one-hot flags or node counts are given, and spec_verify_sample_tree without
+ * node counts, stream their logits rows BEFORE they wait for the previous
+ * kernel in the stream to complete, and wait only before they read any other
+ * input or write anything (spec_verify_sample_tree also reads the tree's
+ * parents early, to know which draft rows are used).  Back-to-back
  * calls then overlap one call's tail with the next call's stream (the serving
  * workload on GB300: 38.5 -> 27.1 us per call); results are unchanged.
- * The caller guarantees that the logits a call reads are completely written
- * by the time the previous kernel in its stream allows its dependents to
- * launch: true when that kernel does not use programmatic dependent launch
+ * The caller guarantees that the logits (and tree parents) a call reads are
+ * completely written by the time the previous kernel in its stream allows its
+ * dependents to launch: true when that kernel does not use programmatic dependent launch
  * (a kernel without griddepcontrol.launch_dependents allows it only when it
  * completes), when it is a call of this library (no kernel here writes
  * logits), or when a stream operation other than a kernel launch (a copy)

@@ -1477,11 +1477,11 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
   const int slots = 2 * a.N;
   const int b = blockIdx.x / slots;
   const int slot = blockIdx.x - b * slots;
-  // with early logits reads allowed and no per-sequence node counts every
-  // target row is used and streams before this CTA waits for the previous grid
-  // (as in sample_list_kernel); a draft row needs the parents first, to know
-  // whether it is read
-  const bool stream_first = a.early_logits && a.nodes == nullptr && slot < a.N && a.aligned != 0;
+  // with early reads allowed (logits and the tree's parents) and no
+  // per-sequence node counts, a row CTA knows from the parents alone whether
+  // its row is read, streams it, and waits for the previous grid only before
+  // it writes (as in sample_list_kernel)
+  const bool stream_first = a.early_logits && a.nodes == nullptr && a.aligned != 0;
   if (!stream_first) grid_dependency_wait();
   grid_launch_dependents();
   const int n = a.nodes ? a.nodes[b] : a.N;
@@ -1504,6 +1504,7 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
     read = sm.b_i32[6] != 0;
   }
   uint4* dst = a.blocks + (static_cast<size_t>(b) * slots + slot) * a.wpr;
+  if (stream_first && !read) grid_dependency_wait();   // nothing to stream: wait before writing
   if (read) {
     const Row row = make_row<DT>((is_draft ? a.dft : a.tgt) + (static_cast<size_t>(b) * a.N + v) * a.row_bytes,
                                  a.V, a.aligned != 0);
