@@ -904,6 +904,7 @@ def main():
             "emitted_tokens_per_s_last_step": emitted * world / (ms_per_step / 1e3),
             "outcomes": outcome_stats(outs, sets, G),
             "logits_bytes_per_verified_position": logits_bytes / rt,
+            "dram_bytes_per_verified_position": (traffic / rt) if traffic else None,
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
             "gpu_launches": K * (2 if full_target else 1),
             "clocks": clk.summary(),
