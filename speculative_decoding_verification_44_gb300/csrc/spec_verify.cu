@@ -2585,12 +2585,13 @@ cudaError_t prepare(K kernel, std::atomic<uint64_t>& done, size_t smem = sizeof(
   return err;
 }
 // The kernels' status codes are the header's.
-static_assert(SEQ_OK == SPEC_SEQ_OK && SEQ_BAD_LENGTH == SPEC_SEQ_BAD_LENGTH && SEQ_BAD_TOKEN == SPEC_SEQ_BAD_TOKEN &&
-              SEQ_BAD_UNIFORM == SPEC_SEQ_BAD_UNIFORM && SEQ_NONFINITE == SPEC_SEQ_NONFINITE &&
-              SEQ_EMPTY_SUPPORT == SPEC_SEQ_EMPTY_SUPPORT && SEQ_BAD_PARAMS == SPEC_SEQ_BAD_PARAMS &&
-              SEQ_BAD_TREE == SPEC_SEQ_BAD_TREE && SEQ_STALLED == SPEC_SEQ_STALLED &&
-              SEQ_FLAG_ZERO_Q == SPEC_SEQ_FLAG_ZERO_Q && SEQ_FLAG_Z_ZERO == SPEC_SEQ_FLAG_Z_ZERO &&
-              SEQ_FLAG_EOS == SPEC_SEQ_FLAG_EOS, "status codes");
+static_assert(int(SEQ_OK) == int(SPEC_SEQ_OK) && int(SEQ_BAD_LENGTH) == int(SPEC_SEQ_BAD_LENGTH) &&
+              int(SEQ_BAD_TOKEN) == int(SPEC_SEQ_BAD_TOKEN) && int(SEQ_BAD_UNIFORM) == int(SPEC_SEQ_BAD_UNIFORM) &&
+              int(SEQ_NONFINITE) == int(SPEC_SEQ_NONFINITE) && int(SEQ_EMPTY_SUPPORT) == int(SPEC_SEQ_EMPTY_SUPPORT) &&
+              int(SEQ_BAD_PARAMS) == int(SPEC_SEQ_BAD_PARAMS) && int(SEQ_BAD_TREE) == int(SPEC_SEQ_BAD_TREE) &&
+              int(SEQ_STALLED) == int(SPEC_SEQ_STALLED) && int(SEQ_FLAG_ZERO_Q) == int(SPEC_SEQ_FLAG_ZERO_Q) &&
+              int(SEQ_FLAG_Z_ZERO) == int(SPEC_SEQ_FLAG_Z_ZERO) && int(SEQ_FLAG_EOS) == int(SPEC_SEQ_FLAG_EOS),
+              "status codes");
 
 std::atomic<uint64_t> g_ready[18];
 std::atomic<int> g_early_logits{0};   // spec_set_early_logits_reads  // sample, greedy, transform, draw, greedy-early, sample-ex, tree, kept-list, sample-tree x {bf16, f32}
@@ -2655,9 +2656,13 @@ cudaError_t launch_draw(K kernel, const SampleArgs& a, dim3 grid, cudaStream_t s
 
 // Dynamic shared memory of a launch: the bracketing top-p of PATH_FULL rows
 // needs FullExtra after Smem; launches without such rows keep their occupancy.
-size_t smem_for(const RowParams& a, const RowParams& b) {
-  const bool topp_full = (a.path == PATH_FULL && a.top_p < 1.0f) || (b.path == PATH_FULL && b.top_p < 1.0f);
-  return sizeof(Smem) + (topp_full ? sizeof(FullExtra) : 0);
+size_t smem_for(const RowParams& a, const RowParams& b, spec_dtype_t dt) {
+  auto topp_full = [](const RowParams& r) { return r.path == PATH_FULL && r.top_p < 1.0f; };
+  if (!topp_full(a) && !topp_full(b)) return sizeof(Smem);
+  // bf16 top-p rows without top-k take the value counts, which use only the
+  // count tables (four CTAs per SM); any other full-row top-p row brackets
+  auto counts_only = [&](const RowParams& r) { return !topp_full(r) || (dt == SPEC_BF16 && r.k == 0); };
+  return sizeof(Smem) + ((counts_only(a) && counts_only(b)) ? kKCExtraBytes : sizeof(FullExtra));
 }
 
 }  // namespace
@@ -2789,7 +2794,7 @@ static spec_status_t verify_sample_impl(const void* target_logits, const void* d
   a.out_status = out_status;
   a.defer = ((any_path && tps) || a.tp.path == PATH_FULL) ? 1 : 0;
   // per-sequence rules: any row may take the full-row path with a top-p cut
-  const size_t smem = any_path ? sizeof(Smem) + sizeof(FullExtra) : smem_for(a.tp, a.dp);
+  const size_t smem = any_path ? sizeof(Smem) + sizeof(FullExtra) : smem_for(a.tp, a.dp, dtype);
   a.chunk_vecs = kChunkVecs;
   a.nchunk = draw_chunks(vocab, dtype);
   a.dcount = reinterpret_cast<uint32_t*>(ws + L.dcount);
@@ -3201,11 +3206,13 @@ spec_status_t spec_transform_probs(const void* logits, spec_dtype_t dtype, int32
   if (dtype == SPEC_BF16) {
     err = prepare(transform_kernel<DT_BF16>, g_ready[4]);
     if (err == cudaSuccess)
-      transform_kernel<DT_BF16><<<rows, kThreads, smem_for(P, P), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
+      transform_kernel<DT_BF16><<<rows, kThreads, smem_for(P, P, SPEC_BF16), s>>>(lg, vocab, P, aligned, rb, out_probs,
+                                                                               out_row_status);
   } else {
     err = prepare(transform_kernel<DT_F32>, g_ready[5]);
     if (err == cudaSuccess)
-      transform_kernel<DT_F32><<<rows, kThreads, smem_for(P, P), s>>>(lg, vocab, P, aligned, rb, out_probs, out_row_status);
+      transform_kernel<DT_F32><<<rows, kThreads, smem_for(P, P, SPEC_F32), s>>>(lg, vocab, P, aligned, rb, out_probs,
+                                                                             out_row_status);
   }
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

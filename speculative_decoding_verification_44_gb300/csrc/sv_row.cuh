@@ -789,18 +789,21 @@ static_assert(kNT == kThreads, "one table slot per thread");
 //     element, no key check;
 //   * any other value goes to a small open-addressing table keyed by its
 //     16-bit order key; -inf is skipped (probability 0).
-// Counts are kept per warp pair (each pair streams its own quarter of the
-// row).  The cut then follows from the tables:
+// Counts are kept per half of the row (warps 0-3 and 4-7 each stream their
+// own half; two tables count as fast as four and leave room for four CTAs
+// per SM instead of three).  The cut then follows from the tables:
 //   * per value: weight 2^((z - m) cT) as a 64-bit fixed-point mass, times
 //     its count, summed into 256 log-probability bins (exact integer sums);
 //   * the bin where the cumulative mass (largest first) reaches
 //     ceil(top_p x total) -- the same tau as the radix rounds -- and, inside
 //     it, the values in descending order give the crossing value K* and how
 //     many of its ties the prefix takes;
-//   * the per-pair counts of K* name the quarter of the row holding the last
-//     tie taken, and a hierarchical count over that quarter finds its index.
+//   * for a row that needs it (an exact cut), the per-half counts of K* name
+//     the half holding the last tie taken, and a hierarchical count over that
+//     half finds its index; a lazy cut leaves it to the draw.
 // An overflow of the small table (too many distinct values outside the
-// window) hands the row to bracketing, which reuses the maximum.
+// window) hands the row to bracketing, which reuses the maximum (or, in a
+// launch given only the count tables' memory, to the radix rounds).
 constexpr int kKCDirect = 2048;         // 2 signs x 8 binades x 128 mantissas
 constexpr int kKCExpLo = 124;           // biased exponent of 2^-3
 constexpr int kKHBits = 8;
@@ -808,15 +811,21 @@ constexpr int kKH = 1 << kKHBits;       // small table slots
 constexpr int kKHProbe = 16;            // linear probes before overflow
 constexpr int kKCSlots = kKCDirect + kKH;
 constexpr int kKCList = kCandCap / 2;   // values of the crossing bin (unsorted, then sorted, in sm.cand)
-constexpr int kPairs = kWarps / 2;
-static_assert(kWarps % 2 == 0, "rows are counted per warp pair");
+constexpr int kCountTables = 2;         // count rows: one per half of the row (warps 0-3, 4-7)
+constexpr int kWarpsPerTable = kWarps / kCountTables;
+static_assert(kWarps % kCountTables == 0, "each count table serves whole warps");
 
 struct KeyCount {
-  uint32_t cnt[kPairs][kKCSlots];       // direct slots, then small-table slots
+  uint32_t cnt[kCountTables][kKCSlots]; // direct slots, then small-table slots
   uint32_t keys[kKH];                   // 16-bit order keys of the small table
 };
 
+// Extra shared memory of full-row top-p rows, after Smem.  The value counts
+// use only its prefix (bi, bd and the count tables), so a launch whose
+// full-row rows all take them asks for kKCExtraBytes and fits more CTAs.
 struct __align__(16) FullExtra {
+  int bi[8];
+  double bd[2];
   union {
     float priv[kNC][kThreads];          // bucket pass: column tid is thread tid's
     struct {
@@ -831,9 +840,8 @@ struct __align__(16) FullExtra {
     KeyCount kc;                        // bf16 key counts
   } u;
   float csum[kNC];
-  int bi[8];
-  double bd[2];
 };
+constexpr size_t kKCExtraBytes = offsetof(FullExtra, u) + sizeof(KeyCount);
 
 // Bytes of dynamic shared memory this launch was given.
 __device__ __forceinline__ unsigned dyn_smem_bytes() {
@@ -1225,22 +1233,22 @@ __device__ __forceinline__ void kc_loop(const Row row, int v0, int v1, uint32_t 
   }
 }
 
-// Pass 1 of a bf16 top-p row: the value counts, warp pair j over its own
-// quarter of the row; then the maximum (the largest value counted) and the
+// Pass 1 of a bf16 top-p row: the value counts, table j for the warps of
+// half j of the row; then the maximum (the largest value counted) and the
 // NaN / +inf flag.  Returns 1 if the small table overflowed -- the maximum is
 // then incomplete and the caller takes it with full_max.
 __device__ __noinline__ int kc_pass(const Row row, Smem& sm, FullExtra& fx, float& m_out, int& bad_out,
                                     const StopCheck sc, int& abandoned) {
   const int tid = threadIdx.x, warp = tid >> 5;
   for (int s = tid; s < kKH; s += kThreads) fx.u.kc.keys[s] = kNoKey;
-  for (int s = tid; s < kPairs * kKCSlots; s += kThreads) (&fx.u.kc.cnt[0][0])[s] = 0u;
+  for (int s = tid; s < kCountTables * kKCSlots; s += kThreads) (&fx.u.kc.cnt[0][0])[s] = 0u;
   if (tid == 0) {
     fx.bi[0] = 0;
     fx.bi[1] = 0;
     fx.bi[4] = 0;
   }
   __syncthreads();
-  const uint32_t keys = smem_u32(fx.u.kc.keys), cnt = smem_u32(fx.u.kc.cnt[warp >> 1]);
+  const uint32_t keys = smem_u32(fx.u.kc.keys), cnt = smem_u32(fx.u.kc.cnt[warp / kWarpsPerTable]);
   const int Ls = seg_len(row);
   const int v0 = warp * Ls, v1 = min(row.nvec, v0 + Ls);
   if (row.aligned) kc_loop<true>(row, v0, v1, keys, cnt, &fx.bi[0], &fx.bi[1], sc, &fx.bi[4]);
@@ -1252,11 +1260,10 @@ __device__ __noinline__ int kc_pass(const Row row, Smem& sm, FullExtra& fx, floa
   const KeyCount& T = fx.u.kc;
   float m = -__int_as_float(0x7f800000);
   for (int s = tid; s < kKCSlots; s += kThreads) {
-    const bool used = s < kKCDirect ? (T.cnt[0][s] | T.cnt[1][s] | T.cnt[2][s] | T.cnt[3][s]) != 0u
-                                    : T.keys[s - kKCDirect] != kNoKey;
+    const bool used = s < kKCDirect ? (T.cnt[0][s] | T.cnt[1][s]) != 0u : T.keys[s - kKCDirect] != kNoKey;
     if (used) m = fmaxf(m, __uint_as_float(kc_slot_bits(T, s) << 16));
   }
-  static_assert(kPairs == 4, "the used-slot test reads four count rows");
+  static_assert(kCountTables == 2, "the used-slot test reads two count rows");
   m_out = block_max_f(m, sm);
   bad_out = fx.bi[1];
   return fx.bi[0];
@@ -1271,7 +1278,7 @@ __device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float 
   auto count_of = [&](int s) {
     uint32_t c = 0;
 #pragma unroll
-    for (int j = 0; j < kPairs; ++j) c += T.cnt[j][s];
+    for (int j = 0; j < kCountTables; ++j) c += T.cnt[j][s];
     return c;
   };
   auto used = [&](int s) { return s < kKCDirect ? count_of(s) != 0u : T.keys[s - kKCDirect] != kNoKey; };
@@ -1371,8 +1378,8 @@ __device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float 
       if (need > c) need = c;
       const int slot = static_cast<int>((e >> 32) & 0xffffu);
       uint32_t acc = 0, r = static_cast<uint32_t>(need);
-      int Q = kPairs - 1;
-      for (int j = 0; j < kPairs; ++j) {
+      int Q = kCountTables - 1;
+      for (int j = 0; j < kCountTables; ++j) {
         const uint32_t cj = T.cnt[j][slot];
         if (acc + cj >= need) { Q = j; r = static_cast<uint32_t>(need) - acc; break; }
         acc += cj;
@@ -1401,7 +1408,7 @@ __device__ __noinline__ bool kc_resolve(const Row row, float m, float cT, float 
     return true;
   }
   ties = 0;
-  const int v0 = min(row.nvec, 2 * Q * Ls), v1 = min(row.nvec, v0 + 2 * Ls);
+  const int v0 = min(row.nvec, kWarpsPerTable * Q * Ls), v1 = min(row.nvec, v0 + kWarpsPerTable * Ls);
   const int idx = range_find_nth<DT_BF16>(row, K32, v0, v1, r, sm);
   if (idx < 0) return false;
   cut = composite(K32, static_cast<uint32_t>(idx));
@@ -1415,9 +1422,10 @@ __device__ void full_row(const Row row, const RowParams& P, int dtok, Smem& sm, 
   double S = 0.0;
   int bad;
   // top-p needs the launch's extra shared memory for key counts or bracketing
-  const bool extra = dyn_smem_bytes() >= sizeof(Smem) + sizeof(FullExtra);
+  const unsigned dyn = dyn_smem_bytes();
+  const bool extra = dyn >= sizeof(Smem) + sizeof(FullExtra);            // bracketing
   FullExtra& fx = *reinterpret_cast<FullExtra*>(reinterpret_cast<unsigned char*>(&sm) + sizeof(Smem));
-  const bool keycount = DT == DT_BF16 && extra && P.k == 0 && P.top_p < 1.0f;
+  const bool keycount = DT == DT_BF16 && dyn >= sizeof(Smem) + kKCExtraBytes && P.k == 0 && P.top_p < 1.0f;
   int kc_overflow = 1;
   if (keycount) {
     int abandoned = 0;
