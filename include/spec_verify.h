@@ -498,7 +498,7 @@ SPEC_API const char* spec_status_string(spec_status_t status);
  * input or write anything (spec_verify_sample_tree also reads the tree's
  * parents early, to know which draft rows are used).  Back-to-back
  * calls then overlap one call's tail with the next call's stream (the serving
- * workload on GB300: 38.5 -> 27.1 us per call); results are unchanged.
+ * workload on GB300: 38.5 -> 26.8 us per call); results are unchanged.
  * The caller guarantees that the logits (and tree parents) a call reads are
  * completely written by the time the previous kernel in its stream allows its
  * dependents to launch: true when that kernel does not use programmatic dependent launch
