@@ -1575,8 +1575,9 @@ struct __align__(16) ChunkSum {
 static_assert(sizeof(ChunkSum) == 48, "ChunkSum layout");
 
 constexpr int kDrawMaxRun = 32;   // chunks one draw CTA sums (its per-warp partials live in shared memory)
-constexpr int kDrawStages = 2;    // chunks of each row in flight per draw CTA (bulk copies)
-constexpr int kStageRowBytes = kChunkVecs * 16;
+constexpr int kDrawStages = 2;    // half-chunks of each row in flight per draw CTA (bulk copies)
+constexpr int kStageVecs = kChunkVecs / 2;
+constexpr int kStageRowBytes = kStageVecs * 16;
 
 struct DrawCtx {
   Row trow, drow;
@@ -1645,46 +1646,53 @@ __device__ __forceinline__ int tie_status(int n, uint32_t idx, uint32_t before, 
 
 // Weights of chunk k with every tie decided: by rank for a lazy cut (bt / bd
 // ties before the chunk, then in index order), by index for an exact one.
-// Thread t takes the chunk's vectors 4t..4t+3 (one round trip), so thread
-// order is index order.  Returns the chunk's sum (every thread); with find,
-// also the first token where the running sum exceeds tl (else the last token
-// with weight) in *tok.  Block-wide; c lives in shared memory, and wbuf
-// (shared memory, 32 floats per thread) keeps each element's weight for the find.
+// The chunk is taken in two halves; in each, thread t takes two consecutive
+// vectors, so thread order is index order within a half.  Returns the
+// chunk's sum (every thread); with find, also the first token where the
+// running sum exceeds tl (else the last token with weight) in *tok.
+// Block-wide; c lives in shared memory, and wbuf (shared memory, 32 floats per
+// thread) keeps each element's weight for the find.
 template <int DT, int MODE>
 __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int k, int bt, int bd, bool find,
                                            double tl, int* tok, Smem& sm, float* wbuf) {
   constexpr int P = Elem<DT>::kPer;
-  constexpr int kVPT = 4;
-  static_assert(kVPT * kThreads == kChunkVecs, "a thread takes four consecutive vectors of a chunk");
+  constexpr int kVPT = 2;
+  static_assert(2 * kVPT * kThreads == kChunkVecs, "two halves of two vectors per thread make a chunk");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nv = c.trow.nvec;
-  const int v0 = k * chunk_vecs + tid * kVPT;
-  uint4 rt[kVPT], rd[kVPT];
-  int n[kVPT];
-#pragma unroll
-  for (int i = 0; i < kVPT; ++i) n[i] = (v0 + i < nv) ? draw_load<DT, MODE>(c, v0 + i, rt[i], rd[i]) : 0;
-  // ties of each cut in this thread's elements, then their exclusive prefix over the block
-  uint32_t ct = 0, cd = 0;
-#pragma unroll
-  for (int i = 0; i < kVPT; ++i) {
-    float zt[P], zd[P];
-    unpack<DT>(rt[i], zt);
-    unpack<DT>(rd[i], zd);
-#pragma unroll
-    for (int e = 0; e < P; ++e) {
-      ct += (e < n[i] && zt[e] == c.tt) ? 1u : 0u;
-      cd += (MODE == 1 && e < n[i] && zd[e] == c.td) ? 1u : 0u;
-    }
-  }
-  const uint32_t it_ = warp_incl_scan_u32(ct, lane), id_ = warp_incl_scan_u32(cd, lane);
-  if (lane == 31) { sm.nw[warp] = static_cast<int>(it_); sm.red_i[warp] = static_cast<int>(id_); }
   if (tid == 0) { sm.b_i32[5] = -1; sm.b_i32[6] = -1; sm.b_i32[7] = -1; }
-  __syncthreads();
-  uint32_t rt0 = static_cast<uint32_t>(bt) + it_ - ct, rd0 = static_cast<uint32_t>(bd) + id_ - cd;
-  for (int w = 0; w < warp; ++w) { rt0 += static_cast<uint32_t>(sm.nw[w]); rd0 += static_cast<uint32_t>(sm.red_i[w]); }
-  // the weights, in index order, every tie decided
-  auto walk = [&](auto&& visit) {
-    uint32_t rt_ = rt0, rd_ = rd0;
+  double run = 0.0;            // weight of the halves before
+  uint32_t rbt = static_cast<uint32_t>(bt), rbd = static_cast<uint32_t>(bd);
+  for (int half = 0; half < 2; ++half) {
+    const int v0 = k * chunk_vecs + half * kVPT * kThreads + tid * kVPT;
+    uint4 rt[kVPT], rd[kVPT];
+    int n[kVPT];
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) n[i] = (v0 + i < nv) ? draw_load<DT, MODE>(c, v0 + i, rt[i], rd[i]) : 0;
+    uint32_t ct = 0, cd = 0;
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+      float zt[P], zd[P];
+      unpack<DT>(rt[i], zt);
+      unpack<DT>(rd[i], zd);
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        ct += (e < n[i] && zt[e] == c.tt) ? 1u : 0u;
+        cd += (MODE == 1 && e < n[i] && zd[e] == c.td) ? 1u : 0u;
+      }
+    }
+    const uint32_t it_ = warp_incl_scan_u32(ct, lane), id_ = warp_incl_scan_u32(cd, lane);
+    if (lane == 31) { sm.nw[warp] = static_cast<int>(it_); sm.red_i[warp] = static_cast<int>(id_); }
+    __syncthreads();
+    uint32_t rt_ = rbt + it_ - ct, rd_ = rbd + id_ - cd;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) { rt_ += static_cast<uint32_t>(sm.nw[w]); rd_ += static_cast<uint32_t>(sm.red_i[w]); }
+      rbt += static_cast<uint32_t>(sm.nw[w]);
+      rbd += static_cast<uint32_t>(sm.red_i[w]);
+    }
+    // the weights, in index order, every tie decided; kept for the find
+    float ts = 0.0f;
+    int last = -1, e0 = half * kVPT * P;
 #pragma unroll
     for (int i = 0; i < kVPT; ++i) {
       float zt[P], zd[P];
@@ -1698,52 +1706,49 @@ __device__ __noinline__ double chunk_exact(const DrawCtx& c, int chunk_vecs, int
         if (zt[e] == c.tt && !(c.nt > 0 ? rt_++ < static_cast<uint32_t>(c.nt) : x <= c.it)) p = 0.0f;
         float q = draw_qk<MODE>(c, zd[e], x, sm);
         if (MODE == 1 && zd[e] == c.td && !(c.nd > 0 ? rd_++ < static_cast<uint32_t>(c.nd) : x <= c.id)) q = 0.0f;
-        visit(static_cast<int>(x), draw_w<MODE>(p, q, c.beta));
+        const float w = draw_w<MODE>(p, q, c.beta);
+        ts += w;
+        if (w > 0.0f) last = static_cast<int>(x);
+        wbuf[(e0 + i * P + e) * kThreads + tid] = w;
       }
     }
-  };
-  float ts = 0.0f;
-  int last = -1, e = 0;
-  walk([&](int x, float w) {
-    ts += w;
-    if (w > 0.0f) last = x;
-    wbuf[(e++) * kThreads + tid] = w;       // element e of this thread (index order)
-  });
-  const df incl = warp_incl_scan_df(df_from(ts), lane);
-  if (lane == 31) { sm.red_f[warp] = incl.hi; sm.red_lo[warp] = incl.lo; }
-  __syncthreads();
-  df base = df_add(incl, df_from(-ts)), tot = df_from(0.0f);
-  for (int w = 0; w < kWarps; ++w) {
-    const df x = {sm.red_f[w], sm.red_lo[w]};
-    if (w < warp) base = df_add(base, x);
-    tot = df_add(tot, x);
-  }
-  if (find) {
-    const double b0 = df_to_double(base);
-    if (ts > 0.0f && b0 + static_cast<double>(ts) > tl)
-      atomicMin(reinterpret_cast<unsigned*>(&sm.b_i32[5]), static_cast<unsigned>(tid));
-    if (last >= 0) atomicMax(&sm.b_i32[6], last);
+    const df incl = warp_incl_scan_df(df_from(ts), lane);
+    if (lane == 31) { sm.red_f[warp] = incl.hi; sm.red_lo[warp] = incl.lo; }
     __syncthreads();
-    if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
-      // the same weights, from the buffer, in index order
-      float c32 = 0.0f;
-      int found = -1, ei = 0;
-      for (int i = 0; i < kVPT && found < 0; ++i) {
-        for (int ee = 0; ee < n[i] && found < 0; ++ee, ++ei) {
-          const float w = wbuf[ei * kThreads + tid];
-          if (w > 0.0f) {
-            c32 += w;
-            if (b0 + static_cast<double>(c32) > tl) found = (v0 + i) * P + ee;
+    df base = df_add(incl, df_from(-ts)), tot = df_from(0.0f);
+    for (int w = 0; w < kWarps; ++w) {
+      const df x = {sm.red_f[w], sm.red_lo[w]};
+      if (w < warp) base = df_add(base, x);
+      tot = df_add(tot, x);
+    }
+    const double b0 = run + df_to_double(base);
+    if (find && sm.b_i32[5] == -1) {         // not found in an earlier half (same in every thread)
+      __syncthreads();
+      if (ts > 0.0f && b0 + static_cast<double>(ts) > tl)
+        atomicMin(reinterpret_cast<unsigned*>(&sm.b_i32[5]), static_cast<unsigned>(tid));
+      if (last >= 0) atomicMax(&sm.b_i32[6], last);
+      __syncthreads();
+      if (static_cast<unsigned>(sm.b_i32[5]) == static_cast<unsigned>(tid)) {
+        float c32 = 0.0f;
+        int found = -1;
+        for (int i = 0; i < kVPT && found < 0; ++i) {
+          for (int e = 0; e < n[i] && found < 0; ++e) {
+            const float w = wbuf[(e0 + i * P + e) * kThreads + tid];
+            if (w > 0.0f) {
+              c32 += w;
+              if (b0 + static_cast<double>(c32) > tl) found = (v0 + i) * P + e;
+            }
           }
         }
+        sm.b_i32[7] = found >= 0 ? found : last;
       }
-      sm.b_i32[7] = found >= 0 ? found : last;
     }
+    run += df_to_double(tot);
     __syncthreads();
-    *tok = sm.b_i32[5] == -1 ? sm.b_i32[6] : sm.b_i32[7];   // rounding: the last weighted token
   }
+  if (find) *tok = sm.b_i32[5] == -1 ? sm.b_i32[6] : sm.b_i32[7];   // rounding: the last weighted token
   __syncthreads();
-  return df_to_double(tot);
+  return run;
 }
 
 template <int DT, int MODE>
@@ -1835,36 +1840,43 @@ __device__ __noinline__ void draw_body(const SampleArgs& a, int b, const DrawRec
   };
   bool stalled = false;
   if (c.trow.aligned && (MODE != 1 || c.drow.aligned)) {
-    // bulk copies: one thread streams whole chunks of both rows into the
+    // bulk copies: one thread streams half-chunks of both rows into the
     // stages, kDrawStages ahead; every thread reads its vectors from there
+    // (small stages leave room for three CTAs per SM)
     const uint32_t bar = smem_u32(&dp.bar[0]);
     if (tid == 0) {
       for (int st = 0; st < kDrawStages; ++st) mbar_init(bar + 8u * st, 1u);
       mbar_init_fence();
     }
     __syncthreads();
-    auto issue = [&](int k, int st) {
-      const int v0 = k * a.chunk_vecs;
-      const uint32_t bytes = static_cast<uint32_t>(min(a.chunk_vecs, nv - v0)) * 16u;
-      mbar_expect_tx(bar + 8u * st, (MODE == 1 ? 2u : 1u) * bytes);
-      bulk_g2s(stage0 + 2u * st * kStageRowBytes, c.trow.base + static_cast<size_t>(v0) * 16, bytes, bar + 8u * st);
-      if (MODE == 1)
-        bulk_g2s(stage0 + (2u * st + 1u) * kStageRowBytes, c.drow.base + static_cast<size_t>(v0) * 16, bytes,
+    const int nq = 2 * (k1 - k0);                   // half-chunks of this CTA's run
+    auto issue = [&](int q, int st) {
+      const int v0 = (k0 + q / 2) * a.chunk_vecs + (q & 1) * kStageVecs;
+      const int nvq = min(kStageVecs, nv - v0);
+      const uint32_t bytes = nvq > 0 ? static_cast<uint32_t>(nvq) * 16u : 0u;
+      mbar_expect_tx(bar + 8u * st, (MODE == 1 ? 2u : 1u) * bytes);   // 0 bytes: the phase completes now
+      if (bytes) {
+        bulk_g2s(stage0 + 2u * st * kStageRowBytes, c.trow.base + static_cast<size_t>(v0) * 16, bytes,
                  bar + 8u * st);
+        if (MODE == 1)
+          bulk_g2s(stage0 + (2u * st + 1u) * kStageRowBytes, c.drow.base + static_cast<size_t>(v0) * 16, bytes,
+                   bar + 8u * st);
+      }
     };
     if (tid == 0)
-      for (int st = 0; st < kDrawStages && k0 + st < k1; ++st) issue(k0 + st, st);
-    int k = k0;
-    for (; k < k1; ++k) {
-      const int r = k - k0, st = r % kDrawStages;
-      const bool ok = mbar_wait(bar + 8u * st, static_cast<uint32_t>(r / kDrawStages) & 1u);
+      for (int st = 0; st < kDrawStages && st < nq; ++st) issue(st, st);
+    int q = 0;
+    for (; q < nq; ++q) {
+      const int st = q % kDrawStages;
+      const bool ok = mbar_wait(bar + 8u * st, static_cast<uint32_t>(q / kDrawStages) & 1u);
       if (__syncthreads_or(!ok)) { stalled = true; break; }
-      const int v0 = k * a.chunk_vecs, nvk = min(a.chunk_vecs, nv - v0);
+      const int k = k0 + q / 2;
+      const int v0 = k * a.chunk_vecs + (q & 1) * kStageVecs, nvq = min(kStageVecs, nv - v0);
       const uint32_t srow = stage0 + 2u * st * kStageRowBytes;
 #pragma unroll
-      for (int i = 0; i < kVPT; ++i) {
+      for (int i = 0; i < kStageVecs / kThreads; ++i) {
         const int vl = i * kThreads + tid;
-        if (vl >= nvk) continue;
+        if (vl >= nvq) continue;
         const uint4 rt = lds128(srow + 16u * vl);
         const uint4 rd = MODE == 1 ? lds128(srow + kStageRowBytes + 16u * vl) : make_uint4(0u, 0u, 0u, 0u);
         float zt[P], zd[P];
@@ -1873,17 +1885,17 @@ __device__ __noinline__ void draw_body(const SampleArgs& a, int b, const DrawRec
 #pragma unroll
         for (int e = 0; e < P; ++e) elem(zt[e], zd[e], static_cast<uint32_t>((v0 + vl) * P + e));
       }
-      chunk_done(k);
+      if (q & 1) chunk_done(k);
       __syncthreads();                            // every thread is done with stage st
-      if (tid == 0 && k + kDrawStages < k1) {
+      if (tid == 0 && q + kDrawStages < nq) {
         fence_proxy_async_smem();
-        issue(k + kDrawStages, st);
+        issue(q + kDrawStages, st);
       }
     }
     if (stalled && tid == 0) {
       // let the copies still in flight land (bounded) before the CTA leaves
-      for (int q = k; q < min(k1, k + kDrawStages); ++q)
-        mbar_wait(bar + 8u * ((q - k0) % kDrawStages), static_cast<uint32_t>((q - k0) / kDrawStages) & 1u);
+      for (int r = q; r < min(nq, q + kDrawStages); ++r)
+        mbar_wait(bar + 8u * (r % kDrawStages), static_cast<uint32_t>(r / kDrawStages) & 1u);
     }
   } else {
     for (int k = k0; k < k1; ++k) {
@@ -2121,7 +2133,7 @@ __device__ __noinline__ void draw_pick(const SampleArgs& a, int b, int j, int mo
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) draw_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) draw_kernel(const SampleArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   DrawPart& dp = *reinterpret_cast<DrawPart*>(smem_raw + sizeof(Smem));
@@ -2609,10 +2621,10 @@ int sm_count() {
   return n;
 }
 
-// Chunks per draw CTA: about two waves of two draw CTAs per SM over the
+// Chunks per draw CTA: about two waves of three draw CTAs per SM over the
 // batch, each CTA summing at least one and at most kDrawMaxRun chunks.
 int draw_run(int B, int nchunk) {
-  const int target = 2 * 2 * sm_count();
+  const int target = 2 * 3 * sm_count();
   int splits = std::max(1, std::min(nchunk, (target + B - 1) / B));
   splits = std::max(splits, (nchunk + kDrawMaxRun - 1) / kDrawMaxRun);
   return (nchunk + splits - 1) / splits;
