@@ -162,7 +162,7 @@ SPEC_API spec_status_t spec_verify_workspace_size(int32_t batch, int32_t gamma_m
 /* Sampling-mode verification of `batch` sequences, asynchronous on `stream`:
  * one kernel launch, or two when the target's rows take the full-row path
  * (top_k off or above 128) -- the residual or bonus draw over a whole row
- * then runs in a second, chunk-parallel launch on the same stream.
+ * then runs in a second launch on the same stream, several CTAs per row.
  *
  * target_logits   [batch][gamma_max+1][vocab] of dtype.
  * draft_logits    [batch][gamma_max][vocab] of dtype, or NULL when every

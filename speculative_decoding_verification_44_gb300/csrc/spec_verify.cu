@@ -718,7 +718,7 @@ __device__ __noinline__ void sample_epilogue(const SampleArgs& a, int b, int gb,
     tok = list_draw<DT>(a, b, r, residual, onehot, dj, ds, uf, Z_resid, flags, sm);
     if (a.defer && tid == 0) a.drec[b].j = -1;   // per-sequence rules: nothing for draw_kernel
   } else if (a.defer) {
-    // a full-row draw: draw_kernel does it, chunk-parallel, and writes the drawn
+    // a full-row draw: draw_kernel does it, over runs of chunks, and writes the drawn
     // token, residual_Z and status
     if (tid == 0) {
       DrawRec rec;
@@ -1538,16 +1538,6 @@ __global__ void __launch_bounds__(kThreads, 5) sample_tree_kernel(const SampleTr
   else tree_sample_epilogue<kListCap / 32>(a, b, n, sm);
 }
 
-// ------------------------------------------------------------------ chunk-parallel full-row draw
-// The residual or bonus draw over a PATH_FULL target row reads up to two whole
-// rows; one CTA doing it alone is latency-bound.  Here every sequence with a
-// pending draw gets nchunk CTAs: CTA (b, c) sums the draw weights of chunk c
-// (chunk_vecs vectors of the row, in vocabulary order) into dsum[b][c]; the
-// last of them to finish forms Z = sum_c dsum[b][c] in chunk order, finds the
-// chunk whose range of the cumulative sum holds u Z, and re-scans that chunk
-// block-wide with identical per-element arithmetic for the first x with
-// C(x) > u Z [wrblog §5, §6].  Z == 0 after a rejection falls back to the
-// draw from p, over the whole row, as the sequence epilogue did.
 // ------------------------------------------------------------------ full-row draw
 // The draw at the position the epilogue chose, over whole rows: the inverse
 // CDF, in vocabulary order, of w(x) = p(x) (the bonus draw) or
